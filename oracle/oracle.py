@@ -1,0 +1,258 @@
+"""NumPy front end of the FP64 CPU oracle for HSTU jagged attention.
+
+TEST INFRASTRUCTURE ONLY: the tests, the package smoke check and the
+benchmark's CPU-baseline leg are the only callers.  Nothing here is shared
+with the CUDA path.
+
+All floating-point inputs are widened to float64 (bf16/fp32 values widen
+exactly), all computation is float64 in ``hstu_oracle.c`` or in NumPy.
+The full HSTU layer (ai6s.net survey, section 2.1.2: pointwise projection
+eq. (1), spatial aggregation eq. (2), pointwise transformation eq. (3), with
+residual connections between layers) is composed here from NumPy matmuls and
+the C attention routines:
+
+    [U | V | Q | K] = SiLU(X W1)           (split in that order, no bias)
+    Y   = LayerNorm(attention(Q, K, V)) * U
+    out = X + Y W2                         (no bias)
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import numpy as np
+
+from .build import build_oracle
+
+_lib = None
+
+P_DEFAULT = 128
+TB_DEFAULT = 64
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(build_oracle())
+        i32, i64, dbl, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
+        _lib.hstu_oracle_fwd.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, i32, vp, i32,
+                                         dbl, dbl, vp, vp, vp, vp, vp]
+        _lib.hstu_oracle_norm_gate.argtypes = [i64, i32, i32, dbl, vp, vp, vp, vp, vp, vp]
+        _lib.hstu_oracle_norm_gate_bwd.argtypes = [i64, i32, i32, dbl, vp, vp, vp, vp, vp, vp]
+        _lib.hstu_oracle_attn_bwd.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, i32, vp, i32,
+                                              dbl, dbl, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        _lib.hstu_oracle_tile_count.argtypes = [i32, vp, i32, i32]
+        _lib.hstu_oracle_tile_count.restype = i64
+        _lib.hstu_oracle_tile_classes.argtypes = [i32, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp]
+        _lib.hstu_oracle_allowed_pairs.argtypes = [i32, vp, vp, vp, vp]
+        _lib.hstu_oracle_time_bucket.argtypes = [i64, i64, i32]
+        _lib.hstu_oracle_pos_bucket.argtypes = [i64, i64, i64, i32]
+        _lib.hstu_oracle_num_threads.restype = i32
+    return _lib
+
+
+def num_threads() -> int:
+    return int(lib().hstu_oracle_num_threads())
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f64(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _i64(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.int64)
+
+
+def _i32(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _u8(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.uint8)
+
+
+def time_bucket(ti: int, tj: int, Tb: int = TB_DEFAULT) -> int:
+    return int(lib().hstu_oracle_time_bucket(int(ti), int(tj), int(Tb)))
+
+
+def pos_bucket(i: int, j: int, h_end: int, P: int = P_DEFAULT) -> int:
+    return int(lib().hstu_oracle_pos_bucket(int(i), int(j), int(h_end), int(P)))
+
+
+class Problem:
+    """The attention inputs in float64 / int64, in the jagged layout."""
+
+    def __init__(self, offsets, q, k, v, alpha, N, num_targets=None, num_contexts=None,
+                 timestamps=None, rab_pos=None, rab_time=None):
+        self.offsets = _i64(offsets)
+        self.B = len(self.offsets) - 1
+        self.q, self.k, self.v = _f64(q), _f64(k), _f64(v)
+        self.T, self.H, self.dqk = self.q.shape
+        self.dv = self.v.shape[2]
+        self.alpha, self.N = float(alpha), float(N)
+        self.nt, self.nc = _i32(num_targets), _i32(num_contexts)
+        self.ts = _i64(timestamps)
+        self.rp, self.rt = _f64(rab_pos), _f64(rab_time)
+        self.P = self.rp.shape[1] if self.rp is not None else P_DEFAULT
+        self.Tb = self.rt.shape[1] if self.rt is not None else TB_DEFAULT
+
+    @classmethod
+    def from_batch(cls, b, q=None, k=None, v=None):
+        return cls(b.offsets, b.q if q is None else q, b.k if k is None else k,
+                   b.v if v is None else v, b.alpha, b.max_seq_len, b.num_targets,
+                   b.num_contexts, b.timestamps, b.rab_pos, b.rab_time)
+
+    def _head(self):
+        return (self.B, self.H, self.dqk, self.dv, _p(self.offsets), _p(self.nt), _p(self.nc),
+                _p(self.ts), _p(self.rp), self.P, _p(self.rt), self.Tb, self.alpha, self.N)
+
+
+def attn_fwd(pb: Problem, rows: Optional[np.ndarray] = None) -> np.ndarray:
+    """o [T, H, dv] float64; rows (bool/uint8 [T]) restricts the computed rows
+    (the others are returned as zeros)."""
+    o = np.zeros((pb.T, pb.H, pb.dv), np.float64)
+    rows = _u8(rows)
+    rc = lib().hstu_oracle_fwd(*pb._head(), _p(pb.q), _p(pb.k), _p(pb.v), _p(o), _p(rows))
+    if rc != 0:
+        raise ValueError("oracle: invalid jagged metadata")
+    return o
+
+
+def norm_gate(o, u, norm="layernorm", eps=1e-5, rows=None):
+    """y [T, F], mean [T], rstd [T] from o [T, H, dv] (or [T, F]) and u [T, F] (or None)."""
+    o = _f64(o).reshape(o.shape[0], -1)
+    T, F = o.shape
+    u = _f64(u)
+    y = np.zeros((T, F), np.float64)
+    mean = np.zeros(T, np.float64)
+    rstd = np.zeros(T, np.float64)
+    lib().hstu_oracle_norm_gate(T, F, 1 if norm == "layernorm" else 0, float(eps), _p(o), _p(u),
+                                _p(y), _p(mean), _p(rstd), _p(_u8(rows)))
+    return y, mean, rstd
+
+
+def norm_gate_bwd(o, u, dy, norm="layernorm", eps=1e-5, rows=None):
+    """(dx [T, F], du [T, F] or None)."""
+    o = _f64(o).reshape(o.shape[0], -1)
+    T, F = o.shape
+    u, dy = _f64(u), _f64(dy).reshape(T, F)
+    dx = np.zeros((T, F), np.float64)
+    du = np.zeros((T, F), np.float64) if u is not None else None
+    lib().hstu_oracle_norm_gate_bwd(T, F, 1 if norm == "layernorm" else 0, float(eps), _p(o), _p(u),
+                                    _p(dy), _p(dx), _p(du), _p(_u8(rows)))
+    return dx, du
+
+
+def attn_bwd(pb: Problem, dO, q_rows=None, kv_rows=None, want_rab=True):
+    """dq, dk, dv [T, H, d] and d_rab_pos [H, P], d_rab_time [H, Tb] (None when
+    the table is absent or rows are restricted)."""
+    dO = _f64(dO).reshape(pb.T, pb.H, pb.dv)
+    dq = np.zeros_like(pb.q)
+    dk = np.zeros_like(pb.k)
+    dv = np.zeros_like(pb.v)
+    full = q_rows is None and kv_rows is None
+    drp = np.zeros((pb.H, pb.P), np.float64) if (pb.rp is not None and full and want_rab) else None
+    drt = (np.zeros((pb.H, pb.Tb), np.float64)
+           if (pb.rt is not None and pb.ts is not None and full and want_rab) else None)
+    rc = lib().hstu_oracle_attn_bwd(*pb._head(), _p(pb.q), _p(pb.k), _p(pb.v), _p(dO),
+                                    _p(dq), _p(dk), _p(dv), _p(drp), _p(drt),
+                                    _p(_u8(q_rows)), _p(_u8(kv_rows)))
+    if rc != 0:
+        raise ValueError("oracle: invalid jagged metadata")
+    return dq, dk, dv, drp, drt
+
+
+def forward(b, rows=None):
+    """Whole forward of a synth.Batch: dict with o [T,H,dv], y [T,F], mean, rstd."""
+    pb = Problem.from_batch(b)
+    o = attn_fwd(pb, rows)
+    y, mean, rstd = norm_gate(o, b.u, b.norm, b.eps, rows)
+    return {"o": o, "y": y, "mean": mean, "rstd": rstd}
+
+
+def backward(b, o=None):
+    """Whole backward of a synth.Batch given its dy: dict with dq, dk, dv, du,
+    d_rab_pos, d_rab_time (and the forward's o, y)."""
+    pb = Problem.from_batch(b)
+    if o is None:
+        o = attn_fwd(pb)
+    dO, du = norm_gate_bwd(o, b.u, b.dy, b.norm, b.eps)
+    dq, dk, dv, drp, drt = attn_bwd(pb, dO)
+    return {"o": o, "dO": dO.reshape(pb.T, pb.H, pb.dv), "dq": dq, "dk": dk, "dv": dv, "du": du,
+            "d_rab_pos": drp, "d_rab_time": drt}
+
+
+def tile_classes(offsets, num_targets, num_contexts, BM, BN):
+    """Brute-force tile classes: structured array of (b, qb, kb, cls, allowed),
+    cls 0 = skip, 1 = partial, 2 = full."""
+    off = _i64(offsets)
+    B = len(off) - 1
+    n = int(lib().hstu_oracle_tile_count(B, _p(off), BM, BN))
+    cols = [np.zeros(n, np.int32) for _ in range(4)]
+    allowed = np.zeros(n, np.int64)
+    lib().hstu_oracle_tile_classes(B, _p(off), _p(_i32(num_targets)), _p(_i32(num_contexts)), BM, BN,
+                                   *[_p(c) for c in cols], _p(allowed))
+    return {"b": cols[0], "qb": cols[1], "kb": cols[2], "cls": cols[3], "allowed": allowed}
+
+
+def allowed_pairs(offsets, num_targets=None, num_contexts=None):
+    off = _i64(offsets)
+    out = np.zeros(len(off) - 1, np.int64)
+    lib().hstu_oracle_allowed_pairs(len(off) - 1, _p(off), _p(_i32(num_targets)),
+                                    _p(_i32(num_contexts)), _p(out))
+    return out
+
+
+# ------------------------------------------------------------- full layer
+
+def _silu(x):
+    return x / (1.0 + np.exp(-x))
+
+
+def _silu_grad(x):
+    s = 1.0 / (1.0 + np.exp(-x))
+    return s * (1.0 + x * (1.0 - s))
+
+
+def _split_uvqk(a, H, d):
+    T = a.shape[0]
+    D = H * d
+    return (a[:, 0:D], a[:, D:2 * D].reshape(T, H, d), a[:, 2 * D:3 * D].reshape(T, H, d),
+            a[:, 3 * D:4 * D].reshape(T, H, d))
+
+
+def layer_forward(b, rows=None):
+    """Full HSTU layer forward in float64: dict with z1, u, v, q, k, o, y, out."""
+    x, w1, w2 = _f64(b.x), _f64(b.w1), _f64(b.w2)
+    z1 = x @ w1
+    a1 = _silu(z1)
+    u, v, q, k = _split_uvqk(a1, b.H, b.d_v)
+    pb = Problem(b.offsets, q, k, v, b.alpha, b.max_seq_len, b.num_targets, b.num_contexts,
+                 b.timestamps, b.rab_pos, b.rab_time)
+    o = attn_fwd(pb, rows)
+    y, mean, rstd = norm_gate(o, u, "layernorm", b.eps, rows)
+    out = x + y @ w2
+    return {"z1": z1, "u": u, "v": pb.v, "q": pb.q, "k": pb.k, "o": o, "y": y, "out": out,
+            "mean": mean, "rstd": rstd, "pb": pb}
+
+
+def layer_backward(b, fwd=None):
+    """Full HSTU layer backward given d(out) = b.dout: dict with dx, dw1, dw2
+    and the attention intermediates dq, dk, dv, du, d_rab_pos, d_rab_time."""
+    f = layer_forward(b) if fwd is None else fwd
+    x, w1, w2, dout = _f64(b.x), _f64(b.w1), _f64(b.w2), _f64(b.dout)
+    dw2 = f["y"].T @ dout
+    dy = dout @ w2.T
+    dO, du = norm_gate_bwd(f["o"], f["u"], dy, "layernorm", b.eps)
+    dq, dk, dv, drp, drt = attn_bwd(f["pb"], dO)
+    T = x.shape[0]
+    da1 = np.concatenate([du, dv.reshape(T, -1), dq.reshape(T, -1), dk.reshape(T, -1)], axis=1)
+    dz1 = da1 * _silu_grad(f["z1"])
+    dw1 = x.T @ dz1
+    dx = dout + dz1 @ w1.T
+    return {"dx": dx, "dw1": dw1, "dw2": dw2, "dq": dq, "dk": dk, "dv": dv, "du": du,
+            "d_rab_pos": drp, "d_rab_time": drt, "dy": dy, "dO": dO}
