@@ -1,0 +1,415 @@
+#!/usr/bin/env python
+"""Benchmark of HSTU jagged attention, forward + backward, on one GB300.
+
+Workload: the heavy-tailed training batch -- 64 jagged sequences with
+Zipf(1.2) history lengths on [1, 8192] after stochastic-length sampling, plus
+32 candidates each; 4 heads of 128; BF16 inputs, FP32 outputs; causal +
+candidate mask; relative-position (128) and log2 time-gap (64) bias.  One
+step = forward (attention + LayerNorm gate) and backward (dq, dk, dv, du,
+d_rab) of one batch.  16 distinct seeded batches are resident in HBM and
+taken in turn, so consecutive steps never find their inputs in L2.
+
+Metric: useful TFLOP/s, counting allowed (unmasked) query-key pairs only:
+forward 2 (d_qk + d_v) and backward 2 (3 d_qk + 2 d_v) FLOPs per pair.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from hstu_jagged_attention_02_gb300 import synth  # noqa: E402
+
+METRIC = "HSTU jagged attention useful TFLOP/s (fwd+bwd), % of GB300 BF16 tensor peak"
+UNIT = "TFLOP/s"
+WORKLOAD = ("heavy_tailed: 64 jagged sequences, Zipf(1.2) history lengths on [1,8192] with "
+            "stochastic-length sampling + 32 candidates, 4 heads x 128, BF16 in / FP32 out, "
+            "causal + candidate mask, position + time rab, forward + backward")
+N_SEEDS = 16
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def allowed_pairs(b) -> int:
+    """Allowed (i, j) pairs of a batch summed over sequences and heads."""
+    n = b.lengths.astype(np.int64)
+    c = b.num_contexts.astype(np.int64) if b.num_contexts is not None else np.zeros_like(n)
+    m = b.num_targets.astype(np.int64) if b.num_targets is not None else np.zeros_like(n)
+    h_end = n - m
+    per_seq = h_end * (h_end + 1) // 2 + c * (c - 1) // 2 + m * (h_end + 1)
+    return int(per_seq.sum()) * b.H
+
+
+def useful_flops(b):
+    p = allowed_pairs(b)
+    fwd = 2 * (b.d_qk + b.d_v) * p
+    bwd = 2 * (3 * b.d_qk + 2 * b.d_v) * p
+    return fwd, bwd
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def config_dict(extra=None):
+    d = {"workload": WORKLOAD, "batches": N_SEEDS, "seeds": f"0..{N_SEEDS - 1} (+rank*{N_SEEDS})",
+         "l2": "inputs larger than L2: 16 distinct resident batches taken in turn"}
+    if extra:
+        d.update(extra)
+    return d
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [ln.strip().split(",") for ln in self.f.read().splitlines() if ln.strip()]
+        self.f.close()
+        os.unlink(self.f.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_sources_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "hstu_jagged_attention_02_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(kernel_role: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+        rec = d.get(kernel_role)
+        if rec and rec.get("sources_sha") == kernel_sources_sha():
+            return rec
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------ CPU oracle arm
+
+def time_oracle(batches, budget_s):
+    """Runs the FP64 oracle (fwd + bwd) over batches until budget_s is spent;
+    returns (useful flops, seconds, description, threads)."""
+    from oracle import oracle as O
+    done_flops, t0, used = 0, time.perf_counter(), []
+    for b in batches:
+        f = O.forward(b)
+        O.backward(b, o=f["o"])
+        fw, bw = useful_flops(b)
+        done_flops += fw + bw
+        used.append(b)
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    desc = (f"fwd+bwd of {len(used)} batch(es) / {sum(x.B for x in used)} sequences / "
+            f"{sum(x.T for x in used)} tokens")
+    return done_flops, dt, desc, O.num_threads()
+
+
+def sub_batch(b, n_seq):
+    """The first n_seq sequences of a batch (a bounded sample of the workload)."""
+    end = int(b.offsets[n_seq])
+    sl = slice(0, end)
+    return synth.Batch(
+        name=b.name, seed=b.seed, dtype=b.dtype, B=n_seq, H=b.H, d_qk=b.d_qk, d_v=b.d_v,
+        lengths=b.lengths[:n_seq].copy(), offsets=b.offsets[: n_seq + 1].copy(),
+        num_targets=None if b.num_targets is None else b.num_targets[:n_seq].copy(),
+        num_contexts=None if b.num_contexts is None else b.num_contexts[:n_seq].copy(),
+        timestamps=None if b.timestamps is None else b.timestamps[sl].copy(),
+        q=b.q[sl], k=b.k[sl], v=b.v[sl], u=None if b.u is None else b.u[sl],
+        dy=None if b.dy is None else b.dy[sl], rab_pos=b.rab_pos, rab_time=b.rab_time,
+        alpha=b.alpha, max_seq_len=b.max_seq_len, norm=b.norm, eps=b.eps)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from oracle import oracle as O
+    full = [synth.heavy_tailed(s) for s in range(N_SEEDS)]
+    samples = [sub_batch(b, 16) for b in full]   # 16 of 64 sequences per step
+    for w in range(args.warmup):
+        b = samples[w % N_SEEDS]
+        O.backward(b, o=O.forward(b)["o"])
+    flops, t0 = 0, time.perf_counter()
+    for k in range(args.steps):
+        b = samples[k % N_SEEDS]
+        O.backward(b, o=O.forward(b)["o"])
+        fw, bw = useful_flops(b)
+        flops += fw + bw
+    dt = time.perf_counter() - t0
+    val = flops / dt / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / max(args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": config_dict({"sample": "first 16 of the 64 sequences of each batch"}),
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": O.num_threads(), "kind": "oracle",
+                             "sample": "per step: fwd+bwd of the first 16 sequences of one batch"},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from hstu_jagged_attention_02_gb300 import binding as C
+    from hstu_jagged_attention_02_gb300.attention import Problem
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    seeds = [rank * N_SEEDS + s for s in range(N_SEEDS)]
+    batches = [synth.heavy_tailed(s) for s in seeds]
+    probs = [Problem(b, device=dev, out_dtype="fp32") for b in batches]
+    flops = [useful_flops(b) for b in batches]
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        pr = probs[i % N_SEEDS]
+        if ev is not None:
+            C.hstu_time_next_attention_kernel(ev[0].cuda_event, ev[1].cuda_event)
+        pr.forward()
+        n = C.hstu_last_launch_count()
+        if ev is not None:
+            C.hstu_time_next_attention_kernel(ev[2].cuda_event, ev[3].cuda_event)
+        pr.backward()
+        return n + C.hstu_last_launch_count()
+
+    for w in range(max(args.warmup, 0)):
+        step(w)
+    torch.cuda.synchronize()
+    for pr in probs:
+        assert pr.device_error() == 0, "device error during warm-up"
+
+    # ---- timed region: K steps, kernel events on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clock = ClockSampler(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clock.start()
+    time.sleep(0.3)  # let the sampler start before the region
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    start.record(stream)
+    for k in range(args.steps):
+        launches += step(k, evs[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    clocks = clock.stop()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    step_flops = [flops[k % N_SEEDS] for k in range(args.steps)]
+    tot_flops = sum(f + b for f, b in step_flops)
+    for pr in probs:
+        assert pr.device_error() == 0, "device error in the timed region"
+
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        f = torch.tensor([float(tot_flops)], device=dev, dtype=torch.float64)
+        dist.all_reduce(f, op=dist.ReduceOp.SUM)
+        tot_flops = float(f.item())
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = run_e2e(args, probs, flops, stream, world)
+
+    if rank != 0:
+        return
+    pk, pk_kind = peaks()
+    value = tot_flops / (elapsed_ms * 1e-3) / 1e12
+    fwd_total, bwd_total = sum(fwd_ms), sum(bwd_ms)
+    dom = "bwd" if bwd_total >= fwd_total else "fwd"
+    dom_ms = bwd_ms if dom == "bwd" else fwd_ms
+    dom_flops = [f[1] if dom == "bwd" else f[0] for f in step_flops]
+    achieved = sum(dom_flops) / (sum(dom_ms) * 1e-3) / 1e12
+    peak_sust = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    peak_burst = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    tr = traffic_record(dom)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_sust, "unit": "TFLOP/s",
+                "frac": achieved / peak_sust, "traffic": tr["dram_bytes_per_launch"] if tr else None,
+                "kernel": f"attention {dom} kernel",
+                "peak_source": f"{pk_kind} bf16_tflops_sustained (kernel timed inside the step loop)",
+                "avg_launch_ms": sum(dom_ms) / len(dom_ms),
+                "share_of_step": sum(dom_ms) / elapsed_ms}
+    # CPU oracle baseline (rank 0, N = 1 only)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cf, cdt, cdesc, cores = time_oracle(batches, budget_s=args.cpu_budget)
+        cpu = {"value": cf / cdt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": cdesc, "seconds": cdt}
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_dict({"per_rank_batches": N_SEEDS,
+                                   "mean_tokens_per_batch": float(np.mean([b.T for b in batches]))}),
+            "pct_of_bf16_peak": 100.0 * value / peak_burst,
+            "peak_bf16_tflops": {"burst": peak_burst, "sustained": peak_sust, "source": pk_kind},
+            "fwd_kernel_ms_avg": fwd_total / args.steps, "bwd_kernel_ms_avg": bwd_total / args.steps,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks}
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, probs, flops, stream, world):
+    """Same metric through the public C ABI with pinned host buffers: each step
+    copies its inputs host -> device, runs forward + backward and copies the
+    results back.  Returns the e2e dict."""
+    import torch
+    hosts = []
+    for pr in probs:
+        ins = [t for t in (pr.offsets, pr.num_targets, pr.num_contexts, pr.timestamps, pr.rab_pos,
+                           pr.rab_time, pr.q, pr.k, pr.v, pr.u, pr.dy) if t is not None]
+        outs = [t for t in (pr.y, pr.dq, pr.dk, pr.dvv, pr.du, pr.d_rab_pos, pr.d_rab_time)
+                if t is not None]
+        h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in ins]
+        h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        hosts.append((ins, h_in, outs, h_out))
+    bi = sum(t.numel() * t.element_size() for t in hosts[0][1])
+    bo = sum(t.numel() * t.element_size() for t in hosts[0][3])
+
+    def one(i):
+        pr = probs[i % N_SEEDS]
+        ins, h_in, outs, h_out = hosts[i % N_SEEDS]
+        for d, h in zip(ins, h_in):
+            d.copy_(h, non_blocking=True)
+        pr.forward()
+        pr.backward()
+        for d, h in zip(outs, h_out):
+            h.copy_(d, non_blocking=True)
+
+    for w in range(max(args.warmup, 1)):
+        one(w)
+    torch.cuda.synchronize()
+    k = args.steps
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(k):
+        one(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    fl = sum(sum(flops[i % N_SEEDS]) for i in range(k))
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=t0.device if hasattr(t0, "device") else "cuda",
+                         dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        f = torch.tensor([float(fl)], device="cuda", dtype=torch.float64)
+        dist.all_reduce(f, op=dist.ReduceOp.SUM)
+        fl = float(f.item())
+    return {"value": fl / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo, "ms_per_step": ms / k}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_gpu(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,163 @@
+"""Torch-facing helpers around the C ABI: device buffers for one jagged batch,
+and an autograd function.  Marshalling only; the arithmetic is in the CUDA
+kernels of libhstu_attn.so."""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import binding as C
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream] = None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def torch_dtype(name: str):
+    return torch.bfloat16 if name == "bf16" else torch.float32
+
+
+class Problem:
+    """Device copies of one synth.Batch plus every output buffer and the
+    workspace, with the C argument structs filled once."""
+
+    def __init__(self, batch, device="cuda", flags: int = 0, want_y: bool = True,
+                 want_stats: bool = False, want_drab: bool = True, out_dtype: str = "fp32"):
+        self.batch = batch
+        dev = torch.device(device)
+        self.dev = dev
+        td = torch_dtype(batch.dtype)
+        self.td = td
+        out_dtype = "fp32" if batch.dtype == "fp32" else out_dtype
+        self.out_dtype = out_dtype
+        to = torch_dtype(out_dtype)
+        self.to = to
+        T, H, dqk, dv = batch.T, batch.H, batch.d_qk, batch.d_v
+        F = H * dv
+        self.T, self.H, self.F = T, H, F
+
+        def up(a, dt=None):
+            if a is None:
+                return None
+            t = torch.from_numpy(np.ascontiguousarray(a))
+            return t.to(device=dev, dtype=dt if dt is not None else t.dtype)
+
+        self.offsets = up(batch.offsets, torch.int64)
+        self.num_targets = up(batch.num_targets, torch.int32)
+        self.num_contexts = up(batch.num_contexts, torch.int32)
+        self.timestamps = up(batch.timestamps, torch.int64)
+        self.rab_pos = up(batch.rab_pos, torch.float32)
+        self.rab_time = up(batch.rab_time, torch.float32)
+        self.q, self.k, self.v = up(batch.q, td), up(batch.k, td), up(batch.v, td)
+        self.u = up(batch.u, td)
+        self.dy = up(batch.dy, to)
+        z = lambda *s, dt=to: torch.empty(*s, device=dev, dtype=dt)
+        self.o = z(T, H, dv)
+        self.y = z(T, F) if want_y else None
+        self.mean = z(T, dt=torch.float32) if want_stats else None
+        self.rstd = z(T, dt=torch.float32) if want_stats else None
+        self.backward_enabled = batch.dy is not None
+        if self.backward_enabled:
+            self.dq, self.dk, self.dvv = z(T, H, dqk), z(T, H, dqk), z(T, H, dv)
+            self.du = z(T, F) if self.u is not None else None
+            self.d_rab_pos = (z(H, self.rab_pos.shape[1], dt=torch.float32)
+                              if (self.rab_pos is not None and want_drab) else None)
+            self.d_rab_time = (z(H, self.rab_time.shape[1], dt=torch.float32)
+                               if (self.rab_time is not None and want_drab) else None)
+        self.desc = C.make_desc(
+            dtype=batch.dtype, out_dtype=out_dtype, B=batch.B, H=H, d_qk=dqk, d_v=dv, total_tokens=T,
+            max_seq_len=batch.max_seq_len, alpha=batch.alpha,
+            num_pos_buckets=batch.rab_pos.shape[1] if batch.rab_pos is not None else 128,
+            num_time_buckets=batch.rab_time.shape[1] if batch.rab_time is not None else 64,
+            norm=batch.norm, ln_eps=batch.eps, flags=flags)
+        fwd_b, bwd_b = C.hstu_attn_workspace_size(self.desc)
+        self.ws_bytes = max(fwd_b, bwd_b if self.backward_enabled else 0)
+        self.ws = torch.empty(self.ws_bytes, device=dev, dtype=torch.uint8)
+        self.fwd_args = C.hstu_attn_fwd_args(
+            _ptr(self.offsets), _ptr(self.num_targets), _ptr(self.num_contexts), _ptr(self.timestamps),
+            _ptr(self.rab_pos), _ptr(self.rab_time), _ptr(self.q), _ptr(self.k), _ptr(self.v),
+            _ptr(self.u), _ptr(self.o), _ptr(self.y), _ptr(self.mean), _ptr(self.rstd))
+        if self.backward_enabled:
+            self.bwd_args = C.hstu_attn_bwd_args(
+                _ptr(self.offsets), _ptr(self.num_targets), _ptr(self.num_contexts),
+                _ptr(self.timestamps), _ptr(self.rab_pos), _ptr(self.rab_time), _ptr(self.q),
+                _ptr(self.k), _ptr(self.v), _ptr(self.u), _ptr(self.o), _ptr(self.dy),
+                _ptr(self.dq), _ptr(self.dk), _ptr(self.dvv), _ptr(self.du), _ptr(self.d_rab_pos),
+                _ptr(self.d_rab_time))
+
+    def forward(self, stream=None):
+        C.hstu_attn_fwd(self.desc, self.fwd_args, self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
+
+    def backward(self, stream=None):
+        C.hstu_attn_bwd(self.desc, self.bwd_args, self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
+
+    def device_error(self, stream=None) -> int:
+        return C.hstu_get_device_error(self.ws.data_ptr(), _stream_handle(stream))
+
+    def debug_plan(self, pass_: int, capacity: int, stream=None):
+        need = self.ws_bytes + 20 * capacity + 512
+        ws = torch.empty(need, device=self.dev, dtype=torch.uint8)
+        return C.hstu_attn_debug_plan(self.desc, _ptr(self.offsets), _ptr(self.num_targets),
+                                      _ptr(self.num_contexts), pass_, ws.data_ptr(), need, capacity,
+                                      _stream_handle(stream))
+
+
+class HSTUAttnFunction(torch.autograd.Function):
+    """y = Norm(A V) * u with A = SiLU(alpha Q K^T + rab) / N under the
+    compound mask; gradients for q, k, v, u, rab_pos, rab_time."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, u, rab_pos, rab_time, seq_offsets, num_targets, num_contexts,
+                timestamps, max_seq_len: int, alpha: float, norm: str = "layernorm",
+                eps: float = 1e-5):
+        T, H, dqk = q.shape
+        dv = v.shape[2]
+        dtype = "bf16" if q.dtype == torch.bfloat16 else "fp32"
+        desc = C.make_desc(dtype=dtype, B=seq_offsets.numel() - 1, H=H, d_qk=dqk, d_v=dv,
+                           total_tokens=T, max_seq_len=max_seq_len, alpha=alpha,
+                           num_pos_buckets=rab_pos.shape[1] if rab_pos is not None else 128,
+                           num_time_buckets=rab_time.shape[1] if rab_time is not None else 64,
+                           norm=norm, ln_eps=eps)
+        fwd_b, bwd_b = C.hstu_attn_workspace_size(desc)
+        ws = torch.empty(max(fwd_b, bwd_b), device=q.device, dtype=torch.uint8)
+        o = torch.empty(T, H, dv, device=q.device, dtype=q.dtype)
+        y = torch.empty(T, H * dv, device=q.device, dtype=q.dtype)
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        u = u.contiguous() if u is not None else None
+        args = C.hstu_attn_fwd_args(_ptr(seq_offsets), _ptr(num_targets), _ptr(num_contexts),
+                                    _ptr(timestamps), _ptr(rab_pos), _ptr(rab_time), _ptr(q), _ptr(k),
+                                    _ptr(v), _ptr(u), _ptr(o), _ptr(y), None, None)
+        C.hstu_attn_fwd(desc, args, ws.data_ptr(), ws.numel(), _stream_handle())
+        ctx.save_for_backward(q, k, v, u, rab_pos, rab_time, seq_offsets, num_targets, num_contexts,
+                              timestamps, o)
+        ctx.desc, ctx.ws = desc, ws
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        q, k, v, u, rab_pos, rab_time, off, nt, nc, ts, o = ctx.saved_tensors
+        dy = dy.contiguous().to(q.dtype)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        du = torch.empty_like(u) if u is not None else None
+        drp = torch.empty_like(rab_pos, dtype=torch.float32) if rab_pos is not None else None
+        drt = torch.empty_like(rab_time, dtype=torch.float32) if rab_time is not None else None
+        args = C.hstu_attn_bwd_args(_ptr(off), _ptr(nt), _ptr(nc), _ptr(ts), _ptr(rab_pos), _ptr(rab_time),
+                                    _ptr(q), _ptr(k), _ptr(v), _ptr(u), _ptr(o), _ptr(dy), _ptr(dq),
+                                    _ptr(dk), _ptr(dv), _ptr(du), _ptr(drp), _ptr(drt))
+        C.hstu_attn_bwd(ctx.desc, args, ctx.ws.data_ptr(), ctx.ws.numel(), _stream_handle())
+        return (dq, dk, dv, du, drp, drt, None, None, None, None, None, None, None, None)
+
+
+def hstu_attention(q, k, v, u, seq_offsets, max_seq_len, alpha, *, num_targets=None, num_contexts=None,
+                   timestamps=None, rab_pos=None, rab_time=None, norm="layernorm", eps=1e-5):
+    """Differentiable HSTU jagged attention: returns y [T, H*d_v]."""
+    return HSTUAttnFunction.apply(q, k, v, u, rab_pos, rab_time, seq_offsets, num_targets, num_contexts,
+                                  timestamps, int(max_seq_len), float(alpha), norm, float(eps))

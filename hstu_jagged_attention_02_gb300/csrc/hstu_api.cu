@@ -1,0 +1,322 @@
+// C ABI entry points of libhstu_attn.so (declared in include/hstu_attn.h):
+// argument checks, workspace layout, path selection and the stream-ordered
+// launch sequence of each pass.  No device memory is allocated here.
+#include <cmath>
+#include <cstring>
+
+#include "hstu_internal.h"
+
+using namespace hstu;
+
+namespace {
+
+thread_local int32_t g_launches = 0;
+thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
+
+// Records the measurement-hook events around one launch, then clears them.
+struct KernelTimer {
+  cudaStream_t st;
+  cudaEvent_t a, b;
+  explicit KernelTimer(cudaStream_t s) : st(s), a(g_ev_start), b(g_ev_stop) {
+    g_ev_start = g_ev_stop = nullptr;
+    if (a) cudaEventRecord(a, st);
+  }
+  ~KernelTimer() { if (b) cudaEventRecord(b, st); }
+};
+
+constexpr uint32_t kKnownFlags = HSTU_FLAG_FORCE_SIMT | HSTU_FLAG_TEST_TIMEOUT;
+
+size_t align_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
+size_t esize(int dtype) { return dtype == HSTU_BF16 ? 2 : 4; }
+
+struct WsLayout {
+  size_t seq_start, tmp, blocks, plan_end, dO, dq_acc, total;
+  int cap_blocks;
+};
+
+WsLayout ws_layout(const hstu_attn_desc* d, bool bwd) {
+  WsLayout L{};
+  const int64_t cap = (d->total_tokens + kSimtTile - 1) / kSimtTile + d->B;  // blocks at the smallest edge
+  L.cap_blocks = (int)cap;
+  size_t off = kWsHeaderBytes;
+  L.seq_start = off; off = align_up(off + sizeof(int) * (size_t)(d->B + 1));
+  L.tmp = off;       off = align_up(off + sizeof(Block) * (size_t)cap);
+  L.blocks = off;    off = align_up(off + sizeof(Block) * (size_t)cap);
+  L.plan_end = off;
+  if (bwd) {
+    const size_t rows = (size_t)d->total_tokens * (size_t)d->H;
+    L.dO = off;     off = align_up(off + esize(d->dtype) * rows * (size_t)d->d_v);
+    L.dq_acc = off; off = align_up(off + sizeof(float) * rows * (size_t)d->d_qk);
+  }
+  L.total = off;
+  return L;
+}
+
+hstu_status_t check_desc(const hstu_attn_desc* d) {
+  if (!d || d->struct_size != sizeof(hstu_attn_desc)) return HSTU_ERR_INVALID_ARG;
+  if (d->dtype != HSTU_BF16 && d->dtype != HSTU_FP32) return HSTU_ERR_INVALID_ARG;
+  if (d->out_dtype != HSTU_BF16 && d->out_dtype != HSTU_FP32) return HSTU_ERR_INVALID_ARG;
+  if (d->dtype == HSTU_FP32 && d->out_dtype != HSTU_FP32) return HSTU_ERR_UNSUPPORTED;
+  if (d->B < 0 || d->H < 1 || d->total_tokens < 0 || d->d_qk < 1 || d->d_v < 1) return HSTU_ERR_INVALID_ARG;
+  if (d->max_seq_len < 1 || d->num_pos_buckets < 1 || d->num_time_buckets < 1) return HSTU_ERR_INVALID_ARG;
+  if (d->norm != HSTU_NORM_NONE && d->norm != HSTU_NORM_LAYERNORM) return HSTU_ERR_INVALID_ARG;
+  if (d->norm == HSTU_NORM_LAYERNORM && !(d->ln_eps > 0.f && std::isfinite(d->ln_eps))) return HSTU_ERR_INVALID_ARG;
+  if (!std::isfinite(d->alpha)) return HSTU_ERR_INVALID_ARG;
+  if (d->flags & ~kKnownFlags) return HSTU_ERR_INVALID_ARG;
+  if (d->d_qk != d->d_v || (d->d_qk != 32 && d->d_qk != 64 && d->d_qk != 128)) return HSTU_ERR_UNSUPPORTED;
+  if (d->H * d->d_v > 2048) return HSTU_ERR_UNSUPPORTED;
+  if (d->max_seq_len > kCostBins * kSimtTile) return HSTU_ERR_UNSUPPORTED;
+  if (d->num_pos_buckets > 4096 || d->num_time_buckets > 4096) return HSTU_ERR_UNSUPPORTED;
+  if ((d->total_tokens + kSimtTile - 1) / kSimtTile + d->B > (int64_t)0x3fffffff / d->H) return HSTU_ERR_UNSUPPORTED;
+  return HSTU_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+hstu_status_t check_ws(void* ws, size_t bytes, size_t need) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kWsAlign - 1)) != 0) return HSTU_ERR_WORKSPACE;
+  if (bytes < need) return HSTU_ERR_WORKSPACE;
+  return HSTU_OK;
+}
+
+// Device properties, cached per device.
+struct DevInfo { int cc = -1; int sms = 0; };
+DevInfo dev_info() {
+  static DevInfo cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DevInfo{};
+  if (cache[dev].cc < 0) {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev].sms = sms;
+    cache[dev].cc = major * 10 + minor;
+  }
+  return cache[dev];
+}
+
+bool use_tc(const hstu_attn_desc* d, bool bwd) {
+  if (d->flags & HSTU_FLAG_FORCE_SIMT) return false;
+  if (dev_info().cc != 103) return false;
+  return bwd ? tc_bwd_supported(d->dtype, d->d_qk, d->d_v) : tc_fwd_supported(d->dtype, d->d_qk, d->d_v);
+}
+
+PlanParams plan_params(const hstu_attn_desc* d, const int64_t* off, const int32_t* nt, const int32_t* nc,
+                       int pass, bool tc, char* ws, const WsLayout& L) {
+  PlanParams p{};
+  p.off = off; p.nt = nt; p.nc = nc;
+  p.B = d->B; p.T = d->total_tokens; p.max_n = d->max_seq_len;
+  p.BM = p.BN = tc ? kTcTile : kSimtTile;
+  p.pass = pass;
+  p.hdr = reinterpret_cast<int*>(ws);
+  p.seq_start = reinterpret_cast<int*>(ws + L.seq_start);
+  p.tmp = reinterpret_cast<Block*>(ws + L.tmp);
+  p.blocks = reinterpret_cast<Block*>(ws + L.blocks);
+  p.cap_blocks = L.cap_blocks;
+  return p;
+}
+
+#define HSTU_CUDA_TRY(expr)                                   \
+  do {                                                        \
+    cudaError_t e_ = (expr);                                  \
+    if (e_ != cudaSuccess) { (void)cudaGetLastError(); return HSTU_ERR_CUDA; } \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* hstu_status_string(hstu_status_t s) {
+  switch (s) {
+    case HSTU_OK: return "ok";
+    case HSTU_ERR_INVALID_ARG: return "invalid argument";
+    case HSTU_ERR_UNSUPPORTED: return "unsupported configuration";
+    case HSTU_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case HSTU_ERR_CUDA: return "CUDA runtime error";
+    case HSTU_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case HSTU_ERR_DEVICE_CHECK: return "device check failed: offsets or counts inconsistent";
+  }
+  return "unknown status";
+}
+
+int32_t hstu_last_launch_count(void) { return g_launches; }
+
+hstu_status_t hstu_time_next_attention_kernel(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr)) return HSTU_ERR_INVALID_ARG;
+  g_ev_start = static_cast<cudaEvent_t>(start_event);
+  g_ev_stop = static_cast<cudaEvent_t>(stop_event);
+  return HSTU_OK;
+}
+
+hstu_status_t hstu_attn_workspace_size(const hstu_attn_desc* desc, size_t* fwd_bytes, size_t* bwd_bytes) {
+  const hstu_status_t s = check_desc(desc);
+  if (s != HSTU_OK) return s;
+  if (fwd_bytes) *fwd_bytes = ws_layout(desc, false).total;
+  if (bwd_bytes) *bwd_bytes = ws_layout(desc, true).total;
+  return HSTU_OK;
+}
+
+hstu_status_t hstu_attn_fwd(const hstu_attn_desc* d, const hstu_attn_fwd_args* a, void* workspace,
+                            size_t workspace_bytes, hstu_stream_t stream) {
+  hstu_status_t s = check_desc(d);
+  if (s != HSTU_OK) return s;
+  if (!a || !a->seq_offsets || !a->q || !a->k || !a->v || !a->o) return HSTU_ERR_INVALID_ARG;
+  for (const void* ptr : {a->q, a->k, a->v, (const void*)a->o, a->u, (const void*)a->y})
+    if (ptr && !aligned16(ptr)) return HSTU_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(d, false);
+  if ((s = check_ws(workspace, workspace_bytes, L.total)) != HSTU_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  g_launches = 0;
+
+  const bool tc = use_tc(d, false);
+  const PlanParams pp = plan_params(d, a->seq_offsets, a->num_targets, a->num_contexts, 0, tc, ws, L);
+  HSTU_CUDA_TRY(launch_plan(pp, st));
+  ++g_launches;
+
+  AttnParams p{};
+  p.off = a->seq_offsets; p.nt = a->num_targets; p.nc = a->num_contexts;
+  p.ts = a->timestamps; p.rab_pos = a->rab_pos; p.rab_time = a->timestamps ? a->rab_time : nullptr;
+  p.q = a->q; p.k = a->k; p.v = a->v; p.o = a->o;
+  p.hdr = pp.hdr; p.hdr_rw = pp.hdr; p.blocks = pp.blocks;
+  p.B = d->B; p.H = d->H; p.dqk = d->d_qk; p.dv_dim = d->d_v; p.T = d->total_tokens;
+  p.dtype = d->dtype; p.out_dtype = d->out_dtype;
+  p.alpha = d->alpha; p.inv_n = 1.0f / (float)d->max_seq_len;
+  p.P = d->num_pos_buckets; p.Tb = d->num_time_buckets; p.flags = d->flags;
+  p.num_sms = dev_info().sms;
+  if (d->total_tokens > 0) {
+    {
+      KernelTimer timer(st);
+      if (tc) {
+        HSTU_CUDA_TRY(launch_tc_fwd(p, st));
+      } else {
+        const int max_items = ((int)((d->total_tokens + kSimtTile - 1) / kSimtTile) + d->B) * d->H;
+        HSTU_CUDA_TRY(launch_simt_fwd(p, max_items, st));
+      }
+    }
+    ++g_launches;
+    if (a->y || a->ln_mean || a->ln_rstd) {
+      NormParams np{};
+      np.dtype = d->dtype; np.out_dtype = d->out_dtype;
+      np.o = a->o; np.u = a->u; np.y = a->y; np.mean = a->ln_mean; np.rstd = a->ln_rstd;
+      np.T = d->total_tokens; np.F = d->H * d->d_v; np.norm = d->norm; np.eps = d->ln_eps;
+      HSTU_CUDA_TRY(launch_norm_gate_fwd(np, st));
+      ++g_launches;
+    }
+  }
+  return HSTU_OK;
+}
+
+hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a, void* workspace,
+                            size_t workspace_bytes, hstu_stream_t stream) {
+  hstu_status_t s = check_desc(d);
+  if (s != HSTU_OK) return s;
+  if (!a || !a->seq_offsets || !a->q || !a->k || !a->v || !a->o || !a->dy || !a->dq || !a->dk || !a->dv)
+    return HSTU_ERR_INVALID_ARG;
+  if ((a->u == nullptr) != (a->du == nullptr)) return HSTU_ERR_INVALID_ARG;
+  for (const void* ptr : {a->q, a->k, a->v, a->o, a->u, a->dy, (const void*)a->dq, (const void*)a->dk,
+                          (const void*)a->dv, (const void*)a->du})
+    if (ptr && !aligned16(ptr)) return HSTU_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(d, true);
+  if ((s = check_ws(workspace, workspace_bytes, L.total)) != HSTU_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  g_launches = 0;
+
+  const bool tc = use_tc(d, true);
+  const PlanParams pp = plan_params(d, a->seq_offsets, a->num_targets, a->num_contexts, 1, tc, ws, L);
+  HSTU_CUDA_TRY(launch_plan(pp, st));
+  ++g_launches;
+
+  const size_t rows = (size_t)d->total_tokens * (size_t)d->H;
+  float* dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
+  const bool has_rp = a->rab_pos != nullptr;
+  const bool has_rt = a->rab_time != nullptr && a->timestamps != nullptr;
+  if (a->d_rab_pos) HSTU_CUDA_TRY(cudaMemsetAsync(a->d_rab_pos, 0, sizeof(float) * d->H * d->num_pos_buckets, st));
+  if (a->d_rab_time) HSTU_CUDA_TRY(cudaMemsetAsync(a->d_rab_time, 0, sizeof(float) * d->H * d->num_time_buckets, st));
+  if (d->total_tokens == 0) return HSTU_OK;
+  HSTU_CUDA_TRY(cudaMemsetAsync(dq_acc, 0, sizeof(float) * rows * d->d_qk, st));
+
+  // gradient w.r.t. o, in the input type (an MMA operand of the attention backward)
+  {
+    NormParams np{};
+    np.dtype = d->dtype; np.out_dtype = d->out_dtype;
+    np.o = a->o; np.u = a->u; np.dy = a->dy; np.dO = ws + L.dO; np.du = a->du;
+    np.T = d->total_tokens; np.F = d->H * d->d_v; np.norm = d->norm; np.eps = d->ln_eps;
+    HSTU_CUDA_TRY(launch_norm_gate_bwd(np, st));
+    ++g_launches;
+  }
+  const void* dO = ws + L.dO;
+
+  AttnParams p{};
+  p.off = a->seq_offsets; p.nt = a->num_targets; p.nc = a->num_contexts;
+  p.ts = a->timestamps; p.rab_pos = a->rab_pos; p.rab_time = has_rt ? a->rab_time : nullptr;
+  p.q = a->q; p.k = a->k; p.v = a->v; p.dO = dO; p.dk = a->dk; p.dv = a->dv; p.dq_acc = dq_acc;
+  p.d_rab_pos = has_rp ? a->d_rab_pos : nullptr;
+  p.d_rab_time = has_rt ? a->d_rab_time : nullptr;
+  p.hdr = pp.hdr; p.hdr_rw = pp.hdr; p.blocks = pp.blocks;
+  p.B = d->B; p.H = d->H; p.dqk = d->d_qk; p.dv_dim = d->d_v; p.T = d->total_tokens;
+  p.dtype = d->dtype; p.out_dtype = d->out_dtype;
+  p.alpha = d->alpha; p.inv_n = 1.0f / (float)d->max_seq_len;
+  p.P = d->num_pos_buckets; p.Tb = d->num_time_buckets; p.flags = d->flags;
+  p.num_sms = dev_info().sms;
+  {
+    KernelTimer timer(st);
+    if (tc) {
+      HSTU_CUDA_TRY(launch_tc_bwd(p, st));
+    } else {
+      const int max_items = ((int)((d->total_tokens + kSimtTile - 1) / kSimtTile) + d->B) * d->H;
+      HSTU_CUDA_TRY(launch_simt_bwd(p, max_items, st));
+    }
+  }
+  ++g_launches;
+  HSTU_CUDA_TRY(launch_convert_f32(dq_acc, a->dq, (int64_t)(rows * d->d_qk), d->out_dtype, st));
+  ++g_launches;
+  return HSTU_OK;
+}
+
+hstu_status_t hstu_attn_debug_plan(const hstu_attn_desc* d, const int64_t* seq_offsets,
+                                   const int32_t* num_targets, const int32_t* num_contexts, int32_t pass,
+                                   void* workspace, size_t workspace_bytes, int32_t* host_tiles,
+                                   int64_t host_capacity, int64_t* n_tiles, hstu_stream_t stream) {
+  hstu_status_t s = check_desc(d);
+  if (s != HSTU_OK) return s;
+  if (!seq_offsets || !n_tiles || (pass != 0 && pass != 1) || host_capacity < 0 ||
+      (host_capacity > 0 && !host_tiles))
+    return HSTU_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(d, false);
+  const size_t need = L.plan_end + align_up(sizeof(int32_t) * 5 * (size_t)host_capacity);
+  if ((s = check_ws(workspace, workspace_bytes, need)) != HSTU_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const bool tc = use_tc(d, pass == 1);
+  const PlanParams pp = plan_params(d, seq_offsets, num_targets, num_contexts, pass, tc, ws, L);
+  int32_t* rec = reinterpret_cast<int32_t*>(ws + L.plan_end);
+  HSTU_CUDA_TRY(launch_plan(pp, st));
+  HSTU_CUDA_TRY(launch_debug_tiles(pp, rec, host_capacity, st));
+  int32_t hdr[4] = {0, 0, 0, 0};
+  HSTU_CUDA_TRY(cudaMemcpyAsync(hdr, ws, sizeof(hdr), cudaMemcpyDeviceToHost, st));
+  HSTU_CUDA_TRY(cudaStreamSynchronize(st));
+  if (hdr[WS_ERR] != 0) return (hstu_status_t)hdr[WS_ERR];
+  *n_tiles = hdr[WS_NTILES];
+  const int64_t copy = hdr[WS_NTILES] < host_capacity ? hdr[WS_NTILES] : host_capacity;
+  if (copy > 0) {
+    HSTU_CUDA_TRY(cudaMemcpyAsync(host_tiles, rec, sizeof(int32_t) * 5 * (size_t)copy,
+                                  cudaMemcpyDeviceToHost, st));
+    HSTU_CUDA_TRY(cudaStreamSynchronize(st));
+  }
+  return HSTU_OK;
+}
+
+hstu_status_t hstu_get_device_error(const void* workspace, hstu_stream_t stream, int32_t* code) {
+  if (!workspace || !code) return HSTU_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  HSTU_CUDA_TRY(cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, st));
+  HSTU_CUDA_TRY(cudaStreamSynchronize(st));
+  *code = v;
+  return HSTU_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,90 @@
+// Internal launch interfaces between the C ABI (hstu_api.cu) and the kernels.
+#pragma once
+
+#include "hstu_common.cuh"
+
+namespace hstu {
+
+struct PlanParams {
+  const int64_t* off;
+  const int32_t* nt;
+  const int32_t* nc;
+  int B;
+  int64_t T;
+  int max_n;
+  int BM, BN;       // tile edges of the path that will run
+  int pass;         // 0 forward (query blocks), 1 backward (key blocks)
+  int* hdr;         // workspace header
+  int* seq_start;   // [B+1] scratch
+  Block* tmp;       // [cap_blocks] scratch
+  Block* blocks;    // [cap_blocks] result, longest first
+  int cap_blocks;
+};
+
+// Everything a forward or backward attention kernel needs.
+struct AttnParams {
+  const int64_t* off;
+  const int32_t* nt;
+  const int32_t* nc;
+  const int64_t* ts;     // NULL: no time bias
+  const float* rab_pos;  // NULL: no position bias
+  const float* rab_time; // NULL (or ts NULL): no time bias
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;               // forward output [T,H,dv]
+  const void* dO;        // backward: gradient w.r.t. o [T,H,dv]
+  void* dk;              // backward outputs [T,H,d]
+  void* dv;
+  float* dq_acc;         // backward: FP32 accumulator [T,H,dqk], zeroed before
+  float* d_rab_pos;      // backward: [H,P] accumulated (zeroed before), or NULL
+  float* d_rab_time;
+  const int* hdr;        // workspace header (block count)
+  int* hdr_rw;           // same, writable (error word)
+  const Block* blocks;
+  int B, H, dqk, dv_dim;
+  int dtype, out_dtype;  // hstu_dtype_t of the inputs / of the outputs
+  int64_t T;
+  float alpha, inv_n;
+  int P, Tb;
+  uint32_t flags;
+  int num_sms;
+};
+
+struct NormParams {
+  int dtype, out_dtype;  // u and dO have dtype; o, y, dy, du have out_dtype
+  const void* o;
+  const void* u;   // NULL: gate of one
+  const void* dy;
+  void* y;
+  void* dO;        // backward: gradient w.r.t. o
+  void* du;
+  float* mean;
+  float* rstd;
+  int64_t T;
+  int F;           // H * d_v
+  int norm;
+  float eps;
+};
+
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
+cudaError_t launch_debug_tiles(const PlanParams& p, int32_t* rec, int64_t cap, cudaStream_t stream);
+
+// CUDA-core path (FP32 and BF16), 32 x 32 tiles
+constexpr int kSimtTile = 32;
+cudaError_t launch_simt_fwd(const AttnParams& p, int max_items, cudaStream_t stream);
+cudaError_t launch_simt_bwd(const AttnParams& p, int max_items, cudaStream_t stream);
+
+// norm + gate, forward and backward; dq FP32 -> dtype
+cudaError_t launch_norm_gate_fwd(const NormParams& p, cudaStream_t stream);
+cudaError_t launch_norm_gate_bwd(const NormParams& p, cudaStream_t stream);
+cudaError_t launch_convert_f32(const float* src, void* dst, int64_t count, int dtype, cudaStream_t stream);
+
+// Tensor-core path (BF16, d in {64, 128}), 128 x 128 tiles
+constexpr int kTcTile = 128;
+bool tc_fwd_supported(int dtype, int dqk, int dv);
+bool tc_bwd_supported(int dtype, int dqk, int dv);
+cudaError_t launch_tc_fwd(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_tc_bwd(const AttnParams& p, cudaStream_t stream);
+
+}  // namespace hstu

@@ -1,0 +1,191 @@
+/*
+ * hstu_attn.h -- C ABI of the GB300 (sm_103a) HSTU jagged attention library
+ * (libhstu_attn.so).
+ *
+ * The operation (HSTU "Spatial Aggregation" and "Pointwise Transformation",
+ * ai6s.net generative-recommendation survey, section 2.1.2, equations (2)
+ * and (3); the equations are images on the page, the prose describes a
+ * softmax-free "pointwise aggregated attention" with a position/time bias and
+ * a U gate):
+ *
+ *   for each sequence b and head h, tokens i, j of the sequence:
+ *     z_ij = alpha * <q_i, k_j> + rab_pos[h][bp(i,j)] + rab_time[h][bt(i,j)]
+ *     o_i  = sum over allowed j of SiLU(z_ij) / N * v_j        (no softmax)
+ *   y_t = Norm(concat_h o_t) * u_t
+ *
+ * Jagged layout (KeyedJaggedTensor convention, same survey, section 3.1.2):
+ * tokens of all sequences are packed back to back, row-major, no padding;
+ * seq_offsets[b] is the first token of sequence b, seq_offsets[B] == T.
+ *   q, k     [T, H, d_qk]     v, o  [T, H, d_v]     u, y, dy, du  [T, H*d_v]
+ * Every row is dense and contiguous; every tensor pointer must be 16-byte
+ * aligned.  q, k, v, u have the element type `dtype`; o, y, dy and the
+ * gradients have `out_dtype` (BF16 inputs with FP32 outputs keep the final
+ * rounding out of the result; BF16 outputs halve the output traffic).
+ *
+ * Mask (the ranking task's candidates, section 2.1.2, and the compound
+ * causal + context/target mask of the Ascend HSTU fused operator, wmrh.cn
+ * RecSDK page, "HSTU acceleration operator" paragraph).  A sequence of n
+ * tokens has c = num_contexts[b] context tokens in front and
+ * m = num_targets[b] candidates at the end; h_end = n - m:
+ *   j >= h_end : allowed iff i == j
+ *   j <  h_end : allowed iff j <= i  or  (i < c and j < c)
+ * Buckets: pos(i) = min(i, h_end);  bp = min(|pos(i) - pos(j)|, P - 1);
+ *          bt = 0 if t_i == t_j else min(Tb - 1, floor(log2|t_i - t_j|) + 1).
+ * Norm:    LAYERNORM normalises each token's H*d_v features (population
+ *          variance, eps = ln_eps, no affine); NONE leaves them as they are.
+ *
+ * Conventions
+ *  - Every pointer is a device pointer except the host_* outputs of
+ *    hstu_attn_debug_plan and hstu_get_device_error.  The caller owns every
+ *    buffer, including the workspace; the library never allocates device
+ *    memory and keeps no state between calls.
+ *  - Calls are stream-ordered and return without synchronising, except
+ *    hstu_attn_debug_plan and hstu_get_device_error, which synchronise the
+ *    given stream.  Concurrent calls must use distinct workspaces.
+ *  - Host-side checks return an error code before anything is launched.
+ *    Problems seen on the device (inconsistent offsets or counts, a pipeline
+ *    wait that ran out) are recorded in the workspace and read back with
+ *    hstu_get_device_error; outputs are undefined then.  The library never
+ *    traps or aborts.
+ */
+#ifndef HSTU_ATTN_H_
+#define HSTU_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HSTU_ATTN_ABI_VERSION 1
+
+typedef struct CUstream_st* hstu_stream_t; /* same type as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  HSTU_OK = 0,
+  HSTU_ERR_INVALID_ARG = 1,   /* a NULL required pointer, bad size or misalignment */
+  HSTU_ERR_UNSUPPORTED = 2,   /* a valid request this build does not implement */
+  HSTU_ERR_WORKSPACE = 3,     /* workspace NULL, misaligned or too small */
+  HSTU_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+  HSTU_ERR_TIMEOUT = 5,       /* device: a pipeline wait ran out of its limit */
+  HSTU_ERR_DEVICE_CHECK = 6   /* device: offsets/counts inconsistent with the descriptor */
+} hstu_status_t;
+
+typedef enum { HSTU_BF16 = 0, HSTU_FP32 = 1 } hstu_dtype_t;
+typedef enum { HSTU_NORM_NONE = 0, HSTU_NORM_LAYERNORM = 1 } hstu_norm_t;
+
+/* Flags */
+#define HSTU_FLAG_FORCE_SIMT (1u << 0)   /* use the CUDA-core kernels even where the tensor-core path applies */
+#define HSTU_FLAG_TEST_TIMEOUT (1u << 1) /* test only: the tensor-core forward withholds one load and its
+                                            waits give up after about a millisecond, so the timeout path
+                                            runs without a hang; the result is HSTU_ERR_TIMEOUT */
+
+typedef struct {
+  uint32_t struct_size;     /* sizeof(hstu_attn_desc) */
+  int32_t dtype;            /* hstu_dtype_t of the inputs q, k, v, u */
+  int32_t out_dtype;        /* hstu_dtype_t of o, y, dy, dq, dk, dv, du; FP32 when dtype is FP32 */
+  int32_t B;                /* number of sequences, >= 0 */
+  int32_t H;                /* heads, >= 1 */
+  int32_t d_qk, d_v;        /* head dims; this build: d_qk == d_v in {32, 64, 128} */
+  int64_t total_tokens;     /* T == seq_offsets[B] */
+  int32_t max_seq_len;      /* N of the 1/N scale; every sequence must have n <= N */
+  float alpha;              /* scale of <q, k> */
+  int32_t num_pos_buckets;  /* P >= 1 (128 in the reference workloads) */
+  int32_t num_time_buckets; /* Tb >= 1 (64) */
+  int32_t norm;             /* hstu_norm_t */
+  float ln_eps;             /* LayerNorm epsilon (1e-5) */
+  uint32_t flags;           /* HSTU_FLAG_* */
+} hstu_attn_desc;
+
+typedef struct {
+  const int64_t* seq_offsets;  /* [B+1], non-decreasing, seq_offsets[0] == 0 */
+  const int32_t* num_targets;  /* [B] candidates at the end of each sequence, or NULL (none) */
+  const int32_t* num_contexts; /* [B] context tokens at the front, or NULL (none) */
+  const int64_t* timestamps;   /* [T] integer seconds, or NULL (no time bias) */
+  const float* rab_pos;        /* [H, P] position-bucket bias, or NULL */
+  const float* rab_time;       /* [H, Tb] time-bucket bias, or NULL; ignored without timestamps */
+  const void* q;               /* [T, H, d_qk] */
+  const void* k;               /* [T, H, d_qk] */
+  const void* v;               /* [T, H, d_v] */
+  const void* u;               /* [T, H*d_v] gate, or NULL (gate of one) */
+  void* o;                     /* out [T, H, d_v]: A.V, kept for the backward */
+  void* y;                     /* out [T, H*d_v]: Norm(o) * u, or NULL (not produced) */
+  float* ln_mean;              /* out [T] or NULL: per-token mean of o (LAYERNORM) */
+  float* ln_rstd;              /* out [T] or NULL: per-token 1/sqrt(var + eps) (LAYERNORM) */
+} hstu_attn_fwd_args;
+
+typedef struct {
+  /* the forward's inputs, unchanged */
+  const int64_t* seq_offsets;
+  const int32_t* num_targets;
+  const int32_t* num_contexts;
+  const int64_t* timestamps;
+  const float* rab_pos;
+  const float* rab_time;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* u;
+  const void* o;               /* the forward's o */
+  const void* dy;              /* [T, H*d_v] gradient of the loss w.r.t. y */
+  /* outputs, overwritten (not accumulated) */
+  void* dq;                    /* [T, H, d_qk] */
+  void* dk;                    /* [T, H, d_qk] */
+  void* dv;                    /* [T, H, d_v] */
+  void* du;                    /* [T, H*d_v]; required iff u != NULL */
+  float* d_rab_pos;            /* [H, P] or NULL (not wanted) */
+  float* d_rab_time;           /* [H, Tb] or NULL */
+} hstu_attn_bwd_args;
+
+/* Workspace bytes the forward and the backward need for this descriptor
+ * (a bound valid for any seq_offsets consistent with it).  The workspace must
+ * be 256-byte aligned.  Either output pointer may be NULL. */
+hstu_status_t hstu_attn_workspace_size(const hstu_attn_desc* desc, size_t* fwd_bytes, size_t* bwd_bytes);
+
+/* Forward: o = A.V and, if y != NULL, y = Norm(o) * u (eqs. (2), (3)). */
+hstu_status_t hstu_attn_fwd(const hstu_attn_desc* desc, const hstu_attn_fwd_args* args,
+                            void* workspace, size_t workspace_bytes, hstu_stream_t stream);
+
+/* Backward: dq, dk, dv, du, d_rab_pos, d_rab_time from dy; A is recomputed
+ * tile by tile, never stored (HSTU's memory design, section 2.1.3 "memory
+ * optimisation": sub-layer activations are not kept). */
+hstu_status_t hstu_attn_bwd(const hstu_attn_desc* desc, const hstu_attn_bwd_args* args,
+                            void* workspace, size_t workspace_bytes, hstu_stream_t stream);
+
+/* The tile plan of one pass, as the kernels walk it (compound-mask tile
+ * skipping, wmrh.cn RecSDK page, "HSTU acceleration operator" paragraph).
+ * pass 0 = forward (query-block work items), 1 = backward (key-block items).
+ * Writes up to host_capacity records of 5 int32 (b, q_block, k_block, class,
+ * tile_rows) to host_tiles for every tile that is not skipped; class 1 =
+ * partial, 2 = full; tile_rows = the tile edge (the tensor-core or the
+ * CUDA-core tile, whichever path this descriptor selects).  *n_tiles receives
+ * the total count.  The workspace must hold the forward workspace plus
+ * 20 * host_capacity bytes (rounded up to 256).  Synchronises the stream. */
+hstu_status_t hstu_attn_debug_plan(const hstu_attn_desc* desc, const int64_t* seq_offsets,
+                                   const int32_t* num_targets, const int32_t* num_contexts, int32_t pass,
+                                   void* workspace, size_t workspace_bytes, int32_t* host_tiles,
+                                   int64_t host_capacity, int64_t* n_tiles, hstu_stream_t stream);
+
+/* Reads the device error word of the last call that used this workspace
+ * (HSTU_OK when none).  Synchronises the stream. */
+hstu_status_t hstu_get_device_error(const void* workspace, hstu_stream_t stream, int32_t* code);
+
+/* Static string for a status code. */
+const char* hstu_status_string(hstu_status_t status);
+
+/* Number of kernels the last successful hstu_attn_fwd / hstu_attn_bwd call on
+ * this thread launched (for launch accounting). */
+int32_t hstu_last_launch_count(void);
+
+/* Measurement hook.  start_event and stop_event are cudaEvent_t handles (or
+ * both NULL to clear).  The next hstu_attn_fwd or hstu_attn_bwd call on this
+ * thread records start_event on its stream right before launching its
+ * attention kernel and stop_event right after, then forgets them. */
+hstu_status_t hstu_time_next_attention_kernel(void* start_event, void* stop_event);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HSTU_ATTN_H_ */

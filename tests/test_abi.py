@@ -1,0 +1,110 @@
+"""The C ABI library builds, loads, exports every declared entry point and
+rejects bad arguments on the host (no GPU needed: these paths return before
+any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from hstu_jagged_attention_02_gb300 import binding as C
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(hstu_[a-z0-9_]+)\s*\(",
+                                    src, flags=re.M))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = C.load()
+    declared = _declared_functions()
+    assert "hstu_attn_fwd" in declared and "hstu_attn_bwd" in declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(C.EXPORTED) <= set(declared)
+
+
+def test_struct_sizes_match_the_header():
+    # the library checks struct_size; a desc whose struct_size is the ctypes size is accepted
+    d = C.make_desc(dtype="bf16", B=2, H=4, d_qk=128, d_v=128, total_tokens=100, max_seq_len=64,
+                    alpha=0.1)
+    f, b = C.hstu_attn_workspace_size(d)
+    assert 0 < f < b
+    d.struct_size += 4
+    with pytest.raises(C.HSTUError) as e:
+        C.hstu_attn_workspace_size(d)
+    assert e.value.status == C.HSTU_ERR_INVALID_ARG
+
+
+def _desc(**kw):
+    base = dict(dtype="bf16", B=3, H=2, d_qk=64, d_v=64, total_tokens=50, max_seq_len=30, alpha=0.125)
+    base.update(kw)
+    return C.make_desc(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=-1), C.HSTU_ERR_INVALID_ARG),
+    (dict(H=0), C.HSTU_ERR_INVALID_ARG),
+    (dict(total_tokens=-5), C.HSTU_ERR_INVALID_ARG),
+    (dict(max_seq_len=0), C.HSTU_ERR_INVALID_ARG),
+    (dict(d_qk=96, d_v=96), C.HSTU_ERR_UNSUPPORTED),
+    (dict(d_qk=64, d_v=128), C.HSTU_ERR_UNSUPPORTED),
+    (dict(dtype="fp32", out_dtype="bf16"), C.HSTU_ERR_UNSUPPORTED),
+    (dict(alpha=float("nan")), C.HSTU_ERR_INVALID_ARG),
+    (dict(ln_eps=0.0), C.HSTU_ERR_INVALID_ARG),
+    (dict(flags=1 << 20), C.HSTU_ERR_INVALID_ARG),
+    (dict(num_pos_buckets=0), C.HSTU_ERR_INVALID_ARG),
+    (dict(max_seq_len=10**7), C.HSTU_ERR_UNSUPPORTED),
+])
+def test_descriptor_validation(kw, status):
+    with pytest.raises(C.HSTUError) as e:
+        C.hstu_attn_workspace_size(_desc(**kw))
+    assert e.value.status == status
+
+
+def test_workspace_grows_with_tokens():
+    f1, b1 = C.hstu_attn_workspace_size(_desc(total_tokens=1000))
+    f2, b2 = C.hstu_attn_workspace_size(_desc(total_tokens=2000))
+    assert f2 > f1 and b2 > b1
+    # backward holds the FP32 dq accumulator and the dO buffer
+    assert b2 - f2 >= 2000 * 2 * 64 * (4 + 2)
+
+
+def test_forward_rejects_bad_arguments_before_any_launch():
+    lib = C.load()
+    d = _desc()
+    args = C.hstu_attn_fwd_args()
+    # missing q/k/v/o
+    assert lib.hstu_attn_fwd(ctypes.byref(d), ctypes.byref(args), None, 0, None) == C.HSTU_ERR_INVALID_ARG
+    for name in ("seq_offsets", "q", "k", "v", "o"):
+        setattr(args, name, 4096)
+    # workspace NULL / misaligned / too small
+    assert lib.hstu_attn_fwd(ctypes.byref(d), ctypes.byref(args), None, 0, None) == C.HSTU_ERR_WORKSPACE
+    assert lib.hstu_attn_fwd(ctypes.byref(d), ctypes.byref(args), 4096 + 16, 1 << 20, None) == C.HSTU_ERR_WORKSPACE
+    assert lib.hstu_attn_fwd(ctypes.byref(d), ctypes.byref(args), 4096, 16, None) == C.HSTU_ERR_WORKSPACE
+    # misaligned tensor
+    args.q = 4096 + 2
+    assert lib.hstu_attn_fwd(ctypes.byref(d), ctypes.byref(args), 4096, 1 << 30, None) == C.HSTU_ERR_INVALID_ARG
+
+
+def test_backward_requires_du_with_u():
+    lib = C.load()
+    d = _desc()
+    args = C.hstu_attn_bwd_args()
+    for name in ("seq_offsets", "q", "k", "v", "o", "dy", "dq", "dk", "dv", "u"):
+        setattr(args, name, 4096)
+    assert lib.hstu_attn_bwd(ctypes.byref(d), ctypes.byref(args), 4096, 1 << 30, None) == C.HSTU_ERR_INVALID_ARG
+
+
+def test_status_strings():
+    for s in range(7):
+        assert C.hstu_status_string(s) and C.hstu_status_string(s) != "unknown status"
+    assert C.hstu_status_string(99) == "unknown status"

@@ -1,0 +1,230 @@
+"""GPU parity: the CUDA path (through the C ABI) against the FP64 oracle, on the
+same seeded inputs.
+
+Bar (per output tensor, RMS taken over the oracle tensor):
+    max |gpu - oracle| <= 1e-2 * RMS   for BF16 inputs
+    max |gpu - oracle| <= 1e-4 * RMS   for FP32 inputs
+Tile plans and device checks are compared exactly.
+"""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from hstu_jagged_attention_02_gb300 import binding as C  # noqa: E402
+from hstu_jagged_attention_02_gb300 import synth  # noqa: E402
+from oracle import oracle as O  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 1e-2, "fp32": 1e-4}
+
+
+def _problem(batch, **kw):
+    from hstu_jagged_attention_02_gb300.attention import Problem
+    return Problem(batch, **kw)
+
+
+def run_gpu(batch, flags=0, out_dtype="fp32"):
+    pr = _problem(batch, flags=flags, out_dtype=out_dtype, want_stats=True)
+    pr.forward()
+    if pr.backward_enabled:
+        pr.backward()
+    torch.cuda.synchronize()
+    assert pr.device_error() == 0
+    out = {"o": pr.o, "y": pr.y}
+    if pr.backward_enabled:
+        out.update(dq=pr.dq, dk=pr.dk, dv=pr.dvv, du=pr.du, d_rab_pos=pr.d_rab_pos,
+                   d_rab_time=pr.d_rab_time)
+    return pr, {k: (None if v is None else v.double().cpu().numpy()) for k, v in out.items()}
+
+
+def run_oracle(batch):
+    f = O.forward(batch)
+    want = {"o": f["o"], "y": f["y"]}
+    if batch.dy is not None:
+        g = O.backward(batch, o=f["o"])
+        want.update(dq=g["dq"], dk=g["dk"], dv=g["dv"], du=g["du"], d_rab_pos=g["d_rab_pos"],
+                    d_rab_time=g["d_rab_time"])
+    return want
+
+
+def check(got, want, tol, names=None):
+    for name in (names or want.keys()):
+        w = want.get(name)
+        if w is None:
+            assert got.get(name) is None, name
+            continue
+        g = got[name]
+        assert g is not None, name
+        w = np.asarray(w, np.float64)
+        g = np.asarray(g, np.float64).reshape(w.shape)
+        if w.size == 0:
+            continue
+        rms = math.sqrt(float(np.mean(w * w)))
+        err = float(np.max(np.abs(g - w)))
+        assert np.all(np.isfinite(g)), name
+        assert err <= tol * rms, f"{name}: max abs err {err:.3e} > {tol:g} x rms {rms:.3e}"
+
+
+# ------------------------------------------------------------ named configs
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "retrieval", "ranking", "heavy_tailed"])
+def test_named_config_parity(name):
+    b = synth.by_name(name, 0)
+    _, got = run_gpu(b)
+    check(got, run_oracle(b), TOL[b.dtype])
+
+
+@pytest.mark.parametrize("name", ["retrieval", "heavy_tailed"])
+def test_named_config_parity_cuda_core_path(name):
+    b = synth.by_name(name, 1)
+    _, got = run_gpu(b, flags=C.HSTU_FLAG_FORCE_SIMT)
+    check(got, run_oracle(b), TOL[b.dtype])
+
+
+# ------------------------------------------------- ragged, all mask modes
+
+RAGGED = [1, 5, 31, 32, 33, 127, 128, 129, 200, 257, 300]
+
+
+def _ragged_batch(dtype, d, seed, contexts=True, targets=True, time=True, rab=True, lengths=None):
+    r = np.random.default_rng(seed)
+    hist = np.array(lengths if lengths is not None else RAGGED)
+    nc = r.integers(0, 9, size=len(hist)) if contexts else 0
+    nt = r.integers(0, 40, size=len(hist)) if targets else 0
+    return synth.make_batch(hist, H=2, d_qk=d, d_v=d, dtype=dtype, num_contexts=nc, num_targets=nt,
+                            with_time=time, with_rab=rab, seed=seed)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("mode", ["causal", "targets", "contexts", "both"])
+def test_ragged_mask_modes(dtype, d, mode):
+    b = _ragged_batch(dtype, d, seed=100 + d, contexts=mode in ("contexts", "both"),
+                      targets=mode in ("targets", "both"))
+    _, got = run_gpu(b)
+    check(got, run_oracle(b), TOL[dtype])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_ragged_cuda_core_path_bf16(d):
+    b = _ragged_batch("bf16", d, seed=7 + d)
+    _, got = run_gpu(b, flags=C.HSTU_FLAG_FORCE_SIMT)
+    check(got, run_oracle(b), TOL["bf16"])
+
+
+@pytest.mark.parametrize("time,rab", [(False, True), (False, False)])
+def test_without_bias_tables(time, rab):
+    b = _ragged_batch("bf16", 128, seed=55, time=time, rab=rab)
+    _, got = run_gpu(b)
+    check(got, run_oracle(b), TOL["bf16"])
+
+
+def test_norm_none_and_no_gate():
+    b = _ragged_batch("bf16", 64, seed=56)
+    b.norm = "none"
+    _, got = run_gpu(b)
+    check(got, run_oracle(b), TOL["bf16"])
+    b2 = _ragged_batch("fp32", 32, seed=57)
+    b2.u = None
+    _, got2 = run_gpu(b2)
+    check(got2, run_oracle(b2), TOL["fp32"])
+
+
+def test_bf16_outputs_round_the_fp32_outputs():
+    b = _ragged_batch("bf16", 128, seed=58)
+    _, g32 = run_gpu(b, out_dtype="fp32")
+    _, g16 = run_gpu(b, out_dtype="bf16")
+    for name in ("o", "y", "dk", "dv", "dq", "du"):
+        a, r = g16[name], g32[name]
+        # one bf16 rounding of the output plus the bf16 operands it feeds
+        assert np.max(np.abs(a - r)) <= 2 ** -7 * np.max(np.abs(r)) + 1e-6, name
+
+
+# ------------------------------------------------------------- edge cases
+
+def test_edge_shapes():
+    # empty sequences inside the batch, n = 1, only candidates, only context
+    hist = np.array([0, 1, 0, 3, 0, 64, 0])
+    nc = np.array([0, 0, 0, 0, 0, 0, 0])
+    b = synth.make_batch(hist, H=2, d_qk=64, d_v=64, dtype="bf16", num_contexts=nc,
+                         num_targets=np.array([0, 0, 0, 4, 5, 0, 0]), seed=60)
+    _, got = run_gpu(b)
+    check(got, run_oracle(b), TOL["bf16"])
+    b2 = synth.make_batch(np.array([0, 0, 0]), H=1, d_qk=32, d_v=32, dtype="fp32",
+                          num_contexts=np.array([7, 0, 130]), num_targets=np.array([0, 9, 0]), seed=61)
+    _, got2 = run_gpu(b2)
+    check(got2, run_oracle(b2), TOL["fp32"])
+
+
+def test_no_tokens():
+    b = synth.make_batch(np.array([0, 0]), H=2, d_qk=64, d_v=64, dtype="bf16", seed=62)
+    pr, got = run_gpu(b)
+    assert got["o"].size == 0
+    assert np.all(got["d_rab_pos"] == 0)
+
+
+def test_forward_is_deterministic():
+    b = synth.by_name("heavy_tailed", 3)
+    pr = _problem(b)
+    pr.forward()
+    o1 = pr.o.clone()
+    y1 = pr.y.clone()
+    pr.forward()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, pr.o) and torch.equal(y1, pr.y)
+
+
+# --------------------------------------------------------- plan and checks
+
+@pytest.mark.parametrize("pass_", [0, 1])
+@pytest.mark.parametrize("flags", [0, C.HSTU_FLAG_FORCE_SIMT])
+def test_debug_plan_matches_bruteforce_tile_classes(pass_, flags):
+    b = _ragged_batch("bf16", 128, seed=70, lengths=[1, 40, 127, 128, 129, 260, 513, 700])
+    pr = _problem(b, flags=flags)
+    tiles = pr.debug_plan(pass_, capacity=200000)
+    edge = int(tiles[0, 4])
+    assert np.all(tiles[:, 4] == edge)
+    ref = O.tile_classes(b.offsets, b.num_targets, b.num_contexts, edge, edge)
+    keep = ref["cls"] != 0
+    want = sorted(zip(ref["b"][keep].tolist(), ref["qb"][keep].tolist(), ref["kb"][keep].tolist(),
+                      ref["cls"][keep].tolist()))
+    got = sorted(map(tuple, tiles[:, :4].tolist()))
+    assert got == want
+
+
+def test_named_config_plan_heavy_tailed():
+    b = synth.by_name("heavy_tailed", 0)
+    pr = _problem(b)
+    for pass_ in (0, 1):
+        tiles = pr.debug_plan(pass_, capacity=400000)
+        edge = int(tiles[0, 4])
+        ref = O.tile_classes(b.offsets, b.num_targets, b.num_contexts, edge, edge)
+        keep = ref["cls"] != 0
+        want = sorted(zip(ref["b"][keep].tolist(), ref["qb"][keep].tolist(), ref["kb"][keep].tolist(),
+                          ref["cls"][keep].tolist()))
+        assert sorted(map(tuple, tiles[:, :4].tolist())) == want
+
+
+@pytest.mark.parametrize("bad", ["decreasing", "targets_overflow", "too_long", "last_offset"])
+def test_device_checks_reject_inconsistent_metadata(bad):
+    b = _ragged_batch("bf16", 64, seed=80)
+    pr = _problem(b)
+    if bad == "decreasing":
+        pr.offsets[3] = pr.offsets[2] - 1
+    elif bad == "targets_overflow":
+        pr.num_targets[4] = 10_000
+    elif bad == "too_long":
+        pr.desc.max_seq_len = 16
+    else:
+        pr.offsets[-1] += 1
+    pr.forward()
+    torch.cuda.synchronize()
+    assert pr.device_error() == C.HSTU_ERR_DEVICE_CHECK
+    # the context stays usable: a good call afterwards succeeds
+    b2 = _ragged_batch("bf16", 64, seed=81)
+    _, got = run_gpu(b2)
+    check(got, run_oracle(b2), TOL["bf16"], names=["o", "y"])
