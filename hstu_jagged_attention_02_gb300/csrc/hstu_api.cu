@@ -45,7 +45,7 @@ WsLayout ws_layout(const hstu_attn_desc* d, bool bwd) {
   L.plan_end = off;
   if (bwd) {
     const size_t rows = (size_t)d->total_tokens * (size_t)d->H;
-    L.dO = off;     off = align_up(off + esize(d->dtype) * rows * (size_t)d->d_v);
+    L.dO = off;     off = align_up(off + sizeof(float) * rows * (size_t)d->d_v);  // FP32 or a BF16 pair
     L.dq_acc = off; off = align_up(off + sizeof(float) * rows * (size_t)d->d_qk);
   }
   L.total = off;
@@ -98,8 +98,11 @@ DevInfo dev_info() {
 
 bool use_tc(const hstu_attn_desc* d, bool bwd) {
   if (d->flags & HSTU_FLAG_FORCE_SIMT) return false;
+  if (d->total_tokens < kTcTile) return false;  // TMA boxes of 128 rows
   if (dev_info().cc != 103) return false;
-  return bwd ? tc_bwd_supported(d->dtype, d->d_qk, d->d_v) : tc_fwd_supported(d->dtype, d->d_qk, d->d_v);
+  if (bwd) return tc_bwd_supported(d->dtype, d->d_qk, d->d_v);
+  return tc_fwd_supported(d->dtype, d->d_qk, d->d_v) &&
+         tc_fwd_smem_bytes(d->d_qk, d->H, d->num_pos_buckets, d->num_time_buckets) <= kMaxSmemPerCta;
 }
 
 PlanParams plan_params(const hstu_attn_desc* d, const int64_t* off, const int32_t* nt, const int32_t* nc,
@@ -243,11 +246,13 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
     NormParams np{};
     np.dtype = d->dtype; np.out_dtype = d->out_dtype;
     np.o = a->o; np.u = a->u; np.dy = a->dy; np.dO = ws + L.dO; np.du = a->du;
+    np.split = tc ? 1 : 0;
+    np.dO_lo = ws + L.dO + sizeof(__nv_bfloat16) * rows * (size_t)d->d_v;
     np.T = d->total_tokens; np.F = d->H * d->d_v; np.norm = d->norm; np.eps = d->ln_eps;
     HSTU_CUDA_TRY(launch_norm_gate_bwd(np, st));
     ++g_launches;
   }
-  const void* dO = ws + L.dO;
+  const void* dO = ws + L.dO;  // FP32, or the hi part followed by the lo part
 
   AttnParams p{};
   p.off = a->seq_offsets; p.nt = a->num_targets; p.nc = a->num_contexts;

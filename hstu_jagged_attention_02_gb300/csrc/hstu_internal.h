@@ -57,7 +57,9 @@ struct NormParams {
   const void* u;   // NULL: gate of one
   const void* dy;
   void* y;
-  void* dO;        // backward: gradient w.r.t. o
+  void* dO;        // backward: gradient w.r.t. o, FP32 [T, F] (split == 0) or the BF16 high part
+  void* dO_lo;     // backward, split == 1: BF16 low part, dO ~= hi + lo
+  int split;
   void* du;
   float* mean;
   float* rstd;
@@ -83,6 +85,8 @@ cudaError_t launch_convert_f32(const float* src, void* dst, int64_t count, int d
 // Tensor-core path (BF16, d in {64, 128}), 128 x 128 tiles
 constexpr int kTcTile = 128;
 bool tc_fwd_supported(int dtype, int dqk, int dv);
+size_t tc_fwd_smem_bytes(int d, int H, int P, int Tb);
+constexpr size_t kMaxSmemPerCta = 227 * 1024;
 bool tc_bwd_supported(int dtype, int dqk, int dv);
 cudaError_t launch_tc_fwd(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_tc_bwd(const AttnParams& p, cudaStream_t stream);

@@ -3,8 +3,9 @@
 // backward.  Norm is LayerNorm with population variance and no affine, or
 // the identity.  One warp per token; HBM-bound (reads o and u, writes y).
 //
-// Element types: u and the backward's dO (an input of the attention
-// backward) have the input type TI; o, y, dy and du have the output type TO.
+// Element types: u has the input type TI; o, y, dy and du have the output
+// type TO.  The backward's dO (an input of the attention backward) is FP32, or
+// a BF16 hi/lo pair for the tensor-core path.
 #include "hstu_internal.h"
 
 namespace hstu {
@@ -106,15 +107,30 @@ __global__ void __launch_bounds__(kWarps * 32) norm_gate_bwd_kernel(NormParams p
     }
     g[r] = gg;
   }
-  TI* dO = static_cast<TI*>(p.dO) + t * F;
   if (ln) {
     mg = warp_sum(mg) / F;
     mgx = warp_sum(mgx) / F;
   }
+  if (p.split) {  // BF16 pair: hi = bf16(x), lo = bf16(x - hi)
+    __nv_bfloat16* hi = static_cast<__nv_bfloat16*>(p.dO) + t * F;
+    __nv_bfloat16* lo = static_cast<__nv_bfloat16*>(p.dO_lo) + t * F;
 #pragma unroll
-  for (int r = 0; r < PER; ++r) {
-    const int f = r * 32 + lane;
-    if (f < F) dO[f] = from_f<TI>(ln ? rstd * (g[r] - mg - x[r] * mgx) : g[r]);
+    for (int r = 0; r < PER; ++r) {
+      const int f = r * 32 + lane;
+      if (f < F) {
+        const float val = ln ? rstd * (g[r] - mg - x[r] * mgx) : g[r];
+        const __nv_bfloat16 h = __float2bfloat16_rn(val);
+        hi[f] = h;
+        lo[f] = __float2bfloat16_rn(val - __bfloat162float(h));
+      }
+    }
+  } else {
+    float* dO = static_cast<float*>(p.dO) + t * F;
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+      const int f = r * 32 + lane;
+      if (f < F) dO[f] = ln ? rstd * (g[r] - mg - x[r] * mgx) : g[r];
+    }
   }
 }
 

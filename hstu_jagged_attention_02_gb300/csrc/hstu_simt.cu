@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(NT) simt_bwd_kernel(AttnParams p) {
   const TI* q = static_cast<const TI*>(p.q);
   const TI* k = static_cast<const TI*>(p.k);
   const TI* v = static_cast<const TI*>(p.v);
-  const TI* dO = static_cast<const TI*>(p.dO);
+  const float* dO = static_cast<const float*>(p.dO);  // FP32: no rounding of the incoming gradient
   const size_t ld = (size_t)p.H * D;
   const bool want_rp = p.d_rab_pos && p.rab_pos;
   const bool want_rt = p.d_rab_time && p.rab_time && p.ts;
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(NT) simt_bwd_kernel(AttnParams p) {
       const bool in = row < s.n;
       const size_t g = (size_t)(s.s0 + row) * ld + (size_t)h * D + e;
       const float qv = in ? to_f(q[g]) : 0.f;
-      const float dv = in ? to_f(dO[g]) : 0.f;
+      const float dv = in ? dO[g] : 0.f;
       Qt[e * TS + i] = qv;
       Qr[i * D + e] = qv;
       dOt[e * TS + i] = dv;

@@ -1,0 +1,460 @@
+// Tensor-core forward of HSTU jagged attention for sm_103a (BF16 inputs,
+// d in {64, 128}): tcgen05 MMA with FP32 accumulators in TMEM, operands
+// staged by TMA, a fused score epilogue, persistent CTAs.
+//
+// Per work item (sequence b, head h, 128-row query block), for every key
+// block the compound mask keeps:
+//   S   = Q K^T                      tcgen05.mma, SMEM x SMEM -> TMEM (FP32)
+//   P   = mask ? SiLU(alpha S + rab_pos[bp] + rab_time[bt]) / N : 0
+//                                    epilogue warps, TMEM -> regs -> TMEM
+//   O  += P V                        tcgen05.mma, TMEM x SMEM -> TMEM
+// (HSTU spatial aggregation, ai6s.net survey section 2.1.2 eq. (2); tiling,
+// Cube/Vector overlap and mask skipping follow the ideas of the Ascend HSTU
+// fused operator on the wmrh.cn RecSDK page, re-planned for TMEM/TMA.)
+//
+// P is written back as two BF16 halves, P = P_hi + P_lo, and O accumulates
+// P_hi V + P_lo V: one BF16 rounding of P alone costs ~1.5% of the output
+// RMS on heavy-tailed batches, the pair keeps ~16 bits.
+//
+// Roles (320 threads): warps 0-7 epilogue (warp w reads TMEM lanes
+// 32*(w%4).., columns half w/4 of each tile), warp 8 TMA producer (plus key
+// timestamps), warp 9 MMA issuer and TMEM owner.
+// TMEM columns: S/P buffers at 0 and 128, O buffers at 256 and 256 + d.
+#include "hstu_internal.h"
+#include "tc_ptx.cuh"
+
+namespace hstu {
+
+namespace {
+
+using namespace tc;
+
+constexpr int BM = kTcTile, BN = kTcTile;
+constexpr int kEpiWarps = 8;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = 10 * 32;
+constexpr int kStages = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSColStride = 128;  // S/P buffer sb starts at column sb * 128
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum : int { BAR_QFULL = 0, BAR_QEMPTY, BAR_KVFULL, BAR_KVEMPTY = BAR_KVFULL + kStages,
+             BAR_SFULL = BAR_KVEMPTY + kStages, BAR_PREADY = BAR_SFULL + 2, BAR_OFULL = BAR_PREADY + 2,
+             BAR_OEMPTY = BAR_OFULL + 2, BAR_DRAIN = BAR_OEMPTY + 2, BAR_COUNT };
+
+template <int D>
+struct Layout {
+  static constexpr int NCH = D / 64;            // 128-byte column chunks per row
+  static constexpr int BOX = 128 * 128;         // one TMA box: 128 rows x 64 bf16 = 16 KB
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_BYTES = NCH * BOX;
+  static constexpr int STAGE = 2 * K_BYTES;     // K then V
+  static constexpr int KV_OFF = Q_OFF + NCH * BOX;
+  static constexpr int TS_OFF = KV_OFF + kStages * STAGE;       // int64 [kStages][BN]
+  static constexpr int BAR_OFF = TS_OFF + kStages * BN * 8;
+  static constexpr int MISC_OFF = BAR_OFF + BAR_COUNT * 8;      // tmem slot, abort flag
+  static constexpr int TAB_OFF = MISC_OFF + 16;                 // float [H][P + Tb]
+  static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
+};
+
+__device__ __forceinline__ float fast_sigmoid(float z) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-z * kLog2e));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return r;
+}
+
+struct ItemInfo {
+  int b, h, q0;
+  SeqInfo s;
+};
+
+__device__ __forceinline__ bool item_of(const AttnParams& p, int r, int nitems, ItemInfo& it) {
+  const int G = gridDim.x;
+  const int idx = r * G + ((r & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);  // snake order
+  if (idx >= nitems) return false;
+  const Block blk = p.blocks[idx / p.H];
+  it.b = blk.b;
+  it.h = idx % p.H;
+  it.q0 = blk.blk * BM;
+  it.s = seq_info(p.off, p.nt, p.nc, blk.b);
+  return true;
+}
+
+// waits for a phase, ignoring the abort flag (used to drain async copies)
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > 200000000ull) break;
+  }
+}
+
+template <int D, typename TO>
+__global__ void __launch_bounds__(kThreads, 1)
+hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmq,
+                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  const uint32_t sQ = base_u32 + L::Q_OFF;
+  const uint32_t sKV = base_u32 + L::KV_OFF;
+  int64_t* ts_s = reinterpret_cast<int64_t*>(base + L::TS_OFF);
+  const uint32_t bar0 = base_u32 + L::BAR_OFF;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L::MISC_OFF + 4);
+  float* tab = reinterpret_cast<float*>(base + L::TAB_OFF);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = p.H, P = p.P, Tb = p.Tb, PT = p.P + p.Tb;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(BAR_QFULL), 1);
+    mbar_init(bar(BAR_QEMPTY), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(BAR_KVFULL + s), 1);
+      mbar_init(bar(BAR_KVEMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(BAR_SFULL + s), 1);
+      mbar_init(bar(BAR_PREADY + s), kEpiWarps);
+      mbar_init(bar(BAR_OFULL + s), 1);
+      mbar_init(bar(BAR_OEMPTY + s), kEpiWarps);
+    }
+    mbar_init(bar(BAR_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // bias tables of every head: [h][0, P) position, [h][P, P+Tb) time
+  for (int x = threadIdx.x; x < H * PT; x += kThreads) {
+    const int h = x / PT, e = x % PT;
+    float v = 0.f;
+    if (e < P) {
+      if (p.rab_pos) v = p.rab_pos[h * P + e];
+    } else if (p.rab_time && p.ts) {
+      v = p.rab_time[h * Tb + (e - P)];
+    }
+    tab[x] = v;
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmq);
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  Watchdog wd;
+  wd.abort = abort_flag;
+  wd.err = p.hdr_rw + WS_ERR;
+  wd.err_info = p.hdr_rw + WS_ERR_INFO;
+  wd.limit_ns = (p.flags & HSTU_FLAG_TEST_TIMEOUT) ? 1000000ull : 2000000000ull;
+  const int nitems = p.hdr[WS_NBLK] * H;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    uint32_t kv_it = 0, q_it = 0;
+    uint32_t armed[kStages] = {0, 0};   // phases armed per stage
+    bool ok = true;
+    ItemInfo it;
+    for (int r = 0; ok && item_of(p, r, nitems, it); ++r) {
+      const int n = it.s.n;
+      if (lane == 0) {
+        ok = mbar_wait(bar(BAR_QEMPTY), (q_it & 1) ^ 1, wd, 1);
+        if (ok) {
+          mbar_arrive_expect_tx(bar(BAR_QFULL), L::NCH * L::BOX);
+          for (int c = 0; c < L::NCH; ++c)
+            tma_load_2d(sQ + c * L::BOX, &tmq, bar(BAR_QFULL), it.h * D + c * 64, (int)(it.s.s0 + it.q0));
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ++q_it;
+      const int nkb = fwd_kv_blocks(it.q0, n, it.s.c, BM, BN);
+      for (int kb = 0; ok && kb < nkb; ++kb) {
+        const int k0 = kb * BN;
+        if (tile_class(it.q0, k0, BM, BN, n, it.s.c, it.s.h_end) == 0) continue;
+        const int stage = kv_it % kStages;
+        ok = mbar_wait(bar(BAR_KVEMPTY + stage), ((kv_it / kStages) & 1) ^ 1, wd, 2);
+        if (!ok) break;
+        for (int rr = lane; rr < BN; rr += 32) {
+          const int row = k0 + rr;
+          ts_s[stage * BN + rr] = (p.ts && row < n) ? p.ts[it.s.s0 + row] : 0;
+        }
+        __syncwarp();
+        const bool withhold = (p.flags & HSTU_FLAG_TEST_TIMEOUT) && blockIdx.x == 0 && kv_it == 0;
+        if (lane == 0 && !withhold) {
+          mbar_arrive_expect_tx(bar(BAR_KVFULL + stage), L::STAGE);
+          const uint32_t dstK = sKV + stage * L::STAGE;
+          const int y = (int)(it.s.s0 + k0);
+          for (int c = 0; c < L::NCH; ++c) {
+            tma_load_2d(dstK + c * L::BOX, &tmk, bar(BAR_KVFULL + stage), it.h * D + c * 64, y);
+            tma_load_2d(dstK + L::K_BYTES + c * L::BOX, &tmv, bar(BAR_KVFULL + stage), it.h * D + c * 64, y);
+          }
+          armed[stage] += 1;
+        }
+        ++kv_it;
+      }
+    }
+    // make sure no copy is still landing in shared memory when the CTA ends
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s)
+        if (armed[s]) drain_wait(bar(BAR_KVFULL + s), (armed[s] - 1) & 1);
+      if (q_it) drain_wait(bar(BAR_QFULL), (q_it - 1) & 1);
+    }
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false, false);
+      constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, false, true);
+      uint32_t kv_it = 0, q_it = 0, o_it = 0;
+      bool ok = true;
+      ItemInfo it;
+      for (int r = 0; ok && item_of(p, r, nitems, it); ++r) {
+        const int n = it.s.n;
+        const uint32_t ob = o_it & 1;
+        const uint32_t ocol = ob ? L::O_COL1 : L::O_COL0;
+        ok = mbar_wait(bar(BAR_QFULL), q_it & 1, wd, 3) &&
+             mbar_wait(bar(BAR_OEMPTY + ob), ((o_it >> 1) & 1) ^ 1, wd, 4);
+        if (!ok) break;
+        fence_after_sync();
+        bool have_prev = false, first_pv = true;
+        uint32_t prev_it = 0;
+        const int nkb = fwd_kv_blocks(it.q0, n, it.s.c, BM, BN);
+        auto issue_pv = [&](uint32_t t) -> bool {
+          const uint32_t sb = t & 1, stage = t % kStages;
+          if (!mbar_wait(bar(BAR_PREADY + sb), (t >> 1) & 1, wd, 5)) return false;
+          fence_after_sync();
+          const uint32_t vbase = sKV + stage * L::STAGE + L::K_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint32_t a_hi = tmem + (sb * kSColStride) + 64u * (kk >> 2) + 8u * (kk & 3);
+            const uint64_t bd = sdesc_sw128(vbase + kk * 2048, L::BOX, 1024);
+            mma_ts(tmem + ocol, a_hi, bd, IDESC_PV, (first_pv && kk == 0) ? 0u : 1u);
+            mma_ts(tmem + ocol, a_hi + 32, bd, IDESC_PV, 1u);
+          }
+          first_pv = false;
+          mma_commit(bar(BAR_KVEMPTY + stage));
+          return true;
+        };
+        for (int kb = 0; ok && kb < nkb; ++kb) {
+          const int k0 = kb * BN;
+          if (tile_class(it.q0, k0, BM, BN, n, it.s.c, it.s.h_end) == 0) continue;
+          const uint32_t stage = kv_it % kStages, sb = kv_it & 1;
+          ok = mbar_wait(bar(BAR_KVFULL + stage), (kv_it / kStages) & 1, wd, 6);
+          if (!ok) break;
+          fence_after_sync();
+          const uint32_t kbase = sKV + stage * L::STAGE;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * L::BOX + (kk & 3) * 32;
+            mma_ss(tmem + (sb * kSColStride), sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+                   IDESC_S, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(BAR_SFULL + sb));
+          if (have_prev) ok = issue_pv(prev_it);
+          have_prev = true;
+          prev_it = kv_it;
+          ++kv_it;
+        }
+        if (ok && have_prev) ok = issue_pv(prev_it);
+        if (!ok) break;
+        mma_commit(bar(BAR_QEMPTY));
+        mma_commit(bar(BAR_OFULL + ob));
+        ++q_it;
+        ++o_it;
+      }
+      // every MMA issued by this thread is complete before TMEM is released
+      mma_commit(bar(BAR_DRAIN));
+      drain_wait(bar(BAR_DRAIN), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int wq = warp & 3, hh = warp >> 2;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    const float alpha = p.alpha, inv_n = p.inv_n;
+    uint32_t kv_it = 0, o_it = 0;
+    bool ok = true;
+    ItemInfo it;
+    for (int r = 0; ok && item_of(p, r, nitems, it); ++r) {
+      const int n = it.s.n, cx = it.s.c, h_end = it.s.h_end;
+      const int i = it.q0 + row;
+      const bool row_ok = i < n;
+      const int pos_i = i < h_end ? i : h_end;
+      const int64_t t_i = (p.ts && row_ok) ? p.ts[it.s.s0 + i] : 0;
+      const float* tp = tab + it.h * PT;
+      const float* tt = tp + P;
+      const int nkb = fwd_kv_blocks(it.q0, n, cx, BM, BN);
+      for (int kb = 0; ok && kb < nkb; ++kb) {
+        const int k0 = kb * BN;
+        const int cls = tile_class(it.q0, k0, BM, BN, n, cx, h_end);
+        if (cls == 0) continue;
+        const uint32_t stage = kv_it % kStages, sb = kv_it & 1;
+        ok = mbar_wait(bar(BAR_KVFULL + stage), (kv_it / kStages) & 1, wd, 7) &&
+             mbar_wait(bar(BAR_SFULL + sb), (kv_it >> 1) & 1, wd, 8);
+        if (!ok) break;
+        fence_after_sync();
+        const uint32_t scol = lane_base + (sb * kSColStride) + hh * 64;
+        uint32_t sv[2][32];
+        tmem_ld32(scol, sv[0]);
+        tmem_ld32(scol + 32, sv[1]);
+        tmem_wait_ld();
+        const int64_t* tsk = ts_s + stage * BN + hh * 64;
+        const int jb = k0 + hh * 64;
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float a2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int cc = ch * 32 + c + e;
+              const int j = jb + cc;
+              const int pj = j < h_end ? j : h_end;
+              int dp = pos_i - pj;
+              dp = dp < 0 ? -dp : dp;
+              const int bp = dp < P - 1 ? dp : P - 1;
+              const int64_t tj = tsk[cc];
+              const uint64_t dt = t_i >= tj ? (uint64_t)(t_i - tj) : (uint64_t)(tj - t_i);
+              int bt = 64 - __clzll((long long)dt);
+              bt = bt < Tb - 1 ? bt : Tb - 1;
+              const float z = fmaf(alpha, __uint_as_float(sv[ch][c + e]), tp[bp] + tt[bt]);
+              float a = z * fast_sigmoid(z) * inv_n;
+              const bool valid = cls == 2 || (row_ok && j < n && allowed(i, j, cx, h_end));
+              a2[e] = valid ? a : 0.f;
+            }
+            const uint32_t h2 = pack_bf16(a2[0], a2[1]);
+            hi[c >> 1] = h2;
+            lo[c >> 1] = pack_bf16(a2[0] - bf16_lo_f(h2), a2[1] - bf16_hi_f(h2));
+          }
+          // P_hi of this half at [64 hh, 64 hh + 32), P_lo at [64 hh + 32, 64 hh + 64)
+          tmem_st16(scol + ch * 16, hi);
+          tmem_st16(scol + 32 + ch * 16, lo);
+        }
+        tmem_wait_st();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_PREADY + sb));
+        ++kv_it;
+      }
+      if (!ok) break;
+      // O out
+      const uint32_t ob = o_it & 1;
+      ok = mbar_wait(bar(BAR_OFULL + ob), (o_it >> 1) & 1, wd, 9);
+      if (!ok) break;
+      fence_after_sync();
+      const uint32_t ocol = lane_base + (ob ? L::O_COL1 : L::O_COL0) + hh * (D / 2);
+      TO* orow = static_cast<TO*>(p.o) + ((size_t)(it.s.s0 + i) * H + it.h) * D + hh * (D / 2);
+#pragma unroll
+      for (int c = 0; c < D / 2; c += 32) {
+        uint32_t ov[32];
+        tmem_ld32(ocol + c, ov);
+        tmem_wait_ld();
+        if (row_ok) {
+          if constexpr (sizeof(TO) == 4) {
+            float4* dst = reinterpret_cast<float4*>(orow + c);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                                   __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]));
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              dst[e] = make_uint4(pack_bf16(__uint_as_float(ov[8 * e]), __uint_as_float(ov[8 * e + 1])),
+                                  pack_bf16(__uint_as_float(ov[8 * e + 2]), __uint_as_float(ov[8 * e + 3])),
+                                  pack_bf16(__uint_as_float(ov[8 * e + 4]), __uint_as_float(ov[8 * e + 5])),
+                                  pack_bf16(__uint_as_float(ov[8 * e + 6]), __uint_as_float(ov[8 * e + 7])));
+          }
+        }
+      }
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_OEMPTY + ob));
+      ++o_it;
+    }
+  }
+
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+}  // namespace
+
+// 2-D BF16 tensor map over [rows, cols] (row-major), box 64 cols x 128 rows,
+// 128-byte swizzle, zero fill outside.
+bool make_tmap_bf16(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tc_fwd_supported(int dtype, int dqk, int dv) {
+  return dtype == HSTU_BF16 && dqk == dv && (dqk == 64 || dqk == 128);
+}
+
+size_t tc_fwd_smem_bytes(int d, int H, int P, int Tb) {
+  const size_t tab = sizeof(float) * (size_t)H * (P + Tb);
+  return (d == 64 ? Layout<64>::TAB_OFF : Layout<128>::TAB_OFF) + tab + 1024;
+}
+
+template <int D, typename TO>
+static cudaError_t launch_fwd_t(const AttnParams& p, cudaStream_t st) {
+  CUtensorMap mq, mk, mv;
+  const int64_t cols = (int64_t)p.H * D;
+  if (!make_tmap_bf16(&mq, p.q, p.T, cols) || !make_tmap_bf16(&mk, p.k, p.T, cols) ||
+      !make_tmap_bf16(&mv, p.v, p.T, cols))
+    return cudaErrorInvalidValue;
+  const size_t smem = tc_fwd_smem_bytes(D, p.H, p.P, p.Tb);
+  cudaError_t e = cudaFuncSetAttribute(hstu_fwd_tc_kernel<D, TO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t max_items = ((p.T + BM - 1) / BM + p.B) * (int64_t)p.H;
+  const int grid = (int)(max_items < p.num_sms ? max_items : p.num_sms);
+  hstu_fwd_tc_kernel<D, TO><<<grid, kThreads, smem, st>>>(p, mq, mk, mv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_fwd(const AttnParams& p, cudaStream_t st) {
+  const bool f32 = p.out_dtype == HSTU_FP32;
+  if (p.dqk == 128) return f32 ? launch_fwd_t<128, float>(p, st) : launch_fwd_t<128, __nv_bfloat16>(p, st);
+  if (p.dqk == 64) return f32 ? launch_fwd_t<64, float>(p, st) : launch_fwd_t<64, __nv_bfloat16>(p, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace hstu
