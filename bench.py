@@ -253,6 +253,9 @@ def run_gpu(args, rank, world, local_rank):
 
     # ---- timed region: K steps, kernel events on the launching stream
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for e4 in evs:   # torch only times events it has recorded once; the library re-records them
+        for e in e4:
+            e.record(stream)
     clock = ClockSampler(local_rank)
     if world > 1:
         dist.barrier()

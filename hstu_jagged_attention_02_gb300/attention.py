@@ -103,7 +103,7 @@ class Problem:
         return C.hstu_get_device_error(self.ws.data_ptr(), _stream_handle(stream))
 
     def debug_plan(self, pass_: int, capacity: int, stream=None):
-        need = self.ws_bytes + 20 * capacity + 512
+        need = self.ws_bytes + 24 * capacity + 512
         ws = torch.empty(need, device=self.dev, dtype=torch.uint8)
         return C.hstu_attn_debug_plan(self.desc, _ptr(self.offsets), _ptr(self.num_targets),
                                       _ptr(self.num_contexts), pass_, ws.data_ptr(), need, capacity,

@@ -154,9 +154,9 @@ def hstu_time_next_attention_kernel(start_event: Optional[int], stop_event: Opti
 
 def hstu_attn_debug_plan(desc, seq_offsets: int, num_targets: Optional[int], num_contexts: Optional[int],
                          pass_: int, workspace: int, workspace_bytes: int, capacity: int, stream: int):
-    """Returns an int32 numpy array [n, 5] of (b, q_block, k_block, class, tile_edge)."""
+    """Returns an int32 numpy array [n, 6] of (b, q_block, k_block, class, q_rows, k_rows)."""
     import numpy as np
-    host = np.zeros((max(capacity, 1), 5), np.int32)
+    host = np.zeros((max(capacity, 1), 6), np.int32)
     n = ctypes.c_int64(0)
     _check(load().hstu_attn_debug_plan(ctypes.byref(desc), seq_offsets, num_targets, num_contexts, pass_,
                                        workspace, workspace_bytes, host.ctypes.data, capacity,

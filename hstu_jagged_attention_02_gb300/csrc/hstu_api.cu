@@ -100,7 +100,9 @@ bool use_tc(const hstu_attn_desc* d, bool bwd) {
   if (d->flags & HSTU_FLAG_FORCE_SIMT) return false;
   if (d->total_tokens < kTcTile) return false;  // TMA boxes of 128 rows
   if (dev_info().cc != 103) return false;
-  if (bwd) return tc_bwd_supported(d->dtype, d->d_qk, d->d_v);
+  if (bwd)
+    return tc_bwd_supported(d->dtype, d->d_qk, d->d_v) &&
+           tc_bwd_smem_bytes(d->H, d->num_pos_buckets, d->num_time_buckets) <= kMaxSmemPerCta;
   return tc_fwd_supported(d->dtype, d->d_qk, d->d_v) &&
          tc_fwd_smem_bytes(d->d_qk, d->H, d->num_pos_buckets, d->num_time_buckets) <= kMaxSmemPerCta;
 }
@@ -110,7 +112,14 @@ PlanParams plan_params(const hstu_attn_desc* d, const int64_t* off, const int32_
   PlanParams p{};
   p.off = off; p.nt = nt; p.nc = nc;
   p.B = d->B; p.T = d->total_tokens; p.max_n = d->max_seq_len;
-  p.BM = p.BN = tc ? kTcTile : kSimtTile;
+  if (!tc) {
+    p.BM = p.BN = kSimtTile;
+  } else if (pass == 0) {
+    p.BM = p.BN = kTcTile;
+  } else {
+    p.BM = kTcBwdQTile;  // the tensor-core backward walks 64-row query tiles per 128-row key block
+    p.BN = kTcTile;
+  }
   p.pass = pass;
   p.hdr = reinterpret_cast<int*>(ws);
   p.seq_start = reinterpret_cast<int*>(ws + L.seq_start);
@@ -291,7 +300,7 @@ hstu_status_t hstu_attn_debug_plan(const hstu_attn_desc* d, const int64_t* seq_o
       (host_capacity > 0 && !host_tiles))
     return HSTU_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(d, false);
-  const size_t need = L.plan_end + align_up(sizeof(int32_t) * 5 * (size_t)host_capacity);
+  const size_t need = L.plan_end + align_up(sizeof(int32_t) * 6 * (size_t)host_capacity);
   if ((s = check_ws(workspace, workspace_bytes, need)) != HSTU_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
@@ -307,7 +316,7 @@ hstu_status_t hstu_attn_debug_plan(const hstu_attn_desc* d, const int64_t* seq_o
   *n_tiles = hdr[WS_NTILES];
   const int64_t copy = hdr[WS_NTILES] < host_capacity ? hdr[WS_NTILES] : host_capacity;
   if (copy > 0) {
-    HSTU_CUDA_TRY(cudaMemcpyAsync(host_tiles, rec, sizeof(int32_t) * 5 * (size_t)copy,
+    HSTU_CUDA_TRY(cudaMemcpyAsync(host_tiles, rec, sizeof(int32_t) * 6 * (size_t)copy,
                                   cudaMemcpyDeviceToHost, st));
     HSTU_CUDA_TRY(cudaStreamSynchronize(st));
   }

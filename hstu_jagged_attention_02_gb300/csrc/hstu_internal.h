@@ -1,6 +1,8 @@
 // Internal launch interfaces between the C ABI (hstu_api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
+
 #include "hstu_common.cuh"
 
 namespace hstu {
@@ -82,8 +84,12 @@ cudaError_t launch_norm_gate_fwd(const NormParams& p, cudaStream_t stream);
 cudaError_t launch_norm_gate_bwd(const NormParams& p, cudaStream_t stream);
 cudaError_t launch_convert_f32(const float* src, void* dst, int64_t count, int dtype, cudaStream_t stream);
 
-// Tensor-core path (BF16, d in {64, 128}), 128 x 128 tiles
+// Tensor-core path (BF16): forward d in {64, 128} on 128 x 128 tiles;
+// backward d = 128 on 64 (query) x 128 (key) tiles
 constexpr int kTcTile = 128;
+constexpr int kTcBwdQTile = 64;
+bool make_tmap_bf16(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_rows);
+size_t tc_bwd_smem_bytes(int H, int P, int Tb);
 bool tc_fwd_supported(int dtype, int dqk, int dv);
 size_t tc_fwd_smem_bytes(int d, int H, int P, int Tb);
 constexpr size_t kMaxSmemPerCta = 227 * 1024;

@@ -146,7 +146,8 @@ plan_kernel(PlanParams p) {
 }
 
 // Lists every non-skipped tile of every planned block, walking the blocks the
-// same way the kernels do.  Record: b, q_block, k_block, class, tile edge.
+// same way the kernels do.  Record: b, q_block, k_block, class, query edge,
+// key edge.
 __global__ void debug_tiles_kernel(PlanParams p, int32_t* rec, int64_t cap) {
   const int nblk = p.hdr[WS_NBLK];
   for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < nblk; idx += gridDim.x * blockDim.x) {
@@ -160,8 +161,8 @@ __global__ void debug_tiles_kernel(PlanParams p, int32_t* rec, int64_t cap) {
         if (!cls) continue;
         const int slot = atomicAdd(p.hdr + WS_NTILES, 1);
         if (slot < cap) {
-          int32_t* r = rec + (int64_t)slot * 5;
-          r[0] = blk.b; r[1] = blk.blk; r[2] = kb; r[3] = cls; r[4] = p.BM;
+          int32_t* r = rec + (int64_t)slot * 6;
+          r[0] = blk.b; r[1] = blk.blk; r[2] = kb; r[3] = cls; r[4] = p.BM; r[5] = p.BN;
         }
       }
     } else {
@@ -172,8 +173,8 @@ __global__ void debug_tiles_kernel(PlanParams p, int32_t* rec, int64_t cap) {
         if (!cls) continue;
         const int slot = atomicAdd(p.hdr + WS_NTILES, 1);
         if (slot < cap) {
-          int32_t* r = rec + (int64_t)slot * 5;
-          r[0] = blk.b; r[1] = qb; r[2] = blk.blk; r[3] = cls; r[4] = p.BM;
+          int32_t* r = rec + (int64_t)slot * 6;
+          r[0] = blk.b; r[1] = qb; r[2] = blk.blk; r[3] = cls; r[4] = p.BM; r[5] = p.BN;
         }
       }
     }

@@ -410,14 +410,14 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-// 2-D BF16 tensor map over [rows, cols] (row-major), box 64 cols x 128 rows,
-// 128-byte swizzle, zero fill outside.
-bool make_tmap_bf16(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols) {
+// 2-D BF16 tensor map over [rows, cols] (row-major), box 64 cols x box_rows
+// rows, 128-byte swizzle, zero fill outside.
+bool make_tmap_bf16(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -437,8 +437,8 @@ template <int D, typename TO>
 static cudaError_t launch_fwd_t(const AttnParams& p, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   const int64_t cols = (int64_t)p.H * D;
-  if (!make_tmap_bf16(&mq, p.q, p.T, cols) || !make_tmap_bf16(&mk, p.k, p.T, cols) ||
-      !make_tmap_bf16(&mv, p.v, p.T, cols))
+  if (!make_tmap_bf16(&mq, p.q, p.T, cols, BM) || !make_tmap_bf16(&mk, p.k, p.T, cols, BN) ||
+      !make_tmap_bf16(&mv, p.v, p.T, cols, BN))
     return cudaErrorInvalidValue;
   const size_t smem = tc_fwd_smem_bytes(D, p.H, p.P, p.Tb);
   cudaError_t e = cudaFuncSetAttribute(hstu_fwd_tc_kernel<D, TO>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -175,7 +175,7 @@ def make_batch(lengths_hist, *, H, d_qk, d_v, dtype="bf16", num_contexts=0,
         timestamps=ts, q=q, k=k, v=v, u=u, dy=dy, rab_pos=rp, rab_time=rt,
         alpha=float(alpha if alpha is not None else 1.0 / math.sqrt(d_qk)),
         max_seq_len=int(max_seq_len if max_seq_len is not None
-                        else (int(lengths.max()) if B else 1)),
+                        else (max(int(lengths.max()), 1) if B else 1)),
         norm=norm, backward=backward)
 
 

@@ -156,12 +156,12 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* desc, const hstu_attn_bwd_args
 /* The tile plan of one pass, as the kernels walk it (compound-mask tile
  * skipping, wmrh.cn RecSDK page, "HSTU acceleration operator" paragraph).
  * pass 0 = forward (query-block work items), 1 = backward (key-block items).
- * Writes up to host_capacity records of 5 int32 (b, q_block, k_block, class,
- * tile_rows) to host_tiles for every tile that is not skipped; class 1 =
- * partial, 2 = full; tile_rows = the tile edge (the tensor-core or the
- * CUDA-core tile, whichever path this descriptor selects).  *n_tiles receives
- * the total count.  The workspace must hold the forward workspace plus
- * 20 * host_capacity bytes (rounded up to 256).  Synchronises the stream. */
+ * Writes up to host_capacity records of 6 int32 (b, q_block, k_block, class,
+ * q_rows, k_rows) to host_tiles for every tile that is not skipped; class 1 =
+ * partial, 2 = full; q_rows x k_rows = the tile shape of the path this
+ * descriptor selects (tensor-core or CUDA-core).  *n_tiles receives the total
+ * count.  The workspace must hold the forward workspace plus
+ * 24 * host_capacity bytes (rounded up to 256).  Synchronises the stream. */
 hstu_status_t hstu_attn_debug_plan(const hstu_attn_desc* desc, const int64_t* seq_offsets,
                                    const int32_t* num_targets, const int32_t* num_contexts, int32_t pass,
                                    void* workspace, size_t workspace_bytes, int32_t* host_tiles,

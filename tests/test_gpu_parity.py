@@ -186,9 +186,9 @@ def test_debug_plan_matches_bruteforce_tile_classes(pass_, flags):
     b = _ragged_batch("bf16", 128, seed=70, lengths=[1, 40, 127, 128, 129, 260, 513, 700])
     pr = _problem(b, flags=flags)
     tiles = pr.debug_plan(pass_, capacity=200000)
-    edge = int(tiles[0, 4])
-    assert np.all(tiles[:, 4] == edge)
-    ref = O.tile_classes(b.offsets, b.num_targets, b.num_contexts, edge, edge)
+    bm, bn = int(tiles[0, 4]), int(tiles[0, 5])
+    assert np.all(tiles[:, 4] == bm) and np.all(tiles[:, 5] == bn)
+    ref = O.tile_classes(b.offsets, b.num_targets, b.num_contexts, bm, bn)
     keep = ref["cls"] != 0
     want = sorted(zip(ref["b"][keep].tolist(), ref["qb"][keep].tolist(), ref["kb"][keep].tolist(),
                       ref["cls"][keep].tolist()))
@@ -201,8 +201,7 @@ def test_named_config_plan_heavy_tailed():
     pr = _problem(b)
     for pass_ in (0, 1):
         tiles = pr.debug_plan(pass_, capacity=400000)
-        edge = int(tiles[0, 4])
-        ref = O.tile_classes(b.offsets, b.num_targets, b.num_contexts, edge, edge)
+        ref = O.tile_classes(b.offsets, b.num_targets, b.num_contexts, int(tiles[0, 4]), int(tiles[0, 5]))
         keep = ref["cls"] != 0
         want = sorted(zip(ref["b"][keep].tolist(), ref["qb"][keep].tolist(), ref["kb"][keep].tolist(),
                           ref["cls"][keep].tolist()))
