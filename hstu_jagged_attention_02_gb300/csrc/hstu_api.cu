@@ -173,7 +173,9 @@ hstu_status_t hstu_attn_fwd(const hstu_attn_desc* d, const hstu_attn_fwd_args* a
                             size_t workspace_bytes, hstu_stream_t stream) {
   hstu_status_t s = check_desc(d);
   if (s != HSTU_OK) return s;
-  if (!a || !a->seq_offsets || !a->q || !a->k || !a->v || !a->o) return HSTU_ERR_INVALID_ARG;
+  // token tensors may be NULL only when there are no tokens
+  if (!a || !a->seq_offsets || (d->total_tokens > 0 && (!a->q || !a->k || !a->v || !a->o)))
+    return HSTU_ERR_INVALID_ARG;
   for (const void* ptr : {a->q, a->k, a->v, (const void*)a->o, a->u, (const void*)a->y})
     if (ptr && !aligned16(ptr)) return HSTU_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(d, false);
@@ -224,9 +226,10 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
                             size_t workspace_bytes, hstu_stream_t stream) {
   hstu_status_t s = check_desc(d);
   if (s != HSTU_OK) return s;
-  if (!a || !a->seq_offsets || !a->q || !a->k || !a->v || !a->o || !a->dy || !a->dq || !a->dk || !a->dv)
+  if (!a || !a->seq_offsets ||
+      (d->total_tokens > 0 && (!a->q || !a->k || !a->v || !a->o || !a->dy || !a->dq || !a->dk || !a->dv)))
     return HSTU_ERR_INVALID_ARG;
-  if ((a->u == nullptr) != (a->du == nullptr)) return HSTU_ERR_INVALID_ARG;
+  if (d->total_tokens > 0 && (a->u == nullptr) != (a->du == nullptr)) return HSTU_ERR_INVALID_ARG;
   for (const void* ptr : {a->q, a->k, a->v, a->o, a->u, a->dy, (const void*)a->dq, (const void*)a->dk,
                           (const void*)a->dv, (const void*)a->du})
     if (ptr && !aligned16(ptr)) return HSTU_ERR_INVALID_ARG;

@@ -345,6 +345,10 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         tmem_wait_ld();
         const int64_t* tq = tsq + stage * BQ + hh * 32;
         uint32_t ahi[16], alo[16], zhi[16], zlo[16];
+        // d_rab partial sums: the clamped position bucket in a register, the
+        // time bucket run-length along the row (timestamps are mostly sorted)
+        float rp_far = 0.f, rt_run = 0.f;
+        int rt_cur = -1;
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           float av[2], zv[2];
@@ -366,8 +370,19 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
             if (valid) {
               a = z * sg * inv_n;
               dz = __uint_as_float(dav[c + e]) * sg * fmaf(z, 1.f - sg, 1.f) * inv_n;
-              if (want_rp) atomicAdd(drp + bp, dz);
-              if (want_rt) atomicAdd(drt + bt, dz);
+              if (want_rp) {
+                if (bp == P - 1) rp_far += dz;
+                else atomicAdd(drp + bp, dz);
+              }
+              if (want_rt) {
+                if (bt == rt_cur) {
+                  rt_run += dz;
+                } else {
+                  if (rt_cur >= 0) atomicAdd(drt + rt_cur, rt_run);
+                  rt_cur = bt;
+                  rt_run = dz;
+                }
+              }
             }
             av[e] = a;
             zv[e] = dz;
@@ -378,6 +393,12 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           alo[c >> 1] = pack_bf16(av[0] - bf16_lo_f(ah), av[1] - bf16_hi_f(ah));
           zhi[c >> 1] = zh;
           zlo[c >> 1] = pack_bf16(zv[0] - bf16_lo_f(zh), zv[1] - bf16_hi_f(zh));
+        }
+        if (want_rt && rt_cur >= 0) atomicAdd(drt + rt_cur, rt_run);
+        if (want_rp) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) rp_far += __shfl_xor_sync(0xffffffffu, rp_far, o);
+          if (lane == 0 && rp_far != 0.f) atomicAdd(drp + (P - 1), rp_far);
         }
         // A and dZ back into TMEM: hi at [32 hh, 32 hh + 16), lo at [32 hh + 16, 32 hh + 32)
         tmem_st16(lane_base + S_COL + hh * 32, ahi);
