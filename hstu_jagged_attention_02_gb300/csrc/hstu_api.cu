@@ -108,9 +108,9 @@ bool use_tc(const hstu_attn_desc* d, bool bwd) {
 }
 
 PlanParams plan_params(const hstu_attn_desc* d, const int64_t* off, const int32_t* nt, const int32_t* nc,
-                       int pass, bool tc, char* ws, const WsLayout& L) {
+                       const int64_t* ts, int pass, bool tc, char* ws, const WsLayout& L) {
   PlanParams p{};
-  p.off = off; p.nt = nt; p.nc = nc;
+  p.off = off; p.nt = nt; p.nc = nc; p.ts = ts;
   p.B = d->B; p.T = d->total_tokens; p.max_n = d->max_seq_len;
   if (!tc) {
     p.BM = p.BN = kSimtTile;
@@ -185,7 +185,8 @@ hstu_status_t hstu_attn_fwd(const hstu_attn_desc* d, const hstu_attn_fwd_args* a
   g_launches = 0;
 
   const bool tc = use_tc(d, false);
-  const PlanParams pp = plan_params(d, a->seq_offsets, a->num_targets, a->num_contexts, 0, tc, ws, L);
+  const PlanParams pp =
+      plan_params(d, a->seq_offsets, a->num_targets, a->num_contexts, a->timestamps, 0, tc, ws, L);
   HSTU_CUDA_TRY(launch_plan(pp, st));
   ++g_launches;
 
@@ -240,7 +241,8 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
   g_launches = 0;
 
   const bool tc = use_tc(d, true);
-  const PlanParams pp = plan_params(d, a->seq_offsets, a->num_targets, a->num_contexts, 1, tc, ws, L);
+  const PlanParams pp =
+      plan_params(d, a->seq_offsets, a->num_targets, a->num_contexts, a->timestamps, 1, tc, ws, L);
   HSTU_CUDA_TRY(launch_plan(pp, st));
   ++g_launches;
 
@@ -308,7 +310,7 @@ hstu_status_t hstu_attn_debug_plan(const hstu_attn_desc* d, const int64_t* seq_o
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   const bool tc = use_tc(d, pass == 1);
-  const PlanParams pp = plan_params(d, seq_offsets, num_targets, num_contexts, pass, tc, ws, L);
+  const PlanParams pp = plan_params(d, seq_offsets, num_targets, num_contexts, nullptr, pass, tc, ws, L);
   int32_t* rec = reinterpret_cast<int32_t*>(ws + L.plan_end);
   HSTU_CUDA_TRY(launch_plan(pp, st));
   HSTU_CUDA_TRY(launch_debug_tiles(pp, rec, host_capacity, st));

@@ -23,7 +23,10 @@ enum : int {
   WS_NBLK = 1,      // number of planner blocks of the current pass
   WS_ERR_INFO = 2,  // detail of the first error (sequence index or wait site)
   WS_NTILES = 3,    // debug-plan tile counter
+  WS_FLAGS = 4,     // planner findings (WS_FLAG_*)
 };
+// some timestamp is 2^30 s or more away from its sequence's first token
+constexpr int WS_FLAG_WIDE_TS = 1;
 constexpr size_t kWsHeaderBytes = 256;
 constexpr size_t kWsAlign = 256;
 constexpr int kCostBins = 4096;  // planner histogram bins (cost = tiles per block)

@@ -11,6 +11,7 @@ struct PlanParams {
   const int64_t* off;
   const int32_t* nt;
   const int32_t* nc;
+  const int64_t* ts;  // timestamps or NULL (span check only)
   int B;
   int64_t T;
   int max_n;

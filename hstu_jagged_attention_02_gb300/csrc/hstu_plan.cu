@@ -57,6 +57,7 @@ plan_kernel(PlanParams p) {
     p.hdr[WS_ERR_INFO] = 0;
     p.hdr[WS_NBLK] = 0;
     p.hdr[WS_NTILES] = 0;
+    p.hdr[WS_FLAGS] = 0;
     sh_bad = 0;
   }
   for (int i = t; i < kCostBins; i += kPlanThreads) sh_hist[i] = 0;
@@ -75,6 +76,23 @@ plan_kernel(PlanParams p) {
   if (sh_bad) {
     if (t == 0) atomicCAS(p.hdr + WS_ERR, 0, HSTU_ERR_DEVICE_CHECK);
     return;
+  }
+
+  // 1b. can every timestamp be held relative to its sequence's first token in
+  // 31 bits (so gaps fit in 32)?  Otherwise the kernels take their 64-bit path.
+  if (p.ts) {
+    const int warp = t >> 5, lane = t & 31;
+    int wide = 0;
+    for (int b = warp; b < p.B; b += kPlanThreads / 32) {
+      const int64_t s0 = p.off[b], n = p.off[b + 1] - s0;
+      if (n == 0) continue;
+      const int64_t base = p.ts[s0];
+      for (int64_t i = lane; i < n; i += 32) {
+        const int64_t d = p.ts[s0 + i] - base;
+        wide |= (d >= (int64_t)1 << 30 || d < -((int64_t)1 << 30));
+      }
+    }
+    if (__any_sync(0xffffffffu, wide) && lane == 0) atomicOr(p.hdr + WS_FLAGS, WS_FLAG_WIDE_TS);
   }
 
   // 2. blocks per sequence -> exclusive prefix (seq_start[b]), chunked scan

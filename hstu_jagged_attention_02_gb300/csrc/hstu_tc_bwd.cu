@@ -17,8 +17,8 @@
 // x = hi + lo; a single BF16 rounding of any of them costs ~1.5% of the
 // output RMS on heavy-tailed batches.
 //
-// Roles (320 threads): warps 0-7 epilogue (TMEM lane quarter warp%4, column
-// half warp/4), warp 8 TMA producer, warp 9 MMA issuer and TMEM owner.
+// Roles (576 threads): warps 0-15 epilogue (TMEM lane quarter warp%4, column
+// quarter warp/4), warp 16 TMA producer, warp 17 MMA issuer and TMEM owner.
 #include "hstu_internal.h"
 #include "tc_ptx.cuh"
 
@@ -31,9 +31,9 @@ using namespace tc;
 constexpr int D = 128;
 constexpr int BQ = kTcBwdQTile;   // 64 query rows per tile
 constexpr int BK = kTcTile;       // 128 key rows per item
-constexpr int kEpiWarps = 8;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
-constexpr int kThreads = 10 * 32;
+constexpr int kEpiWarps = 16;
+constexpr int kProducerWarp = 16, kMmaWarp = 17;
+constexpr int kThreads = 18 * 32;
 constexpr int kQStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t DV_COL = 0, DK_COL = 128, S_COL = 256, DA_COL = 320, DQ_COL = 384;
@@ -53,17 +53,22 @@ struct Lay {
   static constexpr int QSTAGE = 3 * Q_BYTES;
   static constexpr int DZ_OFF = QS_OFF + kQStages * QSTAGE;  // dZ^T hi then lo: [128 key][64 query] bf16
   static constexpr int DZ_BYTES = BK * 128;
-  static constexpr int TSQ_OFF = DZ_OFF + 2 * DZ_BYTES;      // int64 [kQStages][BQ]
-  static constexpr int BAR_OFF = TSQ_OFF + kQStages * BQ * 8;
+  static constexpr int TS64_OFF = DZ_OFF + 2 * DZ_BYTES;     // int64 [kQStages][BQ] absolute
+  static constexpr int TS32_OFF = TS64_OFF + kQStages * BQ * 8;  // int32 [kQStages][BQ] relative
+  static constexpr int BAR_OFF = TS32_OFF + kQStages * BQ * 4;
   static constexpr int MISC_OFF = BAR_OFF + BAR_COUNT * 8;
   static constexpr int TAB_OFF = MISC_OFF + 16;              // float [H][P+Tb] bias, then [H][P+Tb] d_rab
 };
 
-__device__ __forceinline__ float fast_sigmoid(float z) {
-  float e, r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-z * kLog2e));
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
-  return r;
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ void fence_async_smem() {
@@ -98,8 +103,114 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Per-thread context of the epilogue: one key row j of the item.
+struct KeyCtx {
+  int j, n, cx, h_end, pos_j, P, Tb;
+  bool j_ok, want_rp, want_rt;
+  int32_t tj32;
+  int64_t tj64;
+  const float* tp;   // position table of the head (times -log2 e)
+  const float* tt;   // time table of the head (times -log2 e)
+  float* drp;        // shared d_rab accumulators of the head
+  float* drt;
+  float kA, kC, kZ, inv_n;  // -log2(e) alpha, -1/(log2(e) N), -1/log2(e), 1/N
+};
+
+// 16 query columns ib.. of one key row: A and dZ as packed BF16 hi/lo pairs,
+// plus the d_rab contributions.  FAST_POS: every column is a history/context
+// query at or after the key (position gap = i - j).  WIDE: 64-bit gaps.
+// PARTIAL: evaluate the mask per element.
+template <bool FAST_POS, bool WIDE, bool PARTIAL>
+__device__ __forceinline__ void grad16(const uint32_t (&sv)[16], const uint32_t (&dav)[16], uint32_t (&ahi)[8],
+                                       uint32_t (&alo)[8], uint32_t (&zhi)[8], uint32_t (&zlo)[8],
+                                       const KeyCtx& kc, int ib, const int32_t* ts32, const int64_t* ts64) {
+  float bias[16];
+  int bps[16], bts[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    int bp;
+    if (FAST_POS) {
+      const int dp = ib + c - kc.j;
+      bp = dp < kc.P - 1 ? dp : kc.P - 1;
+    } else {
+      const int i = ib + c;
+      const int pi = i < kc.h_end ? i : kc.h_end;
+      int dp = pi - kc.pos_j;
+      dp = dp < 0 ? -dp : dp;
+      bp = dp < kc.P - 1 ? dp : kc.P - 1;
+    }
+    int bt;
+    if (WIDE) {
+      const int64_t ti = ts64[c];
+      const uint64_t dt = ti >= kc.tj64 ? (uint64_t)(ti - kc.tj64) : (uint64_t)(kc.tj64 - ti);
+      bt = 64 - __clzll((long long)dt);
+    } else {
+      int d = ts32[c] - kc.tj32;
+      d = d < 0 ? -d : d;
+      bt = 32 - __clz(d);
+    }
+    bt = bt < kc.Tb - 1 ? bt : kc.Tb - 1;
+    bps[c] = bp;
+    bts[c] = bt;
+    bias[c] = kc.tp[bp] + kc.tt[bt];
+  }
+  float rp_far = 0.f, rt_run = 0.f;
+  int rt_cur = -1;
+#pragma unroll
+  for (int c = 0; c < 16; c += 2) {
+    float av[2], zv[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float w = fmaf(kc.kA, __uint_as_float(sv[c + e]), bias[c + e]);
+      const float sg = rcp_approx(1.0f + ex2_approx(w));
+      const float z = w * kc.kZ;
+      float a = (w * kc.kC) * sg;
+      float dz = __uint_as_float(dav[c + e]) * sg * fmaf(z, 1.f - sg, 1.f) * kc.inv_n;
+      bool valid = true;
+      if (PARTIAL) {
+        const int i = ib + c + e;
+        valid = kc.j_ok && i < kc.n && allowed(i, kc.j, kc.cx, kc.h_end);
+        a = valid ? a : 0.f;
+        dz = valid ? dz : 0.f;
+      }
+      av[e] = a;
+      zv[e] = dz;
+      if (valid) {
+        // d_rab: the clamped position bucket in a register, the time bucket
+        // run-length along the row
+        if (kc.want_rp) {
+          if (bps[c + e] == kc.P - 1) rp_far += dz;
+          else atomicAdd(kc.drp + bps[c + e], dz);
+        }
+        if (kc.want_rt) {
+          if (bts[c + e] == rt_cur) {
+            rt_run += dz;
+          } else {
+            if (rt_cur >= 0) atomicAdd(kc.drt + rt_cur, rt_run);
+            rt_cur = bts[c + e];
+            rt_run = dz;
+          }
+        }
+      }
+    }
+    const uint32_t ah = pack_bf16(av[0], av[1]);
+    const uint32_t zh = pack_bf16(zv[0], zv[1]);
+    ahi[c >> 1] = ah;
+    alo[c >> 1] = pack_bf16(av[0] - bf16_lo_f(ah), av[1] - bf16_hi_f(ah));
+    zhi[c >> 1] = zh;
+    zlo[c >> 1] = pack_bf16(zv[0] - bf16_lo_f(zh), zv[1] - bf16_hi_f(zh));
+  }
+  if (kc.want_rt && rt_cur >= 0) atomicAdd(kc.drt + rt_cur, rt_run);
+  if (kc.want_rp) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) rp_far += __shfl_xor_sync(0xffffffffu, rp_far, o);
+    if ((threadIdx.x & 31) == 0 && rp_far != 0.f) atomicAdd(kc.drp + (kc.P - 1), rp_far);
+  }
+}
+
+// 18 warps x 32 threads x 112 registers = 64512 <= 65536
 template <typename TO>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(112)
 hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const __grid_constant__ CUtensorMap tmdh, const __grid_constant__ CUtensorMap tmdl) {
@@ -109,7 +220,8 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
   const uint32_t sK = base_u32 + Lay::K_OFF, sV = base_u32 + Lay::V_OFF;
   const uint32_t sQS = base_u32 + Lay::QS_OFF, sDZ = base_u32 + Lay::DZ_OFF;
-  int64_t* tsq = reinterpret_cast<int64_t*>(base + Lay::TSQ_OFF);
+  int64_t* ts64_s = reinterpret_cast<int64_t*>(base + Lay::TS64_OFF);
+  int32_t* ts32_s = reinterpret_cast<int32_t*>(base + Lay::TS32_OFF);
   const uint32_t bar0 = base_u32 + Lay::BAR_OFF;
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + Lay::MISC_OFF);
@@ -147,7 +259,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     } else if (has_rt) {
       v = p.rab_time[h * Tb + (e - P)];
     }
-    tab[x] = v;
+    tab[x] = -kLog2e * v;
     drab[x] = 0.f;
   }
   if (warp == kMmaWarp) {
@@ -172,6 +284,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   wd.err_info = p.hdr_rw + WS_ERR_INFO;
   wd.limit_ns = (p.flags & HSTU_FLAG_TEST_TIMEOUT) ? 1000000ull : 2000000000ull;
   const int nitems = p.hdr[WS_NBLK] * H;
+  const bool wide_ts = (p.hdr[WS_FLAGS] & WS_FLAG_WIDE_TS) != 0;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -181,6 +294,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     Item it;
     for (int r = 0; ok && item_of(p, r, nitems, it); ++r) {
       const int n = it.s.n;
+      const int64_t tbase = p.ts ? p.ts[it.s.s0] : 0;
       if (lane == 0) {
         ok = mbar_wait(bar(BAR_KVEMPTY), (item_it & 1) ^ 1, wd, 21);
         if (ok) {
@@ -204,7 +318,9 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         if (!ok) break;
         for (int rr = lane; rr < BQ; rr += 32) {
           const int row = q0 + rr;
-          tsq[stage * BQ + rr] = (p.ts && row < n) ? p.ts[it.s.s0 + row] : 0;
+          const int64_t t = (p.ts && row < n) ? p.ts[it.s.s0 + row] : tbase;
+          ts64_s[stage * BQ + rr] = t;
+          ts32_s[stage * BQ + rr] = (int32_t)(t - tbase);
         }
         __syncwarp();
         if (lane == 0) {
@@ -273,20 +389,20 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
                mbar_wait(bar(BAR_DQEMPTY), (qt_it & 1) ^ 1, wd, 27);
           if (!ok) break;
           fence_after_sync();
-          // dV += A^T dO ; dK += dZ^T Q   (K = 64 queries: 4 steps of 16)
+          // dV += A^T dO ; dK += dZ^T Q   (K = 64 queries: 4 steps of 16, one per column quarter)
 #pragma unroll
           for (int kk = 0; kk < BQ / 16; ++kk) {
-            const uint32_t a_hi = tmem + S_COL + 32u * (kk >> 1) + 8u * (kk & 1);
-            const uint32_t z_hi = tmem + DA_COL + 32u * (kk >> 1) + 8u * (kk & 1);
+            const uint32_t a_hi = tmem + S_COL + 16u * kk;
+            const uint32_t z_hi = tmem + DA_COL + 16u * kk;
             const uint64_t bdh = sdesc_sw128(sDh + kk * 2048, Lay::QBOX, 1024);
             const uint64_t bdl = sdesc_sw128(sDl + kk * 2048, Lay::QBOX, 1024);
             const uint64_t bq = sdesc_sw128(sQ + kk * 2048, Lay::QBOX, 1024);
             const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
             mma_ts(tmem + DV_COL, a_hi, bdh, IDESC_DVK, acc0);
-            mma_ts(tmem + DV_COL, a_hi + 16, bdh, IDESC_DVK, 1u);
+            mma_ts(tmem + DV_COL, a_hi + 8, bdh, IDESC_DVK, 1u);
             mma_ts(tmem + DV_COL, a_hi, bdl, IDESC_DVK, 1u);
             mma_ts(tmem + DK_COL, z_hi, bq, IDESC_DVK, acc0);
-            mma_ts(tmem + DK_COL, z_hi + 16, bq, IDESC_DVK, 1u);
+            mma_ts(tmem + DK_COL, z_hi + 8, bq, IDESC_DVK, 1u);
           }
           // dQ^T = K^T dZ^T  (K = 128 keys: 8 steps of 16)
 #pragma unroll
@@ -312,105 +428,73 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int wq = warp & 3, hh = warp >> 2;
+    const int wq = warp & 3, hq = warp >> 2;
     const int lrow = wq * 32 + lane;                  // TMEM lane: key row (S^T, dV, dK) or d (dQ^T)
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
-    const float alpha = p.alpha, inv_n = p.inv_n;
     uint32_t item_it = 0, qt_it = 0;
     bool ok = true;
     Item it;
+    KeyCtx kc;
+    kc.P = P;
+    kc.Tb = Tb;
+    kc.want_rp = want_rp;
+    kc.want_rt = want_rt;
+    kc.kA = -kLog2e * p.alpha;
+    kc.kC = -p.inv_n / kLog2e;
+    kc.kZ = -1.0f / kLog2e;
+    kc.inv_n = p.inv_n;
     for (int r = 0; ok && item_of(p, r, nitems, it); ++r) {
-      const int n = it.s.n, cx = it.s.c, h_end = it.s.h_end;
-      const int j = it.k0 + lrow;
-      const bool j_ok = j < n;
-      const int pos_j = j < h_end ? j : h_end;
-      const int64_t t_j = (p.ts && j_ok) ? p.ts[it.s.s0 + j] : 0;
-      const float* tp = tab + it.h * PT;
-      const float* tt = tp + P;
-      float* drp = drab + it.h * PT;
-      float* drt = drp + P;
-      const int nqt = (n + BQ - 1) / BQ;
-      for (int qt = bwd_q_begin(it.k0, cx, BQ); ok && qt < nqt; ++qt) {
+      kc.n = it.s.n;
+      kc.cx = it.s.c;
+      kc.h_end = it.s.h_end;
+      kc.j = it.k0 + lrow;
+      kc.j_ok = kc.j < kc.n;
+      kc.pos_j = kc.j < kc.h_end ? kc.j : kc.h_end;
+      const int64_t tbase = p.ts ? p.ts[it.s.s0] : 0;
+      kc.tj64 = (p.ts && kc.j_ok) ? p.ts[it.s.s0 + kc.j] : tbase;
+      kc.tj32 = (int32_t)(kc.tj64 - tbase);
+      kc.tp = tab + it.h * PT;
+      kc.tt = kc.tp + P;
+      kc.drp = drab + it.h * PT;
+      kc.drt = kc.drp + P;
+      const int nqt = (kc.n + BQ - 1) / BQ;
+      for (int qt = bwd_q_begin(it.k0, kc.cx, BQ); ok && qt < nqt; ++qt) {
         const int q0 = qt * BQ;
-        const int cls = tile_class(q0, it.k0, BQ, BK, n, cx, h_end);
+        const int cls = tile_class(q0, it.k0, BQ, BK, kc.n, kc.cx, kc.h_end);
         if (cls == 0) continue;
         const uint32_t stage = qt_it % kQStages;
         ok = mbar_wait(bar(BAR_QFULL + stage), (qt_it / kQStages) & 1, wd, 28) &&
              mbar_wait(bar(BAR_SFULL), qt_it & 1, wd, 29);
         if (!ok) break;
         fence_after_sync();
-        uint32_t sv[32], dav[32];
-        tmem_ld32(lane_base + S_COL + hh * 32, sv);
-        tmem_ld32(lane_base + DA_COL + hh * 32, dav);
+        uint32_t sv[16], dav[16];
+        tmem_ld16(lane_base + S_COL + hq * 16, sv);
+        tmem_ld16(lane_base + DA_COL + hq * 16, dav);
         tmem_wait_ld();
-        const int64_t* tq = tsq + stage * BQ + hh * 32;
-        uint32_t ahi[16], alo[16], zhi[16], zlo[16];
-        // d_rab partial sums: the clamped position bucket in a register, the
-        // time bucket run-length along the row (timestamps are mostly sorted)
-        float rp_far = 0.f, rt_run = 0.f;
-        int rt_cur = -1;
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float av[2], zv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int i = q0 + hh * 32 + c + e;
-            const int pi = i < h_end ? i : h_end;
-            int dp = pi - pos_j;
-            dp = dp < 0 ? -dp : dp;
-            const int bp = dp < P - 1 ? dp : P - 1;
-            const int64_t ti = tq[c + e];
-            const uint64_t dt = ti >= t_j ? (uint64_t)(ti - t_j) : (uint64_t)(t_j - ti);
-            int bt = 64 - __clzll((long long)dt);
-            bt = bt < Tb - 1 ? bt : Tb - 1;
-            const float z = fmaf(alpha, __uint_as_float(sv[c + e]), tp[bp] + tt[bt]);
-            const float sg = fast_sigmoid(z);
-            const bool valid = cls == 2 || (j_ok && i < n && allowed(i, j, cx, h_end));
-            float a = 0.f, dz = 0.f;
-            if (valid) {
-              a = z * sg * inv_n;
-              dz = __uint_as_float(dav[c + e]) * sg * fmaf(z, 1.f - sg, 1.f) * inv_n;
-              if (want_rp) {
-                if (bp == P - 1) rp_far += dz;
-                else atomicAdd(drp + bp, dz);
-              }
-              if (want_rt) {
-                if (bt == rt_cur) {
-                  rt_run += dz;
-                } else {
-                  if (rt_cur >= 0) atomicAdd(drt + rt_cur, rt_run);
-                  rt_cur = bt;
-                  rt_run = dz;
-                }
-              }
-            }
-            av[e] = a;
-            zv[e] = dz;
-          }
-          const uint32_t ah = pack_bf16(av[0], av[1]);
-          const uint32_t zh = pack_bf16(zv[0], zv[1]);
-          ahi[c >> 1] = ah;
-          alo[c >> 1] = pack_bf16(av[0] - bf16_lo_f(ah), av[1] - bf16_hi_f(ah));
-          zhi[c >> 1] = zh;
-          zlo[c >> 1] = pack_bf16(zv[0] - bf16_lo_f(zh), zv[1] - bf16_hi_f(zh));
+        const int ib = q0 + hq * 16;
+        const int32_t* t32 = ts32_s + stage * BQ + hq * 16;
+        const int64_t* t64 = ts64_s + stage * BQ + hq * 16;
+        uint32_t ahi[8], alo[8], zhi[8], zlo[8];
+        const bool fast = cls == 2 && it.k0 + BK - 1 <= q0 && q0 + BQ <= kc.h_end;
+        if (!wide_ts) {
+          if (fast) grad16<true, false, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
+          else if (cls == 2) grad16<false, false, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
+          else grad16<false, false, true>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
+        } else {
+          if (cls == 2) grad16<false, true, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
+          else grad16<false, true, true>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
         }
-        if (want_rt && rt_cur >= 0) atomicAdd(drt + rt_cur, rt_run);
-        if (want_rp) {
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) rp_far += __shfl_xor_sync(0xffffffffu, rp_far, o);
-          if (lane == 0 && rp_far != 0.f) atomicAdd(drp + (P - 1), rp_far);
-        }
-        // A and dZ back into TMEM: hi at [32 hh, 32 hh + 16), lo at [32 hh + 16, 32 hh + 32)
-        tmem_st16(lane_base + S_COL + hh * 32, ahi);
-        tmem_st16(lane_base + S_COL + hh * 32 + 16, alo);
-        tmem_st16(lane_base + DA_COL + hh * 32, zhi);
-        tmem_st16(lane_base + DA_COL + hh * 32 + 16, zlo);
+        // A and dZ back into TMEM: quarter hq = columns [16 hq, 16 hq + 16): hi 8, lo 8
+        tmem_st8(lane_base + S_COL + hq * 16, ahi);
+        tmem_st8(lane_base + S_COL + hq * 16 + 8, alo);
+        tmem_st8(lane_base + DA_COL + hq * 16, zhi);
+        tmem_st8(lane_base + DA_COL + hq * 16 + 8, zlo);
         // dZ^T into SMEM (row = key, 64 queries = 128 B, 128-byte swizzle) for the dQ MMA
         {
           const uint32_t rowh = sDZ + (uint32_t)lrow * 128u, rowl = rowh + Lay::DZ_BYTES;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t chunk = (uint32_t)((hh * 4 + k) ^ (lrow & 7));
+          for (int k = 0; k < 2; ++k) {
+            const uint32_t chunk = (uint32_t)((hq * 2 + k) ^ (lrow & 7));
             st_shared_v4(rowh + chunk * 16, zhi[4 * k], zhi[4 * k + 1], zhi[4 * k + 2], zhi[4 * k + 3]);
             st_shared_v4(rowl + chunk * 16, zlo[4 * k], zlo[4 * k + 1], zlo[4 * k + 2], zlo[4 * k + 3]);
           }
@@ -420,67 +504,69 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_PREADY));
-        // dQ^T drain: lane = d, columns = 32 queries of this half
+        // dQ^T drain: lane = d, columns = the 16 queries of this quarter
         ok = mbar_wait(bar(BAR_DQFULL), qt_it & 1, wd, 30);
         if (!ok) break;
         fence_after_sync();
-        uint32_t qv[32];
-        tmem_ld32(lane_base + DQ_COL + hh * 32, qv);
+        uint32_t qv[16];
+        tmem_ld16(lane_base + DQ_COL + hq * 16, qv);
         tmem_wait_ld();
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_DQEMPTY));
         {
-          const int ib = q0 + hh * 32;
           float* dst = p.dq_acc + ((size_t)(it.s.s0 + ib) * H + it.h) * D + lrow;
           const size_t ld = (size_t)H * D;
+          const float alpha = p.alpha;
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (ib + c < n) atomicAdd(dst + c * ld, alpha * __uint_as_float(qv[c]));
+          for (int c = 0; c < 16; ++c)
+            if (ib + c < kc.n) atomicAdd(dst + c * ld, alpha * __uint_as_float(qv[c]));
         }
         ++qt_it;
       }
       if (!ok) break;
-      // dV, dK out: lane = key row, columns half hh of d
+      // dV, dK out: lane = key row, column quarter hq of d (32 columns each)
       ok = mbar_wait(bar(BAR_DKVFULL), item_it & 1, wd, 31);
       if (!ok) break;
       fence_after_sync();
-      const size_t g = ((size_t)(it.s.s0 + j) * H + it.h) * D + hh * 64;
-      TO* dvp = static_cast<TO*>(p.dv) + g;
-      TO* dkp = static_cast<TO*>(p.dk) + g;
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        const uint32_t col = (part == 0 ? DV_COL : DK_COL) + hh * 64;
-        TO* dst = part == 0 ? dvp : dkp;
-        const float scale = part == 0 ? 1.f : alpha;
-#pragma unroll
-        for (int c = 0; c < 64; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(lane_base + col + c, v);
-          tmem_wait_ld();
-          if (j_ok) {
-            if constexpr (sizeof(TO) == 4) {
-              float4* o4 = reinterpret_cast<float4*>(dst + c);
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                o4[e] = make_float4(scale * __uint_as_float(v[4 * e]), scale * __uint_as_float(v[4 * e + 1]),
-                                    scale * __uint_as_float(v[4 * e + 2]), scale * __uint_as_float(v[4 * e + 3]));
-            } else {
-              uint4* o4 = reinterpret_cast<uint4*>(dst + c);
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                o4[e] = make_uint4(
-                    pack_bf16(scale * __uint_as_float(v[8 * e]), scale * __uint_as_float(v[8 * e + 1])),
-                    pack_bf16(scale * __uint_as_float(v[8 * e + 2]), scale * __uint_as_float(v[8 * e + 3])),
-                    pack_bf16(scale * __uint_as_float(v[8 * e + 4]), scale * __uint_as_float(v[8 * e + 5])),
-                    pack_bf16(scale * __uint_as_float(v[8 * e + 6]), scale * __uint_as_float(v[8 * e + 7])));
-            }
-          }
-        }
-      }
+      uint32_t vv[32], kv[32];
+      tmem_ld32(lane_base + DV_COL + hq * 32, vv);
+      tmem_ld32(lane_base + DK_COL + hq * 32, kv);
+      tmem_wait_ld();
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_DKVEMPTY));
+      if (kc.j_ok) {
+        const size_t g = ((size_t)(it.s.s0 + kc.j) * H + it.h) * D + hq * 32;
+        TO* dvp = static_cast<TO*>(p.dv) + g;
+        TO* dkp = static_cast<TO*>(p.dk) + g;
+        const float alpha = p.alpha;
+        if constexpr (sizeof(TO) == 4) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            reinterpret_cast<float4*>(dvp)[e] =
+                make_float4(__uint_as_float(vv[4 * e]), __uint_as_float(vv[4 * e + 1]),
+                            __uint_as_float(vv[4 * e + 2]), __uint_as_float(vv[4 * e + 3]));
+            reinterpret_cast<float4*>(dkp)[e] =
+                make_float4(alpha * __uint_as_float(kv[4 * e]), alpha * __uint_as_float(kv[4 * e + 1]),
+                            alpha * __uint_as_float(kv[4 * e + 2]), alpha * __uint_as_float(kv[4 * e + 3]));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            reinterpret_cast<uint4*>(dvp)[e] =
+                make_uint4(pack_bf16(__uint_as_float(vv[8 * e]), __uint_as_float(vv[8 * e + 1])),
+                           pack_bf16(__uint_as_float(vv[8 * e + 2]), __uint_as_float(vv[8 * e + 3])),
+                           pack_bf16(__uint_as_float(vv[8 * e + 4]), __uint_as_float(vv[8 * e + 5])),
+                           pack_bf16(__uint_as_float(vv[8 * e + 6]), __uint_as_float(vv[8 * e + 7])));
+            reinterpret_cast<uint4*>(dkp)[e] =
+                make_uint4(pack_bf16(alpha * __uint_as_float(kv[8 * e]), alpha * __uint_as_float(kv[8 * e + 1])),
+                           pack_bf16(alpha * __uint_as_float(kv[8 * e + 2]), alpha * __uint_as_float(kv[8 * e + 3])),
+                           pack_bf16(alpha * __uint_as_float(kv[8 * e + 4]), alpha * __uint_as_float(kv[8 * e + 5])),
+                           pack_bf16(alpha * __uint_as_float(kv[8 * e + 6]), alpha * __uint_as_float(kv[8 * e + 7])));
+          }
+        }
+      }
       ++item_it;
     }
   }

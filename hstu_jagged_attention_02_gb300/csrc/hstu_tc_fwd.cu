@@ -16,9 +16,13 @@
 // P_hi V + P_lo V: one BF16 rounding of P alone costs ~1.5% of the output
 // RMS on heavy-tailed batches, the pair keeps ~16 bits.
 //
-// Roles (320 threads): warps 0-7 epilogue (warp w reads TMEM lanes
-// 32*(w%4).., columns half w/4 of each tile), warp 8 TMA producer (plus key
-// timestamps), warp 9 MMA issuer and TMEM owner.
+// Score arithmetic: with w = -log2(e) z, SiLU(z) / N = (w * c) / (1 + 2^w),
+// c = -1 / (log2(e) N); the bias tables are stored pre-multiplied by
+// -log2(e) so one FFMA gives w.
+//
+// Roles (576 threads): warps 0-15 epilogue (warp w reads TMEM lanes
+// 32*(w%4).. and the 32-column quarter w/4 of each tile), warp 16 TMA
+// producer (plus key timestamps), warp 17 MMA issuer and TMEM owner.
 // TMEM columns: S/P buffers at 0 and 128, O buffers at 256 and 256 + d.
 #include "hstu_internal.h"
 #include "tc_ptx.cuh"
@@ -30,9 +34,9 @@ namespace {
 using namespace tc;
 
 constexpr int BM = kTcTile, BN = kTcTile;
-constexpr int kEpiWarps = 8;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
-constexpr int kThreads = 10 * 32;
+constexpr int kEpiWarps = 16;
+constexpr int kProducerWarp = 16, kMmaWarp = 17;
+constexpr int kThreads = 18 * 32;
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSColStride = 128;  // S/P buffer sb starts at column sb * 128
@@ -50,19 +54,13 @@ struct Layout {
   static constexpr int K_BYTES = NCH * BOX;
   static constexpr int STAGE = 2 * K_BYTES;     // K then V
   static constexpr int KV_OFF = Q_OFF + NCH * BOX;
-  static constexpr int TS_OFF = KV_OFF + kStages * STAGE;       // int64 [kStages][BN]
-  static constexpr int BAR_OFF = TS_OFF + kStages * BN * 8;
+  static constexpr int TS64_OFF = KV_OFF + kStages * STAGE;     // int64 [kStages][BN] absolute
+  static constexpr int TS32_OFF = TS64_OFF + kStages * BN * 8;  // int32 [kStages][BN] relative
+  static constexpr int BAR_OFF = TS32_OFF + kStages * BN * 4;
   static constexpr int MISC_OFF = BAR_OFF + BAR_COUNT * 8;      // tmem slot, abort flag
   static constexpr int TAB_OFF = MISC_OFF + 16;                 // float [H][P + Tb]
   static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
 };
-
-__device__ __forceinline__ float fast_sigmoid(float z) {
-  float e, r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-z * kLog2e));
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
-  return r;
-}
 
 struct ItemInfo {
   int b, h, q0;
@@ -89,8 +87,90 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Per-thread row context of the epilogue (one query row i of the item).
+struct RowCtx {
+  int i, n, cx, h_end, pos_i, P, Tb;
+  bool row_ok;
+  int32_t ti32;      // timestamp relative to the sequence's first token
+  int64_t ti64;      // absolute timestamp
+  const float* tp;   // position table of the head (pre-scaled)
+  const float* tt;   // time table of the head (pre-scaled)
+  float kA, kC;      // -log2(e) alpha, -1 / (log2(e) N)
+};
+
+// Scores of 32 consecutive key columns jb.. of one row -> P_hi, P_lo packed
+// pairs.  FAST_POS: every column is a history/context token at or before the
+// row (position gap = pos_i - j >= 0).  WIDE: 64-bit timestamp gaps.
+// PARTIAL: evaluate the mask per element.
+template <bool FAST_POS, bool WIDE, bool PARTIAL>
+__device__ __forceinline__ void score32(const uint32_t (&sv)[32], uint32_t (&hi)[16], uint32_t (&lo)[16],
+                                        const RowCtx& rc, int jb, const int32_t* ts32, const int64_t* ts64) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    float bias[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int cc = half * 16 + c;
+      int bp;
+      if (FAST_POS) {
+        const int dp = rc.pos_i - (jb + cc);
+        bp = dp < rc.P - 1 ? dp : rc.P - 1;
+      } else {
+        const int j = jb + cc;
+        const int pj = j < rc.h_end ? j : rc.h_end;
+        int dp = rc.pos_i - pj;
+        dp = dp < 0 ? -dp : dp;
+        bp = dp < rc.P - 1 ? dp : rc.P - 1;
+      }
+      int bt;
+      if (WIDE) {
+        const int64_t tj = ts64[cc];
+        const uint64_t dt = rc.ti64 >= tj ? (uint64_t)(rc.ti64 - tj) : (uint64_t)(tj - rc.ti64);
+        bt = 64 - __clzll((long long)dt);
+      } else {
+        int d = rc.ti32 - ts32[cc];
+        d = d < 0 ? -d : d;
+        bt = 32 - __clz(d);
+      }
+      bt = bt < rc.Tb - 1 ? bt : rc.Tb - 1;
+      bias[c] = rc.tp[bp] + rc.tt[bt];
+    }
+#pragma unroll
+    for (int c = 0; c < 16; c += 2) {
+      float a2[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int cc = half * 16 + c + e;
+        const float w = fmaf(rc.kA, __uint_as_float(sv[cc]), bias[c + e]);
+        float a = (w * rc.kC) * rcp_approx(1.0f + ex2_approx(w));
+        if (PARTIAL) {
+          const int j = jb + cc;
+          const bool valid = rc.row_ok && j < rc.n && allowed(rc.i, j, rc.cx, rc.h_end);
+          a = valid ? a : 0.f;
+        }
+        a2[e] = a;
+      }
+      const uint32_t h2 = pack_bf16(a2[0], a2[1]);
+      hi[(half * 16 + c) >> 1] = h2;
+      lo[(half * 16 + c) >> 1] = pack_bf16(a2[0] - bf16_lo_f(h2), a2[1] - bf16_hi_f(h2));
+    }
+  }
+}
+
+// 18 warps x 32 threads x 112 registers = 64512 <= 65536
 template <int D, typename TO>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(112)
 hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   using L = Layout<D>;
@@ -100,7 +180,8 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
   const uint32_t sQ = base_u32 + L::Q_OFF;
   const uint32_t sKV = base_u32 + L::KV_OFF;
-  int64_t* ts_s = reinterpret_cast<int64_t*>(base + L::TS_OFF);
+  int64_t* ts64_s = reinterpret_cast<int64_t*>(base + L::TS64_OFF);
+  int32_t* ts32_s = reinterpret_cast<int32_t*>(base + L::TS32_OFF);
   const uint32_t bar0 = base_u32 + L::BAR_OFF;
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::MISC_OFF);
@@ -127,7 +208,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // bias tables of every head: [h][0, P) position, [h][P, P+Tb) time
+  // bias tables of every head, times -log2(e): [h][0, P) position, [h][P, P+Tb) time
   for (int x = threadIdx.x; x < H * PT; x += kThreads) {
     const int h = x / PT, e = x % PT;
     float v = 0.f;
@@ -136,7 +217,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     } else if (p.rab_time && p.ts) {
       v = p.rab_time[h * Tb + (e - P)];
     }
-    tab[x] = v;
+    tab[x] = -kLog2e * v;
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -158,6 +239,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   wd.err_info = p.hdr_rw + WS_ERR_INFO;
   wd.limit_ns = (p.flags & HSTU_FLAG_TEST_TIMEOUT) ? 1000000ull : 2000000000ull;
   const int nitems = p.hdr[WS_NBLK] * H;
+  const bool wide_ts = (p.hdr[WS_FLAGS] & WS_FLAG_WIDE_TS) != 0;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -167,6 +249,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     ItemInfo it;
     for (int r = 0; ok && item_of(p, r, nitems, it); ++r) {
       const int n = it.s.n;
+      const int64_t tbase = p.ts ? p.ts[it.s.s0] : 0;
       if (lane == 0) {
         ok = mbar_wait(bar(BAR_QEMPTY), (q_it & 1) ^ 1, wd, 1);
         if (ok) {
@@ -186,7 +269,9 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         if (!ok) break;
         for (int rr = lane; rr < BN; rr += 32) {
           const int row = k0 + rr;
-          ts_s[stage * BN + rr] = (p.ts && row < n) ? p.ts[it.s.s0 + row] : 0;
+          const int64_t t = (p.ts && row < n) ? p.ts[it.s.s0 + row] : tbase;
+          ts64_s[stage * BN + rr] = t;
+          ts32_s[stage * BN + rr] = (int32_t)(t - tbase);
         }
         __syncwarp();
         const bool withhold = (p.flags & HSTU_FLAG_TEST_TIMEOUT) && blockIdx.x == 0 && kv_it == 0;
@@ -228,6 +313,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         bool have_prev = false, first_pv = true;
         uint32_t prev_it = 0;
         const int nkb = fwd_kv_blocks(it.q0, n, it.s.c, BM, BN);
+        // P of tile t: quarter k/2 of the S buffer, hi at [32 q, 32 q + 16), lo 16 columns later
         auto issue_pv = [&](uint32_t t) -> bool {
           const uint32_t sb = t & 1, stage = t % kStages;
           if (!mbar_wait(bar(BAR_PREADY + sb), (t >> 1) & 1, wd, 5)) return false;
@@ -235,10 +321,10 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           const uint32_t vbase = sKV + stage * L::STAGE + L::K_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint32_t a_hi = tmem + (sb * kSColStride) + 64u * (kk >> 2) + 8u * (kk & 3);
+            const uint32_t a_hi = tmem + sb * kSColStride + 32u * (kk >> 1) + 8u * (kk & 1);
             const uint64_t bd = sdesc_sw128(vbase + kk * 2048, L::BOX, 1024);
             mma_ts(tmem + ocol, a_hi, bd, IDESC_PV, (first_pv && kk == 0) ? 0u : 1u);
-            mma_ts(tmem + ocol, a_hi + 32, bd, IDESC_PV, 1u);
+            mma_ts(tmem + ocol, a_hi + 16, bd, IDESC_PV, 1u);
           }
           first_pv = false;
           mma_commit(bar(BAR_KVEMPTY + stage));
@@ -255,7 +341,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * L::BOX + (kk & 3) * 32;
-            mma_ss(tmem + (sb * kSColStride), sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+            mma_ss(tmem + sb * kSColStride, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
                    IDESC_S, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(BAR_SFULL + sb));
@@ -277,69 +363,59 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int wq = warp & 3, hh = warp >> 2;
+    const int wq = warp & 3, hq = warp >> 2;      // TMEM lane quarter, column quarter
     const int row = wq * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
-    const float alpha = p.alpha, inv_n = p.inv_n;
     uint32_t kv_it = 0, o_it = 0;
     bool ok = true;
     ItemInfo it;
+    RowCtx rc;
+    rc.P = P;
+    rc.Tb = Tb;
+    rc.kA = -kLog2e * p.alpha;
+    rc.kC = -p.inv_n / kLog2e;
     for (int r = 0; ok && item_of(p, r, nitems, it); ++r) {
-      const int n = it.s.n, cx = it.s.c, h_end = it.s.h_end;
-      const int i = it.q0 + row;
-      const bool row_ok = i < n;
-      const int pos_i = i < h_end ? i : h_end;
-      const int64_t t_i = (p.ts && row_ok) ? p.ts[it.s.s0 + i] : 0;
-      const float* tp = tab + it.h * PT;
-      const float* tt = tp + P;
-      const int nkb = fwd_kv_blocks(it.q0, n, cx, BM, BN);
+      rc.n = it.s.n;
+      rc.cx = it.s.c;
+      rc.h_end = it.s.h_end;
+      rc.i = it.q0 + row;
+      rc.row_ok = rc.i < rc.n;
+      rc.pos_i = rc.i < rc.h_end ? rc.i : rc.h_end;
+      const int64_t tbase = p.ts ? p.ts[it.s.s0] : 0;
+      rc.ti64 = (p.ts && rc.row_ok) ? p.ts[it.s.s0 + rc.i] : tbase;
+      rc.ti32 = (int32_t)(rc.ti64 - tbase);
+      rc.tp = tab + it.h * PT;
+      rc.tt = rc.tp + P;
+      const int nkb = fwd_kv_blocks(it.q0, rc.n, rc.cx, BM, BN);
       for (int kb = 0; ok && kb < nkb; ++kb) {
         const int k0 = kb * BN;
-        const int cls = tile_class(it.q0, k0, BM, BN, n, cx, h_end);
+        const int cls = tile_class(it.q0, k0, BM, BN, rc.n, rc.cx, rc.h_end);
         if (cls == 0) continue;
         const uint32_t stage = kv_it % kStages, sb = kv_it & 1;
         ok = mbar_wait(bar(BAR_KVFULL + stage), (kv_it / kStages) & 1, wd, 7) &&
              mbar_wait(bar(BAR_SFULL + sb), (kv_it >> 1) & 1, wd, 8);
         if (!ok) break;
         fence_after_sync();
-        const uint32_t scol = lane_base + (sb * kSColStride) + hh * 64;
-        uint32_t sv[2][32];
-        tmem_ld32(scol, sv[0]);
-        tmem_ld32(scol + 32, sv[1]);
+        const uint32_t scol = lane_base + sb * kSColStride + hq * 32;
+        uint32_t sv[32];
+        tmem_ld32(scol, sv);
         tmem_wait_ld();
-        const int64_t* tsk = ts_s + stage * BN + hh * 64;
-        const int jb = k0 + hh * 64;
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          uint32_t hi[16], lo[16];
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float a2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int cc = ch * 32 + c + e;
-              const int j = jb + cc;
-              const int pj = j < h_end ? j : h_end;
-              int dp = pos_i - pj;
-              dp = dp < 0 ? -dp : dp;
-              const int bp = dp < P - 1 ? dp : P - 1;
-              const int64_t tj = tsk[cc];
-              const uint64_t dt = t_i >= tj ? (uint64_t)(t_i - tj) : (uint64_t)(tj - t_i);
-              int bt = 64 - __clzll((long long)dt);
-              bt = bt < Tb - 1 ? bt : Tb - 1;
-              const float z = fmaf(alpha, __uint_as_float(sv[ch][c + e]), tp[bp] + tt[bt]);
-              float a = z * fast_sigmoid(z) * inv_n;
-              const bool valid = cls == 2 || (row_ok && j < n && allowed(i, j, cx, h_end));
-              a2[e] = valid ? a : 0.f;
-            }
-            const uint32_t h2 = pack_bf16(a2[0], a2[1]);
-            hi[c >> 1] = h2;
-            lo[c >> 1] = pack_bf16(a2[0] - bf16_lo_f(h2), a2[1] - bf16_hi_f(h2));
-          }
-          // P_hi of this half at [64 hh, 64 hh + 32), P_lo at [64 hh + 32, 64 hh + 64)
-          tmem_st16(scol + ch * 16, hi);
-          tmem_st16(scol + 32 + ch * 16, lo);
+        const int jb = k0 + hq * 32;
+        const int32_t* t32 = ts32_s + stage * BN + hq * 32;
+        const int64_t* t64 = ts64_s + stage * BN + hq * 32;
+        uint32_t hi[16], lo[16];
+        const bool fast = cls == 2 && k0 + BN - 1 <= it.q0;
+        if (!wide_ts) {
+          if (fast) score32<true, false, false>(sv, hi, lo, rc, jb, t32, t64);
+          else if (cls == 2) score32<false, false, false>(sv, hi, lo, rc, jb, t32, t64);
+          else score32<false, false, true>(sv, hi, lo, rc, jb, t32, t64);
+        } else {
+          if (cls == 2) score32<false, true, false>(sv, hi, lo, rc, jb, t32, t64);
+          else score32<false, true, true>(sv, hi, lo, rc, jb, t32, t64);
         }
+        // P_hi of this quarter at [32 hq, 32 hq + 16), P_lo at [32 hq + 16, 32 hq + 32)
+        tmem_st16(scol, hi);
+        tmem_st16(scol + 16, lo);
         tmem_wait_st();
         fence_before_sync();
         __syncwarp();
@@ -347,39 +423,44 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         ++kv_it;
       }
       if (!ok) break;
-      // O out
+      // O out: this warp's lane quarter, column quarter hq of d
       const uint32_t ob = o_it & 1;
       ok = mbar_wait(bar(BAR_OFULL + ob), (o_it >> 1) & 1, wd, 9);
       if (!ok) break;
       fence_after_sync();
-      const uint32_t ocol = lane_base + (ob ? L::O_COL1 : L::O_COL0) + hh * (D / 2);
-      TO* orow = static_cast<TO*>(p.o) + ((size_t)(it.s.s0 + i) * H + it.h) * D + hh * (D / 2);
+      constexpr int QC = D / 4;  // columns per quarter
+      const uint32_t ocol = lane_base + (ob ? L::O_COL1 : L::O_COL0) + hq * QC;
+      uint32_t ov[32];
+      if constexpr (QC == 32) {
+        tmem_ld32(ocol, ov);
+      } else {
+        uint32_t o16[16];
+        tmem_ld16(ocol, o16);
 #pragma unroll
-      for (int c = 0; c < D / 2; c += 32) {
-        uint32_t ov[32];
-        tmem_ld32(ocol + c, ov);
-        tmem_wait_ld();
-        if (row_ok) {
-          if constexpr (sizeof(TO) == 4) {
-            float4* dst = reinterpret_cast<float4*>(orow + c);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              dst[e] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
-                                   __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]));
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              dst[e] = make_uint4(pack_bf16(__uint_as_float(ov[8 * e]), __uint_as_float(ov[8 * e + 1])),
-                                  pack_bf16(__uint_as_float(ov[8 * e + 2]), __uint_as_float(ov[8 * e + 3])),
-                                  pack_bf16(__uint_as_float(ov[8 * e + 4]), __uint_as_float(ov[8 * e + 5])),
-                                  pack_bf16(__uint_as_float(ov[8 * e + 6]), __uint_as_float(ov[8 * e + 7])));
-          }
-        }
+        for (int e = 0; e < 16; ++e) ov[e] = o16[e];
       }
+      tmem_wait_ld();
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_OEMPTY + ob));
+      if (rc.row_ok) {
+        TO* orow = static_cast<TO*>(p.o) + ((size_t)(it.s.s0 + rc.i) * H + it.h) * D + hq * QC;
+        if constexpr (sizeof(TO) == 4) {
+          float4* dst = reinterpret_cast<float4*>(orow);
+#pragma unroll
+          for (int e = 0; e < QC / 4; ++e)
+            dst[e] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                                 __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]));
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+          for (int e = 0; e < QC / 8; ++e)
+            dst[e] = make_uint4(pack_bf16(__uint_as_float(ov[8 * e]), __uint_as_float(ov[8 * e + 1])),
+                                pack_bf16(__uint_as_float(ov[8 * e + 2]), __uint_as_float(ov[8 * e + 3])),
+                                pack_bf16(__uint_as_float(ov[8 * e + 4]), __uint_as_float(ov[8 * e + 5])),
+                                pack_bf16(__uint_as_float(ov[8 * e + 6]), __uint_as_float(ov[8 * e + 7])));
+        }
+      }
       ++o_it;
     }
   }
