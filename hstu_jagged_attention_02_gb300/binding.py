@@ -48,7 +48,7 @@ class hstu_attn_bwd_args(ctypes.Structure):
 
 EXPORTED = ("hstu_attn_workspace_size", "hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_debug_plan",
             "hstu_get_device_error", "hstu_status_string", "hstu_last_launch_count",
-            "hstu_time_next_attention_kernel")
+            "hstu_time_next_attention_kernel", "hstu_last_error_detail")
 
 _lib = None
 
@@ -78,6 +78,7 @@ def load(build_if_missing: bool = True):
     L.hstu_last_launch_count.restype = ctypes.c_int32
     L.hstu_time_next_attention_kernel.argtypes = [_vp, _vp]
     L.hstu_time_next_attention_kernel.restype = ctypes.c_int
+    L.hstu_last_error_detail.restype = ctypes.c_char_p
     for name in ("hstu_attn_workspace_size", "hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_debug_plan",
                  "hstu_get_device_error"):
         getattr(L, name).restype = ctypes.c_int
@@ -88,7 +89,14 @@ def load(build_if_missing: bool = True):
 class HSTUError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {hstu_status_string(status)} (status {status})")
+        msg = f"{where}: {hstu_status_string(status)} (status {status})"
+        if status == HSTU_ERR_CUDA:
+            msg += f": {hstu_last_error_detail()}"
+        super().__init__(msg)
+
+
+def hstu_last_error_detail() -> str:
+    return load().hstu_last_error_detail().decode()
 
 
 def hstu_status_string(status: int) -> str:

@@ -2,6 +2,7 @@
 // argument checks, workspace layout, path selection and the stream-ordered
 // launch sequence of each pass.  No device memory is allocated here.
 #include <cmath>
+#include <cstdio>
 #include <cstring>
 
 #include "hstu_internal.h"
@@ -12,6 +13,10 @@ namespace {
 
 thread_local int32_t g_launches = 0;
 thread_local cudaEvent_t g_ev_start = nullptr, g_ev_stop = nullptr;
+thread_local char g_detail[320] = {0};
+
+bool detail_is_set() { return g_detail[0] != 0; }
+void clear_detail() { g_detail[0] = 0; }
 
 // Records the measurement-hook events around one launch, then clears them.
 struct KernelTimer {
@@ -129,15 +134,43 @@ PlanParams plan_params(const hstu_attn_desc* d, const int64_t* off, const int32_
   return p;
 }
 
-#define HSTU_CUDA_TRY(expr)                                   \
-  do {                                                        \
-    cudaError_t e_ = (expr);                                  \
-    if (e_ != cudaSuccess) { (void)cudaGetLastError(); return HSTU_ERR_CUDA; } \
+#define HSTU_CUDA_TRY(expr)                                    \
+  do {                                                         \
+    cudaError_t e_ = (expr);                                   \
+    if (e_ != cudaSuccess) {                                   \
+      (void)cudaGetLastError();                                \
+      if (!detail_is_set()) set_error_detail(e_, #expr);       \
+      return HSTU_ERR_CUDA;                                    \
+    }                                                          \
   } while (0)
 
 }  // namespace
 
+namespace hstu {
+
+void set_error_detail(cudaError_t e, const char* where) {
+  snprintf(g_detail, sizeof(g_detail), "%s in %s", cudaGetErrorName(e), where);
+}
+
+void set_launch_detail(cudaError_t e, const char* kernel, const void* func, int threads, size_t smem) {
+  cudaFuncAttributes fa{};
+  const cudaError_t ea = cudaFuncGetAttributes(&fa, func);
+  (void)cudaGetLastError();
+  if (ea == cudaSuccess)
+    snprintf(g_detail, sizeof(g_detail),
+             "%s launching %s: %d threads, %zu B dynamic smem; kernel uses %d registers, "
+             "allows %d threads per block, %zu B static smem",
+             cudaGetErrorName(e), kernel, threads, smem, fa.numRegs, fa.maxThreadsPerBlock, fa.sharedSizeBytes);
+  else
+    snprintf(g_detail, sizeof(g_detail), "%s launching %s (%d threads, %zu B smem)", cudaGetErrorName(e), kernel,
+             threads, smem);
+}
+
+}  // namespace hstu
+
 extern "C" {
+
+const char* hstu_last_error_detail(void) { return g_detail; }
 
 const char* hstu_status_string(hstu_status_t s) {
   switch (s) {
@@ -183,6 +216,7 @@ hstu_status_t hstu_attn_fwd(const hstu_attn_desc* d, const hstu_attn_fwd_args* a
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   g_launches = 0;
+  clear_detail();
 
   const bool tc = use_tc(d, false);
   const PlanParams pp =
@@ -239,6 +273,7 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   g_launches = 0;
+  clear_detail();
 
   const bool tc = use_tc(d, true);
   const PlanParams pp =

@@ -72,6 +72,11 @@ struct NormParams {
   float eps;
 };
 
+// Diagnostics behind HSTU_ERR_CUDA (read with hstu_last_error_detail):
+// the failing call, or the kernel launch with its resource attributes.
+void set_error_detail(cudaError_t e, const char* where);
+void set_launch_detail(cudaError_t e, const char* kernel, const void* func, int threads, size_t smem);
+
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 cudaError_t launch_debug_tiles(const PlanParams& p, int32_t* rec, int64_t cap, cudaStream_t stream);
 

@@ -116,18 +116,19 @@ struct KeyCtx {
   float kA, kC, kZ, inv_n;  // -log2(e) alpha, -1/(log2(e) N), -1/log2(e), 1/N
 };
 
-// 16 query columns ib.. of one key row: A and dZ as packed BF16 hi/lo pairs,
+// NC query columns ib.. of one key row: A and dZ as packed BF16 hi/lo pairs,
 // plus the d_rab contributions.  FAST_POS: every column is a history/context
 // query at or after the key (position gap = i - j).  WIDE: 64-bit gaps.
 // PARTIAL: evaluate the mask per element.
-template <bool FAST_POS, bool WIDE, bool PARTIAL>
-__device__ __forceinline__ void grad16(const uint32_t (&sv)[16], const uint32_t (&dav)[16], uint32_t (&ahi)[8],
-                                       uint32_t (&alo)[8], uint32_t (&zhi)[8], uint32_t (&zlo)[8],
-                                       const KeyCtx& kc, int ib, const int32_t* ts32, const int64_t* ts64) {
-  float bias[16];
-  int bps[16], bts[16];
+template <int NC, bool FAST_POS, bool WIDE, bool PARTIAL>
+__device__ __forceinline__ void grad_cols(const uint32_t (&sv)[NC], const uint32_t (&dav)[NC],
+                                          uint32_t (&ahi)[NC / 2], uint32_t (&alo)[NC / 2], uint32_t (&zhi)[NC / 2],
+                                          uint32_t (&zlo)[NC / 2], const KeyCtx& kc, int ib, const int32_t* ts32,
+                                          const int64_t* ts64) {
+  float bias[NC];
+  int bps[NC], bts[NC];
 #pragma unroll
-  for (int c = 0; c < 16; ++c) {
+  for (int c = 0; c < NC; ++c) {
     int bp;
     if (FAST_POS) {
       const int dp = ib + c - kc.j;
@@ -157,7 +158,7 @@ __device__ __forceinline__ void grad16(const uint32_t (&sv)[16], const uint32_t 
   float rp_far = 0.f, rt_run = 0.f;
   int rt_cur = -1;
 #pragma unroll
-  for (int c = 0; c < 16; c += 2) {
+  for (int c = 0; c < NC; c += 2) {
     float av[2], zv[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -208,9 +209,10 @@ __device__ __forceinline__ void grad16(const uint32_t (&sv)[16], const uint32_t 
   }
 }
 
-// 18 warps x 32 threads x 112 registers = 64512 <= 65536
+// Registers go to a block in groups of 4 warps: 18 warps are charged as 20,
+// and 20 x 32 threads x 96 registers = 61440 <= 65536.
 template <typename TO>
-__global__ void __maxnreg__(112)
+__global__ void __maxnreg__(96)
 hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                    const __grid_constant__ CUtensorMap tmdh, const __grid_constant__ CUtensorMap tmdl) {
@@ -467,37 +469,46 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
              mbar_wait(bar(BAR_SFULL), qt_it & 1, wd, 29);
         if (!ok) break;
         fence_after_sync();
-        uint32_t sv[16], dav[16];
-        tmem_ld16(lane_base + S_COL + hq * 16, sv);
-        tmem_ld16(lane_base + DA_COL + hq * 16, dav);
-        tmem_wait_ld();
-        const int ib = q0 + hq * 16;
-        const int32_t* t32 = ts32_s + stage * BQ + hq * 16;
-        const int64_t* t64 = ts64_s + stage * BQ + hq * 16;
-        uint32_t ahi[8], alo[8], zhi[8], zlo[8];
         const bool fast = cls == 2 && it.k0 + BK - 1 <= q0 && q0 + BQ <= kc.h_end;
-        if (!wide_ts) {
-          if (fast) grad16<true, false, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
-          else if (cls == 2) grad16<false, false, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
-          else grad16<false, false, true>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
-        } else {
-          if (cls == 2) grad16<false, true, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
-          else grad16<false, true, true>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
-        }
-        // A and dZ back into TMEM: quarter hq = columns [16 hq, 16 hq + 16): hi 8, lo 8
-        tmem_st8(lane_base + S_COL + hq * 16, ahi);
-        tmem_st8(lane_base + S_COL + hq * 16 + 8, alo);
-        tmem_st8(lane_base + DA_COL + hq * 16, zhi);
-        tmem_st8(lane_base + DA_COL + hq * 16 + 8, zlo);
-        // dZ^T into SMEM (row = key, 64 queries = 128 B, 128-byte swizzle) for the dQ MMA
-        {
-          const uint32_t rowh = sDZ + (uint32_t)lrow * 128u, rowl = rowh + Lay::DZ_BYTES;
+        // all 16 columns of the quarter are read before any is overwritten
+        uint32_t svq[16], daq[16];
+        tmem_ld16(lane_base + S_COL + hq * 16, svq);
+        tmem_ld16(lane_base + DA_COL + hq * 16, daq);
+        tmem_wait_ld();
+        // then computed and written back in two halves of 8 (register budget)
 #pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const uint32_t chunk = (uint32_t)((hq * 2 + k) ^ (lrow & 7));
-            st_shared_v4(rowh + chunk * 16, zhi[4 * k], zhi[4 * k + 1], zhi[4 * k + 2], zhi[4 * k + 3]);
-            st_shared_v4(rowl + chunk * 16, zlo[4 * k], zlo[4 * k + 1], zlo[4 * k + 2], zlo[4 * k + 3]);
+        for (int half = 0; half < 2; ++half) {
+          const int c0 = hq * 16 + half * 8;    // first query column of this half within the tile
+          uint32_t sv[8], dav[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            sv[e] = svq[half * 8 + e];
+            dav[e] = daq[half * 8 + e];
           }
+          const int ib = q0 + c0;
+          const int32_t* t32 = ts32_s + stage * BQ + c0;
+          const int64_t* t64 = ts64_s + stage * BQ + c0;
+          uint32_t ahi[4], alo[4], zhi[4], zlo[4];
+          if (!wide_ts) {
+            if (fast) grad_cols<8, true, false, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
+            else if (cls == 2) grad_cols<8, false, false, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
+            else grad_cols<8, false, false, true>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
+          } else {
+            if (cls == 2) grad_cols<8, false, true, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
+            else grad_cols<8, false, true, true>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
+          }
+          // A and dZ back into TMEM.  Quarter hq owns columns [16 hq, 16 hq + 16):
+          // hi pairs in the first 8, lo pairs in the last 8; this half's 8
+          // queries are 4 packed columns of each.
+          tmem_st4(lane_base + S_COL + hq * 16 + half * 4, ahi);
+          tmem_st4(lane_base + S_COL + hq * 16 + 8 + half * 4, alo);
+          tmem_st4(lane_base + DA_COL + hq * 16 + half * 4, zhi);
+          tmem_st4(lane_base + DA_COL + hq * 16 + 8 + half * 4, zlo);
+          // dZ^T into SMEM (row = key, 64 queries = 128 B, 128-byte swizzle) for the dQ MMA
+          const uint32_t rowh = sDZ + (uint32_t)lrow * 128u, rowl = rowh + Lay::DZ_BYTES;
+          const uint32_t chunk = (uint32_t)((hq * 2 + half) ^ (lrow & 7));
+          st_shared_v4(rowh + chunk * 16, zhi[0], zhi[1], zhi[2], zhi[3]);
+          st_shared_v4(rowl + chunk * 16, zlo[0], zlo[1], zlo[2], zlo[3]);
         }
         fence_async_smem();
         tmem_wait_st();
@@ -515,6 +526,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_DQEMPTY));
         {
+          const int ib = q0 + hq * 16;
           float* dst = p.dq_acc + ((size_t)(it.s.s0 + ib) * H + it.h) * D + lrow;
           const size_t ld = (size_t)H * D;
           const float alpha = p.alpha;
@@ -599,13 +611,19 @@ cudaError_t launch_t(const AttnParams& p, cudaStream_t st) {
       !make_tmap_bf16(&mdl, dl, p.T, cols, BQ))
     return cudaErrorInvalidValue;
   const size_t smem = tc_bwd_smem_bytes(p.H, p.P, p.Tb);
+  const void* fn = reinterpret_cast<const void*>(hstu_bwd_tc_kernel<TO>);
   cudaError_t e = cudaFuncSetAttribute(hstu_bwd_tc_kernel<TO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess) {
+    set_launch_detail(e, "hstu_bwd_tc_kernel (smem attribute)", fn, kThreads, smem);
+    return e;
+  }
   const int64_t max_items = ((p.T + BK - 1) / BK + p.B) * (int64_t)p.H;
   const int grid = (int)(max_items < p.num_sms ? max_items : p.num_sms);
   hstu_bwd_tc_kernel<TO><<<grid, kThreads, smem, st>>>(p, mq, mk, mv, mdh, mdl);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) set_launch_detail(e, "hstu_bwd_tc_kernel", fn, kThreads, smem);
+  return e;
 }
 
 }  // namespace

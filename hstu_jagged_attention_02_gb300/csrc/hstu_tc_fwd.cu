@@ -168,9 +168,10 @@ __device__ __forceinline__ void score32(const uint32_t (&sv)[32], uint32_t (&hi)
   }
 }
 
-// 18 warps x 32 threads x 112 registers = 64512 <= 65536
+// Registers go to a block in groups of 4 warps: 18 warps are charged as 20,
+// and 20 x 32 threads x 96 registers = 61440 <= 65536.
 template <int D, typename TO>
-__global__ void __maxnreg__(112)
+__global__ void __maxnreg__(96)
 hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   using L = Layout<D>;
@@ -522,13 +523,19 @@ static cudaError_t launch_fwd_t(const AttnParams& p, cudaStream_t st) {
       !make_tmap_bf16(&mv, p.v, p.T, cols, BN))
     return cudaErrorInvalidValue;
   const size_t smem = tc_fwd_smem_bytes(D, p.H, p.P, p.Tb);
+  const void* fn = reinterpret_cast<const void*>(hstu_fwd_tc_kernel<D, TO>);
   cudaError_t e = cudaFuncSetAttribute(hstu_fwd_tc_kernel<D, TO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess) {
+    set_launch_detail(e, "hstu_fwd_tc_kernel (smem attribute)", fn, kThreads, smem);
+    return e;
+  }
   const int64_t max_items = ((p.T + BM - 1) / BM + p.B) * (int64_t)p.H;
   const int grid = (int)(max_items < p.num_sms ? max_items : p.num_sms);
   hstu_fwd_tc_kernel<D, TO><<<grid, kThreads, smem, st>>>(p, mq, mk, mv);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) set_launch_detail(e, "hstu_fwd_tc_kernel", fn, kThreads, smem);
+  return e;
 }
 
 cudaError_t launch_tc_fwd(const AttnParams& p, cudaStream_t st) {

@@ -174,6 +174,13 @@ hstu_status_t hstu_get_device_error(const void* workspace, hstu_stream_t stream,
 /* Static string for a status code. */
 const char* hstu_status_string(hstu_status_t status);
 
+/* After HSTU_ERR_CUDA: the failing CUDA call of the last call on this thread,
+ * by name, or the kernel launch with its resource attributes (registers,
+ * threads per block, shared memory).  Empty when the last call did not fail
+ * in CUDA.  The string belongs to the library and lives until the next call
+ * on this thread. */
+const char* hstu_last_error_detail(void);
+
 /* Number of kernels the last successful hstu_attn_fwd / hstu_attn_bwd call on
  * this thread launched (for launch accounting). */
 int32_t hstu_last_launch_count(void);
