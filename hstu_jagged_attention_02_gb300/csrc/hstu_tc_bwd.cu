@@ -116,15 +116,31 @@ struct KeyCtx {
   float kA, kC, kZ, inv_n;  // -log2(e) alpha, -1/(log2(e) N), -1/log2(e), 1/N
 };
 
+// d_rab partial sums one epilogue thread carries.  A thread owns one key row
+// j and sees that row's query columns i in increasing order over the whole
+// work item, so:
+//  - the clamped position bucket (far from the diagonal) sums in rp_far;
+//  - the time bucket changes only where |t_i - t_j| crosses a power of two,
+//    so a run sum (rt_cur, rt_run) rarely has to be flushed;
+//  - on causal full tiles the position bucket is i - j, constant along
+//    diagonals: diag holds the running sum of the diagonal this lane sits on,
+//    passed one lane up per column, and flushed when it leaves the warp.
+struct RabAcc {
+  float rp_far, diag, rt_run;
+  int rt_cur;
+};
+
 // NC query columns ib.. of one key row: A and dZ as packed BF16 hi/lo pairs,
 // plus the d_rab contributions.  FAST_POS: every column is a history/context
-// query at or after the key (position gap = i - j).  WIDE: 64-bit gaps.
-// PARTIAL: evaluate the mask per element.
+// query at or after the key (position gap = i - j); cg0 is the index of the
+// first column in the warp's 16-column sweep and kbase the gap of lane 0 at
+// sweep column 0.  WIDE: 64-bit gaps.  PARTIAL: evaluate the mask per element.
 template <int NC, bool FAST_POS, bool WIDE, bool PARTIAL>
 __device__ __forceinline__ void grad_cols(const uint32_t (&sv)[NC], const uint32_t (&dav)[NC],
                                           uint32_t (&ahi)[NC / 2], uint32_t (&alo)[NC / 2], uint32_t (&zhi)[NC / 2],
                                           uint32_t (&zlo)[NC / 2], const KeyCtx& kc, int ib, const int32_t* ts32,
-                                          const int64_t* ts64) {
+                                          const int64_t* ts64, RabAcc& acc, int cg0, int kbase) {
+  const int lane = threadIdx.x & 31;
   float bias[NC];
   int bps[NC], bts[NC];
 #pragma unroll
@@ -155,8 +171,6 @@ __device__ __forceinline__ void grad_cols(const uint32_t (&sv)[NC], const uint32
     bts[c] = bt;
     bias[c] = kc.tp[bp] + kc.tt[bt];
   }
-  float rp_far = 0.f, rt_run = 0.f;
-  int rt_cur = -1;
 #pragma unroll
   for (int c = 0; c < NC; c += 2) {
     float av[2], zv[2];
@@ -176,21 +190,30 @@ __device__ __forceinline__ void grad_cols(const uint32_t (&sv)[NC], const uint32
       }
       av[e] = a;
       zv[e] = dz;
-      if (valid) {
-        // d_rab: the clamped position bucket in a register, the time bucket
-        // run-length along the row
-        if (kc.want_rp) {
-          if (bps[c + e] == kc.P - 1) rp_far += dz;
+      if (kc.want_rp) {
+        if (FAST_POS) {
+          const int cg = cg0 + c + e;
+          if (cg > 0) {
+            // the diagonal held by lane 31 is complete: flush it, shift the rest up
+            const int key_out = kbase + (cg - 1) - 31;
+            if (lane == 31 && acc.diag != 0.f && key_out < kc.P - 1) atomicAdd(kc.drp + key_out, acc.diag);
+            acc.diag = __shfl_up_sync(0xffffffffu, acc.diag, 1);
+            if (lane == 0) acc.diag = 0.f;
+          }
+          if (bps[c + e] < kc.P - 1) acc.diag += dz;
+          else acc.rp_far += dz;
+        } else if (valid) {
+          if (bps[c + e] == kc.P - 1) acc.rp_far += dz;
           else atomicAdd(kc.drp + bps[c + e], dz);
         }
-        if (kc.want_rt) {
-          if (bts[c + e] == rt_cur) {
-            rt_run += dz;
-          } else {
-            if (rt_cur >= 0) atomicAdd(kc.drt + rt_cur, rt_run);
-            rt_cur = bts[c + e];
-            rt_run = dz;
-          }
+      }
+      if (kc.want_rt && valid) {
+        if (bts[c + e] == acc.rt_cur) {
+          acc.rt_run += dz;
+        } else {
+          if (acc.rt_cur >= 0) atomicAdd(kc.drt + acc.rt_cur, acc.rt_run);
+          acc.rt_cur = bts[c + e];
+          acc.rt_run = dz;
         }
       }
     }
@@ -200,12 +223,6 @@ __device__ __forceinline__ void grad_cols(const uint32_t (&sv)[NC], const uint32
     alo[c >> 1] = pack_bf16(av[0] - bf16_lo_f(ah), av[1] - bf16_hi_f(ah));
     zhi[c >> 1] = zh;
     zlo[c >> 1] = pack_bf16(zv[0] - bf16_lo_f(zh), zv[1] - bf16_hi_f(zh));
-  }
-  if (kc.want_rt && rt_cur >= 0) atomicAdd(kc.drt + rt_cur, rt_run);
-  if (kc.want_rp) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) rp_far += __shfl_xor_sync(0xffffffffu, rp_far, o);
-    if ((threadIdx.x & 31) == 0 && rp_far != 0.f) atomicAdd(kc.drp + (kc.P - 1), rp_far);
   }
 }
 
@@ -316,13 +333,19 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         const int q0 = qt * BQ;
         if (tile_class(q0, it.k0, BQ, BK, n, it.s.c, it.s.h_end) == 0) continue;
         const int stage = qt_it % kQStages;
+        // query timestamps: loads issued before waiting for the stage, stored after
+        int64_t tv[BQ / 32];
+#pragma unroll
+        for (int x = 0; x < BQ / 32; ++x) {
+          const int row = q0 + lane + 32 * x;
+          tv[x] = (p.ts && row < n) ? p.ts[it.s.s0 + row] : tbase;
+        }
         ok = mbar_wait(bar(BAR_QEMPTY + stage), ((qt_it / kQStages) & 1) ^ 1, wd, 22);
         if (!ok) break;
-        for (int rr = lane; rr < BQ; rr += 32) {
-          const int row = q0 + rr;
-          const int64_t t = (p.ts && row < n) ? p.ts[it.s.s0 + row] : tbase;
-          ts64_s[stage * BQ + rr] = t;
-          ts32_s[stage * BQ + rr] = (int32_t)(t - tbase);
+#pragma unroll
+        for (int x = 0; x < BQ / 32; ++x) {
+          ts64_s[stage * BQ + lane + 32 * x] = tv[x];
+          ts32_s[stage * BQ + lane + 32 * x] = (int32_t)(tv[x] - tbase);
         }
         __syncwarp();
         if (lane == 0) {
@@ -459,6 +482,9 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       kc.tt = kc.tp + P;
       kc.drp = drab + it.h * PT;
       kc.drt = kc.drp + P;
+      RabAcc racc;
+      racc.rp_far = racc.diag = racc.rt_run = 0.f;
+      racc.rt_cur = -1;
       const int nqt = (kc.n + BQ - 1) / BQ;
       for (int qt = bwd_q_begin(it.k0, kc.cx, BQ); ok && qt < nqt; ++qt) {
         const int q0 = qt * BQ;
@@ -470,6 +496,8 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         if (!ok) break;
         fence_after_sync();
         const bool fast = cls == 2 && it.k0 + BK - 1 <= q0 && q0 + BQ <= kc.h_end;
+        // position gap of lane 0 at this warp's first query column (causal full tiles)
+        const int kbase = (q0 + hq * 16) - (it.k0 + wq * 32);
         // all 16 columns of the quarter are read before any is overwritten
         uint32_t svq[16], daq[16];
         tmem_ld16(lane_base + S_COL + hq * 16, svq);
@@ -490,12 +518,12 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           const int64_t* t64 = ts64_s + stage * BQ + c0;
           uint32_t ahi[4], alo[4], zhi[4], zlo[4];
           if (!wide_ts) {
-            if (fast) grad_cols<8, true, false, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
-            else if (cls == 2) grad_cols<8, false, false, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
-            else grad_cols<8, false, false, true>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
+            if (fast) grad_cols<8, true, false, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc, half * 8, kbase);
+            else if (cls == 2) grad_cols<8, false, false, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc, half * 8, kbase);
+            else grad_cols<8, false, false, true>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc, half * 8, kbase);
           } else {
-            if (cls == 2) grad_cols<8, false, true, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
-            else grad_cols<8, false, true, true>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64);
+            if (cls == 2) grad_cols<8, false, true, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc, half * 8, kbase);
+            else grad_cols<8, false, true, true>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc, half * 8, kbase);
           }
           // A and dZ back into TMEM.  Quarter hq owns columns [16 hq, 16 hq + 16):
           // hi pairs in the first 8, lo pairs in the last 8; this half's 8
@@ -509,6 +537,11 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           const uint32_t chunk = (uint32_t)((hq * 2 + half) ^ (lrow & 7));
           st_shared_v4(rowh + chunk * 16, zhi[0], zhi[1], zhi[2], zhi[3]);
           st_shared_v4(rowl + chunk * 16, zlo[0], zlo[1], zlo[2], zlo[3]);
+        }
+        if (fast && kc.want_rp) {  // diagonals still held at the end of the 16-column sweep
+          const int key = kbase + 15 - lane;
+          if (racc.diag != 0.f && key < P - 1) atomicAdd(kc.drp + key, racc.diag);
+          racc.diag = 0.f;
         }
         fence_async_smem();
         tmem_wait_st();
@@ -537,6 +570,13 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         ++qt_it;
       }
       if (!ok) break;
+      // the item's remaining d_rab partial sums
+      if (want_rt && racc.rt_cur >= 0) atomicAdd(kc.drt + racc.rt_cur, racc.rt_run);
+      if (want_rp) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) racc.rp_far += __shfl_xor_sync(0xffffffffu, racc.rp_far, o);
+        if (lane == 0 && racc.rp_far != 0.f) atomicAdd(kc.drp + (P - 1), racc.rp_far);
+      }
       // dV, dK out: lane = key row, column quarter hq of d (32 columns each)
       ok = mbar_wait(bar(BAR_DKVFULL), item_it & 1, wd, 31);
       if (!ok) break;

@@ -266,13 +266,19 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         const int k0 = kb * BN;
         if (tile_class(it.q0, k0, BM, BN, n, it.s.c, it.s.h_end) == 0) continue;
         const int stage = kv_it % kStages;
+        // key timestamps: loads issued before waiting for the stage, stored after
+        int64_t tv[BN / 32];
+#pragma unroll
+        for (int x = 0; x < BN / 32; ++x) {
+          const int row = k0 + lane + 32 * x;
+          tv[x] = (p.ts && row < n) ? p.ts[it.s.s0 + row] : tbase;
+        }
         ok = mbar_wait(bar(BAR_KVEMPTY + stage), ((kv_it / kStages) & 1) ^ 1, wd, 2);
         if (!ok) break;
-        for (int rr = lane; rr < BN; rr += 32) {
-          const int row = k0 + rr;
-          const int64_t t = (p.ts && row < n) ? p.ts[it.s.s0 + row] : tbase;
-          ts64_s[stage * BN + rr] = t;
-          ts32_s[stage * BN + rr] = (int32_t)(t - tbase);
+#pragma unroll
+        for (int x = 0; x < BN / 32; ++x) {
+          ts64_s[stage * BN + lane + 32 * x] = tv[x];
+          ts32_s[stage * BN + lane + 32 * x] = (int32_t)(tv[x] - tbase);
         }
         __syncwarp();
         const bool withhold = (p.flags & HSTU_FLAG_TEST_TIMEOUT) && blockIdx.x == 0 && kv_it == 0;
