@@ -48,7 +48,7 @@ class hstu_attn_bwd_args(ctypes.Structure):
 
 EXPORTED = ("hstu_attn_workspace_size", "hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_debug_plan",
             "hstu_get_device_error", "hstu_status_string", "hstu_last_launch_count",
-            "hstu_time_next_attention_kernel", "hstu_last_error_detail")
+            "hstu_time_next_attention_kernel", "hstu_last_error_detail", "hstu_attn_fwd_noalloc")
 
 _lib = None
 
@@ -79,6 +79,8 @@ def load(build_if_missing: bool = True):
     L.hstu_time_next_attention_kernel.argtypes = [_vp, _vp]
     L.hstu_time_next_attention_kernel.restype = ctypes.c_int
     L.hstu_last_error_detail.restype = ctypes.c_char_p
+    L.hstu_attn_fwd_noalloc.argtypes = [P(hstu_attn_desc), P(hstu_attn_fwd_args), _vp, P(ctypes.c_int32)]
+    L.hstu_attn_fwd_noalloc.restype = ctypes.c_int
     for name in ("hstu_attn_workspace_size", "hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_debug_plan",
                  "hstu_get_device_error"):
         getattr(L, name).restype = ctypes.c_int
@@ -144,6 +146,17 @@ def hstu_attn_fwd(desc, args, workspace: int, workspace_bytes: int, stream: int)
 def hstu_attn_bwd(desc, args, workspace: int, workspace_bytes: int, stream: int):
     _check(load().hstu_attn_bwd(ctypes.byref(desc), ctypes.byref(args), workspace, workspace_bytes,
                                 stream), "hstu_attn_bwd")
+
+
+def hstu_attn_fwd_noalloc(desc, args, stream: int, want_device_error: bool = True) -> Optional[int]:
+    """The forward with the library's built-in scratch buffer (no workspace).
+    Returns the device error code when want_device_error (the call then
+    synchronises the stream), else None."""
+    code = ctypes.c_int32(-1)
+    _check(load().hstu_attn_fwd_noalloc(ctypes.byref(desc), ctypes.byref(args), stream,
+                                        ctypes.byref(code) if want_device_error else None),
+           "hstu_attn_fwd_noalloc")
+    return int(code.value) if want_device_error else None
 
 
 def hstu_get_device_error(workspace: int, stream: int) -> int:

@@ -152,6 +152,8 @@ void set_error_detail(cudaError_t e, const char* where) {
   snprintf(g_detail, sizeof(g_detail), "%s in %s", cudaGetErrorName(e), where);
 }
 
+void set_detail_message(const char* msg) { snprintf(g_detail, sizeof(g_detail), "%s", msg); }
+
 void set_launch_detail(cudaError_t e, const char* kernel, const void* func, int threads, size_t smem) {
   cudaFuncAttributes fa{};
   const cudaError_t ea = cudaFuncGetAttributes(&fa, func);

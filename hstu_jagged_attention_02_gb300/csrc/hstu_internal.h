@@ -76,6 +76,7 @@ struct NormParams {
 // the failing call, or the kernel launch with its resource attributes.
 void set_error_detail(cudaError_t e, const char* where);
 void set_launch_detail(cudaError_t e, const char* kernel, const void* func, int threads, size_t smem);
+void set_detail_message(const char* msg);
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 cudaError_t launch_debug_tiles(const PlanParams& p, int32_t* rec, int64_t cap, cudaStream_t stream);

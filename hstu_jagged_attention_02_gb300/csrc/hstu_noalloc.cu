@@ -1,0 +1,69 @@
+// Forward entry point for callers that cannot allocate device memory.
+//
+// Some callers of this library are not allowed to call cudaMalloc: a host
+// framework that owns every byte of device memory through its own pool, a
+// serving process whose latency budget cannot absorb an allocation (which can
+// synchronise the device), or an integration that simply has no allocator to
+// hand.  hstu_attn_fwd_noalloc takes the forward pass's scratch (the tile
+// plan: workspace header, per-sequence block starts, block lists) from a
+// fixed buffer compiled into the library instead of a caller workspace.
+//
+// The buffer is a file-scope __device__ array of kScratchBytes; every GPU that
+// loads the library holds it until the process exits.  Host code cannot hand
+// the array's name to a kernel (on the host it is only a stand-in, not a
+// device address), so the first call on each device looks its device address
+// up with cudaGetSymbolAddress while that device is current.
+#include <cstdio>
+#include <mutex>
+
+#include "hstu_internal.h"
+
+static constexpr size_t kScratchBytes = size_t(1) << 20;  // 1 MiB
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+namespace {
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {};  // per device
+
+}  // namespace
+
+extern "C" hstu_status_t hstu_attn_fwd_noalloc(const hstu_attn_desc* desc, const hstu_attn_fwd_args* args,
+                                               hstu_stream_t stream, int32_t* host_device_error) {
+  size_t need = 0;
+  hstu_status_t s = hstu_attn_workspace_size(desc, &need, nullptr);
+  if (s != HSTU_OK) return s;
+  if (need > kScratchBytes) {
+    char msg[160];
+    snprintf(msg, sizeof(msg), "this problem needs %zu bytes of forward scratch; the built-in buffer holds %zu",
+             need, kScratchBytes);
+    hstu::set_detail_message(msg);
+    return HSTU_ERR_WORKSPACE;
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    return HSTU_ERR_CUDA;
+  }
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+      void* ptr = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+      if (e != cudaSuccess || ptr == nullptr) {
+        (void)cudaGetLastError();
+        hstu::set_error_detail(e, "cudaGetSymbolAddress of the built-in forward scratch");
+        return HSTU_ERR_CUDA;
+      }
+      g_scratch_addr[dev] = ptr;
+    }
+    scratch = g_scratch_addr[dev];
+  }
+  // The planner rewrites the whole plan region, header first, on every call,
+  // so nothing left by an earlier call is read.
+  s = hstu_attn_fwd(desc, args, scratch, kScratchBytes, stream);
+  if (s != HSTU_OK || host_device_error == nullptr) return s;
+  return hstu_get_device_error(scratch, stream, host_device_error);
+}

@@ -167,6 +167,34 @@ hstu_status_t hstu_attn_debug_plan(const hstu_attn_desc* desc, const int64_t* se
                                    void* workspace, size_t workspace_bytes, int32_t* host_tiles,
                                    int64_t host_capacity, int64_t* n_tiles, hstu_stream_t stream);
 
+/* Forward without a caller workspace, for callers that are not allowed to
+ * allocate device memory (a framework that owns all device memory through its
+ * own pool, a latency-bound server that cannot afford an allocation, an
+ * integration with no allocator at hand).  The pages describe no counterpart;
+ * this is a library convenience.
+ *
+ * Same operation, arguments and outputs as hstu_attn_fwd; the caller still
+ * passes every input and output buffer.  The scratch comes from a 1 MiB
+ * buffer built into the library (every GPU that loads the library holds it
+ * until the process exits).  The plan of T tokens in B sequences needs
+ * 256 + 4 (B + 1) + 32 (ceil(T / 32) + B) bytes (each part rounded up to
+ * 256), roughly T + 36 B + 1 KiB, which must fit in 1 MiB: e.g. 500,000
+ * tokens in 10,000 sequences.  Larger problems return HSTU_ERR_WORKSPACE
+ * (hstu_last_error_detail says how much was needed) without launching.
+ *
+ * The first call on each device looks up the buffer's device address with
+ * that device current, so make that first call before any stream capture.
+ * Every call shares the one buffer: calls that may overlap on the GPU (other
+ * streams, other host threads) race and must be serialised by the caller.
+ * The buffer keeps the last call's contents; the planner rewrites everything
+ * it reads on every call.
+ *
+ * host_device_error: NULL, or a host int32 that receives the call's device
+ * error code (as hstu_get_device_error reports it); non-NULL makes the call
+ * synchronise the stream. */
+hstu_status_t hstu_attn_fwd_noalloc(const hstu_attn_desc* desc, const hstu_attn_fwd_args* args,
+                                    hstu_stream_t stream, int32_t* host_device_error);
+
 /* Reads the device error word of the last call that used this workspace
  * (HSTU_OK when none).  Synchronises the stream. */
 hstu_status_t hstu_get_device_error(const void* workspace, hstu_stream_t stream, int32_t* code);
