@@ -284,7 +284,10 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
   ++g_launches;
 
   const size_t rows = (size_t)d->total_tokens * (size_t)d->H;
-  float* dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
+  // dq is reduced in FP32: straight into the output when it is FP32, else in
+  // the workspace and converted at the end
+  const bool dq_direct = d->out_dtype == HSTU_FP32;
+  float* dq_acc = dq_direct ? static_cast<float*>(a->dq) : reinterpret_cast<float*>(ws + L.dq_acc);
   const bool has_rp = a->rab_pos != nullptr;
   const bool has_rt = a->rab_time != nullptr && a->timestamps != nullptr;
   if (a->d_rab_pos) HSTU_CUDA_TRY(cudaMemsetAsync(a->d_rab_pos, 0, sizeof(float) * d->H * d->num_pos_buckets, st));
@@ -327,8 +330,10 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
     }
   }
   ++g_launches;
-  HSTU_CUDA_TRY(launch_convert_f32(dq_acc, a->dq, (int64_t)(rows * d->d_qk), d->out_dtype, st));
-  ++g_launches;
+  if (!dq_direct) {
+    HSTU_CUDA_TRY(launch_convert_f32(dq_acc, a->dq, (int64_t)(rows * d->d_qk), d->out_dtype, st));
+    ++g_launches;
+  }
   return HSTU_OK;
 }
 

@@ -6,6 +6,10 @@
 // Element types: u has the input type TI; o, y, dy and du have the output
 // type TO.  The backward's dO (an input of the attention backward) is FP32, or
 // a BF16 hi/lo pair for the tensor-core path.
+//
+// Lane l of the warp owns features (r * 32 + l) * VEC + [0, VEC) for
+// r < PER: with VEC = 4 every access is a 16-byte (FP32) or 8-byte (BF16)
+// vector and a warp touches 512 / 256 contiguous bytes per access.
 #include "hstu_internal.h"
 
 namespace hstu {
@@ -20,25 +24,62 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// mean and 1/sqrt(var + eps) of the PER*32-strided row held in x (lanes own
-// features f = r*32 + lane, f < F)
-template <int PER>
-__device__ __forceinline__ void row_stats(const float* x, int F, float eps, float& mean, float& rstd) {
+template <int VEC> struct Vec;
+template <> struct Vec<1> {
+  template <typename T> __device__ static void load(const T* p, float* v) { v[0] = to_f(p[0]); }
+  template <typename T> __device__ static void store(T* p, const float* v) { p[0] = from_f<T>(v[0]); }
+};
+template <> struct Vec<4> {
+  __device__ static void load(const float* p, float* v) {
+    const float4 x = *reinterpret_cast<const float4*>(p);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  }
+  __device__ static void load(const __nv_bfloat16* p, float* v) {
+    const uint2 x = *reinterpret_cast<const uint2*>(p);
+    v[0] = __uint_as_float(x.x << 16); v[1] = __uint_as_float(x.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(x.y << 16); v[3] = __uint_as_float(x.y & 0xFFFF0000u);
+  }
+  __device__ static void store(float* p, const float* v) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+  __device__ static void store(__nv_bfloat16* p, const float* v) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+    uint2 x;
+    x.x = *reinterpret_cast<const uint32_t*>(&a);
+    x.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = x;
+  }
+};
+
+// feature index of element e of chunk r of this lane
+template <int VEC>
+__device__ __forceinline__ int feat(int r, int lane) { return (r * 32 + lane) * VEC; }
+
+// mean and 1/sqrt(var + eps) of the row held in x (PER chunks of VEC values)
+template <int VEC, int PER>
+__device__ __forceinline__ void row_stats(const float (&x)[PER][VEC], int F, float eps, float& mean, float& rstd) {
   const int lane = threadIdx.x & 31;
   float s = 0.f;
 #pragma unroll
-  for (int r = 0; r < PER; ++r) s += x[r];
+  for (int r = 0; r < PER; ++r)
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) s += x[r][e];
   mean = warp_sum(s) / F;
   float v = 0.f;
 #pragma unroll
   for (int r = 0; r < PER; ++r) {
-    const float d = (r * 32 + lane) < F ? x[r] - mean : 0.f;
-    v += d * d;
+    if (feat<VEC>(r, lane) < F) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const float d = x[r][e] - mean;
+        v += d * d;
+      }
+    }
   }
   rstd = rsqrtf(warp_sum(v) / F + eps);
 }
 
-template <typename TI, typename TO, int PER>
+template <typename TI, typename TO, int VEC, int PER>
 __global__ void __launch_bounds__(kWarps * 32) norm_gate_fwd_kernel(NormParams p) {
   const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (t >= p.T) return;
@@ -46,23 +87,31 @@ __global__ void __launch_bounds__(kWarps * 32) norm_gate_fwd_kernel(NormParams p
   const int F = p.F;
   const TO* o = static_cast<const TO*>(p.o) + t * F;
   const TI* u = p.u ? static_cast<const TI*>(p.u) + t * F : nullptr;
-  float x[PER];
+  float x[PER][VEC];
 #pragma unroll
   for (int r = 0; r < PER; ++r) {
-    const int f = r * 32 + lane;
-    x[r] = f < F ? to_f(o[f]) : 0.f;
+    const int f = feat<VEC>(r, lane);
+    if (f < F) Vec<VEC>::load(o + f, x[r]);
+    else
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) x[r][e] = 0.f;
   }
   float mean = 0.f, rstd = 1.f;
-  if (p.norm == HSTU_NORM_LAYERNORM) row_stats<PER>(x, F, p.eps, mean, rstd);
+  if (p.norm == HSTU_NORM_LAYERNORM) row_stats<VEC, PER>(x, F, p.eps, mean, rstd);
   if (p.y) {
     TO* y = static_cast<TO*>(p.y) + t * F;
 #pragma unroll
     for (int r = 0; r < PER; ++r) {
-      const int f = r * 32 + lane;
-      if (f < F) {
-        const float xn = (x[r] - mean) * rstd;
-        y[f] = from_f<TO>(u ? xn * to_f(u[f]) : xn);
-      }
+      const int f = feat<VEC>(r, lane);
+      if (f >= F) continue;
+      float g[VEC], out[VEC];
+      if (u) Vec<VEC>::load(u + f, g);
+      else
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) g[e] = 1.f;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) out[e] = (x[r][e] - mean) * rstd * g[e];
+      Vec<VEC>::store(y + f, out);
     }
   }
   if (lane == 0) {
@@ -72,7 +121,7 @@ __global__ void __launch_bounds__(kWarps * 32) norm_gate_fwd_kernel(NormParams p
 }
 
 // du = xn * dy;  g = dy * u;  LayerNorm: dO = rstd * (g - mean(g) - xn * mean(g xn)); none: dO = g
-template <typename TI, typename TO, int PER>
+template <typename TI, typename TO, int VEC, int PER>
 __global__ void __launch_bounds__(kWarps * 32) norm_gate_bwd_kernel(NormParams p) {
   const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (t >= p.T) return;
@@ -81,55 +130,65 @@ __global__ void __launch_bounds__(kWarps * 32) norm_gate_bwd_kernel(NormParams p
   const TO* o = static_cast<const TO*>(p.o) + t * F;
   const TI* u = p.u ? static_cast<const TI*>(p.u) + t * F : nullptr;
   const TO* dy = static_cast<const TO*>(p.dy) + t * F;
-  float x[PER], g[PER];
+  float x[PER][VEC], g[PER][VEC];
 #pragma unroll
   for (int r = 0; r < PER; ++r) {
-    const int f = r * 32 + lane;
-    x[r] = f < F ? to_f(o[f]) : 0.f;
+    const int f = feat<VEC>(r, lane);
+    if (f < F) Vec<VEC>::load(o + f, x[r]);
+    else
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) x[r][e] = 0.f;
   }
   float mean = 0.f, rstd = 1.f;
   const bool ln = p.norm == HSTU_NORM_LAYERNORM;
-  if (ln) row_stats<PER>(x, F, p.eps, mean, rstd);
+  if (ln) row_stats<VEC, PER>(x, F, p.eps, mean, rstd);
   float mg = 0.f, mgx = 0.f;
   TO* du = p.du ? static_cast<TO*>(p.du) + t * F : nullptr;
 #pragma unroll
   for (int r = 0; r < PER; ++r) {
-    const int f = r * 32 + lane;
-    float gg = 0.f;
-    if (f < F) {
-      const float xn = (x[r] - mean) * rstd;
-      const float d = to_f(dy[f]);
-      gg = u ? d * to_f(u[f]) : d;
-      if (du) du[f] = from_f<TO>(xn * d);
+    const int f = feat<VEC>(r, lane);
+    if (f >= F) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) g[r][e] = 0.f;
+      continue;
+    }
+    float d[VEC], uu[VEC], dun[VEC];
+    Vec<VEC>::load(dy + f, d);
+    if (u) Vec<VEC>::load(u + f, uu);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      const float xn = (x[r][e] - mean) * rstd;
+      const float gg = u ? d[e] * uu[e] : d[e];
+      dun[e] = xn * d[e];
       mg += gg;
       mgx += gg * xn;
-      x[r] = xn;
+      x[r][e] = xn;
+      g[r][e] = gg;
     }
-    g[r] = gg;
+    if (du) Vec<VEC>::store(du + f, dun);
   }
   if (ln) {
     mg = warp_sum(mg) / F;
     mgx = warp_sum(mgx) / F;
   }
-  if (p.split) {  // BF16 pair: hi = bf16(x), lo = bf16(x - hi)
-    __nv_bfloat16* hi = static_cast<__nv_bfloat16*>(p.dO) + t * F;
-    __nv_bfloat16* lo = static_cast<__nv_bfloat16*>(p.dO_lo) + t * F;
 #pragma unroll
-    for (int r = 0; r < PER; ++r) {
-      const int f = r * 32 + lane;
-      if (f < F) {
-        const float val = ln ? rstd * (g[r] - mg - x[r] * mgx) : g[r];
-        const __nv_bfloat16 h = __float2bfloat16_rn(val);
-        hi[f] = h;
-        lo[f] = __float2bfloat16_rn(val - __bfloat162float(h));
+  for (int r = 0; r < PER; ++r) {
+    const int f = feat<VEC>(r, lane);
+    if (f >= F) continue;
+    float val[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) val[e] = ln ? rstd * (g[r][e] - mg - x[r][e] * mgx) : g[r][e];
+    if (p.split) {  // BF16 pair: hi = bf16(x), lo = bf16(x - hi)
+      float hi[VEC], lo[VEC];
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        hi[e] = __bfloat162float(__float2bfloat16_rn(val[e]));
+        lo[e] = val[e] - hi[e];
       }
-    }
-  } else {
-    float* dO = static_cast<float*>(p.dO) + t * F;
-#pragma unroll
-    for (int r = 0; r < PER; ++r) {
-      const int f = r * 32 + lane;
-      if (f < F) dO[f] = ln ? rstd * (g[r] - mg - x[r] * mgx) : g[r];
+      Vec<VEC>::store(static_cast<__nv_bfloat16*>(p.dO) + t * F + f, hi);
+      Vec<VEC>::store(static_cast<__nv_bfloat16*>(p.dO_lo) + t * F + f, lo);
+    } else {
+      Vec<VEC>::store(static_cast<float*>(p.dO) + t * F + f, val);
     }
   }
 }
@@ -141,25 +200,33 @@ __global__ void convert_kernel(const float* __restrict__ src, TO* __restrict__ d
     dst[i] = from_f<TO>(src[i]);
 }
 
-template <typename TI, typename TO, int PER>
+template <typename TI, typename TO, int VEC, int PER>
 cudaError_t launch_t(const NormParams& p, bool bwd, cudaStream_t st) {
   const int64_t grid = (p.T + kWarps - 1) / kWarps;
   if (bwd)
-    norm_gate_bwd_kernel<TI, TO, PER><<<(unsigned)grid, kWarps * 32, 0, st>>>(p);
+    norm_gate_bwd_kernel<TI, TO, VEC, PER><<<(unsigned)grid, kWarps * 32, 0, st>>>(p);
   else
-    norm_gate_fwd_kernel<TI, TO, PER><<<(unsigned)grid, kWarps * 32, 0, st>>>(p);
+    norm_gate_fwd_kernel<TI, TO, VEC, PER><<<(unsigned)grid, kWarps * 32, 0, st>>>(p);
   return cudaGetLastError();
 }
 
 template <typename TI, typename TO>
 cudaError_t by_width(const NormParams& p, bool bwd, cudaStream_t st) {
+  if (p.F % 128 == 0) {  // 4-wide vectors
+    const int per = p.F / 128;
+    if (per <= 1) return launch_t<TI, TO, 4, 1>(p, bwd, st);
+    if (per <= 2) return launch_t<TI, TO, 4, 2>(p, bwd, st);
+    if (per <= 4) return launch_t<TI, TO, 4, 4>(p, bwd, st);
+    if (per <= 8) return launch_t<TI, TO, 4, 8>(p, bwd, st);
+    return launch_t<TI, TO, 4, 16>(p, bwd, st);
+  }
   const int per = (p.F + 31) / 32;
-  if (per <= 2) return launch_t<TI, TO, 2>(p, bwd, st);
-  if (per <= 4) return launch_t<TI, TO, 4>(p, bwd, st);
-  if (per <= 8) return launch_t<TI, TO, 8>(p, bwd, st);
-  if (per <= 16) return launch_t<TI, TO, 16>(p, bwd, st);
-  if (per <= 32) return launch_t<TI, TO, 32>(p, bwd, st);
-  return launch_t<TI, TO, 64>(p, bwd, st);
+  if (per <= 2) return launch_t<TI, TO, 1, 2>(p, bwd, st);
+  if (per <= 4) return launch_t<TI, TO, 1, 4>(p, bwd, st);
+  if (per <= 8) return launch_t<TI, TO, 1, 8>(p, bwd, st);
+  if (per <= 16) return launch_t<TI, TO, 1, 16>(p, bwd, st);
+  if (per <= 32) return launch_t<TI, TO, 1, 32>(p, bwd, st);
+  return launch_t<TI, TO, 1, 64>(p, bwd, st);
 }
 
 cudaError_t dispatch(const NormParams& p, bool bwd, cudaStream_t st) {

@@ -81,18 +81,19 @@ plan_kernel(PlanParams p) {
   // 1b. can every timestamp be held relative to its sequence's first token in
   // 31 bits (so gaps fit in 32)?  Otherwise the kernels take their 64-bit path.
   if (p.ts) {
-    const int warp = t >> 5, lane = t & 31;
+    // token-parallel: each thread finds its token's sequence by binary search
+    // (the last b with off[b] <= token, which skips empty sequences)
     int wide = 0;
-    for (int b = warp; b < p.B; b += kPlanThreads / 32) {
-      const int64_t s0 = p.off[b], n = p.off[b + 1] - s0;
-      if (n == 0) continue;
-      const int64_t base = p.ts[s0];
-      for (int64_t i = lane; i < n; i += 32) {
-        const int64_t d = p.ts[s0 + i] - base;
-        wide |= (d >= (int64_t)1 << 30 || d < -((int64_t)1 << 30));
+    for (int64_t tok = t; tok < p.T; tok += kPlanThreads) {
+      int lo = 0, hi = p.B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.off[mid] <= tok) lo = mid; else hi = mid - 1;
       }
+      const int64_t d = p.ts[tok] - p.ts[p.off[lo]];
+      wide |= (d >= (int64_t)1 << 30 || d < -((int64_t)1 << 30));
     }
-    if (__any_sync(0xffffffffu, wide) && lane == 0) atomicOr(p.hdr + WS_FLAGS, WS_FLAG_WIDE_TS);
+    if (__syncthreads_or(wide) && t == 0) atomicOr(p.hdr + WS_FLAGS, WS_FLAG_WIDE_TS);
   }
 
   // 2. blocks per sequence -> exclusive prefix (seq_start[b]), chunked scan
