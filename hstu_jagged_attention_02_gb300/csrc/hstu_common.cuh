@@ -12,7 +12,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/hstu_attn.h"
+#include "hstu_attn.h"  // include/ is on the include path
 
 namespace hstu {
 
