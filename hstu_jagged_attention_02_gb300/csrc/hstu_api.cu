@@ -35,7 +35,7 @@ size_t align_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
 size_t esize(int dtype) { return dtype == HSTU_BF16 ? 2 : 4; }
 
 struct WsLayout {
-  size_t seq_start, tmp, blocks, plan_end, dO, dq_acc, total;
+  size_t seq_start, tmp, blocks, plan_end, dO, dq_acc, drab_part, drab_part_bytes, total;
   int cap_blocks;
 };
 
@@ -52,6 +52,8 @@ WsLayout ws_layout(const hstu_attn_desc* d, bool bwd) {
     const size_t rows = (size_t)d->total_tokens * (size_t)d->H;
     L.dO = off;     off = align_up(off + sizeof(float) * rows * (size_t)d->d_v);  // FP32 or a BF16 pair
     L.dq_acc = off; off = align_up(off + sizeof(float) * rows * (size_t)d->d_qk);
+    L.drab_part_bytes = sizeof(float) * kDrabMaxCtas * (size_t)d->H * (d->num_pos_buckets + d->num_time_buckets);
+    L.drab_part = off; off = align_up(off + L.drab_part_bytes);
   }
   L.total = off;
   return L;
@@ -294,6 +296,9 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
   if (a->d_rab_time) HSTU_CUDA_TRY(cudaMemsetAsync(a->d_rab_time, 0, sizeof(float) * d->H * d->num_time_buckets, st));
   if (d->total_tokens == 0) return HSTU_OK;
   HSTU_CUDA_TRY(cudaMemsetAsync(dq_acc, 0, sizeof(float) * rows * d->d_qk, st));
+  float* drab_partial = reinterpret_cast<float*>(ws + L.drab_part);
+  if (tc && ((has_rp && a->d_rab_pos) || (has_rt && a->d_rab_time)))
+    HSTU_CUDA_TRY(cudaMemsetAsync(drab_partial, 0, L.drab_part_bytes, st));
 
   // gradient w.r.t. o, in the input type (an MMA operand of the attention backward)
   {
@@ -314,6 +319,7 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
   p.q = a->q; p.k = a->k; p.v = a->v; p.dO = dO; p.dk = a->dk; p.dv = a->dv; p.dq_acc = dq_acc;
   p.d_rab_pos = has_rp ? a->d_rab_pos : nullptr;
   p.d_rab_time = has_rt ? a->d_rab_time : nullptr;
+  p.drab_partial = drab_partial;
   p.hdr = pp.hdr; p.hdr_rw = pp.hdr; p.blocks = pp.blocks;
   p.B = d->B; p.H = d->H; p.dqk = d->d_qk; p.dv_dim = d->d_v; p.T = d->total_tokens;
   p.dtype = d->dtype; p.out_dtype = d->out_dtype;
@@ -323,7 +329,7 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
   {
     KernelTimer timer(st);
     if (tc) {
-      HSTU_CUDA_TRY(launch_tc_bwd(p, st));
+      HSTU_CUDA_TRY(launch_tc_bwd(p, st));  // includes the d_rab partial-sum reduction
     } else {
       const int max_items = ((int)((d->total_tokens + kSimtTile - 1) / kSimtTile) + d->B) * d->H;
       HSTU_CUDA_TRY(launch_simt_bwd(p, max_items, st));

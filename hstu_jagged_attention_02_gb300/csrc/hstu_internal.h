@@ -42,6 +42,7 @@ struct AttnParams {
   float* dq_acc;         // backward: FP32 accumulator [T,H,dqk], zeroed before
   float* d_rab_pos;      // backward: [H,P] accumulated (zeroed before), or NULL
   float* d_rab_time;
+  float* drab_partial;   // tensor-core backward: [kDrabMaxCtas][H][P+Tb] zeroed partial sums
   const int* hdr;        // workspace header (block count)
   int* hdr_rw;           // same, writable (error word)
   const Block* blocks;
@@ -95,6 +96,7 @@ cudaError_t launch_convert_f32(const float* src, void* dst, int64_t count, int d
 // backward d = 128 on 64 (query) x 128 (key) tiles
 constexpr int kTcTile = 128;
 constexpr int kTcBwdQTile = 64;
+constexpr int kDrabMaxCtas = 256;  // tensor-core backward grid cap (one d_rab partial row each)
 bool make_tmap_bf16(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_rows);
 size_t tc_bwd_smem_bytes(int H, int P, int Tb);
 bool tc_fwd_supported(int dtype, int dqk, int dv);

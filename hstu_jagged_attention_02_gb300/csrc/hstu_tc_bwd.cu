@@ -12,7 +12,7 @@
 //   dV  += A^T dO                         (A from TMEM as hi/lo pair)
 //   dK  += dZ^T Q                         (dZ from TMEM as hi/lo pair)
 //   dQ^T = K^T dZ^T                       (both MN-major in SMEM) -> FP32 red
-//   d_rab[bucket] += dZ                   (shared-memory accumulators)
+//   d_rab[bucket] += dZ                   (per-CTA partial sums, summed after)
 // Every derived operand (dO, A, dZ) enters the tensor core as a BF16 pair
 // x = hi + lo; a single BF16 rounding of any of them costs ~1.5% of the
 // output RMS on heavy-tailed batches.
@@ -57,7 +57,7 @@ struct Lay {
   static constexpr int TS32_OFF = TS64_OFF + kQStages * BQ * 8;  // int32 [kQStages][BQ] relative
   static constexpr int BAR_OFF = TS32_OFF + kQStages * BQ * 4;
   static constexpr int MISC_OFF = BAR_OFF + BAR_COUNT * 8;
-  static constexpr int TAB_OFF = MISC_OFF + 16;              // float [H][P+Tb] bias, then [H][P+Tb] d_rab
+  static constexpr int TAB_OFF = MISC_OFF + 16;              // float [H][P+Tb] bias
 };
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -73,6 +73,13 @@ __device__ __forceinline__ float rcp_approx(float x) {
 
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Fire-and-forget global float add when pred holds (no branch, no return value).
+__device__ __forceinline__ void red_add(float* addr, float v, bool pred) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t@p red.global.add.f32 [%0], %1;\n\t}" ::"l"(addr),
+               "f"(v), "r"((int)pred)
+               : "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -111,7 +118,7 @@ struct KeyCtx {
   int64_t tj64;
   const float* tp;   // position table of the head (times -log2 e)
   const float* tt;   // time table of the head (times -log2 e)
-  float* drp;        // shared d_rab accumulators of the head
+  float* drp;        // this CTA's d_rab partial sums of the head (global, private to the CTA)
   float* drt;
   float kA, kC, kZ, inv_n;  // -log2(e) alpha, -1/(log2(e) N), -1/log2(e), 1/N
 };
@@ -196,7 +203,7 @@ __device__ __forceinline__ void grad_cols(const uint32_t (&sv)[NC], const uint32
           if (cg > 0) {
             // the diagonal held by lane 31 is complete: flush it, shift the rest up
             const int key_out = kbase + (cg - 1) - 31;
-            if (lane == 31 && acc.diag != 0.f && key_out < kc.P - 1) atomicAdd(kc.drp + key_out, acc.diag);
+            red_add(kc.drp + key_out, acc.diag, lane == 31 && acc.diag != 0.f && key_out < kc.P - 1);
             acc.diag = __shfl_up_sync(0xffffffffu, acc.diag, 1);
             if (lane == 0) acc.diag = 0.f;
           }
@@ -204,14 +211,14 @@ __device__ __forceinline__ void grad_cols(const uint32_t (&sv)[NC], const uint32
           else acc.rp_far += dz;
         } else if (valid) {
           if (bps[c + e] == kc.P - 1) acc.rp_far += dz;
-          else atomicAdd(kc.drp + bps[c + e], dz);
+          else red_add(kc.drp + bps[c + e], dz, true);
         }
       }
       if (kc.want_rt && valid) {
         if (bts[c + e] == acc.rt_cur) {
           acc.rt_run += dz;
         } else {
-          if (acc.rt_cur >= 0) atomicAdd(kc.drt + acc.rt_cur, acc.rt_run);
+          red_add(kc.drt + acc.rt_cur, acc.rt_run, acc.rt_cur >= 0);
           acc.rt_cur = bts[c + e];
           acc.rt_run = dz;
         }
@@ -247,7 +254,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + Lay::MISC_OFF + 4);
   const int H = p.H, P = p.P, Tb = p.Tb, PT = p.P + p.Tb;
   float* tab = reinterpret_cast<float*>(base + Lay::TAB_OFF);
-  float* drab = tab + H * PT;
+  float* drab = p.drab_partial + (size_t)blockIdx.x * H * PT;  // this CTA's partial sums
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool has_rp = p.rab_pos != nullptr, has_rt = p.rab_time != nullptr && p.ts != nullptr;
@@ -279,7 +286,6 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       v = p.rab_time[h * Tb + (e - P)];
     }
     tab[x] = -kLog2e * v;
-    drab[x] = 0.f;
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -540,7 +546,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         }
         if (fast && kc.want_rp) {  // diagonals still held at the end of the 16-column sweep
           const int key = kbase + 15 - lane;
-          if (racc.diag != 0.f && key < P - 1) atomicAdd(kc.drp + key, racc.diag);
+          red_add(kc.drp + key, racc.diag, racc.diag != 0.f && key < P - 1);
           racc.diag = 0.f;
         }
         fence_async_smem();
@@ -571,11 +577,11 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       }
       if (!ok) break;
       // the item's remaining d_rab partial sums
-      if (want_rt && racc.rt_cur >= 0) atomicAdd(kc.drt + racc.rt_cur, racc.rt_run);
+      red_add(kc.drt + racc.rt_cur, racc.rt_run, want_rt && racc.rt_cur >= 0);
       if (want_rp) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) racc.rp_far += __shfl_xor_sync(0xffffffffu, racc.rp_far, o);
-        if (lane == 0 && racc.rp_far != 0.f) atomicAdd(kc.drp + (P - 1), racc.rp_far);
+        red_add(kc.drp + (P - 1), racc.rp_far, lane == 0 && racc.rp_far != 0.f);
       }
       // dV, dK out: lane = key row, column quarter hq of d (32 columns each)
       ok = mbar_wait(bar(BAR_DKVFULL), item_it & 1, wd, 31);
@@ -627,16 +633,21 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   __syncthreads();
   fence_after_sync();
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
-  // flush the per-CTA d_rab partial sums
-  for (int x = threadIdx.x; x < H * PT; x += kThreads) {
-    const float v = drab[x];
-    if (v == 0.f) continue;
-    const int h = x / PT, e = x % PT;
-    if (e < P) {
-      if (want_rp) atomicAdd(p.d_rab_pos + h * P + e, v);
-    } else if (want_rt) {
-      atomicAdd(p.d_rab_time + h * Tb + (e - P), v);
-    }
+}
+
+// d_rab_pos[h][b] / d_rab_time[h][b] = sum over CTAs of their partial sums.
+__global__ void drab_reduce_kernel(const float* __restrict__ partial, int nctas, int H, int P, int Tb,
+                                   float* d_rab_pos, float* d_rab_time) {
+  const int PT = P + Tb;
+  const int x = blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= H * PT) return;
+  float s = 0.f;
+  for (int c = 0; c < nctas; ++c) s += partial[(size_t)c * H * PT + x];
+  const int h = x / PT, e = x % PT;
+  if (e < P) {
+    if (d_rab_pos) d_rab_pos[h * P + e] = s;
+  } else if (d_rab_time) {
+    d_rab_time[h * Tb + (e - P)] = s;
   }
 }
 
@@ -659,10 +670,21 @@ cudaError_t launch_t(const AttnParams& p, cudaStream_t st) {
     return e;
   }
   const int64_t max_items = ((p.T + BK - 1) / BK + p.B) * (int64_t)p.H;
-  const int grid = (int)(max_items < p.num_sms ? max_items : p.num_sms);
+  int grid = (int)(max_items < p.num_sms ? max_items : p.num_sms);
+  if (grid > kDrabMaxCtas) grid = kDrabMaxCtas;  // one d_rab partial row per CTA
   hstu_bwd_tc_kernel<TO><<<grid, kThreads, smem, st>>>(p, mq, mk, mv, mdh, mdl);
   e = cudaGetLastError();
-  if (e != cudaSuccess) set_launch_detail(e, "hstu_bwd_tc_kernel", fn, kThreads, smem);
+  if (e != cudaSuccess) {
+    set_launch_detail(e, "hstu_bwd_tc_kernel", fn, kThreads, smem);
+    return e;
+  }
+  // d_rab = sum of the CTAs' partial sums (overwrites the outputs)
+  const int entries = p.H * (p.P + p.Tb);
+  if (p.d_rab_pos || p.d_rab_time) {
+    drab_reduce_kernel<<<(entries + 255) / 256, 256, 0, st>>>(p.drab_partial, grid, p.H, p.P, p.Tb,
+                                                              p.d_rab_pos, p.d_rab_time);
+    e = cudaGetLastError();
+  }
   return e;
 }
 
@@ -671,7 +693,7 @@ cudaError_t launch_t(const AttnParams& p, cudaStream_t st) {
 bool tc_bwd_supported(int dtype, int dqk, int dv) { return dtype == HSTU_BF16 && dqk == D && dv == D; }
 
 size_t tc_bwd_smem_bytes(int H, int P, int Tb) {
-  return Lay::TAB_OFF + 2 * sizeof(float) * (size_t)H * (P + Tb) + 1024;
+  return Lay::TAB_OFF + sizeof(float) * (size_t)H * (P + Tb) + 1024;
 }
 
 cudaError_t launch_tc_bwd(const AttnParams& p, cudaStream_t st) {
