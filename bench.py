@@ -39,6 +39,8 @@ WORKLOAD = ("heavy_tailed: 64 jagged sequences, Zipf(1.2) history lengths on [1,
             "stochastic-length sampling + 32 candidates, 4 heads x 128, BF16 in / FP32 out, "
             "causal + candidate mask, position + time rab, forward + backward")
 N_SEEDS = 16
+# algorithmic DRAM bytes per (token, head, dim) of each attention kernel, BF16 in / FP32 out
+KERNEL_BYTES_PER_ELEM = {"fwd": 3 * 2 + 4, "bwd": 3 * 2 + 2 * 2 + 3 * 4}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -299,16 +301,32 @@ def run_gpu(args, rank, world, local_rank):
     dom = "bwd" if bwd_total >= fwd_total else "fwd"
     dom_ms = bwd_ms if dom == "bwd" else fwd_ms
     dom_flops = [f[1] if dom == "bwd" else f[0] for f in step_flops]
-    achieved = sum(dom_flops) / (sum(dom_ms) * 1e-3) / 1e12
     peak_sust = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     peak_burst = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    peak_bw = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    # algorithmic bytes of the kernel per launch: forward reads q, k, v (BF16) and
+    # writes o (FP32); backward reads q, k, v and dO as a BF16 pair and writes dk,
+    # dv and the dq reduction (FP32)
+    per_elem = KERNEL_BYTES_PER_ELEM[dom]
+    dom_bytes = [per_elem * batches[k % N_SEEDS].T * batches[0].H * batches[0].d_qk for k in range(args.steps)]
+    secs = sum(dom_ms) * 1e-3
+    t_tensor = sum(dom_flops) / (peak_sust * 1e12)
+    t_hbm = sum(dom_bytes) / (peak_bw * 1e9)
     tr = traffic_record(dom)
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_sust, "unit": "TFLOP/s",
-                "frac": achieved / peak_sust, "traffic": tr["dram_bytes_per_launch"] if tr else None,
-                "kernel": f"attention {dom} kernel",
-                "peak_source": f"{pk_kind} bf16_tflops_sustained (kernel timed inside the step loop)",
-                "avg_launch_ms": sum(dom_ms) / len(dom_ms),
-                "share_of_step": sum(dom_ms) / elapsed_ms}
+    common = {"traffic": tr["dram_bytes_per_launch"] if tr else None, "kernel": f"attention {dom} kernel",
+              "avg_launch_ms": sum(dom_ms) / len(dom_ms), "share_of_step": sum(dom_ms) / elapsed_ms,
+              "algorithmic_bytes_per_launch": sum(dom_bytes) / len(dom_bytes),
+              "useful_flops_per_launch": sum(dom_flops) / len(dom_flops)}
+    if t_tensor >= t_hbm:
+        achieved = sum(dom_flops) / secs / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_sust, "unit": "TFLOP/s",
+                    "frac": achieved / peak_sust,
+                    "peak_source": f"{pk_kind} bf16_tflops_sustained (kernel timed inside the step loop)"}
+    else:
+        achieved = sum(dom_bytes) / secs / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak_bw, "unit": "GB/s",
+                    "frac": achieved / peak_bw, "peak_source": f"{pk_kind} hbm_gbs"}
+    roofline.update(common)
     # CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
