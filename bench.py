@@ -283,12 +283,8 @@ def run_gpu(args, rank, world, local_rank):
         assert pr.device_error() == 0, "device error in the timed region"
 
     if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-        f = torch.tensor([float(tot_flops)], device=dev, dtype=torch.float64)
-        dist.all_reduce(f, op=dist.ReduceOp.SUM)
-        tot_flops = float(f.item())
+        from hstu_jagged_attention_02_gb300 import dp
+        elapsed_ms, tot_flops = dp.reduce_step_time(elapsed_ms, tot_flops, device=dev)
 
     # ---- end to end through the C ABI with host buffers
     e2e = run_e2e(args, probs, flops, stream, world)
@@ -387,14 +383,8 @@ def run_e2e(args, probs, flops, stream, world):
     ms = t0.elapsed_time(t1)
     fl = sum(sum(flops[i % N_SEEDS]) for i in range(k))
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=t0.device if hasattr(t0, "device") else "cuda",
-                         dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-        f = torch.tensor([float(fl)], device="cuda", dtype=torch.float64)
-        dist.all_reduce(f, op=dist.ReduceOp.SUM)
-        fl = float(f.item())
+        from hstu_jagged_attention_02_gb300 import dp
+        ms, fl = dp.reduce_step_time(ms, fl, device=torch.device("cuda", torch.cuda.current_device()))
     return {"value": fl / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": bi,
             "d2h_bytes_per_step": bo, "ms_per_step": ms / k}
 
