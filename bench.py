@@ -12,7 +12,11 @@ taken in turn, so consecutive steps never find their inputs in L2.
 Metric: useful TFLOP/s, counting allowed (unmasked) query-key pairs only:
 forward 2 (d_qk + d_v) and backward 2 (3 d_qk + 2 d_v) FLOPs per pair.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+With --workload layer it measures the full HSTU layer instead (x W1, SiLU
+split, the same attention, LayerNorm gate, y W2 + x, forward + backward on 8
+sequences of 8K-32K tokens at D = 512), counting the projections' FLOPs too.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload layer]
 """
 from __future__ import annotations
 
@@ -67,14 +71,6 @@ def peaks():
         d = json.load(open(path))
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
-
-
-def config_dict(extra=None):
-    d = {"workload": WORKLOAD, "batches": N_SEEDS, "seeds": f"0..{N_SEEDS - 1} (+rank*{N_SEEDS})",
-         "l2": "inputs larger than L2: 16 distinct resident batches taken in turn"}
-    if extra:
-        d.update(extra)
-    return d
 
 
 class ClockSampler:
@@ -156,25 +152,106 @@ def traffic_record(kernel_role: str):
     return None
 
 
+# ------------------------------------------------------------ workloads
+
+class AttentionWorkload:
+    """The heavy-tailed attention batch (the default line)."""
+    name = "heavy_tailed"
+    metric = METRIC
+    description = WORKLOAD
+    n_batches = N_SEEDS
+
+    def batches(self, rank):
+        return [synth.heavy_tailed(rank * N_SEEDS + s) for s in range(N_SEEDS)]
+
+    def problem(self, b, dev):
+        from hstu_jagged_attention_02_gb300.attention import Problem
+        return Problem(b, device=dev, out_dtype="fp32")
+
+    def flops(self, b):
+        """(attention fwd, attention bwd, whole step) useful FLOPs."""
+        f, bw = useful_flops(b)
+        return f, bw, f + bw
+
+    def host_io(self, pr):
+        ins = [t for t in (pr.offsets, pr.num_targets, pr.num_contexts, pr.timestamps, pr.rab_pos,
+                           pr.rab_time, pr.q, pr.k, pr.v, pr.u, pr.dy) if t is not None]
+        outs = [t for t in (pr.y, pr.dq, pr.dk, pr.dvv, pr.du, pr.d_rab_pos, pr.d_rab_time)
+                if t is not None]
+        return ins, outs
+
+    def oracle_step(self, b):
+        from oracle import oracle as O
+        O.backward(b, o=O.forward(b)["o"])
+
+    def cpu_samples(self, batches):
+        return [sub_batch(b, 16) for b in batches], "fwd+bwd of the first 16 of the 64 sequences of a batch"
+
+    def config(self):
+        return {"batches": N_SEEDS, "seeds": f"0..{N_SEEDS - 1} (+rank*{N_SEEDS})",
+                "l2": "inputs larger than L2: 16 distinct resident batches taken in turn"}
+
+
+class LayerWorkload(AttentionWorkload):
+    """The full HSTU layer: 8 sequences of U[8192, 32768] history + 128
+    candidates, D = 512 (4 heads of 128); x W1 -> SiLU -> attention -> y W2 + x,
+    forward and backward."""
+    name = "layer"
+    metric = "HSTU layer useful TFLOP/s (fwd+bwd: attention + the two projections)"
+    description = ("layer: 8 jagged sequences, history U[8192,32768] + 128 candidates, D=512 = 4 heads x 128, "
+                   "BF16 x/W1/W2, FP32 outputs; Z1 = x W1, SiLU split U|V|Q|K, causal + candidate mask, "
+                   "position + time rab, LayerNorm gate, out = x + y W2; forward + backward")
+    n_batches = 2
+
+    def batches(self, rank):
+        return [synth.layer(rank * 2 + s) for s in range(2)]
+
+    def problem(self, b, dev):
+        from hstu_jagged_attention_02_gb300.layer import LayerProblem
+        return LayerProblem(b, device=dev)
+
+    def flops(self, b):
+        f, bw = useful_flops(b)
+        D = b.H * b.d_v
+        gemm = 3 * (2 * b.T * D * 4 * D + 2 * b.T * D * D)   # forward 2 GEMMs, backward 4
+        return f, bw, f + bw + gemm
+
+    def host_io(self, pr):
+        ins = [t for t in (pr.offsets, pr.num_targets, pr.num_contexts, pr.timestamps, pr.rab_pos,
+                           pr.rab_time, pr.x, pr.w1, pr.w2, pr.dout) if t is not None]
+        outs = [t for t in (pr.out, pr.dx, pr.dw1, pr.dw2, pr.d_rab_pos, pr.d_rab_time) if t is not None]
+        return ins, outs
+
+    def oracle_step(self, b):
+        from oracle import oracle as O
+        O.layer_backward(b)
+
+    def cpu_samples(self, batches):
+        return ([synth.layer(100 + s, n_lo=1024, n_hi=1024, B=1) for s in range(2)],
+                "layer fwd+bwd of one sequence of 1024 history + 128 candidates at D=512")
+
+    def config(self):
+        return {"batches": 2, "seeds": "0..1 (+rank*2)",
+                "l2": "inputs larger than L2: each batch holds several GB of activations"}
+
+
+WORKLOADS = {"heavy_tailed": AttentionWorkload, "layer": LayerWorkload}
+
+
 # ------------------------------------------------------------ CPU oracle arm
 
-def time_oracle(batches, budget_s):
-    """Runs the FP64 oracle (fwd + bwd) over batches until budget_s is spent;
-    returns (useful flops, seconds, description, threads)."""
+def time_oracle(wl, samples, budget_s):
+    """Runs the FP64 oracle over samples until budget_s is spent; returns
+    (useful flops, seconds, batches used, threads)."""
     from oracle import oracle as O
-    done_flops, t0, used = 0, time.perf_counter(), []
-    for b in batches:
-        f = O.forward(b)
-        O.backward(b, o=f["o"])
-        fw, bw = useful_flops(b)
-        done_flops += fw + bw
-        used.append(b)
+    done_flops, t0, used = 0, time.perf_counter(), 0
+    for b in samples:
+        wl.oracle_step(b)
+        done_flops += wl.flops(b)[2]
+        used += 1
         if time.perf_counter() - t0 >= budget_s:
             break
-    dt = time.perf_counter() - t0
-    desc = (f"fwd+bwd of {len(used)} batch(es) / {sum(x.B for x in used)} sequences / "
-            f"{sum(x.T for x in used)} tokens")
-    return done_flops, dt, desc, O.num_threads()
+    return done_flops, time.perf_counter() - t0, used, O.num_threads()
 
 
 def sub_batch(b, n_seq):
@@ -192,52 +269,48 @@ def sub_batch(b, n_seq):
         alpha=b.alpha, max_seq_len=b.max_seq_len, norm=b.norm, eps=b.eps)
 
 
-def run_reference(args, rank, world):
+def run_reference(args, wl, rank, world):
     if rank != 0:
         return
     from oracle import oracle as O
-    full = [synth.heavy_tailed(s) for s in range(N_SEEDS)]
-    samples = [sub_batch(b, 16) for b in full]   # 16 of 64 sequences per step
+    samples, what = wl.cpu_samples(wl.batches(0))
     for w in range(args.warmup):
-        b = samples[w % N_SEEDS]
-        O.backward(b, o=O.forward(b)["o"])
+        wl.oracle_step(samples[w % len(samples)])
     flops, t0 = 0, time.perf_counter()
     for k in range(args.steps):
-        b = samples[k % N_SEEDS]
-        O.backward(b, o=O.forward(b)["o"])
-        fw, bw = useful_flops(b)
-        flops += fw + bw
+        b = samples[k % len(samples)]
+        wl.oracle_step(b)
+        flops += wl.flops(b)[2]
     dt = time.perf_counter() - t0
     val = flops / dt / 1e12
-    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
+    line = {"impl": "reference", "metric": wl.metric, "value": val, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / max(args.steps, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": config_dict({"sample": "first 16 of the 64 sequences of each batch"}),
+            "config": dict({"workload": wl.description, "sample": what}, **wl.config()),
             "cpu_baseline": {"value": val, "unit": UNIT, "cores": O.num_threads(), "kind": "oracle",
-                             "sample": "per step: fwd+bwd of the first 16 sequences of one batch"},
+                             "sample": f"per step: {what}"},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------ GPU arm
 
-def run_gpu(args, rank, world, local_rank):
+def run_gpu(args, wl, rank, world, local_rank):
     import torch
     import torch.distributed as dist
     from hstu_jagged_attention_02_gb300 import binding as C
-    from hstu_jagged_attention_02_gb300.attention import Problem
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    seeds = [rank * N_SEEDS + s for s in range(N_SEEDS)]
-    batches = [synth.heavy_tailed(s) for s in seeds]
-    probs = [Problem(b, device=dev, out_dtype="fp32") for b in batches]
-    flops = [useful_flops(b) for b in batches]
+    batches = wl.batches(rank)
+    nb = len(batches)
+    probs = [wl.problem(b, dev) for b in batches]
+    flops = [wl.flops(b) for b in batches]
     stream = torch.cuda.current_stream()
 
     def step(i, ev=None):
-        pr = probs[i % N_SEEDS]
+        pr = probs[i % nb]
         if ev is not None:
             C.hstu_time_next_attention_kernel(ev[0].cuda_event, ev[1].cuda_event)
         pr.forward()
@@ -277,8 +350,8 @@ def run_gpu(args, rank, world, local_rank):
     elapsed_ms = start.elapsed_time(end)
     fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
     bwd_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    step_flops = [flops[k % N_SEEDS] for k in range(args.steps)]
-    tot_flops = sum(f + b for f, b in step_flops)
+    step_flops = [flops[k % nb] for k in range(args.steps)]
+    tot_flops = sum(f[2] for f in step_flops)
     for pr in probs:
         assert pr.device_error() == 0, "device error in the timed region"
 
@@ -287,7 +360,7 @@ def run_gpu(args, rank, world, local_rank):
         elapsed_ms, tot_flops = dp.reduce_step_time(elapsed_ms, tot_flops, device=dev)
 
     # ---- end to end through the C ABI with host buffers
-    e2e = run_e2e(args, probs, flops, stream, world)
+    e2e = run_e2e(args, wl, probs, flops, stream, world)
 
     if rank != 0:
         return
@@ -304,11 +377,11 @@ def run_gpu(args, rank, world, local_rank):
     # writes o (FP32); backward reads q, k, v and dO as a BF16 pair and writes dk,
     # dv and the dq reduction (FP32)
     per_elem = KERNEL_BYTES_PER_ELEM[dom]
-    dom_bytes = [per_elem * batches[k % N_SEEDS].T * batches[0].H * batches[0].d_qk for k in range(args.steps)]
+    dom_bytes = [per_elem * batches[k % nb].T * batches[0].H * batches[0].d_qk for k in range(args.steps)]
     secs = sum(dom_ms) * 1e-3
     t_tensor = sum(dom_flops) / (peak_sust * 1e12)
     t_hbm = sum(dom_bytes) / (peak_bw * 1e9)
-    tr = traffic_record(dom)
+    tr = traffic_record(f"{wl.name}:{dom}")
     common = {"traffic": tr["dram_bytes_per_launch"] if tr else None, "kernel": f"attention {dom} kernel",
               "avg_launch_ms": sum(dom_ms) / len(dom_ms), "share_of_step": sum(dom_ms) / elapsed_ms,
               "algorithmic_bytes_per_launch": sum(dom_bytes) / len(dom_bytes),
@@ -326,14 +399,17 @@ def run_gpu(args, rank, world, local_rank):
     # CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cf, cdt, cdesc, cores = time_oracle(batches, budget_s=args.cpu_budget)
+        samples, what = wl.cpu_samples(batches)
+        cf, cdt, used, cores = time_oracle(wl, samples, budget_s=args.cpu_budget)
         cpu = {"value": cf / cdt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": cdesc, "seconds": cdt}
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+               "sample": f"{used} x {what}", "seconds": cdt}
+    cfg = {"workload": wl.description}
+    cfg.update(wl.config())
+    cfg.update({"per_rank_batches": nb, "mean_tokens_per_batch": float(np.mean([b.T for b in batches]))})
+    line = {"metric": wl.metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": config_dict({"per_rank_batches": N_SEEDS,
-                                   "mean_tokens_per_batch": float(np.mean([b.T for b in batches]))}),
+            "config": cfg,
             "pct_of_bf16_peak": 100.0 * value / peak_burst,
             "peak_bf16_tflops": {"burst": peak_burst, "sustained": peak_sust, "source": pk_kind},
             "fwd_kernel_ms_avg": fwd_total / args.steps, "bwd_kernel_ms_avg": bwd_total / args.steps,
@@ -342,17 +418,15 @@ def run_gpu(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, probs, flops, stream, world):
+def run_e2e(args, wl, probs, flops, stream, world):
     """Same metric through the public C ABI with pinned host buffers: each step
     copies its inputs host -> device, runs forward + backward and copies the
     results back.  Returns the e2e dict."""
     import torch
+    nb = len(probs)
     hosts = []
     for pr in probs:
-        ins = [t for t in (pr.offsets, pr.num_targets, pr.num_contexts, pr.timestamps, pr.rab_pos,
-                           pr.rab_time, pr.q, pr.k, pr.v, pr.u, pr.dy) if t is not None]
-        outs = [t for t in (pr.y, pr.dq, pr.dk, pr.dvv, pr.du, pr.d_rab_pos, pr.d_rab_time)
-                if t is not None]
+        ins, outs = wl.host_io(pr)
         h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in ins]
         h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
         hosts.append((ins, h_in, outs, h_out))
@@ -360,8 +434,8 @@ def run_e2e(args, probs, flops, stream, world):
     bo = sum(t.numel() * t.element_size() for t in hosts[0][3])
 
     def one(i):
-        pr = probs[i % N_SEEDS]
-        ins, h_in, outs, h_out = hosts[i % N_SEEDS]
+        pr = probs[i % nb]
+        ins, h_in, outs, h_out = hosts[i % nb]
         for d, h in zip(ins, h_in):
             d.copy_(h, non_blocking=True)
         pr.forward()
@@ -381,7 +455,7 @@ def run_e2e(args, probs, flops, stream, world):
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
-    fl = sum(sum(flops[i % N_SEEDS]) for i in range(k))
+    fl = sum(flops[i % nb][2] for i in range(k))
     if world > 1:
         from hstu_jagged_attention_02_gb300 import dp
         ms, fl = dp.reduce_step_time(ms, fl, device=torch.device("cuda", torch.cuda.current_device()))
@@ -398,7 +472,10 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="heavy_tailed", choices=sorted(WORKLOADS),
+                    help="heavy_tailed attention (the default line) or the full layer")
     args = ap.parse_args()
+    wl = WORKLOADS[args.workload]()
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -413,9 +490,9 @@ def main():
         dist.init_process_group(backend)
     try:
         if args.impl == "reference":
-            run_reference(args, rank, world)
+            run_reference(args, wl, rank, world)
         else:
-            run_gpu(args, rank, world, local_rank)
+            run_gpu(args, wl, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

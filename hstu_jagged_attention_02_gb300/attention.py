@@ -57,7 +57,7 @@ class Problem:
         self.rab_pos = up(batch.rab_pos, torch.float32)
         self.rab_time = up(batch.rab_time, torch.float32)
         self.q, self.k, self.v = up(batch.q, td), up(batch.k, td), up(batch.v, td)
-        self.u = up(batch.u, td)
+        self.u = up(batch.u, torch.float32 if flags & C.HSTU_FLAG_U_FP32 else td)
         self.dy = up(batch.dy, to)
         z = lambda *s, dt=to: torch.empty(*s, device=dev, dtype=dt)
         self.o = z(T, H, dv)

@@ -20,6 +20,7 @@ HSTU_BF16, HSTU_FP32 = 0, 1
 HSTU_NORM_NONE, HSTU_NORM_LAYERNORM = 0, 1
 HSTU_FLAG_FORCE_SIMT = 1 << 0
 HSTU_FLAG_TEST_TIMEOUT = 1 << 1
+HSTU_FLAG_U_FP32 = 1 << 2
 
 _vp = ctypes.c_void_p
 
@@ -46,9 +47,21 @@ class hstu_attn_bwd_args(ctypes.Structure):
                                    "dq", "dk", "dv", "du", "d_rab_pos", "d_rab_time")]
 
 
+class hstu_layer_fwd_args(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("seq_offsets", "num_targets", "num_contexts", "timestamps",
+                                   "rab_pos", "rab_time", "x", "w1", "w2", "out", "z1", "u", "vqk", "o", "y")]
+
+
+class hstu_layer_bwd_args(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("seq_offsets", "num_targets", "num_contexts", "timestamps",
+                                   "rab_pos", "rab_time", "x", "w1", "w2", "z1", "u", "vqk", "o", "y",
+                                   "dout", "dx", "dw1", "dw2", "d_rab_pos", "d_rab_time")]
+
+
 EXPORTED = ("hstu_attn_workspace_size", "hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_debug_plan",
             "hstu_get_device_error", "hstu_status_string", "hstu_last_launch_count",
-            "hstu_time_next_attention_kernel", "hstu_last_error_detail", "hstu_attn_fwd_noalloc")
+            "hstu_time_next_attention_kernel", "hstu_last_error_detail", "hstu_attn_fwd_noalloc",
+            "hstu_layer_workspace_size", "hstu_layer_fwd", "hstu_layer_bwd")
 
 _lib = None
 
@@ -81,8 +94,11 @@ def load(build_if_missing: bool = True):
     L.hstu_last_error_detail.restype = ctypes.c_char_p
     L.hstu_attn_fwd_noalloc.argtypes = [P(hstu_attn_desc), P(hstu_attn_fwd_args), _vp, P(ctypes.c_int32)]
     L.hstu_attn_fwd_noalloc.restype = ctypes.c_int
+    L.hstu_layer_workspace_size.argtypes = [P(hstu_attn_desc), P(ctypes.c_size_t), P(ctypes.c_size_t)]
+    L.hstu_layer_fwd.argtypes = [P(hstu_attn_desc), P(hstu_layer_fwd_args), _vp, ctypes.c_size_t, _vp]
+    L.hstu_layer_bwd.argtypes = [P(hstu_attn_desc), P(hstu_layer_bwd_args), _vp, ctypes.c_size_t, _vp]
     for name in ("hstu_attn_workspace_size", "hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_debug_plan",
-                 "hstu_get_device_error"):
+                 "hstu_get_device_error", "hstu_layer_workspace_size", "hstu_layer_fwd", "hstu_layer_bwd"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -157,6 +173,23 @@ def hstu_attn_fwd_noalloc(desc, args, stream: int, want_device_error: bool = Tru
                                         ctypes.byref(code) if want_device_error else None),
            "hstu_attn_fwd_noalloc")
     return int(code.value) if want_device_error else None
+
+
+def hstu_layer_workspace_size(desc: hstu_attn_desc):
+    f, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(load().hstu_layer_workspace_size(ctypes.byref(desc), ctypes.byref(f), ctypes.byref(b)),
+           "hstu_layer_workspace_size")
+    return int(f.value), int(b.value)
+
+
+def hstu_layer_fwd(desc, args, workspace: int, workspace_bytes: int, stream: int):
+    _check(load().hstu_layer_fwd(ctypes.byref(desc), ctypes.byref(args), workspace, workspace_bytes,
+                                 stream), "hstu_layer_fwd")
+
+
+def hstu_layer_bwd(desc, args, workspace: int, workspace_bytes: int, stream: int):
+    _check(load().hstu_layer_bwd(ctypes.byref(desc), ctypes.byref(args), workspace, workspace_bytes,
+                                 stream), "hstu_layer_bwd")
 
 
 def hstu_get_device_error(workspace: int, stream: int) -> int:

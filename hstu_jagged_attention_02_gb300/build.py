@@ -1,7 +1,8 @@
 """Build libhstu_attn.so in-tree for sm_103a with nvcc (no cmake, no torch).
 
 Each .cu file is compiled in parallel into _build/, then linked into
-_build/libhstu_attn.so with the CUDA runtime linked statically.
+_build/libhstu_attn.so with the CUDA runtime linked statically and cuBLAS
+(the layer's plain dense GEMMs) linked dynamically from the toolkit.
 """
 from __future__ import annotations
 
@@ -58,7 +59,9 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), _sources()))
     tmp = LIB + ".tmp"
-    r = subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+    libdir = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc()))), "lib64")
+    r = subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcublas",
+                        "-Xlinker", "-rpath", "-Xlinker", libdir], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)

@@ -29,7 +29,7 @@ struct KernelTimer {
   ~KernelTimer() { if (b) cudaEventRecord(b, st); }
 };
 
-constexpr uint32_t kKnownFlags = HSTU_FLAG_FORCE_SIMT | HSTU_FLAG_TEST_TIMEOUT;
+constexpr uint32_t kKnownFlags = HSTU_FLAG_FORCE_SIMT | HSTU_FLAG_TEST_TIMEOUT | HSTU_FLAG_U_FP32;
 
 size_t align_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
 size_t esize(int dtype) { return dtype == HSTU_BF16 ? 2 : 4; }
@@ -70,6 +70,7 @@ hstu_status_t check_desc(const hstu_attn_desc* d) {
   if (d->norm == HSTU_NORM_LAYERNORM && !(d->ln_eps > 0.f && std::isfinite(d->ln_eps))) return HSTU_ERR_INVALID_ARG;
   if (!std::isfinite(d->alpha)) return HSTU_ERR_INVALID_ARG;
   if (d->flags & ~kKnownFlags) return HSTU_ERR_INVALID_ARG;
+  if ((d->flags & HSTU_FLAG_U_FP32) && d->out_dtype != HSTU_FP32) return HSTU_ERR_UNSUPPORTED;
   if (d->d_qk != d->d_v || (d->d_qk != 32 && d->d_qk != 64 && d->d_qk != 128)) return HSTU_ERR_UNSUPPORTED;
   if (d->H * d->d_v > 2048) return HSTU_ERR_UNSUPPORTED;
   if (d->max_seq_len > kCostBins * kSimtTile) return HSTU_ERR_UNSUPPORTED;
@@ -251,7 +252,7 @@ hstu_status_t hstu_attn_fwd(const hstu_attn_desc* d, const hstu_attn_fwd_args* a
     ++g_launches;
     if (a->y || a->ln_mean || a->ln_rstd) {
       NormParams np{};
-      np.dtype = d->dtype; np.out_dtype = d->out_dtype;
+      np.dtype = (d->flags & HSTU_FLAG_U_FP32) ? HSTU_FP32 : d->dtype; np.out_dtype = d->out_dtype;
       np.o = a->o; np.u = a->u; np.y = a->y; np.mean = a->ln_mean; np.rstd = a->ln_rstd;
       np.T = d->total_tokens; np.F = d->H * d->d_v; np.norm = d->norm; np.eps = d->ln_eps;
       HSTU_CUDA_TRY(launch_norm_gate_fwd(np, st));
@@ -303,7 +304,7 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
   // gradient w.r.t. o, in the input type (an MMA operand of the attention backward)
   {
     NormParams np{};
-    np.dtype = d->dtype; np.out_dtype = d->out_dtype;
+    np.dtype = (d->flags & HSTU_FLAG_U_FP32) ? HSTU_FP32 : d->dtype; np.out_dtype = d->out_dtype;
     np.o = a->o; np.u = a->u; np.dy = a->dy; np.dO = ws + L.dO; np.du = a->du;
     np.split = tc ? 1 : 0;
     np.dO_lo = ws + L.dO + sizeof(__nv_bfloat16) * rows * (size_t)d->d_v;

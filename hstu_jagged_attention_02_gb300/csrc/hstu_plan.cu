@@ -15,6 +15,8 @@ namespace hstu {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+constexpr int kOffStage = 2048;  // sequence offsets staged in shared memory (B + 1 <= this)
+constexpr int kUnroll = 8;       // tokens per thread in flight in the timestamp check
 
 __device__ int block_scan_exclusive(int v, int* sh) {
   // inclusive scan of v over the CTA, returns the exclusive prefix; sh holds
@@ -51,6 +53,7 @@ plan_kernel(PlanParams p) {
   __shared__ int sh_scan[kPlanThreads];
   __shared__ int sh_hist[kCostBins];
   __shared__ int sh_bad;
+  __shared__ int64_t sh_off[kOffStage];
   const int t = threadIdx.x;
   if (t == 0) {
     p.hdr[WS_ERR] = 0;
@@ -80,18 +83,38 @@ plan_kernel(PlanParams p) {
 
   // 1b. can every timestamp be held relative to its sequence's first token in
   // 31 bits (so gaps fit in 32)?  Otherwise the kernels take their 64-bit path.
+  // Token-parallel: each thread finds its tokens' sequences by binary search
+  // over the offsets (staged in shared memory when they fit), kUnroll tokens
+  // at a time so their loads overlap.
   if (p.ts) {
-    // token-parallel: each thread finds its token's sequence by binary search
-    // (the last b with off[b] <= token, which skips empty sequences)
+    const bool staged = p.B + 1 <= kOffStage;
+    if (staged)
+      for (int i = t; i <= p.B; i += kPlanThreads) sh_off[i] = p.off[i];
+    __syncthreads();
     int wide = 0;
-    for (int64_t tok = t; tok < p.T; tok += kPlanThreads) {
-      int lo = 0, hi = p.B - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (p.off[mid] <= tok) lo = mid; else hi = mid - 1;
+    for (int64_t base = t; base < p.T; base += (int64_t)kPlanThreads * kUnroll) {
+      int64_t first[kUnroll], here[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t tok = base + (int64_t)u * kPlanThreads;
+        first[u] = here[u] = 0;
+        if (tok < p.T) {
+          // the last b with off[b] <= tok (skips empty sequences)
+          int lo = 0, hi = p.B - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            const int64_t o = staged ? sh_off[mid] : p.off[mid];
+            if (o <= tok) lo = mid; else hi = mid - 1;
+          }
+          first[u] = p.ts[staged ? sh_off[lo] : p.off[lo]];
+          here[u] = p.ts[tok];
+        }
       }
-      const int64_t d = p.ts[tok] - p.ts[p.off[lo]];
-      wide |= (d >= (int64_t)1 << 30 || d < -((int64_t)1 << 30));
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t d = here[u] - first[u];
+        wide |= (d >= (int64_t)1 << 30 || d < -((int64_t)1 << 30));
+      }
     }
     if (__syncthreads_or(wide) && t == 0) atomicOr(p.hdr + WS_FLAGS, WS_FLAG_WIDE_TS);
   }

@@ -636,18 +636,39 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
 }
 
 // d_rab_pos[h][b] / d_rab_time[h][b] = sum over CTAs of their partial sums.
-__global__ void drab_reduce_kernel(const float* __restrict__ partial, int nctas, int H, int P, int Tb,
-                                   float* d_rab_pos, float* d_rab_time) {
-  const int PT = P + Tb;
-  const int x = blockIdx.x * blockDim.x + threadIdx.x;
-  if (x >= H * PT) return;
+// A block owns 32 consecutive entries (one per lane, coalesced rows); its 8
+// warps split the CTA rows and combine their sums in shared memory.
+constexpr int kReduceWarps = 8;
+__global__ void __launch_bounds__(kReduceWarps * 32)
+drab_reduce_kernel(const float* __restrict__ partial, int nctas, int H, int P, int Tb, float* d_rab_pos,
+                   float* d_rab_time) {
+  __shared__ float part[kReduceWarps][32];
+  const int PT = P + Tb, n = H * PT;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int x = blockIdx.x * 32 + lane;
   float s = 0.f;
-  for (int c = 0; c < nctas; ++c) s += partial[(size_t)c * H * PT + x];
+  if (x < n) {
+    int c = w;
+    for (; c + 3 * kReduceWarps < nctas; c += 4 * kReduceWarps) {
+      const float a0 = partial[(size_t)c * n + x];
+      const float a1 = partial[(size_t)(c + kReduceWarps) * n + x];
+      const float a2 = partial[(size_t)(c + 2 * kReduceWarps) * n + x];
+      const float a3 = partial[(size_t)(c + 3 * kReduceWarps) * n + x];
+      s += (a0 + a1) + (a2 + a3);
+    }
+    for (; c < nctas; c += kReduceWarps) s += partial[(size_t)c * n + x];
+  }
+  part[w][lane] = s;
+  __syncthreads();
+  if (w != 0 || x >= n) return;
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < kReduceWarps; ++i) t += part[i][lane];
   const int h = x / PT, e = x % PT;
   if (e < P) {
-    if (d_rab_pos) d_rab_pos[h * P + e] = s;
+    if (d_rab_pos) d_rab_pos[h * P + e] = t;
   } else if (d_rab_time) {
-    d_rab_time[h * Tb + (e - P)] = s;
+    d_rab_time[h * Tb + (e - P)] = t;
   }
 }
 
@@ -681,8 +702,8 @@ cudaError_t launch_t(const AttnParams& p, cudaStream_t st) {
   // d_rab = sum of the CTAs' partial sums (overwrites the outputs)
   const int entries = p.H * (p.P + p.Tb);
   if (p.d_rab_pos || p.d_rab_time) {
-    drab_reduce_kernel<<<(entries + 255) / 256, 256, 0, st>>>(p.drab_partial, grid, p.H, p.P, p.Tb,
-                                                              p.d_rab_pos, p.d_rab_time);
+    drab_reduce_kernel<<<(entries + 31) / 32, kReduceWarps * 32, 0, st>>>(p.drab_partial, grid, p.H, p.P, p.Tb,
+                                                                         p.d_rab_pos, p.d_rab_time);
     e = cudaGetLastError();
   }
   return e;

@@ -80,6 +80,9 @@ typedef enum { HSTU_NORM_NONE = 0, HSTU_NORM_LAYERNORM = 1 } hstu_norm_t;
 #define HSTU_FLAG_TEST_TIMEOUT (1u << 1) /* test only: the tensor-core forward withholds one load and its
                                             waits give up after about a millisecond, so the timeout path
                                             runs without a hang; the result is HSTU_ERR_TIMEOUT */
+#define HSTU_FLAG_U_FP32 (1u << 2)       /* u is FP32 whatever dtype is (requires out_dtype FP32).  The
+                                            gate multiplies y element by element, so a BF16 rounding of u
+                                            is never averaged out; q, k, v stay in dtype */
 
 typedef struct {
   uint32_t struct_size;     /* sizeof(hstu_attn_desc) */
@@ -108,7 +111,7 @@ typedef struct {
   const void* q;               /* [T, H, d_qk] */
   const void* k;               /* [T, H, d_qk] */
   const void* v;               /* [T, H, d_v] */
-  const void* u;               /* [T, H*d_v] gate, or NULL (gate of one) */
+  const void* u;               /* [T, H*d_v] gate, or NULL (gate of one); FP32 with HSTU_FLAG_U_FP32 */
   void* o;                     /* out [T, H, d_v]: A.V, kept for the backward */
   void* y;                     /* out [T, H*d_v]: Norm(o) * u, or NULL (not produced) */
   float* ln_mean;              /* out [T] or NULL: per-token mean of o (LAYERNORM) */
@@ -194,6 +197,89 @@ hstu_status_t hstu_attn_debug_plan(const hstu_attn_desc* desc, const int64_t* se
  * synchronise the stream. */
 hstu_status_t hstu_attn_fwd_noalloc(const hstu_attn_desc* desc, const hstu_attn_fwd_args* args,
                                     hstu_stream_t stream, int32_t* host_device_error);
+
+/* ------------------------------------------------------------------------
+ * The full HSTU layer around the attention (ai6s.net survey, section 2.1.2,
+ * equations (1)-(3), with the residual connection between layers; section
+ * 2.1.3: two linear layers per block).  With D = H * d_v (= H * d_qk):
+ *
+ *   Z1 = X W1                                   [T, 4D]  (FP32 accumulation)
+ *   U | V | Q | K = SiLU(Z1), column blocks of width D in that order
+ *   o, y = attention(Q, K, V, U) as in hstu_attn_fwd (y = Norm(o) * U)
+ *   out  = X + y W2                             [T, D]
+ *
+ * Precision: X, W1, W2 BF16; V, Q, K = SiLU(Z1) are rounded to BF16 (the
+ * attention's MMA operands) while the gate U stays FP32 (it scales y element
+ * by element, where a rounding is never averaged out).  The computed GEMM
+ * operands y (y W2, y^T dout) and dZ1 (X^T dZ1, dZ1 W1^T) enter as BF16
+ * pairs hi + lo (about 16 bits, two accumulating GEMMs each); dout is
+ * rounded to BF16 for dout W2^T and y^T dout.  Every accumulation, o, y,
+ * out, dx and all gradients are FP32.  The descriptor is the
+ * attention's and must have dtype BF16, out_dtype FP32, d_qk == d_v.
+ *
+ * The four dense GEMMs (and their four backward counterparts) are plain
+ * cuBLAS GEMMs (BF16 x BF16 -> FP32); the SiLU split, residual and SiLU'
+ * steps and the attention are this library's kernels.  cuBLAS's scratch
+ * comes from the caller's workspace, but the first call on each (host
+ * thread, device) creates a cuBLAS handle, which allocates cuBLAS's own
+ * small state: make that first call outside any stream capture.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  const int64_t* seq_offsets;  /* as hstu_attn_fwd_args */
+  const int32_t* num_targets;
+  const int32_t* num_contexts;
+  const int64_t* timestamps;
+  const float* rab_pos;
+  const float* rab_time;
+  const void* x;               /* [T, D] BF16 layer input */
+  const void* w1;              /* [D, 4D] BF16, row-major (x W1) */
+  const void* w2;              /* [D, D] BF16, row-major (y W2) */
+  float* out;                  /* out [T, D] FP32: x + y W2 */
+  float* z1;                   /* out [T, 4D] FP32: x W1, kept for the backward */
+  float* u;                    /* out [T, D] FP32: the gate U */
+  void* vqk;                   /* out [3, T, D] BF16: V, Q, K, each [T, H, d] */
+  void* o;                     /* out [T, D] FP32: A.V, kept for the backward */
+  void* y;                     /* out [T, D] FP32: Norm(o) * U */
+} hstu_layer_fwd_args;
+
+typedef struct {
+  const int64_t* seq_offsets;  /* the forward's inputs, unchanged */
+  const int32_t* num_targets;
+  const int32_t* num_contexts;
+  const int64_t* timestamps;
+  const float* rab_pos;
+  const float* rab_time;
+  const void* x;
+  const void* w1;
+  const void* w2;
+  const float* z1;             /* the forward's z1, u, vqk, o, y */
+  const float* u;
+  const void* vqk;
+  const void* o;
+  const void* y;
+  const float* dout;           /* [T, D] FP32 gradient of the loss w.r.t. out */
+  float* dx;                   /* out [T, D]: dout + dZ1 W1^T */
+  float* dw1;                  /* out [D, 4D]: X^T dZ1 */
+  float* dw2;                  /* out [D, D]: y^T dout */
+  float* d_rab_pos;            /* out [H, P] or NULL */
+  float* d_rab_time;           /* out [H, Tb] or NULL */
+} hstu_layer_bwd_args;
+
+/* Workspace bytes of hstu_layer_fwd / hstu_layer_bwd (256-byte aligned
+ * workspace; either output may be NULL).  HSTU_ERR_UNSUPPORTED unless dtype
+ * is BF16, out_dtype FP32 and D a multiple of 8. */
+hstu_status_t hstu_layer_workspace_size(const hstu_attn_desc* desc, size_t* fwd_bytes, size_t* bwd_bytes);
+
+/* Layer forward (above).  All pointers device, 16-byte aligned; outputs are
+ * overwritten.  Device-side problems land in the attention's error word at
+ * the start of the workspace (hstu_get_device_error). */
+hstu_status_t hstu_layer_fwd(const hstu_attn_desc* desc, const hstu_layer_fwd_args* args,
+                             void* workspace, size_t workspace_bytes, hstu_stream_t stream);
+
+/* Layer backward: dx, dw1, dw2 and the bias-table gradients, recomputing the
+ * attention tile by tile from the saved u, vqk and o. */
+hstu_status_t hstu_layer_bwd(const hstu_attn_desc* desc, const hstu_layer_bwd_args* args,
+                             void* workspace, size_t workspace_bytes, hstu_stream_t stream);
 
 /* Reads the device error word of the last call that used this workspace
  * (HSTU_OK when none).  Synchronises the stream. */

@@ -225,34 +225,67 @@ def _split_uvqk(a, H, d):
             a[:, 3 * D:4 * D].reshape(T, H, d))
 
 
-def layer_forward(b, rows=None):
-    """Full HSTU layer forward in float64: dict with z1, u, v, q, k, o, y, out."""
+def bf16_round(a):
+    """Round float64 values to the nearest bfloat16 value (8 significant bits,
+    ties to even), returned as float64.  Values stay in the normal range of
+    the layer's activations; no overflow or subnormal handling."""
+    a = np.asarray(a, np.float64)
+    m, e = np.frexp(a)                      # a = m * 2**e, 0.5 <= |m| < 1
+    return np.ldexp(np.round(m * 256.0) / 256.0, e)   # np.round: half to even
+
+
+def layer_forward(b, rows=None, act_dtype=None):
+    """Full HSTU layer forward in float64: dict with z1, u, v, q, k, o, y, out.
+
+    act_dtype="bf16" rounds the values a BF16 layer stores once: V, Q and
+    K = SiLU(X W1) are rounded to bfloat16 before the attention.  The gate U
+    and Y (which such a layer carries at about 16 bits) are not rounded.
+    rows (bool [T]) restricts o, y and out to those rows (the others are
+    zero); z1 and the U/V/Q/K split are always complete."""
+    rnd = bf16_round if act_dtype == "bf16" else (lambda a: a)
     x, w1, w2 = _f64(b.x), _f64(b.w1), _f64(b.w2)
     z1 = x @ w1
-    a1 = _silu(z1)
-    u, v, q, k = _split_uvqk(a1, b.H, b.d_v)
+    u, v, q, k = _split_uvqk(_silu(z1), b.H, b.d_v)
+    v, q, k = rnd(v), rnd(q), rnd(k)
     pb = Problem(b.offsets, q, k, v, b.alpha, b.max_seq_len, b.num_targets, b.num_contexts,
                  b.timestamps, b.rab_pos, b.rab_time)
     o = attn_fwd(pb, rows)
     y, mean, rstd = norm_gate(o, u, "layernorm", b.eps, rows)
-    out = x + y @ w2
+    y_op = y
+    out = x + y_op @ w2
+    if rows is not None:
+        out[~np.asarray(rows, bool)] = 0.0
     return {"z1": z1, "u": u, "v": pb.v, "q": pb.q, "k": pb.k, "o": o, "y": y, "out": out,
-            "mean": mean, "rstd": rstd, "pb": pb}
+            "mean": mean, "rstd": rstd, "pb": pb, "y_op": y_op, "act_dtype": act_dtype, "rows": rows}
 
 
-def layer_backward(b, fwd=None):
+def layer_backward(b, fwd=None, act_dtype=None, rows=None):
     """Full HSTU layer backward given d(out) = b.dout: dict with dx, dw1, dw2
-    and the attention intermediates dq, dk, dv, du, d_rab_pos, d_rab_time."""
-    f = layer_forward(b) if fwd is None else fwd
+    and the attention intermediates dq, dk, dv, du, d_rab_pos, d_rab_time.
+
+    act_dtype="bf16" also rounds d(out), an input, to bfloat16 as the
+    operand of the two W2 products; dZ1 is not rounded (carried at about 16
+    bits).
+
+    rows (bool [T]) computes dx (and dq, dk, dv, du) only on those rows and
+    leaves dw1, dw2 and the bias-table gradients out (None).  This is exact
+    for every row whose key is attended only by queries inside rows (the
+    candidate rows and the last history row of a sequence, when rows holds
+    all the candidates of that sequence), because dO is formed on rows only."""
+    f = layer_forward(b, rows=rows, act_dtype=act_dtype) if fwd is None else fwd
+    rnd = bf16_round if act_dtype == "bf16" else (lambda a: a)
     x, w1, w2, dout = _f64(b.x), _f64(b.w1), _f64(b.w2), _f64(b.dout)
-    dw2 = f["y"].T @ dout
-    dy = dout @ w2.T
-    dO, du = norm_gate_bwd(f["o"], f["u"], dy, "layernorm", b.eps)
-    dq, dk, dv, drp, drt = attn_bwd(f["pb"], dO)
+    dout_op = rnd(dout)
+    dw2 = f["y_op"].T @ dout_op if rows is None else None
+    dy = dout_op @ w2.T
+    dO, du = norm_gate_bwd(f["o"], f["u"], dy, "layernorm", b.eps, rows)
+    dq, dk, dv, drp, drt = attn_bwd(f["pb"], dO, q_rows=rows, kv_rows=rows)
     T = x.shape[0]
-    da1 = np.concatenate([du, dv.reshape(T, -1), dq.reshape(T, -1), dk.reshape(T, -1)], axis=1)
-    dz1 = da1 * _silu_grad(f["z1"])
-    dw1 = x.T @ dz1
-    dx = dout + dz1 @ w1.T
+    sel = slice(None) if rows is None else np.asarray(rows, bool)
+    da1 = np.concatenate([du, dv.reshape(T, -1), dq.reshape(T, -1), dk.reshape(T, -1)], axis=1)[sel]
+    dz1 = da1 * _silu_grad(f["z1"][sel])
+    dw1 = x.T @ dz1 if rows is None else None
+    dx = np.zeros_like(dout)
+    dx[sel] = dout[sel] + dz1 @ w1.T
     return {"dx": dx, "dw1": dw1, "dw2": dw2, "dq": dq, "dk": dk, "dv": dv, "du": du,
             "d_rab_pos": drp, "d_rab_time": drt, "dy": dy, "dO": dO}

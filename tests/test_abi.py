@@ -58,6 +58,8 @@ def _desc(**kw):
     (dict(d_qk=96, d_v=96), C.HSTU_ERR_UNSUPPORTED),
     (dict(d_qk=64, d_v=128), C.HSTU_ERR_UNSUPPORTED),
     (dict(dtype="fp32", out_dtype="bf16"), C.HSTU_ERR_UNSUPPORTED),
+    (dict(out_dtype="bf16", flags=C.HSTU_FLAG_U_FP32), C.HSTU_ERR_UNSUPPORTED),
+    (dict(flags=1 << 7), C.HSTU_ERR_INVALID_ARG),
     (dict(alpha=float("nan")), C.HSTU_ERR_INVALID_ARG),
     (dict(ln_eps=0.0), C.HSTU_ERR_INVALID_ARG),
     (dict(flags=1 << 20), C.HSTU_ERR_INVALID_ARG),
@@ -108,3 +110,28 @@ def test_status_strings():
     for s in range(7):
         assert C.hstu_status_string(s) and C.hstu_status_string(s) != "unknown status"
     assert C.hstu_status_string(99) == "unknown status"
+
+
+def test_layer_descriptor_checks():
+    # the layer needs BF16 inputs with FP32 outputs; its workspace holds the
+    # attention backward's plus cuBLAS scratch and the layer's own buffers
+    ok = _desc(out_dtype="fp32", total_tokens=1000)
+    f, b = C.hstu_layer_workspace_size(ok)
+    af, ab = C.hstu_attn_workspace_size(ok)
+    assert f > af and b > ab and b > f
+    for kw in (dict(out_dtype="bf16"), dict(dtype="fp32", out_dtype="fp32")):
+        with pytest.raises(C.HSTUError) as e:
+            C.hstu_layer_workspace_size(_desc(**kw))
+        assert e.value.status == C.HSTU_ERR_UNSUPPORTED
+
+
+def test_layer_rejects_missing_pointers_before_any_launch():
+    d = _desc(out_dtype="fp32", total_tokens=1000)
+    args = C.hstu_layer_fwd_args()          # every pointer NULL
+    with pytest.raises(C.HSTUError) as e:
+        C.hstu_layer_fwd(d, args, 256, 1 << 30, None)
+    assert e.value.status == C.HSTU_ERR_INVALID_ARG
+    bargs = C.hstu_layer_bwd_args()
+    with pytest.raises(C.HSTUError) as e:
+        C.hstu_layer_bwd(d, bargs, 256, 1 << 30, None)
+    assert e.value.status == C.HSTU_ERR_INVALID_ARG

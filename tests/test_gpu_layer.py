@@ -1,0 +1,127 @@
+"""GPU parity of the full HSTU layer (x W1 -> SiLU -> attention -> y W2 + x)
+through hstu_layer_fwd / hstu_layer_bwd against the FP64 oracle with the
+layer's BF16 roundings (V, Q, K = SiLU(X W1), and dout as a GEMM operand)
+taken the same way; the gate U is FP32 and y, dZ1 are carried as BF16 pairs.
+
+Bar, per output, RMS taken over the oracle tensor: max abs err <= 1e-2 * RMS.
+The residual parts are checked without the residual (out - x against y W2,
+dx - dout against dZ1 W1^T), so the bar applies to the computed terms.
+"""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from hstu_jagged_attention_02_gb300 import synth  # noqa: E402
+from oracle import oracle as O  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+
+
+def _small_layer(seed, lengths, H=2, d=64, nt=16, contexts=None):
+    r = np.random.default_rng(seed)
+    D = H * d
+    lengths = np.asarray(lengths, np.int64)
+    off = synth.offsets_from_lengths(lengths)
+    T = int(off[-1])
+    ts = np.concatenate([np.sort(r.integers(0, 10 ** 7, size=n)) for n in lengths]).astype(np.int64)
+    bf = lambda a: synth.bf16_round(a.astype(np.float32))
+    empty = np.zeros((T, H, 0), np.float32)
+    return synth.Batch(
+        name="layer_small", seed=seed, dtype="bf16", B=len(lengths), H=H, d_qk=d, d_v=d, lengths=lengths,
+        offsets=off, num_targets=np.minimum(nt, lengths).astype(np.int32),
+        num_contexts=None if contexts is None else np.asarray(contexts, np.int32), timestamps=ts,
+        q=empty, k=empty, v=empty, u=None, dy=None,
+        rab_pos=r.normal(0, 0.02, (H, 128)).astype(np.float32),
+        rab_time=r.normal(0, 0.02, (H, 64)).astype(np.float32), alpha=1.0 / math.sqrt(d),
+        max_seq_len=int(lengths.max()), x=bf(r.standard_normal((T, D))),
+        w1=bf(r.normal(0, 0.02, (D, 4 * D))), w2=bf(r.normal(0, 0.02, (D, D))),
+        dout=bf(r.standard_normal((T, D))))
+
+
+def _run(batch):
+    from hstu_jagged_attention_02_gb300.layer import LayerProblem
+    pr = LayerProblem(batch)
+    pr.forward()
+    pr.backward()
+    torch.cuda.synchronize()
+    assert pr.device_error() == 0
+    return pr
+
+
+def _np(t):
+    return t.double().cpu().numpy()
+
+
+def _close(name, got, want, tol=TOL):
+    got, want = np.asarray(got, np.float64), np.asarray(want, np.float64)
+    assert np.all(np.isfinite(got)), name
+    rms = math.sqrt(float(np.mean(want * want)))
+    err = float(np.max(np.abs(got - want)))
+    assert err <= tol * rms, f"{name}: max abs err {err:.3e} > {tol:g} x rms {rms:.3e}"
+
+
+@pytest.mark.parametrize("case", ["ragged", "contexts", "d128"])
+def test_layer_parity_small(case):
+    if case == "ragged":
+        b = _small_layer(40, [300, 131, 77, 1, 520])
+    elif case == "contexts":
+        b = _small_layer(41, [260, 400, 95], contexts=[5, 37, 0])
+    else:
+        b = _small_layer(42, [384, 129, 250], H=2, d=128, nt=32)
+    pr = _run(b)
+    f = O.layer_forward(b, act_dtype="bf16")
+    g = O.layer_backward(b, f, act_dtype="bf16")
+    T, D = b.T, b.H * b.d_v
+    x, dout = b.x.astype(np.float64), b.dout.astype(np.float64)
+    _close("z1", _np(pr.z1), f["z1"], 1e-4)
+    _close("u", _np(pr.u), f["u"], 1e-4)
+    vqk = _np(pr.vqk)
+    for i, key in enumerate(("v", "q", "k")):
+        # both sides round SiLU(z1) to bf16; a z1 within the GEMM's FP32
+        # accumulation error (about 1e-4 of the RMS at most here) of a rounding
+        # boundary lands one bf16 step (at most 2^-7 relative) away
+        want = f[key].reshape(T, D)
+        rms = math.sqrt(float(np.mean(want * want)))
+        bound = 2.0 ** -7 * np.abs(want) + 1e-4 * rms
+        assert np.all(np.abs(vqk[i] - want) <= bound), key
+    _close("o", _np(pr.o), f["o"].reshape(T, D))
+    _close("y", _np(pr.y), f["y"])
+    _close("out - x", _np(pr.out) - x, f["out"] - x)
+    _close("dx - dout", _np(pr.dx) - dout, g["dx"] - dout)
+    _close("dw1", _np(pr.dw1), g["dw1"])
+    _close("dw2", _np(pr.dw2), g["dw2"])
+    _close("d_rab_pos", _np(pr.d_rab_pos), g["d_rab_pos"])
+    _close("d_rab_time", _np(pr.d_rab_time), g["d_rab_time"])
+
+
+def _sample_rows(b):
+    rows = np.zeros(b.T, bool)
+    for i in range(b.B):
+        e = int(b.offsets[i + 1])
+        rows[e - int(b.num_targets[i]) - 1:e] = True
+    return rows
+
+
+def test_layer_full_size_sampled_rows():
+    """8 sequences of U[8192, 32768] history + 128 candidates, D = 512: every
+    candidate row and the last history row of each sequence (whose keys only
+    queries of the same set attend), plus dW2 = Y^T dOut for the returned Y."""
+    b = synth.layer(0)
+    pr = _run(b)
+    rows = _sample_rows(b)
+    f = O.layer_forward(b, rows=rows, act_dtype="bf16")
+    g = O.layer_backward(b, f, act_dtype="bf16", rows=rows)
+    D = b.H * b.d_v
+    x, dout = b.x.astype(np.float64)[rows], b.dout.astype(np.float64)[rows]
+    _close("o[rows]", _np(pr.o)[rows], f["o"].reshape(b.T, D)[rows])
+    _close("y[rows]", _np(pr.y)[rows], f["y"][rows])
+    _close("out[rows] - x", _np(pr.out)[rows] - x, f["out"][rows] - x)
+    _close("dx[rows] - dout", _np(pr.dx)[rows] - dout, g["dx"][rows] - dout)
+    # dW2 is Y^T dOut over all tokens (Y as a BF16 pair, dOut BF16)
+    _close("dw2 = y^T dout", _np(pr.dw2), _np(pr.y).T @ b.dout.astype(np.float64), 1e-3)
+

@@ -134,6 +134,24 @@ def test_norm_none_and_no_gate():
     check(got2, run_oracle(b2), TOL["fp32"])
 
 
+@pytest.mark.parametrize("simt", [False, True])
+def test_fp32_gate_with_bf16_operands(simt):
+    # HSTU_FLAG_U_FP32: u is read as FP32 while q, k, v stay BF16; the gate's
+    # values carry more than 8 significant bits, which a BF16 u would drop
+    b = _ragged_batch("bf16", 128, 61)
+    b.u = (b.u * np.float32(1.0 + 2.0 ** -12)).astype(np.float32)
+    flags = C.HSTU_FLAG_U_FP32 | (C.HSTU_FLAG_FORCE_SIMT if simt else 0)
+    pr, got = run_gpu(b, flags=flags)
+    assert pr.u.dtype == torch.float32
+    check(got, run_oracle(b), TOL["bf16"])
+    # without a norm the gate is one FP32 product per element: y == o * u exactly,
+    # which a BF16 copy of u would break
+    b.norm = "none"
+    pr, got = run_gpu(b, flags=flags)
+    o = pr.o.float().cpu().numpy().reshape(b.T, -1)
+    np.testing.assert_array_equal(pr.y.cpu().numpy(), o * b.u)
+
+
 def test_bf16_outputs_round_the_fp32_outputs():
     b = _ragged_batch("bf16", 128, seed=58)
     _, g32 = run_gpu(b, out_dtype="fp32")

@@ -384,3 +384,52 @@ def test_layer_split_order_and_residual():
     a1 = f["z1"] / (1 + np.exp(-f["z1"]))
     np.testing.assert_array_equal(f["u"], a1[:, :D])
     np.testing.assert_array_equal(f["k"].reshape(-1, D), a1[:, 3 * D:])
+
+
+def test_bf16_round_matches_torch_conversion():
+    torch = pytest.importorskip("torch")
+    # float32 -> bfloat16 rounding to nearest even as torch performs it, including exact ties
+    r = np.random.default_rng(33)
+    a = (r.standard_normal(4000) * np.exp(r.uniform(-20, 20, 4000))).astype(np.float32)
+    bits = a.view(np.uint32)
+    ties = ((bits[:1000] & np.uint32(0xFFFF0000)) | np.uint32(0x8000)).view(np.float32)
+    a = np.concatenate([a, ties, np.float32([1.0, -2.5, 3.0e-3])])
+    want = torch.from_numpy(a).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.bf16_round(a.astype(np.float64)), want)
+
+
+def _layer_sample_rows(b):
+    # every candidate row and the last history row of each sequence: the keys of
+    # these rows are attended only by queries of the same set
+    rows = np.zeros(b.T, bool)
+    for i in range(b.B):
+        s, e = int(b.offsets[i]), int(b.offsets[i + 1])
+        rows[e - int(b.num_targets[i]) - 1:e] = True
+    return rows
+
+
+def test_layer_backward_on_rows_equals_full_backward():
+    b = _tiny_layer(34)
+    rows = _layer_sample_rows(b)
+    full = O.layer_backward(b)
+    part = O.layer_backward(b, rows=rows)
+    assert part["dw1"] is None and part["dw2"] is None and part["d_rab_pos"] is None
+    np.testing.assert_allclose(part["dx"][rows], full["dx"][rows], rtol=1e-12, atol=1e-12)
+    assert np.all(part["dx"][~rows] == 0)
+    f = O.layer_forward(b, rows=rows)
+    np.testing.assert_allclose(f["out"][rows], O.layer_forward(b)["out"][rows], rtol=1e-12, atol=1e-12)
+
+
+def test_layer_bf16_storage_stays_within_rounding_error():
+    # rounding the stored activations to bfloat16 (8 significant bits: relative
+    # error <= 2^-8 each) moves every output by a small multiple of 2^-8 of its scale
+    b = _tiny_layer(35)
+    exact_f, round_f = O.layer_forward(b), O.layer_forward(b, act_dtype="bf16")
+    exact_g, round_g = O.layer_backward(b, exact_f), O.layer_backward(b, round_f, act_dtype="bf16")
+    np.testing.assert_array_equal(round_f["u"], exact_f["u"])       # the gate is not rounded
+    assert np.all(np.abs(round_f["q"] - exact_f["q"]) <= 2.0 ** -8 * np.abs(exact_f["q"]))
+    assert not np.array_equal(round_f["q"], exact_f["q"])
+    for got, want in ((round_f["out"], exact_f["out"]), (round_g["dx"], exact_g["dx"]),
+                      (round_g["dw1"], exact_g["dw1"]), (round_g["dw2"], exact_g["dw2"])):
+        scale = math.sqrt(float(np.mean(want * want)))
+        assert np.max(np.abs(got - want)) <= 16 * 2.0 ** -8 * scale
