@@ -24,6 +24,7 @@ enum : int {
   WS_ERR_INFO = 2,  // detail of the first error (sequence index or wait site)
   WS_NTILES = 3,    // debug-plan tile counter
   WS_FLAGS = 4,     // planner findings (WS_FLAG_*)
+  WS_NEXT = 5,      // next work item of the tensor-core kernels (dynamic scheduling)
 };
 // some timestamp is 2^30 s or more away from its sequence's first token
 constexpr int WS_FLAG_WIDE_TS = 1;

@@ -61,6 +61,7 @@ plan_kernel(PlanParams p) {
     p.hdr[WS_NBLK] = 0;
     p.hdr[WS_NTILES] = 0;
     p.hdr[WS_FLAGS] = 0;
+    p.hdr[WS_NEXT] = 0;
     sh_bad = 0;
   }
   for (int i = t; i < kCostBins; i += kPlanThreads) sh_hist[i] = 0;

@@ -9,16 +9,22 @@
 //   dA^T = V dO^T                         (dO = dO_hi + dO_lo, two MMAs)
 //   A    = mask ? SiLU(z) / N : 0,  z = alpha S + rab_pos[bp] + rab_time[bt]
 //   dZ   = mask ? dA SiLU'(z) / N : 0,    SiLU'(z) = s (1 + z (1 - s))
-//   dV  += A^T dO                         (A from TMEM as hi/lo pair)
-//   dK  += dZ^T Q                         (dZ from TMEM as hi/lo pair)
+//   dV  += A^T dO                         (A from its own TMEM buffer, hi/lo)
+//   dK  += dZ^T Q                         (dZ^T staged in SMEM, hi/lo)
 //   dQ^T = K^T dZ^T                       (both MN-major in SMEM) -> FP32 red
 //   d_rab[bucket] += dZ                   (per-CTA partial sums, summed after)
+// S^T and dA^T are released as soon as the epilogue has loaded them, so the
+// next tile's S^T and dA^T are computed while this tile's A and dZ are; the
+// dQ^T of a tile is drained in the middle of the next one.
 // Every derived operand (dO, A, dZ) enters the tensor core as a BF16 pair
 // x = hi + lo; a single BF16 rounding of any of them costs ~1.5% of the
 // output RMS on heavy-tailed batches.
 //
 // Roles (576 threads): warps 0-15 epilogue (TMEM lane quarter warp%4, column
 // quarter warp/4), warp 16 TMA producer, warp 17 MMA issuer and TMEM owner.
+// The planner lists the key blocks longest-first and the producer takes the
+// next work item from a global counter (greedy LPT), passing it to the other
+// roles in a shared-memory slot with the item's key timestamps.
 #include "hstu_internal.h"
 #include "tc_ptx.cuh"
 
@@ -36,12 +42,21 @@ constexpr int kProducerWarp = 16, kMmaWarp = 17;
 constexpr int kThreads = 18 * 32;
 constexpr int kQStages = 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t DV_COL = 0, DK_COL = 128, S_COL = 256, DA_COL = 320, DQ_COL = 384;
+constexpr uint32_t DV_COL = 0, DK_COL = 128, S_COL = 256, DA_COL = 320, A_COL = 384, DQ_COL = 448;
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum : int { BAR_KVFULL = 0, BAR_KVEMPTY, BAR_QFULL, BAR_QEMPTY = BAR_QFULL + kQStages,
-             BAR_SFULL = BAR_QEMPTY + kQStages, BAR_PREADY, BAR_DQFULL, BAR_DQEMPTY, BAR_DKVFULL,
-             BAR_DKVEMPTY, BAR_DRAIN, BAR_COUNT };
+             BAR_SFULL = BAR_QEMPTY + kQStages, BAR_SEMPTY, BAR_PREADY, BAR_DQFULL, BAR_DQEMPTY,
+             BAR_DKVFULL, BAR_DKVEMPTY, BAR_DRAIN, BAR_COUNT };
+
+// A work item as the producer hands it to the other roles.
+struct __align__(16) ItemSlot {
+  int64_t s0;     // first token of the sequence
+  int64_t tbase;  // timestamp of that token (0 without timestamps)
+  int valid;      // 0: no more work
+  int h, k0, n, c, h_end;
+  int pad[2];
+};
 
 struct Lay {
   static constexpr int KBOX = BK * 128;            // 128 rows x 128 B = 16 KB
@@ -55,7 +70,9 @@ struct Lay {
   static constexpr int DZ_BYTES = BK * 128;
   static constexpr int TS64_OFF = DZ_OFF + 2 * DZ_BYTES;     // int64 [kQStages][BQ] absolute
   static constexpr int TS32_OFF = TS64_OFF + kQStages * BQ * 8;  // int32 [kQStages][BQ] relative
-  static constexpr int BAR_OFF = TS32_OFF + kQStages * BQ * 4;
+  static constexpr int KTS_OFF = TS32_OFF + kQStages * BQ * 4;   // int64 [BK] key times of the item
+  static constexpr int SLOT_OFF = KTS_OFF + BK * 8;              // ItemSlot
+  static constexpr int BAR_OFF = SLOT_OFF + (int)sizeof(ItemSlot);
   static constexpr int MISC_OFF = BAR_OFF + BAR_COUNT * 8;
   static constexpr int TAB_OFF = MISC_OFF + 16;              // float [H][P+Tb] bias
 };
@@ -84,23 +101,6 @@ __device__ __forceinline__ void red_add(float* addr, float v, bool pred) {
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
-struct Item {
-  int b, h, k0;
-  SeqInfo s;
-};
-
-__device__ __forceinline__ bool item_of(const AttnParams& p, int r, int nitems, Item& it) {
-  const int G = gridDim.x;
-  const int idx = r * G + ((r & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);  // snake order
-  if (idx >= nitems) return false;
-  const Block blk = p.blocks[idx / p.H];
-  it.b = blk.b;
-  it.h = idx % p.H;
-  it.k0 = blk.blk * BK;
-  it.s = seq_info(p.off, p.nt, p.nc, blk.b);
-  return true;
 }
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -248,6 +248,8 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   const uint32_t sQS = base_u32 + Lay::QS_OFF, sDZ = base_u32 + Lay::DZ_OFF;
   int64_t* ts64_s = reinterpret_cast<int64_t*>(base + Lay::TS64_OFF);
   int32_t* ts32_s = reinterpret_cast<int32_t*>(base + Lay::TS32_OFF);
+  int64_t* kts_s = reinterpret_cast<int64_t*>(base + Lay::KTS_OFF);
+  ItemSlot* slot = reinterpret_cast<ItemSlot*>(base + Lay::SLOT_OFF);
   const uint32_t bar0 = base_u32 + Lay::BAR_OFF;
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + Lay::MISC_OFF);
@@ -268,6 +270,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       mbar_init(bar(BAR_QEMPTY + s), 1);
     }
     mbar_init(bar(BAR_SFULL), 1);
+    mbar_init(bar(BAR_SEMPTY), kEpiWarps);
     mbar_init(bar(BAR_PREADY), kEpiWarps);
     mbar_init(bar(BAR_DQFULL), 1);
     mbar_init(bar(BAR_DQEMPTY), kEpiWarps);
@@ -313,38 +316,69 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    uint32_t item_it = 0, qt_it = 0, kv_armed = 0;
+    uint32_t item_it = 0, qt_it = 0, kv_phases = 0;
+    bool kv_copy = false;                 // the last KVFULL phase carries a copy
     uint32_t armed[kQStages] = {0, 0};
     bool ok = true;
-    Item it;
-    for (int r = 0; ok && item_of(p, r, nitems, it); ++r) {
-      const int n = it.s.n;
-      const int64_t tbase = p.ts ? p.ts[it.s.s0] : 0;
-      if (lane == 0) {
-        ok = mbar_wait(bar(BAR_KVEMPTY), (item_it & 1) ^ 1, wd, 21);
-        if (ok) {
-          mbar_arrive_expect_tx(bar(BAR_KVFULL), 4 * Lay::KBOX);
-          const int y = (int)(it.s.s0 + it.k0);
-          for (int c = 0; c < 2; ++c) {
-            tma_load_2d(sK + c * Lay::KBOX, &tmk, bar(BAR_KVFULL), it.h * D + c * 64, y);
-            tma_load_2d(sV + c * Lay::KBOX, &tmv, bar(BAR_KVFULL), it.h * D + c * 64, y);
-          }
-          ++kv_armed;
-        }
+    while (ok) {
+      int idx = 0;
+      if (lane == 0) idx = atomicAdd(p.hdr_rw + WS_NEXT, 1);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      const bool valid = idx < nitems;
+      int h = 0, k0 = 0;
+      SeqInfo sq{};
+      if (valid) {
+        const Block blk = p.blocks[idx / H];
+        h = idx % H;
+        k0 = blk.blk * BK;
+        sq = seq_info(p.off, p.nt, p.nc, blk.b);
       }
+      const int n = sq.n;
+      const int64_t tbase = (valid && p.ts) ? p.ts[sq.s0] : 0;
+      // key-row timestamps of the item: loads issued before waiting
+      int64_t kv[BK / 32];
+#pragma unroll
+      for (int x = 0; x < BK / 32; ++x) {
+        const int row = k0 + lane + 32 * x;
+        kv[x] = (valid && p.ts && row < n) ? p.ts[sq.s0 + row] : tbase;
+      }
+      if (lane == 0) ok = mbar_wait(bar(BAR_KVEMPTY), (item_it & 1) ^ 1, wd, 21);
       ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+#pragma unroll
+      for (int x = 0; x < BK / 32; ++x) kts_s[lane + 32 * x] = kv[x];
+      if (lane == 0) {
+        slot->s0 = sq.s0; slot->tbase = tbase; slot->valid = valid ? 1 : 0;
+        slot->h = h; slot->k0 = k0; slot->n = n; slot->c = sq.c; slot->h_end = sq.h_end;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        if (valid) {
+          mbar_arrive_expect_tx(bar(BAR_KVFULL), 4 * Lay::KBOX);
+          const int y = (int)(sq.s0 + k0);
+          for (int c = 0; c < 2; ++c) {
+            tma_load_2d(sK + c * Lay::KBOX, &tmk, bar(BAR_KVFULL), h * D + c * 64, y);
+            tma_load_2d(sV + c * Lay::KBOX, &tmv, bar(BAR_KVFULL), h * D + c * 64, y);
+          }
+        } else {
+          mbar_arrive(bar(BAR_KVFULL));  // the slot says: no more work
+        }
+        kv_phases += 1;
+        kv_copy = valid;
+      }
       ++item_it;
+      if (!valid) break;
       const int nqt = (n + BQ - 1) / BQ;
-      for (int qt = bwd_q_begin(it.k0, it.s.c, BQ); ok && qt < nqt; ++qt) {
+      for (int qt = bwd_q_begin(k0, sq.c, BQ); ok && qt < nqt; ++qt) {
         const int q0 = qt * BQ;
-        if (tile_class(q0, it.k0, BQ, BK, n, it.s.c, it.s.h_end) == 0) continue;
+        if (tile_class(q0, k0, BQ, BK, n, sq.c, sq.h_end) == 0) continue;
         const int stage = qt_it % kQStages;
         // query timestamps: loads issued before waiting for the stage, stored after
         int64_t tv[BQ / 32];
 #pragma unroll
         for (int x = 0; x < BQ / 32; ++x) {
           const int row = q0 + lane + 32 * x;
-          tv[x] = (p.ts && row < n) ? p.ts[it.s.s0 + row] : tbase;
+          tv[x] = (p.ts && row < n) ? p.ts[sq.s0 + row] : tbase;
         }
         ok = mbar_wait(bar(BAR_QEMPTY + stage), ((qt_it / kQStages) & 1) ^ 1, wd, 22);
         if (!ok) break;
@@ -358,11 +392,11 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           const uint32_t full = bar(BAR_QFULL + stage);
           mbar_arrive_expect_tx(full, Lay::QSTAGE);
           const uint32_t dst = sQS + stage * Lay::QSTAGE;
-          const int y = (int)(it.s.s0 + q0);
+          const int y = (int)(sq.s0 + q0);
           for (int c = 0; c < 2; ++c) {
-            tma_load_2d(dst + c * Lay::QBOX, &tmq, full, it.h * D + c * 64, y);
-            tma_load_2d(dst + Lay::Q_BYTES + c * Lay::QBOX, &tmdh, full, it.h * D + c * 64, y);
-            tma_load_2d(dst + 2 * Lay::Q_BYTES + c * Lay::QBOX, &tmdl, full, it.h * D + c * 64, y);
+            tma_load_2d(dst + c * Lay::QBOX, &tmq, full, h * D + c * 64, y);
+            tma_load_2d(dst + Lay::Q_BYTES + c * Lay::QBOX, &tmdh, full, h * D + c * 64, y);
+            tma_load_2d(dst + 2 * Lay::Q_BYTES + c * Lay::QBOX, &tmdl, full, h * D + c * 64, y);
           }
           armed[stage] += 1;
         }
@@ -372,29 +406,66 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     if (lane == 0) {
       for (int s = 0; s < kQStages; ++s)
         if (armed[s]) drain_wait(bar(BAR_QFULL + s), (armed[s] - 1) & 1);
-      if (kv_armed) drain_wait(bar(BAR_KVFULL), (kv_armed - 1) & 1);
+      if (kv_copy) drain_wait(bar(BAR_KVFULL), (kv_phases - 1) & 1);
     }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(BK, BQ, false, false);    // M=128 keys, N=64 queries
-      constexpr uint32_t IDESC_DVK = idesc_bf16(BK, D, false, true);    // A from TMEM, B MN-major
+      constexpr uint32_t IDESC_DVK = idesc_bf16(BK, D, false, true);    // A K-major, B MN-major
       constexpr uint32_t IDESC_DQ = idesc_bf16(D, BQ, true, true);      // A = K^T, B = dZ^T, MN-major
       uint32_t item_it = 0, qt_it = 0;
       bool ok = true;
-      Item it;
-      for (int r = 0; ok && item_of(p, r, nitems, it); ++r) {
-        const int n = it.s.n;
-        ok = mbar_wait(bar(BAR_KVFULL), item_it & 1, wd, 23) &&
-             mbar_wait(bar(BAR_DKVEMPTY), (item_it & 1) ^ 1, wd, 24);
+      // dV += A^T dO, dK += dZ^T Q, dQ^T = K^T dZ^T of query tile g (stage st)
+      auto issue_grad = [&](uint32_t g, uint32_t st, bool first) -> bool {
+        if (!mbar_wait(bar(BAR_PREADY), g & 1, wd, 26) ||
+            !mbar_wait(bar(BAR_DQEMPTY), (g & 1) ^ 1, wd, 27))
+          return false;
+        if (first && !mbar_wait(bar(BAR_DKVEMPTY), (item_it & 1) ^ 1, wd, 24)) return false;
+        fence_after_sync();
+        const uint32_t sQ = sQS + st * Lay::QSTAGE;
+        const uint32_t sDh = sQ + Lay::Q_BYTES, sDl = sQ + 2 * Lay::Q_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {   // K = 64 queries: 4 steps of 16
+          const uint32_t a_hi = tmem + A_COL + 16u * kk;
+          const uint64_t bdh = sdesc_sw128(sDh + kk * 2048, Lay::QBOX, 1024);
+          const uint64_t bdl = sdesc_sw128(sDl + kk * 2048, Lay::QBOX, 1024);
+          const uint64_t bq = sdesc_sw128(sQ + kk * 2048, Lay::QBOX, 1024);
+          const uint64_t zh = sdesc_sw128(sDZ + kk * 32, 16, 1024);
+          const uint64_t zl = sdesc_sw128(sDZ + Lay::DZ_BYTES + kk * 32, 16, 1024);
+          const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
+          mma_ts(tmem + DV_COL, a_hi, bdh, IDESC_DVK, acc0);
+          mma_ts(tmem + DV_COL, a_hi + 8, bdh, IDESC_DVK, 1u);
+          mma_ts(tmem + DV_COL, a_hi, bdl, IDESC_DVK, 1u);
+          mma_ss(tmem + DK_COL, zh, bq, IDESC_DVK, acc0);
+          mma_ss(tmem + DK_COL, zl, bq, IDESC_DVK, 1u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {   // K = 128 keys: 8 steps of 16
+          const uint64_t ak = sdesc_sw128(sK + kk * 2048, Lay::KBOX, 1024);
+          mma_ss(tmem + DQ_COL, ak, sdesc_sw128(sDZ + kk * 2048, Lay::DZ_BYTES, 1024), IDESC_DQ,
+                 kk > 0 ? 1u : 0u);
+          mma_ss(tmem + DQ_COL, ak, sdesc_sw128(sDZ + Lay::DZ_BYTES + kk * 2048, Lay::DZ_BYTES, 1024),
+                 IDESC_DQ, 1u);
+        }
+        mma_commit(bar(BAR_DQFULL));
+        mma_commit(bar(BAR_QEMPTY + st));
+        return true;
+      };
+      while (ok) {
+        ok = mbar_wait(bar(BAR_KVFULL), item_it & 1, wd, 23);
         if (!ok) break;
         fence_after_sync();
-        bool first = true;
-        const int nqt = (n + BQ - 1) / BQ;
-        for (int qt = bwd_q_begin(it.k0, it.s.c, BQ); ok && qt < nqt; ++qt) {
-          if (tile_class(qt * BQ, it.k0, BQ, BK, n, it.s.c, it.s.h_end) == 0) continue;
+        const ItemSlot sl = *slot;
+        if (!sl.valid) break;
+        bool have_prev = false, first = true;
+        uint32_t prev = 0, prev_st = 0;
+        const int nqt = (sl.n + BQ - 1) / BQ;
+        for (int qt = bwd_q_begin(sl.k0, sl.c, BQ); ok && qt < nqt; ++qt) {
+          if (tile_class(qt * BQ, sl.k0, BQ, BK, sl.n, sl.c, sl.h_end) == 0) continue;
           const uint32_t stage = qt_it % kQStages;
-          ok = mbar_wait(bar(BAR_QFULL + stage), (qt_it / kQStages) & 1, wd, 25);
+          ok = mbar_wait(bar(BAR_QFULL + stage), (qt_it / kQStages) & 1, wd, 25) &&
+               mbar_wait(bar(BAR_SEMPTY), (qt_it & 1) ^ 1, wd, 28);
           if (!ok) break;
           fence_after_sync();
           const uint32_t sQ = sQS + stage * Lay::QSTAGE;
@@ -416,39 +487,16 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
             mma_ss(tmem + DA_COL, av, sdesc_sw128(sDl + qb, 16, 1024), IDESC_S, 1u);
           }
           mma_commit(bar(BAR_SFULL));
-          ok = mbar_wait(bar(BAR_PREADY), qt_it & 1, wd, 26) &&
-               mbar_wait(bar(BAR_DQEMPTY), (qt_it & 1) ^ 1, wd, 27);
-          if (!ok) break;
-          fence_after_sync();
-          // dV += A^T dO ; dK += dZ^T Q   (K = 64 queries: 4 steps of 16, one per column quarter)
-#pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk) {
-            const uint32_t a_hi = tmem + S_COL + 16u * kk;
-            const uint32_t z_hi = tmem + DA_COL + 16u * kk;
-            const uint64_t bdh = sdesc_sw128(sDh + kk * 2048, Lay::QBOX, 1024);
-            const uint64_t bdl = sdesc_sw128(sDl + kk * 2048, Lay::QBOX, 1024);
-            const uint64_t bq = sdesc_sw128(sQ + kk * 2048, Lay::QBOX, 1024);
-            const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
-            mma_ts(tmem + DV_COL, a_hi, bdh, IDESC_DVK, acc0);
-            mma_ts(tmem + DV_COL, a_hi + 8, bdh, IDESC_DVK, 1u);
-            mma_ts(tmem + DV_COL, a_hi, bdl, IDESC_DVK, 1u);
-            mma_ts(tmem + DK_COL, z_hi, bq, IDESC_DVK, acc0);
-            mma_ts(tmem + DK_COL, z_hi + 8, bq, IDESC_DVK, 1u);
+          if (have_prev) {
+            ok = issue_grad(prev, prev_st, first);
+            first = false;
           }
-          // dQ^T = K^T dZ^T  (K = 128 keys: 8 steps of 16)
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ak = sdesc_sw128(sK + kk * 2048, Lay::KBOX, 1024);
-            mma_ss(tmem + DQ_COL, ak, sdesc_sw128(sDZ + kk * 2048, Lay::DZ_BYTES, 1024), IDESC_DQ,
-                   kk > 0 ? 1u : 0u);
-            mma_ss(tmem + DQ_COL, ak, sdesc_sw128(sDZ + Lay::DZ_BYTES + kk * 2048, Lay::DZ_BYTES, 1024),
-                   IDESC_DQ, 1u);
-          }
-          mma_commit(bar(BAR_DQFULL));
-          mma_commit(bar(BAR_QEMPTY + stage));
-          first = false;
+          have_prev = true;
+          prev = qt_it;
+          prev_st = stage;
           ++qt_it;
         }
+        if (ok && have_prev) ok = issue_grad(prev, prev_st, first);
         if (!ok) break;
         mma_commit(bar(BAR_DKVFULL));
         mma_commit(bar(BAR_KVEMPTY));
@@ -464,7 +512,6 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
     uint32_t item_it = 0, qt_it = 0;
     bool ok = true;
-    Item it;
     KeyCtx kc;
     kc.P = P;
     kc.Tb = Tb;
@@ -474,42 +521,72 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     kc.kC = -p.inv_n / kLog2e;
     kc.kZ = -1.0f / kLog2e;
     kc.inv_n = p.inv_n;
-    for (int r = 0; ok && item_of(p, r, nitems, it); ++r) {
-      kc.n = it.s.n;
-      kc.cx = it.s.c;
-      kc.h_end = it.s.h_end;
-      kc.j = it.k0 + lrow;
+    // the dQ^T of the previous query tile, drained in the middle of the next
+    auto drain_dq = [&](uint32_t g, int qb0, int64_t s0, int hh) -> bool {
+      if (!mbar_wait(bar(BAR_DQFULL), g & 1, wd, 30)) return false;
+      fence_after_sync();
+      uint32_t qv[16];
+      tmem_ld16(lane_base + DQ_COL + hq * 16, qv);
+      tmem_wait_ld();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_DQEMPTY));
+      const int ib = qb0 + hq * 16;
+      float* dst = p.dq_acc + ((size_t)(s0 + ib) * H + hh) * D + lrow;
+      const size_t ld = (size_t)H * D;
+      const float alpha = p.alpha;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (ib + c < kc.n) atomicAdd(dst + c * ld, alpha * __uint_as_float(qv[c]));
+      return true;
+    };
+    while (ok) {
+      ok = mbar_wait(bar(BAR_KVFULL), item_it & 1, wd, 32);
+      if (!ok) break;
+      // the slot stays until this item's last tile is handed over; keep what
+      // the dV / dK write-out needs in registers
+      const ItemSlot& sl = *slot;
+      if (!sl.valid) break;
+      const int64_t s0 = sl.s0;
+      const int hh = sl.h, k0 = sl.k0;
+      kc.n = sl.n;
+      kc.cx = sl.c;
+      kc.h_end = sl.h_end;
+      kc.j = k0 + lrow;
       kc.j_ok = kc.j < kc.n;
       kc.pos_j = kc.j < kc.h_end ? kc.j : kc.h_end;
-      const int64_t tbase = p.ts ? p.ts[it.s.s0] : 0;
-      kc.tj64 = (p.ts && kc.j_ok) ? p.ts[it.s.s0 + kc.j] : tbase;
-      kc.tj32 = (int32_t)(kc.tj64 - tbase);
-      kc.tp = tab + it.h * PT;
+      kc.tj64 = kts_s[lrow];
+      kc.tj32 = (int32_t)(kc.tj64 - sl.tbase);
+      kc.tp = tab + hh * PT;
       kc.tt = kc.tp + P;
-      kc.drp = drab + it.h * PT;
+      kc.drp = drab + hh * PT;
       kc.drt = kc.drp + P;
       RabAcc racc;
       racc.rp_far = racc.diag = racc.rt_run = 0.f;
       racc.rt_cur = -1;
+      bool pend = false;    // a dQ^T of this item waits to be drained
+      int pend_q0 = 0;
       const int nqt = (kc.n + BQ - 1) / BQ;
-      for (int qt = bwd_q_begin(it.k0, kc.cx, BQ); ok && qt < nqt; ++qt) {
+      for (int qt = bwd_q_begin(k0, kc.cx, BQ); ok && qt < nqt; ++qt) {
         const int q0 = qt * BQ;
-        const int cls = tile_class(q0, it.k0, BQ, BK, kc.n, kc.cx, kc.h_end);
+        const int cls = tile_class(q0, k0, BQ, BK, kc.n, kc.cx, kc.h_end);
         if (cls == 0) continue;
         const uint32_t stage = qt_it % kQStages;
         ok = mbar_wait(bar(BAR_QFULL + stage), (qt_it / kQStages) & 1, wd, 28) &&
              mbar_wait(bar(BAR_SFULL), qt_it & 1, wd, 29);
         if (!ok) break;
         fence_after_sync();
-        const bool fast = cls == 2 && it.k0 + BK - 1 <= q0 && q0 + BQ <= kc.h_end;
+        const bool fast = cls == 2 && k0 + BK - 1 <= q0 && q0 + BQ <= kc.h_end;
         // position gap of lane 0 at this warp's first query column (causal full tiles)
-        const int kbase = (q0 + hq * 16) - (it.k0 + wq * 32);
-        // all 16 columns of the quarter are read before any is overwritten
+        const int kbase = (q0 + hq * 16) - (k0 + wq * 32);
         uint32_t svq[16], daq[16];
         tmem_ld16(lane_base + S_COL + hq * 16, svq);
         tmem_ld16(lane_base + DA_COL + hq * 16, daq);
         tmem_wait_ld();
-        // then computed and written back in two halves of 8 (register budget)
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_SEMPTY));   // S^T, dA^T may be overwritten now
+        // computed and written out in two halves of 8 query columns
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const int c0 = hq * 16 + half * 8;    // first query column of this half within the tile
@@ -531,19 +608,25 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
             if (cls == 2) grad_cols<8, false, true, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc, half * 8, kbase);
             else grad_cols<8, false, true, true>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc, half * 8, kbase);
           }
-          // A and dZ back into TMEM.  Quarter hq owns columns [16 hq, 16 hq + 16):
+          if (half == 0 && pend) {
+            // the previous tile's gradient MMAs are complete once its dQ^T is:
+            // the A buffer and the dZ^T staging are free again
+            ok = drain_dq(qt_it - 1, pend_q0, s0, hh);
+            if (!ok) break;
+            pend = false;
+          }
+          // A into its TMEM buffer.  Quarter hq owns columns [16 hq, 16 hq + 16):
           // hi pairs in the first 8, lo pairs in the last 8; this half's 8
           // queries are 4 packed columns of each.
-          tmem_st4(lane_base + S_COL + hq * 16 + half * 4, ahi);
-          tmem_st4(lane_base + S_COL + hq * 16 + 8 + half * 4, alo);
-          tmem_st4(lane_base + DA_COL + hq * 16 + half * 4, zhi);
-          tmem_st4(lane_base + DA_COL + hq * 16 + 8 + half * 4, zlo);
-          // dZ^T into SMEM (row = key, 64 queries = 128 B, 128-byte swizzle) for the dQ MMA
+          tmem_st4(lane_base + A_COL + hq * 16 + half * 4, ahi);
+          tmem_st4(lane_base + A_COL + hq * 16 + 8 + half * 4, alo);
+          // dZ^T into SMEM (row = key, 64 queries = 128 B, 128-byte swizzle) for the dK and dQ MMAs
           const uint32_t rowh = sDZ + (uint32_t)lrow * 128u, rowl = rowh + Lay::DZ_BYTES;
           const uint32_t chunk = (uint32_t)((hq * 2 + half) ^ (lrow & 7));
           st_shared_v4(rowh + chunk * 16, zhi[0], zhi[1], zhi[2], zhi[3]);
           st_shared_v4(rowl + chunk * 16, zlo[0], zlo[1], zlo[2], zlo[3]);
         }
+        if (!ok) break;
         if (fast && kc.want_rp) {  // diagonals still held at the end of the 16-column sweep
           const int key = kbase + 15 - lane;
           red_add(kc.drp + key, racc.diag, racc.diag != 0.f && key < P - 1);
@@ -554,28 +637,15 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_PREADY));
-        // dQ^T drain: lane = d, columns = the 16 queries of this quarter
-        ok = mbar_wait(bar(BAR_DQFULL), qt_it & 1, wd, 30);
-        if (!ok) break;
-        fence_after_sync();
-        uint32_t qv[16];
-        tmem_ld16(lane_base + DQ_COL + hq * 16, qv);
-        tmem_wait_ld();
-        fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_DQEMPTY));
-        {
-          const int ib = q0 + hq * 16;
-          float* dst = p.dq_acc + ((size_t)(it.s.s0 + ib) * H + it.h) * D + lrow;
-          const size_t ld = (size_t)H * D;
-          const float alpha = p.alpha;
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            if (ib + c < kc.n) atomicAdd(dst + c * ld, alpha * __uint_as_float(qv[c]));
-        }
+        pend = true;
+        pend_q0 = q0;
         ++qt_it;
       }
       if (!ok) break;
+      if (pend) {
+        ok = drain_dq(qt_it - 1, pend_q0, s0, hh);
+        if (!ok) break;
+      }
       // the item's remaining d_rab partial sums
       red_add(kc.drt + racc.rt_cur, racc.rt_run, want_rt && racc.rt_cur >= 0);
       if (want_rp) {
@@ -595,7 +665,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_DKVEMPTY));
       if (kc.j_ok) {
-        const size_t g = ((size_t)(it.s.s0 + kc.j) * H + it.h) * D + hq * 32;
+        const size_t g = ((size_t)(s0 + kc.j) * H + hh) * D + hq * 32;
         TO* dvp = static_cast<TO*>(p.dv) + g;
         TO* dkp = static_cast<TO*>(p.dk) + g;
         const float alpha = p.alpha;

@@ -22,8 +22,14 @@
 //
 // Roles (576 threads): warps 0-15 epilogue (warp w reads TMEM lanes
 // 32*(w%4).. and the 32-column quarter w/4 of each tile), warp 16 TMA
-// producer (plus key timestamps), warp 17 MMA issuer and TMEM owner.
+// producer (plus timestamps), warp 17 MMA issuer and TMEM owner.
 // TMEM columns: S/P buffers at 0 and 128, O buffers at 256 and 256 + d.
+//
+// Scheduling: the planner lists the query blocks longest-first; the producer
+// of each CTA takes the next work item from a global counter (greedy LPT,
+// dynamic), and passes it to the other roles through a shared-memory slot
+// that travels with one of two Q buffers, so the next item's Q and first K/V
+// are loading while the current item's last tiles are computed.
 #include "hstu_internal.h"
 #include "tc_ptx.cuh"
 
@@ -42,42 +48,40 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSColStride = 128;  // S/P buffer sb starts at column sb * 128
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum : int { BAR_QFULL = 0, BAR_QEMPTY, BAR_KVFULL, BAR_KVEMPTY = BAR_KVFULL + kStages,
+constexpr int kQBufs = 2;
+
+enum : int { BAR_QFULL = 0, BAR_QEMPTY = BAR_QFULL + kQBufs, BAR_KVFULL = BAR_QEMPTY + kQBufs,
+             BAR_KVEMPTY = BAR_KVFULL + kStages,
              BAR_SFULL = BAR_KVEMPTY + kStages, BAR_PREADY = BAR_SFULL + 2, BAR_OFULL = BAR_PREADY + 2,
              BAR_OEMPTY = BAR_OFULL + 2, BAR_DRAIN = BAR_OEMPTY + 2, BAR_COUNT };
+
+// A work item as the producer hands it to the other roles (one per Q buffer).
+struct __align__(16) ItemSlot {
+  int64_t s0;     // first token of the sequence
+  int64_t tbase;  // timestamp of that token (0 without timestamps)
+  int valid;      // 0: no more work
+  int h, q0, n, c, h_end;
+  int pad[2];
+};
 
 template <int D>
 struct Layout {
   static constexpr int NCH = D / 64;            // 128-byte column chunks per row
   static constexpr int BOX = 128 * 128;         // one TMA box: 128 rows x 64 bf16 = 16 KB
-  static constexpr int Q_OFF = 0;
+  static constexpr int Q_BYTES = NCH * BOX;
+  static constexpr int Q_OFF = 0;               // kQBufs Q buffers
   static constexpr int K_BYTES = NCH * BOX;
   static constexpr int STAGE = 2 * K_BYTES;     // K then V
-  static constexpr int KV_OFF = Q_OFF + NCH * BOX;
-  static constexpr int TS64_OFF = KV_OFF + kStages * STAGE;     // int64 [kStages][BN] absolute
+  static constexpr int KV_OFF = Q_OFF + kQBufs * Q_BYTES;
+  static constexpr int TS64_OFF = KV_OFF + kStages * STAGE;     // int64 [kStages][BN] key times, absolute
   static constexpr int TS32_OFF = TS64_OFF + kStages * BN * 8;  // int32 [kStages][BN] relative
-  static constexpr int BAR_OFF = TS32_OFF + kStages * BN * 4;
+  static constexpr int QTS_OFF = TS32_OFF + kStages * BN * 4;   // int64 [kQBufs][BM] query times
+  static constexpr int SLOT_OFF = QTS_OFF + kQBufs * BM * 8;    // ItemSlot [kQBufs]
+  static constexpr int BAR_OFF = SLOT_OFF + kQBufs * (int)sizeof(ItemSlot);
   static constexpr int MISC_OFF = BAR_OFF + BAR_COUNT * 8;      // tmem slot, abort flag
   static constexpr int TAB_OFF = MISC_OFF + 16;                 // float [H][P + Tb]
   static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
 };
-
-struct ItemInfo {
-  int b, h, q0;
-  SeqInfo s;
-};
-
-__device__ __forceinline__ bool item_of(const AttnParams& p, int r, int nitems, ItemInfo& it) {
-  const int G = gridDim.x;
-  const int idx = r * G + ((r & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);  // snake order
-  if (idx >= nitems) return false;
-  const Block blk = p.blocks[idx / p.H];
-  it.b = blk.b;
-  it.h = idx % p.H;
-  it.q0 = blk.blk * BM;
-  it.s = seq_info(p.off, p.nt, p.nc, blk.b);
-  return true;
-}
 
 // waits for a phase, ignoring the abort flag (used to drain async copies)
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -179,10 +183,12 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
-  const uint32_t sQ = base_u32 + L::Q_OFF;
+  const uint32_t sQ0 = base_u32 + L::Q_OFF;
   const uint32_t sKV = base_u32 + L::KV_OFF;
   int64_t* ts64_s = reinterpret_cast<int64_t*>(base + L::TS64_OFF);
   int32_t* ts32_s = reinterpret_cast<int32_t*>(base + L::TS32_OFF);
+  int64_t* qts_s = reinterpret_cast<int64_t*>(base + L::QTS_OFF);
+  ItemSlot* slots = reinterpret_cast<ItemSlot*>(base + L::SLOT_OFF);
   const uint32_t bar0 = base_u32 + L::BAR_OFF;
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::MISC_OFF);
@@ -193,8 +199,10 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   const int H = p.H, P = p.P, Tb = p.Tb, PT = p.P + p.Tb;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(BAR_QFULL), 1);
-    mbar_init(bar(BAR_QEMPTY), 1);
+    for (int s = 0; s < kQBufs; ++s) {
+      mbar_init(bar(BAR_QFULL + s), 1);
+      mbar_init(bar(BAR_QEMPTY + s), 1);
+    }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(BAR_KVFULL + s), 1);
       mbar_init(bar(BAR_KVEMPTY + s), 1);
@@ -245,33 +253,69 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     uint32_t kv_it = 0, q_it = 0;
-    uint32_t armed[kStages] = {0, 0};   // phases armed per stage
+    uint32_t armed[kStages] = {0, 0};   // phases armed per KV stage
+    uint32_t q_phases[kQBufs] = {0, 0};  // phases used per Q buffer (a copy or the final no-work arrive)
+    bool q_copy[kQBufs] = {false, false}; // the buffer's last phase carries a copy
     bool ok = true;
-    ItemInfo it;
-    for (int r = 0; ok && item_of(p, r, nitems, it); ++r) {
-      const int n = it.s.n;
-      const int64_t tbase = p.ts ? p.ts[it.s.s0] : 0;
-      if (lane == 0) {
-        ok = mbar_wait(bar(BAR_QEMPTY), (q_it & 1) ^ 1, wd, 1);
-        if (ok) {
-          mbar_arrive_expect_tx(bar(BAR_QFULL), L::NCH * L::BOX);
-          for (int c = 0; c < L::NCH; ++c)
-            tma_load_2d(sQ + c * L::BOX, &tmq, bar(BAR_QFULL), it.h * D + c * 64, (int)(it.s.s0 + it.q0));
-        }
+    while (ok) {
+      const int qb = (int)(q_it % kQBufs);
+      int idx = 0;
+      if (lane == 0) idx = atomicAdd(p.hdr_rw + WS_NEXT, 1);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      const bool valid = idx < nitems;
+      int h = 0, q0 = 0;
+      SeqInfo sq{};
+      if (valid) {
+        const Block blk = p.blocks[idx / H];
+        h = idx % H;
+        q0 = blk.blk * BM;
+        sq = seq_info(p.off, p.nt, p.nc, blk.b);
       }
+      const int64_t tbase = (valid && p.ts) ? p.ts[sq.s0] : 0;
+      // query-row timestamps: loads issued before waiting for the buffer
+      int64_t qv[BM / 32];
+#pragma unroll
+      for (int x = 0; x < BM / 32; ++x) {
+        const int row = q0 + lane + 32 * x;
+        qv[x] = (valid && p.ts && row < sq.n) ? p.ts[sq.s0 + row] : tbase;
+      }
+      if (lane == 0) ok = mbar_wait(bar(BAR_QEMPTY + qb), ((q_it / kQBufs) & 1) ^ 1, wd, 1);
       ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+#pragma unroll
+      for (int x = 0; x < BM / 32; ++x) qts_s[qb * BM + lane + 32 * x] = qv[x];
+      if (lane == 0) {
+        ItemSlot& sl = slots[qb];
+        sl.s0 = sq.s0; sl.tbase = tbase; sl.valid = valid ? 1 : 0;
+        sl.h = h; sl.q0 = q0; sl.n = sq.n; sl.c = sq.c; sl.h_end = sq.h_end;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        if (valid) {
+          mbar_arrive_expect_tx(bar(BAR_QFULL + qb), L::Q_BYTES);
+          for (int c = 0; c < L::NCH; ++c)
+            tma_load_2d(sQ0 + qb * L::Q_BYTES + c * L::BOX, &tmq, bar(BAR_QFULL + qb), h * D + c * 64,
+                        (int)(sq.s0 + q0));
+        } else {
+          mbar_arrive(bar(BAR_QFULL + qb));  // the slot says: no more work
+        }
+        q_phases[qb] += 1;
+        q_copy[qb] = valid;
+      }
       ++q_it;
-      const int nkb = fwd_kv_blocks(it.q0, n, it.s.c, BM, BN);
+      if (!valid) break;
+      const int n = sq.n;
+      const int nkb = fwd_kv_blocks(q0, n, sq.c, BM, BN);
       for (int kb = 0; ok && kb < nkb; ++kb) {
         const int k0 = kb * BN;
-        if (tile_class(it.q0, k0, BM, BN, n, it.s.c, it.s.h_end) == 0) continue;
+        if (tile_class(q0, k0, BM, BN, n, sq.c, sq.h_end) == 0) continue;
         const int stage = kv_it % kStages;
         // key timestamps: loads issued before waiting for the stage, stored after
         int64_t tv[BN / 32];
 #pragma unroll
         for (int x = 0; x < BN / 32; ++x) {
           const int row = k0 + lane + 32 * x;
-          tv[x] = (p.ts && row < n) ? p.ts[it.s.s0 + row] : tbase;
+          tv[x] = (p.ts && row < n) ? p.ts[sq.s0 + row] : tbase;
         }
         ok = mbar_wait(bar(BAR_KVEMPTY + stage), ((kv_it / kStages) & 1) ^ 1, wd, 2);
         if (!ok) break;
@@ -285,10 +329,10 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         if (lane == 0 && !withhold) {
           mbar_arrive_expect_tx(bar(BAR_KVFULL + stage), L::STAGE);
           const uint32_t dstK = sKV + stage * L::STAGE;
-          const int y = (int)(it.s.s0 + k0);
+          const int y = (int)(sq.s0 + k0);
           for (int c = 0; c < L::NCH; ++c) {
-            tma_load_2d(dstK + c * L::BOX, &tmk, bar(BAR_KVFULL + stage), it.h * D + c * 64, y);
-            tma_load_2d(dstK + L::K_BYTES + c * L::BOX, &tmv, bar(BAR_KVFULL + stage), it.h * D + c * 64, y);
+            tma_load_2d(dstK + c * L::BOX, &tmk, bar(BAR_KVFULL + stage), h * D + c * 64, y);
+            tma_load_2d(dstK + L::K_BYTES + c * L::BOX, &tmv, bar(BAR_KVFULL + stage), h * D + c * 64, y);
           }
           armed[stage] += 1;
         }
@@ -299,7 +343,9 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s)
         if (armed[s]) drain_wait(bar(BAR_KVFULL + s), (armed[s] - 1) & 1);
-      if (q_it) drain_wait(bar(BAR_QFULL), (q_it - 1) & 1);
+      // an earlier phase of a Q buffer completed before the buffer was reused
+      for (int s = 0; s < kQBufs; ++s)
+        if (q_copy[s]) drain_wait(bar(BAR_QFULL + s), (q_phases[s] - 1) & 1);
     }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
@@ -308,18 +354,22 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, false, true);
       uint32_t kv_it = 0, q_it = 0, o_it = 0;
       bool ok = true;
-      ItemInfo it;
-      for (int r = 0; ok && item_of(p, r, nitems, it); ++r) {
-        const int n = it.s.n;
+      while (ok) {
+        const uint32_t qb = q_it % kQBufs;
+        ok = mbar_wait(bar(BAR_QFULL + qb), (q_it / kQBufs) & 1, wd, 3);
+        if (!ok) break;
+        fence_after_sync();
+        const ItemSlot sl = slots[qb];
+        if (!sl.valid) break;
+        const uint32_t sQ = sQ0 + qb * L::Q_BYTES;
         const uint32_t ob = o_it & 1;
         const uint32_t ocol = ob ? L::O_COL1 : L::O_COL0;
-        ok = mbar_wait(bar(BAR_QFULL), q_it & 1, wd, 3) &&
-             mbar_wait(bar(BAR_OEMPTY + ob), ((o_it >> 1) & 1) ^ 1, wd, 4);
+        ok = mbar_wait(bar(BAR_OEMPTY + ob), ((o_it >> 1) & 1) ^ 1, wd, 4);
         if (!ok) break;
         fence_after_sync();
         bool have_prev = false, first_pv = true;
         uint32_t prev_it = 0;
-        const int nkb = fwd_kv_blocks(it.q0, n, it.s.c, BM, BN);
+        const int nkb = fwd_kv_blocks(sl.q0, sl.n, sl.c, BM, BN);
         // P of tile t: quarter k/2 of the S buffer, hi at [32 q, 32 q + 16), lo 16 columns later
         auto issue_pv = [&](uint32_t t) -> bool {
           const uint32_t sb = t & 1, stage = t % kStages;
@@ -339,7 +389,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         };
         for (int kb = 0; ok && kb < nkb; ++kb) {
           const int k0 = kb * BN;
-          if (tile_class(it.q0, k0, BM, BN, n, it.s.c, it.s.h_end) == 0) continue;
+          if (tile_class(sl.q0, k0, BM, BN, sl.n, sl.c, sl.h_end) == 0) continue;
           const uint32_t stage = kv_it % kStages, sb = kv_it & 1;
           ok = mbar_wait(bar(BAR_KVFULL + stage), (kv_it / kStages) & 1, wd, 6);
           if (!ok) break;
@@ -359,7 +409,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         }
         if (ok && have_prev) ok = issue_pv(prev_it);
         if (!ok) break;
-        mma_commit(bar(BAR_QEMPTY));
+        mma_commit(bar(BAR_QEMPTY + qb));
         mma_commit(bar(BAR_OFULL + ob));
         ++q_it;
         ++o_it;
@@ -373,30 +423,37 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     const int wq = warp & 3, hq = warp >> 2;      // TMEM lane quarter, column quarter
     const int row = wq * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
-    uint32_t kv_it = 0, o_it = 0;
+    uint32_t kv_it = 0, o_it = 0, q_it = 0;
     bool ok = true;
-    ItemInfo it;
     RowCtx rc;
     rc.P = P;
     rc.Tb = Tb;
     rc.kA = -kLog2e * p.alpha;
     rc.kC = -p.inv_n / kLog2e;
-    for (int r = 0; ok && item_of(p, r, nitems, it); ++r) {
-      rc.n = it.s.n;
-      rc.cx = it.s.c;
-      rc.h_end = it.s.h_end;
-      rc.i = it.q0 + row;
+    while (ok) {
+      const uint32_t qb = q_it % kQBufs;
+      ok = mbar_wait(bar(BAR_QFULL + qb), (q_it / kQBufs) & 1, wd, 10);
+      if (!ok) break;
+      // the slot stays until this item's last P is handed over; keep what the
+      // O write-out needs in registers
+      const ItemSlot& sl = slots[qb];
+      if (!sl.valid) break;
+      const int64_t s0 = sl.s0;
+      const int hh = sl.h, q0 = sl.q0;
+      rc.n = sl.n;
+      rc.cx = sl.c;
+      rc.h_end = sl.h_end;
+      rc.i = q0 + row;
       rc.row_ok = rc.i < rc.n;
       rc.pos_i = rc.i < rc.h_end ? rc.i : rc.h_end;
-      const int64_t tbase = p.ts ? p.ts[it.s.s0] : 0;
-      rc.ti64 = (p.ts && rc.row_ok) ? p.ts[it.s.s0 + rc.i] : tbase;
-      rc.ti32 = (int32_t)(rc.ti64 - tbase);
-      rc.tp = tab + it.h * PT;
+      rc.ti64 = qts_s[qb * BM + row];
+      rc.ti32 = (int32_t)(rc.ti64 - sl.tbase);
+      rc.tp = tab + hh * PT;
       rc.tt = rc.tp + P;
-      const int nkb = fwd_kv_blocks(it.q0, rc.n, rc.cx, BM, BN);
+      const int nkb = fwd_kv_blocks(q0, rc.n, rc.cx, BM, BN);
       for (int kb = 0; ok && kb < nkb; ++kb) {
         const int k0 = kb * BN;
-        const int cls = tile_class(it.q0, k0, BM, BN, rc.n, rc.cx, rc.h_end);
+        const int cls = tile_class(q0, k0, BM, BN, rc.n, rc.cx, rc.h_end);
         if (cls == 0) continue;
         const uint32_t stage = kv_it % kStages, sb = kv_it & 1;
         ok = mbar_wait(bar(BAR_KVFULL + stage), (kv_it / kStages) & 1, wd, 7) &&
@@ -411,7 +468,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         const int32_t* t32 = ts32_s + stage * BN + hq * 32;
         const int64_t* t64 = ts64_s + stage * BN + hq * 32;
         uint32_t hi[16], lo[16];
-        const bool fast = cls == 2 && k0 + BN - 1 <= it.q0;
+        const bool fast = cls == 2 && k0 + BN - 1 <= q0;
         if (!wide_ts) {
           if (fast) score32<true, false, false>(sv, hi, lo, rc, jb, t32, t64);
           else if (cls == 2) score32<false, false, false>(sv, hi, lo, rc, jb, t32, t64);
@@ -451,7 +508,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_OEMPTY + ob));
       if (rc.row_ok) {
-        TO* orow = static_cast<TO*>(p.o) + ((size_t)(it.s.s0 + rc.i) * H + it.h) * D + hq * QC;
+        TO* orow = static_cast<TO*>(p.o) + ((size_t)(s0 + rc.i) * H + hh) * D + hq * QC;
         if constexpr (sizeof(TO) == 4) {
           float4* dst = reinterpret_cast<float4*>(orow);
 #pragma unroll
@@ -469,6 +526,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         }
       }
       ++o_it;
+      ++q_it;
     }
   }
 
