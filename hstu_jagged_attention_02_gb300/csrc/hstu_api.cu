@@ -293,13 +293,18 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
   float* dq_acc = dq_direct ? static_cast<float*>(a->dq) : reinterpret_cast<float*>(ws + L.dq_acc);
   const bool has_rp = a->rab_pos != nullptr;
   const bool has_rt = a->rab_time != nullptr && a->timestamps != nullptr;
-  if (a->d_rab_pos) HSTU_CUDA_TRY(cudaMemsetAsync(a->d_rab_pos, 0, sizeof(float) * d->H * d->num_pos_buckets, st));
-  if (a->d_rab_time) HSTU_CUDA_TRY(cudaMemsetAsync(a->d_rab_time, 0, sizeof(float) * d->H * d->num_time_buckets, st));
+  // the tensor-core path's reduction writes every d_rab entry of a table that
+  // is present; the other outputs start from zero
+  const bool reduced_rp = tc && has_rp && d->total_tokens > 0;
+  const bool reduced_rt = tc && has_rt && d->total_tokens > 0;
+  if (a->d_rab_pos && !reduced_rp)
+    HSTU_CUDA_TRY(cudaMemsetAsync(a->d_rab_pos, 0, sizeof(float) * d->H * d->num_pos_buckets, st));
+  if (a->d_rab_time && !reduced_rt)
+    HSTU_CUDA_TRY(cudaMemsetAsync(a->d_rab_time, 0, sizeof(float) * d->H * d->num_time_buckets, st));
   if (d->total_tokens == 0) return HSTU_OK;
   HSTU_CUDA_TRY(cudaMemsetAsync(dq_acc, 0, sizeof(float) * rows * d->d_qk, st));
+  // per-CTA d_rab partial sums: each tensor-core CTA zeroes its own row first
   float* drab_partial = reinterpret_cast<float*>(ws + L.drab_part);
-  if (tc && ((has_rp && a->d_rab_pos) || (has_rt && a->d_rab_time)))
-    HSTU_CUDA_TRY(cudaMemsetAsync(drab_partial, 0, L.drab_part_bytes, st));
 
   // gradient w.r.t. o, in the input type (an MMA operand of the attention backward)
   {

@@ -22,7 +22,12 @@ struct PlanParams {
   Block* tmp;       // [cap_blocks] scratch
   Block* blocks;    // [cap_blocks] result, longest first
   int cap_blocks;
+  int stage_off;    // set by launch_plan: offsets and block starts staged in shared memory
+  int stage_rec;    // set by launch_plan: block records staged in shared memory
 };
+// planner shared-memory staging limits (sequences, blocks)
+constexpr int kPlanStageSeqs = 2048;
+constexpr int kPlanStageBlocks = 8192;
 
 // Everything a forward or backward attention kernel needs.
 struct AttnParams {

@@ -15,22 +15,34 @@ namespace hstu {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kOffStage = 2048;  // sequence offsets staged in shared memory (B + 1 <= this)
-constexpr int kUnroll = 8;       // tokens per thread in flight in the timestamp check
+constexpr int kPlanWarps = kPlanThreads / 32;
+constexpr int kUnroll = 8;  // tokens per thread in flight in the timestamp check
 
-__device__ int block_scan_exclusive(int v, int* sh) {
-  // inclusive scan of v over the CTA, returns the exclusive prefix; sh holds
-  // kPlanThreads ints; the CTA total is left in sh[kPlanThreads - 1]
-  const int t = threadIdx.x;
-  sh[t] = v;
-  __syncthreads();
-  for (int off = 1; off < kPlanThreads; off <<= 1) {
-    int x = t >= off ? sh[t - off] : 0;
-    __syncthreads();
-    sh[t] += x;
-    __syncthreads();
+// Exclusive prefix sum of v over the CTA (warp shuffles, two barriers); the
+// CTA total goes to *total.  wsum holds kPlanWarps ints.
+__device__ int cta_exclusive_scan(int v, int* wsum, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  return sh[t] - v;
+  if (lane == 31) wsum[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int s = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    wsum[lane] = s;  // inclusive over warps
+  }
+  __syncthreads();
+  *total = wsum[kPlanWarps - 1];
+  const int before = w > 0 ? wsum[w - 1] : 0;
+  return before + x - v;
 }
 
 __device__ int block_cost(const SeqInfo& s, int blk, int pass, int BM, int BN) {
@@ -48,13 +60,23 @@ __device__ int block_cost(const SeqInfo& s, int blk, int pass, int BM, int BN) {
   return cost;
 }
 
+// Dynamic shared memory: histogram, then (when they fit) the offsets, the
+// block starts per sequence and the block records; otherwise the workspace
+// scratch arrays stand in.
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(PlanParams p) {
-  __shared__ int sh_scan[kPlanThreads];
-  __shared__ int sh_hist[kCostBins];
-  __shared__ int sh_bad;
-  __shared__ int64_t sh_off[kOffStage];
+  extern __shared__ __align__(16) uint8_t plan_smem[];
+  __shared__ int sh_wsum[kPlanWarps];
+  __shared__ int sh_bad, sh_wide, sh_bad_b;
+  int* sh_hist = reinterpret_cast<int*>(plan_smem);
+  uint8_t* cur = plan_smem + sizeof(int) * kCostBins;
+  int64_t* off = const_cast<int64_t*>(p.off);
+  if (p.stage_off) { off = reinterpret_cast<int64_t*>(cur); cur += sizeof(int64_t) * ((p.B + 2) & ~1); }
+  int* start = p.seq_start;
+  if (p.stage_off) { start = reinterpret_cast<int*>(cur); cur += sizeof(int) * ((p.B + 1 + 3) & ~3); }
+  Block* rec = p.stage_rec ? reinterpret_cast<Block*>(cur) : p.tmp;
   const int t = threadIdx.x;
+
   if (t == 0) {
     p.hdr[WS_ERR] = 0;
     p.hdr[WS_ERR_INFO] = 0;
@@ -63,36 +85,21 @@ plan_kernel(PlanParams p) {
     p.hdr[WS_FLAGS] = 0;
     p.hdr[WS_NEXT] = 0;
     sh_bad = 0;
+    sh_wide = 0;
+    sh_bad_b = 0;
   }
   for (int i = t; i < kCostBins; i += kPlanThreads) sh_hist[i] = 0;
+  if (p.stage_off)
+    for (int i = t; i <= p.B; i += kPlanThreads) off[i] = p.off[i];
   __syncthreads();
 
-  // 1. validation
-  if (t == 0 && (p.off[0] != 0 || p.off[p.B] != p.T)) atomicExch(&sh_bad, 1);
-  for (int b = t; b < p.B; b += kPlanThreads) {
-    const int64_t n = p.off[b + 1] - p.off[b];
-    const int64_t m = p.nt ? p.nt[b] : 0, c = p.nc ? p.nc[b] : 0;
-    if (n < 0 || n > p.max_n || m < 0 || c < 0 || m + c > n) {
-      if (atomicExch(&sh_bad, 1) == 0) p.hdr[WS_ERR_INFO] = b;
-    }
-  }
-  __syncthreads();
-  if (sh_bad) {
-    if (t == 0) atomicCAS(p.hdr + WS_ERR, 0, HSTU_ERR_DEVICE_CHECK);
-    return;
-  }
-
-  // 1b. can every timestamp be held relative to its sequence's first token in
-  // 31 bits (so gaps fit in 32)?  Otherwise the kernels take their 64-bit path.
-  // Token-parallel: each thread finds its tokens' sequences by binary search
-  // over the offsets (staged in shared memory when they fit), kUnroll tokens
-  // at a time so their loads overlap.
+  // 1. validation, and the timestamp span check: can every timestamp be held
+  // relative to its sequence's first token in 31 bits (so gaps fit in 32)?
+  // Otherwise the kernels take their 64-bit path.  The span check is
+  // token-parallel (binary search for the token's sequence; the last b with
+  // off[b] <= token, which skips empty sequences), kUnroll tokens at a time.
+  int wide = 0;
   if (p.ts) {
-    const bool staged = p.B + 1 <= kOffStage;
-    if (staged)
-      for (int i = t; i <= p.B; i += kPlanThreads) sh_off[i] = p.off[i];
-    __syncthreads();
-    int wide = 0;
     for (int64_t base = t; base < p.T; base += (int64_t)kPlanThreads * kUnroll) {
       int64_t first[kUnroll], here[kUnroll];
 #pragma unroll
@@ -100,14 +107,12 @@ plan_kernel(PlanParams p) {
         const int64_t tok = base + (int64_t)u * kPlanThreads;
         first[u] = here[u] = 0;
         if (tok < p.T) {
-          // the last b with off[b] <= tok (skips empty sequences)
           int lo = 0, hi = p.B - 1;
           while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            const int64_t o = staged ? sh_off[mid] : p.off[mid];
-            if (o <= tok) lo = mid; else hi = mid - 1;
+            if (off[mid] <= tok) lo = mid; else hi = mid - 1;
           }
-          first[u] = p.ts[staged ? sh_off[lo] : p.off[lo]];
+          first[u] = p.ts[off[lo]];
           here[u] = p.ts[tok];
         }
       }
@@ -117,24 +122,41 @@ plan_kernel(PlanParams p) {
         wide |= (d >= (int64_t)1 << 30 || d < -((int64_t)1 << 30));
       }
     }
-    if (__syncthreads_or(wide) && t == 0) atomicOr(p.hdr + WS_FLAGS, WS_FLAG_WIDE_TS);
   }
+  if (t == 0 && (p.off[0] != 0 || p.off[p.B] != p.T)) atomicExch(&sh_bad, 1);
+  for (int b = t; b < p.B; b += kPlanThreads) {
+    const int64_t n = off[b + 1] - off[b];
+    const int64_t m = p.nt ? p.nt[b] : 0, c = p.nc ? p.nc[b] : 0;
+    if (n < 0 || n > p.max_n || m < 0 || c < 0 || m + c > n) {
+      if (atomicExch(&sh_bad, 1) == 0) sh_bad_b = b;
+    }
+  }
+  if (wide) sh_wide = 1;
+  __syncthreads();
+  if (sh_bad) {
+    if (t == 0) {
+      p.hdr[WS_ERR_INFO] = sh_bad_b;
+      atomicCAS(p.hdr + WS_ERR, 0, HSTU_ERR_DEVICE_CHECK);
+    }
+    return;
+  }
+  if (t == 0 && sh_wide) p.hdr[WS_FLAGS] |= WS_FLAG_WIDE_TS;
 
-  // 2. blocks per sequence -> exclusive prefix (seq_start[b]), chunked scan
+  // 2. blocks per sequence -> exclusive prefix (start[b]), one chunk of
+  // kPlanThreads sequences at a time
   const int BR = p.pass == 0 ? p.BM : p.BN;  // rows per block of this pass
   int carry = 0;
   for (int base = 0; base < p.B; base += kPlanThreads) {
     const int b = base + t;
-    int nb = 0;
-    if (b < p.B) nb = (int)((p.off[b + 1] - p.off[b] + BR - 1) / BR);
-    const int ex = block_scan_exclusive(nb, sh_scan);
-    if (b < p.B) p.seq_start[b] = carry + ex;
-    const int total = sh_scan[kPlanThreads - 1];
-    __syncthreads();
+    const int nb = b < p.B ? (int)((off[b + 1] - off[b] + BR - 1) / BR) : 0;
+    int total;
+    const int ex = cta_exclusive_scan(nb, sh_wsum, &total);
+    if (b < p.B) start[b] = carry + ex;
     carry += total;
+    __syncthreads();  // sh_wsum is reused by the next chunk
   }
   const int nblk = carry;
-  if (t == 0) p.seq_start[p.B] = nblk;
+  if (t == 0) start[p.B] = nblk;
   if (nblk > p.cap_blocks) {  // cannot happen when off[B] == T; guard anyway
     if (t == 0) atomicCAS(p.hdr + WS_ERR, 0, HSTU_ERR_DEVICE_CHECK);
     return;
@@ -146,32 +168,38 @@ plan_kernel(PlanParams p) {
     int lo = 0, hi = p.B - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (p.seq_start[mid] <= idx) lo = mid; else hi = mid - 1;
+      if (start[mid] <= idx) lo = mid; else hi = mid - 1;
     }
-    // skip empty sequences sharing the same start
-    const int b = lo;
-    const SeqInfo s = seq_info(p.off, p.nt, p.nc, b);
-    const int blk = idx - p.seq_start[b];
+    const int b = lo;  // the last sequence starting at or before idx (skips empty ones)
+    SeqInfo s;
+    s.s0 = off[b];
+    s.n = (int)(off[b + 1] - s.s0);
+    s.c = p.nc ? p.nc[b] : 0;
+    s.h_end = s.n - (p.nt ? p.nt[b] : 0);
+    const int blk = idx - start[b];
     const int cost = block_cost(s, blk, p.pass, p.BM, p.BN);
-    Block rec;
-    rec.b = b; rec.blk = blk; rec.cost = cost; rec.pad = 0;
-    p.tmp[idx] = rec;
+    Block r;
+    r.b = b; r.blk = blk; r.cost = cost; r.pad = 0;
+    rec[idx] = r;
     atomicAdd(&sh_hist[cost < kCostBins ? cost : kCostBins - 1], 1);
   }
   __syncthreads();
 
-  // 4. exclusive scan of the histogram in descending cost order
+  // 4. exclusive scan of the histogram in descending cost order: thread t
+  // owns bins kCostBins-1-4t .. kCostBins-4-4t
   {
     constexpr int per = kCostBins / kPlanThreads;
     int local[per];
     int sum = 0;
+#pragma unroll
     for (int r = 0; r < per; ++r) {
       local[r] = sh_hist[kCostBins - 1 - (t * per + r)];
       sum += local[r];
     }
-    const int ex = block_scan_exclusive(sum, sh_scan);
-    __syncthreads();
+    int total;
+    const int ex = cta_exclusive_scan(sum, sh_wsum, &total);
     int run = ex;
+#pragma unroll
     for (int r = 0; r < per; ++r) {
       sh_hist[kCostBins - 1 - (t * per + r)] = run;  // start of this bin
       run += local[r];
@@ -181,9 +209,9 @@ plan_kernel(PlanParams p) {
 
   // 5. scatter into longest-first order
   for (int idx = t; idx < nblk; idx += kPlanThreads) {
-    const Block rec = p.tmp[idx];
-    const int pos = atomicAdd(&sh_hist[rec.cost < kCostBins ? rec.cost : kCostBins - 1], 1);
-    p.blocks[pos] = rec;
+    const Block r = rec[idx];
+    const int pos = atomicAdd(&sh_hist[r.cost < kCostBins ? r.cost : kCostBins - 1], 1);
+    p.blocks[pos] = r;
   }
   if (t == 0) p.hdr[WS_NBLK] = nblk;
 }
@@ -226,8 +254,22 @@ __global__ void debug_tiles_kernel(PlanParams p, int32_t* rec, int64_t cap) {
 
 }  // namespace
 
-cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
+size_t plan_smem_bytes(const PlanParams& p) {
+  size_t bytes = sizeof(int) * kCostBins;
+  // every region a multiple of 16 bytes, so the 16-byte block records stay aligned
+  if (p.stage_off) bytes += sizeof(int64_t) * ((p.B + 2) & ~1) + sizeof(int) * ((p.B + 1 + 3) & ~3);
+  if (p.stage_rec) bytes += sizeof(Block) * (size_t)p.cap_blocks;
+  return bytes;
+}
+
+cudaError_t launch_plan(const PlanParams& p_in, cudaStream_t stream) {
+  PlanParams p = p_in;
+  p.stage_off = p.B + 1 <= kPlanStageSeqs;
+  p.stage_rec = p.cap_blocks <= kPlanStageBlocks;
+  const size_t smem = plan_smem_bytes(p);
+  cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  plan_kernel<<<1, kPlanThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

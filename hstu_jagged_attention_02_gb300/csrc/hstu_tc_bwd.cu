@@ -289,6 +289,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       v = p.rab_time[h * Tb + (e - P)];
     }
     tab[x] = -kLog2e * v;
+    if (want_rp || want_rt) drab[x] = 0.f;  // this CTA's partial sums start from zero
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);

@@ -306,6 +306,8 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       if (!valid) break;
       const int n = sq.n;
       const int nkb = fwd_kv_blocks(q0, n, sq.c, BM, BN);
+      // test only: the CTA that takes work item 0 withholds that item's first K/V load
+      bool withhold_next = (p.flags & HSTU_FLAG_TEST_TIMEOUT) && idx == 0;
       for (int kb = 0; ok && kb < nkb; ++kb) {
         const int k0 = kb * BN;
         if (tile_class(q0, k0, BM, BN, n, sq.c, sq.h_end) == 0) continue;
@@ -325,7 +327,8 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           ts32_s[stage * BN + lane + 32 * x] = (int32_t)(tv[x] - tbase);
         }
         __syncwarp();
-        const bool withhold = (p.flags & HSTU_FLAG_TEST_TIMEOUT) && blockIdx.x == 0 && kv_it == 0;
+        const bool withhold = withhold_next;
+        withhold_next = false;
         if (lane == 0 && !withhold) {
           mbar_arrive_expect_tx(bar(BAR_KVFULL + stage), L::STAGE);
           const uint32_t dstK = sKV + stage * L::STAGE;

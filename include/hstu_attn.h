@@ -77,9 +77,10 @@ typedef enum { HSTU_NORM_NONE = 0, HSTU_NORM_LAYERNORM = 1 } hstu_norm_t;
 
 /* Flags */
 #define HSTU_FLAG_FORCE_SIMT (1u << 0)   /* use the CUDA-core kernels even where the tensor-core path applies */
-#define HSTU_FLAG_TEST_TIMEOUT (1u << 1) /* test only: the tensor-core forward withholds one load and its
-                                            waits give up after about a millisecond, so the timeout path
-                                            runs without a hang; the result is HSTU_ERR_TIMEOUT */
+#define HSTU_FLAG_TEST_TIMEOUT (1u << 1) /* test only: the tensor-core forward withholds one load (the
+                                            first K/V tile of work item 0) and its waits give up after about
+                                            a millisecond, so the timeout path runs without a hang; the
+                                            result is HSTU_ERR_TIMEOUT */
 #define HSTU_FLAG_U_FP32 (1u << 2)       /* u is FP32 whatever dtype is (requires out_dtype FP32).  The
                                             gate multiplies y element by element, so a BF16 rounding of u
                                             is never averaged out; q, k, v stay in dtype */
