@@ -23,11 +23,14 @@ enum : int {
   WS_NBLK = 1,      // number of planner blocks of the current pass
   WS_ERR_INFO = 2,  // detail of the first error (sequence index or wait site)
   WS_NTILES = 3,    // debug-plan tile counter
-  WS_FLAGS = 4,     // planner findings (WS_FLAG_*)
+  WS_FLAGS = 4,     // reserved (zero)
   WS_NEXT = 5,      // next work item of the tensor-core kernels (dynamic scheduling)
 };
-// some timestamp is 2^30 s or more away from its sequence's first token
-constexpr int WS_FLAG_WIDE_TS = 1;
+// Timestamps are staged relative to their sequence's first token; a tile
+// whose relative times all lie within +-2^30 s computes its gaps in 32 bits,
+// any other tile takes the 64-bit path.
+constexpr int64_t kNarrowTsSpan = (int64_t)1 << 30;
+__device__ __forceinline__ bool ts_wide(int64_t rel) { return rel >= kNarrowTsSpan || rel <= -kNarrowTsSpan; }
 constexpr size_t kWsHeaderBytes = 256;
 constexpr size_t kWsAlign = 256;
 constexpr int kCostBins = 4096;  // planner histogram bins (cost = tiles per block)

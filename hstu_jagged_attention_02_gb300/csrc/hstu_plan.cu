@@ -16,7 +16,6 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanWarps = kPlanThreads / 32;
-constexpr int kUnroll = 8;  // tokens per thread in flight in the timestamp check
 
 // Exclusive prefix sum of v over the CTA (warp shuffles, two barriers); the
 // CTA total goes to *total.  wsum holds kPlanWarps ints.
@@ -67,7 +66,7 @@ __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(PlanParams p) {
   extern __shared__ __align__(16) uint8_t plan_smem[];
   __shared__ int sh_wsum[kPlanWarps];
-  __shared__ int sh_bad, sh_wide, sh_bad_b;
+  __shared__ int sh_bad, sh_bad_b;
   int* sh_hist = reinterpret_cast<int*>(plan_smem);
   uint8_t* cur = plan_smem + sizeof(int) * kCostBins;
   int64_t* off = const_cast<int64_t*>(p.off);
@@ -85,7 +84,6 @@ plan_kernel(PlanParams p) {
     p.hdr[WS_FLAGS] = 0;
     p.hdr[WS_NEXT] = 0;
     sh_bad = 0;
-    sh_wide = 0;
     sh_bad_b = 0;
   }
   for (int i = t; i < kCostBins; i += kPlanThreads) sh_hist[i] = 0;
@@ -93,36 +91,7 @@ plan_kernel(PlanParams p) {
     for (int i = t; i <= p.B; i += kPlanThreads) off[i] = p.off[i];
   __syncthreads();
 
-  // 1. validation, and the timestamp span check: can every timestamp be held
-  // relative to its sequence's first token in 31 bits (so gaps fit in 32)?
-  // Otherwise the kernels take their 64-bit path.  The span check is
-  // token-parallel (binary search for the token's sequence; the last b with
-  // off[b] <= token, which skips empty sequences), kUnroll tokens at a time.
-  int wide = 0;
-  if (p.ts) {
-    for (int64_t base = t; base < p.T; base += (int64_t)kPlanThreads * kUnroll) {
-      int64_t first[kUnroll], here[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int64_t tok = base + (int64_t)u * kPlanThreads;
-        first[u] = here[u] = 0;
-        if (tok < p.T) {
-          int lo = 0, hi = p.B - 1;
-          while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (off[mid] <= tok) lo = mid; else hi = mid - 1;
-          }
-          first[u] = p.ts[off[lo]];
-          here[u] = p.ts[tok];
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int64_t d = here[u] - first[u];
-        wide |= (d >= (int64_t)1 << 30 || d < -((int64_t)1 << 30));
-      }
-    }
-  }
+  // 1. validation
   if (t == 0 && (p.off[0] != 0 || p.off[p.B] != p.T)) atomicExch(&sh_bad, 1);
   for (int b = t; b < p.B; b += kPlanThreads) {
     const int64_t n = off[b + 1] - off[b];
@@ -131,7 +100,6 @@ plan_kernel(PlanParams p) {
       if (atomicExch(&sh_bad, 1) == 0) sh_bad_b = b;
     }
   }
-  if (wide) sh_wide = 1;
   __syncthreads();
   if (sh_bad) {
     if (t == 0) {
@@ -140,7 +108,6 @@ plan_kernel(PlanParams p) {
     }
     return;
   }
-  if (t == 0 && sh_wide) p.hdr[WS_FLAGS] |= WS_FLAG_WIDE_TS;
 
   // 2. blocks per sequence -> exclusive prefix (start[b]), one chunk of
   // kPlanThreads sequences at a time

@@ -55,7 +55,8 @@ struct __align__(16) ItemSlot {
   int64_t tbase;  // timestamp of that token (0 without timestamps)
   int valid;      // 0: no more work
   int h, k0, n, c, h_end;
-  int pad[2];
+  int wide;       // some key time of the item is 2^30 s or more from tbase
+  int pad;
 };
 
 struct Lay {
@@ -127,42 +128,33 @@ struct KeyCtx {
 // j and sees that row's query columns i in increasing order over the whole
 // work item, so:
 //  - the clamped position bucket (far from the diagonal) sums in rp_far;
+//    the other position buckets go straight to the CTA's partial sums;
 //  - the time bucket changes only where |t_i - t_j| crosses a power of two,
-//    so a run sum (rt_cur, rt_run) rarely has to be flushed;
-//  - on causal full tiles the position bucket is i - j, constant along
-//    diagonals: diag holds the running sum of the diagonal this lane sits on,
-//    passed one lane up per column, and flushed when it leaves the warp.
+//    so a run sum (rt_cur, rt_run) rarely has to be flushed.
 struct RabAcc {
-  float rp_far, diag, rt_run;
+  float rp_far, rt_run;
   int rt_cur;
 };
 
 // NC query columns ib.. of one key row: A and dZ as packed BF16 hi/lo pairs,
-// plus the d_rab contributions.  FAST_POS: every column is a history/context
-// query at or after the key (position gap = i - j); cg0 is the index of the
-// first column in the warp's 16-column sweep and kbase the gap of lane 0 at
-// sweep column 0.  WIDE: 64-bit gaps.  PARTIAL: evaluate the mask per element.
-template <int NC, bool FAST_POS, bool WIDE, bool PARTIAL>
+// plus the d_rab contributions; the mask is evaluated per element.  WIDE:
+// 64-bit timestamp gaps.  (One code path for every tile class: the variants
+// that skip the mask on full tiles cost more in instruction fetch than they
+// save on heavy-tailed batches, where tile classes alternate.)
+template <int NC, bool WIDE>
 __device__ __forceinline__ void grad_cols(const uint32_t (&sv)[NC], const uint32_t (&dav)[NC],
                                           uint32_t (&ahi)[NC / 2], uint32_t (&alo)[NC / 2], uint32_t (&zhi)[NC / 2],
                                           uint32_t (&zlo)[NC / 2], const KeyCtx& kc, int ib, const int32_t* ts32,
-                                          const int64_t* ts64, RabAcc& acc, int cg0, int kbase) {
-  const int lane = threadIdx.x & 31;
+                                          const int64_t* ts64, RabAcc& acc) {
   float bias[NC];
   int bps[NC], bts[NC];
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
-    int bp;
-    if (FAST_POS) {
-      const int dp = ib + c - kc.j;
-      bp = dp < kc.P - 1 ? dp : kc.P - 1;
-    } else {
-      const int i = ib + c;
-      const int pi = i < kc.h_end ? i : kc.h_end;
-      int dp = pi - kc.pos_j;
-      dp = dp < 0 ? -dp : dp;
-      bp = dp < kc.P - 1 ? dp : kc.P - 1;
-    }
+    const int i = ib + c;
+    const int pi = i < kc.h_end ? i : kc.h_end;
+    int dp = pi - kc.pos_j;
+    dp = dp < 0 ? -dp : dp;
+    const int bp = dp < kc.P - 1 ? dp : kc.P - 1;
     int bt;
     if (WIDE) {
       const int64_t ti = ts64[c];
@@ -186,33 +178,15 @@ __device__ __forceinline__ void grad_cols(const uint32_t (&sv)[NC], const uint32
       const float w = fmaf(kc.kA, __uint_as_float(sv[c + e]), bias[c + e]);
       const float sg = rcp_approx(1.0f + ex2_approx(w));
       const float z = w * kc.kZ;
-      float a = (w * kc.kC) * sg;
-      float dz = __uint_as_float(dav[c + e]) * sg * fmaf(z, 1.f - sg, 1.f) * kc.inv_n;
-      bool valid = true;
-      if (PARTIAL) {
-        const int i = ib + c + e;
-        valid = kc.j_ok && i < kc.n && allowed(i, kc.j, kc.cx, kc.h_end);
-        a = valid ? a : 0.f;
-        dz = valid ? dz : 0.f;
-      }
+      const int i = ib + c + e;
+      const bool valid = kc.j_ok && i < kc.n && allowed(i, kc.j, kc.cx, kc.h_end);
+      const float a = valid ? (w * kc.kC) * sg : 0.f;
+      const float dz = valid ? __uint_as_float(dav[c + e]) * sg * fmaf(z, 1.f - sg, 1.f) * kc.inv_n : 0.f;
       av[e] = a;
       zv[e] = dz;
-      if (kc.want_rp) {
-        if (FAST_POS) {
-          const int cg = cg0 + c + e;
-          if (cg > 0) {
-            // the diagonal held by lane 31 is complete: flush it, shift the rest up
-            const int key_out = kbase + (cg - 1) - 31;
-            red_add(kc.drp + key_out, acc.diag, lane == 31 && acc.diag != 0.f && key_out < kc.P - 1);
-            acc.diag = __shfl_up_sync(0xffffffffu, acc.diag, 1);
-            if (lane == 0) acc.diag = 0.f;
-          }
-          if (bps[c + e] < kc.P - 1) acc.diag += dz;
-          else acc.rp_far += dz;
-        } else if (valid) {
-          if (bps[c + e] == kc.P - 1) acc.rp_far += dz;
-          else red_add(kc.drp + bps[c + e], dz, true);
-        }
+      if (kc.want_rp && valid) {
+        if (bps[c + e] == kc.P - 1) acc.rp_far += dz;
+        else red_add(kc.drp + bps[c + e], dz, true);
       }
       if (kc.want_rt && valid) {
         if (bts[c + e] == acc.rt_cur) {
@@ -254,6 +228,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + Lay::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + Lay::MISC_OFF + 4);
+  int* stage_wide = reinterpret_cast<int*>(base + Lay::MISC_OFF + 8);  // [kQStages]: query times need 64 bits
   const int H = p.H, P = p.P, Tb = p.Tb, PT = p.P + p.Tb;
   float* tab = reinterpret_cast<float*>(base + Lay::TAB_OFF);
   float* drab = p.drab_partial + (size_t)blockIdx.x * H * PT;  // this CTA's partial sums
@@ -313,7 +288,6 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   wd.err_info = p.hdr_rw + WS_ERR_INFO;
   wd.limit_ns = (p.flags & HSTU_FLAG_TEST_TIMEOUT) ? 1000000ull : 2000000000ull;
   const int nitems = p.hdr[WS_NBLK] * H;
-  const bool wide_ts = (p.hdr[WS_FLAGS] & WS_FLAG_WIDE_TS) != 0;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -343,6 +317,10 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         const int row = k0 + lane + 32 * x;
         kv[x] = (valid && p.ts && row < n) ? p.ts[sq.s0 + row] : tbase;
       }
+      bool kw = false;
+#pragma unroll
+      for (int x = 0; x < BK / 32; ++x) kw |= ts_wide(kv[x] - tbase);
+      const bool item_wide = __any_sync(0xffffffffu, kw);
       if (lane == 0) ok = mbar_wait(bar(BAR_KVEMPTY), (item_it & 1) ^ 1, wd, 21);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
@@ -351,6 +329,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       if (lane == 0) {
         slot->s0 = sq.s0; slot->tbase = tbase; slot->valid = valid ? 1 : 0;
         slot->h = h; slot->k0 = k0; slot->n = n; slot->c = sq.c; slot->h_end = sq.h_end;
+        slot->wide = item_wide ? 1 : 0;
       }
       __syncwarp();
       if (lane == 0) {
@@ -383,11 +362,15 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         }
         ok = mbar_wait(bar(BAR_QEMPTY + stage), ((qt_it / kQStages) & 1) ^ 1, wd, 22);
         if (!ok) break;
+        bool qw = false;
 #pragma unroll
         for (int x = 0; x < BQ / 32; ++x) {
           ts64_s[stage * BQ + lane + 32 * x] = tv[x];
           ts32_s[stage * BQ + lane + 32 * x] = (int32_t)(tv[x] - tbase);
+          qw |= ts_wide(tv[x] - tbase);
         }
+        qw = __any_sync(0xffffffffu, qw);
+        if (lane == 0) stage_wide[stage] = qw ? 1 : 0;
         __syncwarp();
         if (lane == 0) {
           const uint32_t full = bar(BAR_QFULL + stage);
@@ -550,6 +533,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       if (!sl.valid) break;
       const int64_t s0 = sl.s0;
       const int hh = sl.h, k0 = sl.k0;
+      const bool item_wide = sl.wide != 0;
       kc.n = sl.n;
       kc.cx = sl.c;
       kc.h_end = sl.h_end;
@@ -563,7 +547,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       kc.drp = drab + hh * PT;
       kc.drt = kc.drp + P;
       RabAcc racc;
-      racc.rp_far = racc.diag = racc.rt_run = 0.f;
+      racc.rp_far = racc.rt_run = 0.f;
       racc.rt_cur = -1;
       bool pend = false;    // a dQ^T of this item waits to be drained
       int pend_q0 = 0;
@@ -577,9 +561,6 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
              mbar_wait(bar(BAR_SFULL), qt_it & 1, wd, 29);
         if (!ok) break;
         fence_after_sync();
-        const bool fast = cls == 2 && k0 + BK - 1 <= q0 && q0 + BQ <= kc.h_end;
-        // position gap of lane 0 at this warp's first query column (causal full tiles)
-        const int kbase = (q0 + hq * 16) - (k0 + wq * 32);
         uint32_t svq[16], daq[16];
         tmem_ld16(lane_base + S_COL + hq * 16, svq);
         tmem_ld16(lane_base + DA_COL + hq * 16, daq);
@@ -601,14 +582,8 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           const int32_t* t32 = ts32_s + stage * BQ + c0;
           const int64_t* t64 = ts64_s + stage * BQ + c0;
           uint32_t ahi[4], alo[4], zhi[4], zlo[4];
-          if (!wide_ts) {
-            if (fast) grad_cols<8, true, false, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc, half * 8, kbase);
-            else if (cls == 2) grad_cols<8, false, false, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc, half * 8, kbase);
-            else grad_cols<8, false, false, true>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc, half * 8, kbase);
-          } else {
-            if (cls == 2) grad_cols<8, false, true, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc, half * 8, kbase);
-            else grad_cols<8, false, true, true>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc, half * 8, kbase);
-          }
+          if (!item_wide && !stage_wide[stage]) grad_cols<8, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc);
+          else grad_cols<8, true>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc);
           if (half == 0 && pend) {
             // the previous tile's gradient MMAs are complete once its dQ^T is:
             // the A buffer and the dZ^T staging are free again
@@ -628,11 +603,6 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           st_shared_v4(rowl + chunk * 16, zlo[0], zlo[1], zlo[2], zlo[3]);
         }
         if (!ok) break;
-        if (fast && kc.want_rp) {  // diagonals still held at the end of the 16-column sweep
-          const int key = kbase + 15 - lane;
-          red_add(kc.drp + key, racc.diag, racc.diag != 0.f && key < P - 1);
-          racc.diag = 0.f;
-        }
         fence_async_smem();
         tmem_wait_st();
         fence_before_sync();

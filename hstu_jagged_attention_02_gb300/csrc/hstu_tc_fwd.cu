@@ -61,7 +61,8 @@ struct __align__(16) ItemSlot {
   int64_t tbase;  // timestamp of that token (0 without timestamps)
   int valid;      // 0: no more work
   int h, q0, n, c, h_end;
-  int pad[2];
+  int wide;       // some query time of the item is 2^30 s or more from tbase
+  int pad;
 };
 
 template <int D>
@@ -78,7 +79,7 @@ struct Layout {
   static constexpr int QTS_OFF = TS32_OFF + kStages * BN * 4;   // int64 [kQBufs][BM] query times
   static constexpr int SLOT_OFF = QTS_OFF + kQBufs * BM * 8;    // ItemSlot [kQBufs]
   static constexpr int BAR_OFF = SLOT_OFF + kQBufs * (int)sizeof(ItemSlot);
-  static constexpr int MISC_OFF = BAR_OFF + BAR_COUNT * 8;      // tmem slot, abort flag
+  static constexpr int MISC_OFF = BAR_OFF + BAR_COUNT * 8;      // tmem slot, abort flag, per-stage wide flags
   static constexpr int TAB_OFF = MISC_OFF + 16;                 // float [H][P + Tb]
   static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
 };
@@ -193,6 +194,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L::MISC_OFF + 4);
+  int* stage_wide = reinterpret_cast<int*>(base + L::MISC_OFF + 8);  // [kStages]: key times need 64 bits
   float* tab = reinterpret_cast<float*>(base + L::TAB_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -248,7 +250,6 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   wd.err_info = p.hdr_rw + WS_ERR_INFO;
   wd.limit_ns = (p.flags & HSTU_FLAG_TEST_TIMEOUT) ? 1000000ull : 2000000000ull;
   const int nitems = p.hdr[WS_NBLK] * H;
-  const bool wide_ts = (p.hdr[WS_FLAGS] & WS_FLAG_WIDE_TS) != 0;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -279,6 +280,10 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         const int row = q0 + lane + 32 * x;
         qv[x] = (valid && p.ts && row < sq.n) ? p.ts[sq.s0 + row] : tbase;
       }
+      bool qw = false;
+#pragma unroll
+      for (int x = 0; x < BM / 32; ++x) qw |= ts_wide(qv[x] - tbase);
+      const bool item_wide = __any_sync(0xffffffffu, qw);
       if (lane == 0) ok = mbar_wait(bar(BAR_QEMPTY + qb), ((q_it / kQBufs) & 1) ^ 1, wd, 1);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
@@ -287,7 +292,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       if (lane == 0) {
         ItemSlot& sl = slots[qb];
         sl.s0 = sq.s0; sl.tbase = tbase; sl.valid = valid ? 1 : 0;
-        sl.h = h; sl.q0 = q0; sl.n = sq.n; sl.c = sq.c; sl.h_end = sq.h_end;
+        sl.h = h; sl.q0 = q0; sl.n = sq.n; sl.c = sq.c; sl.h_end = sq.h_end; sl.wide = item_wide ? 1 : 0;
       }
       __syncwarp();
       if (lane == 0) {
@@ -321,11 +326,15 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         }
         ok = mbar_wait(bar(BAR_KVEMPTY + stage), ((kv_it / kStages) & 1) ^ 1, wd, 2);
         if (!ok) break;
+        bool kw = false;
 #pragma unroll
         for (int x = 0; x < BN / 32; ++x) {
           ts64_s[stage * BN + lane + 32 * x] = tv[x];
           ts32_s[stage * BN + lane + 32 * x] = (int32_t)(tv[x] - tbase);
+          kw |= ts_wide(tv[x] - tbase);
         }
+        kw = __any_sync(0xffffffffu, kw);
+        if (lane == 0) stage_wide[stage] = kw ? 1 : 0;
         __syncwarp();
         const bool withhold = withhold_next;
         withhold_next = false;
@@ -443,6 +452,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       if (!sl.valid) break;
       const int64_t s0 = sl.s0;
       const int hh = sl.h, q0 = sl.q0;
+      const bool item_wide = sl.wide != 0;
       rc.n = sl.n;
       rc.cx = sl.c;
       rc.h_end = sl.h_end;
@@ -472,7 +482,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         const int64_t* t64 = ts64_s + stage * BN + hq * 32;
         uint32_t hi[16], lo[16];
         const bool fast = cls == 2 && k0 + BN - 1 <= q0;
-        if (!wide_ts) {
+        if (!item_wide && !stage_wide[stage]) {
           if (fast) score32<true, false, false>(sv, hi, lo, rc, jb, t32, t64);
           else if (cls == 2) score32<false, false, false>(sv, hi, lo, rc, jb, t32, t64);
           else score32<false, false, true>(sv, hi, lo, rc, jb, t32, t64);

@@ -134,6 +134,21 @@ def test_norm_none_and_no_gate():
     check(got2, run_oracle(b2), TOL["fp32"])
 
 
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("fp32", 64)])
+def test_wide_timestamp_gaps(dtype, d):
+    # gaps of 2^31 s and more take the 64-bit path, decided per item and tile;
+    # a whole sequence shifted far away stays on the 32-bit path (times are
+    # taken relative to the sequence's first token)
+    b = _ragged_batch(dtype, d, seed=71, lengths=[700, 300, 129, 40])
+    ts, o = b.timestamps.copy(), b.offsets
+    ts[int(o[0]) + 400:int(o[1])] += np.int64(1) << 34
+    ts[int(o[2]):int(o[3])] -= np.int64(1) << 40
+    ts[int(o[3]) + 5] += np.int64(1) << 31
+    b.timestamps = ts
+    _, got = run_gpu(b)
+    check(got, run_oracle(b), TOL[dtype])
+
+
 @pytest.mark.parametrize("simt", [False, True])
 def test_fp32_gate_with_bf16_operands(simt):
     # HSTU_FLAG_U_FP32: u is read as FP32 while q, k, v stay BF16; the gate's
