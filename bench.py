@@ -137,8 +137,8 @@ def kernel_sources_sha():
 
 
 def traffic_record(kernel_role: str):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, if it was taken on the current kernel sources."""
+    """DRAM bytes per token of the dominant kernel from the committed ncu
+    capture, if it was taken on the current kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -382,7 +382,13 @@ def run_gpu(args, wl, rank, world, local_rank):
     t_tensor = sum(dom_flops) / (peak_sust * 1e12)
     t_hbm = sum(dom_bytes) / (peak_bw * 1e9)
     tr = traffic_record(f"{wl.name}:{dom}")
-    common = {"traffic": tr["dram_bytes_per_launch"] if tr else None, "kernel": f"attention {dom} kernel",
+    # DRAM bytes of one launch, from the committed ncu capture of one batch,
+    # scaled to this run's mean batch by the token count
+    mean_tokens = float(np.mean([batches[k % nb].T for k in range(args.steps)]))
+    traffic = tr["dram_bytes_per_token"] * mean_tokens if tr else None
+    common = {"traffic": traffic, "kernel": f"attention {dom} kernel",
+              "traffic_source": (f"{tr['profile']} (per-token DRAM bytes x {mean_tokens:.0f} tokens)" if tr else
+                                 "no capture on the current kernel sources"),
               "avg_launch_ms": sum(dom_ms) / len(dom_ms), "share_of_step": sum(dom_ms) / elapsed_ms,
               "algorithmic_bytes_per_launch": sum(dom_bytes) / len(dom_bytes),
               "useful_flops_per_launch": sum(dom_flops) / len(dom_flops)}
