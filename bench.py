@@ -157,6 +157,7 @@ def traffic_record(kernel_role: str):
 class AttentionWorkload:
     """The heavy-tailed attention batch (the default line)."""
     name = "heavy_tailed"
+    has_backward = True
     metric = METRIC
     description = WORKLOAD
     n_batches = N_SEEDS
@@ -172,6 +173,10 @@ class AttentionWorkload:
         """(attention fwd, attention bwd, whole step) useful FLOPs."""
         f, bw = useful_flops(b)
         return f, bw, f + bw
+
+    def kernel_bytes(self, b, role):
+        """Algorithmic DRAM bytes of one launch of the attention kernel of a role."""
+        return KERNEL_BYTES_PER_ELEM[role] * b.T * b.H * b.d_qk
 
     def host_io(self, pr):
         ins = [t for t in (pr.offsets, pr.num_targets, pr.num_contexts, pr.timestamps, pr.rab_pos,
@@ -235,7 +240,64 @@ class LayerWorkload(AttentionWorkload):
                 "l2": "inputs larger than L2: each batch holds several GB of activations"}
 
 
-WORKLOADS = {"heavy_tailed": AttentionWorkload, "layer": LayerWorkload}
+class DeltaWorkload(AttentionWorkload):
+    """KV-cached candidate scoring (the delta forward): 32 sequences whose
+    2K-8K cached tokens (context + history) are kept as K/V, each scoring 128
+    new candidates; forward only."""
+    name = "delta"
+    metric = "HSTU delta-forward useful TFLOP/s (KV-cached candidates vs history)"
+    description = ("delta: 32 sequences, cached history U[2048,8192] tokens (K/V kept), 128 candidates each, "
+                   "4 heads x 128, BF16 in / FP32 out, candidates see the cache and themselves, position + time "
+                   "rab, LayerNorm gate; forward only")
+    n_batches = 4
+    has_backward = False
+
+    def batches(self, rank):
+        out = []
+        for s in range(4):
+            rng = np.random.default_rng(1000 + rank * 4 + s)
+            hist = rng.integers(2048, 8192, size=32, endpoint=True)
+            out.append(synth.make_batch(hist, H=4, d_qk=128, d_v=128, dtype="bf16", num_targets=128,
+                                        seed=1000 + rank * 4 + s, backward=False))
+        return out
+
+    def problem(self, b, dev):
+        from hstu_jagged_attention_02_gb300.delta import DeltaProblem
+        return DeltaProblem(b, device=dev)
+
+    def flops(self, b):
+        m = b.num_targets.astype(np.int64)
+        cached = b.lengths.astype(np.int64) - m
+        pairs = int((m * (cached + 1)).sum()) * b.H
+        f = 2 * (b.d_qk + b.d_v) * pairs
+        return f, 0, f
+
+    def kernel_bytes(self, b, role):
+        # cached tokens supply K and V (BF16); candidates read q, k, v and write o (FP32)
+        m = int(b.num_targets.sum())
+        return (4 * (b.T - m) + 10 * m) * b.H * b.d_qk
+
+    def host_io(self, pr):
+        ins = [t for t in (pr.cand_offsets, pr.cache_offsets, pr.cand_ts, pr.cache_ts, pr.rab_pos, pr.rab_time,
+                           pr.q, pr.k, pr.v, pr.u, pr.k_cache, pr.v_cache) if t is not None]
+        return ins, [pr.o, pr.y]
+
+    def oracle_step(self, b):
+        from oracle import oracle as O
+        from hstu_jagged_attention_02_gb300.delta import split_rows
+        rows = np.zeros(b.T, bool)
+        rows[split_rows(b)[1]] = True
+        O.forward(b, rows=rows)
+
+    def cpu_samples(self, batches):
+        return [sub_batch(b, 2) for b in batches], "delta forward of the first 2 of 32 sequences of a batch"
+
+    def config(self):
+        return {"batches": 4, "seeds": "1000..1003 (+rank*4)",
+                "l2": "inputs larger than L2: each batch holds ~300 MB of cached K/V"}
+
+
+WORKLOADS = {"heavy_tailed": AttentionWorkload, "layer": LayerWorkload, "delta": DeltaWorkload}
 
 
 # ------------------------------------------------------------ CPU oracle arm
@@ -315,6 +377,11 @@ def run_gpu(args, wl, rank, world, local_rank):
             C.hstu_time_next_attention_kernel(ev[0].cuda_event, ev[1].cuda_event)
         pr.forward()
         n = C.hstu_last_launch_count()
+        if not wl.has_backward:
+            if ev is not None:  # no backward kernel: an empty interval
+                ev[2].record(stream)
+                ev[3].record(stream)
+            return n
         if ev is not None:
             C.hstu_time_next_attention_kernel(ev[2].cuda_event, ev[3].cuda_event)
         pr.backward()
@@ -376,8 +443,7 @@ def run_gpu(args, wl, rank, world, local_rank):
     # algorithmic bytes of the kernel per launch: forward reads q, k, v (BF16) and
     # writes o (FP32); backward reads q, k, v and dO as a BF16 pair and writes dk,
     # dv and the dq reduction (FP32)
-    per_elem = KERNEL_BYTES_PER_ELEM[dom]
-    dom_bytes = [per_elem * batches[k % nb].T * batches[0].H * batches[0].d_qk for k in range(args.steps)]
+    dom_bytes = [wl.kernel_bytes(batches[k % nb], dom) for k in range(args.steps)]
     secs = sum(dom_ms) * 1e-3
     t_tensor = sum(dom_flops) / (peak_sust * 1e12)
     t_hbm = sum(dom_bytes) / (peak_bw * 1e9)
@@ -445,7 +511,8 @@ def run_e2e(args, wl, probs, flops, stream, world):
         for d, h in zip(ins, h_in):
             d.copy_(h, non_blocking=True)
         pr.forward()
-        pr.backward()
+        if wl.has_backward:
+            pr.backward()
         for d, h in zip(outs, h_out):
             h.copy_(d, non_blocking=True)
 

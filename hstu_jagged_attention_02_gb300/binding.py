@@ -58,10 +58,16 @@ class hstu_layer_bwd_args(ctypes.Structure):
                                    "dout", "dx", "dw1", "dw2", "d_rab_pos", "d_rab_time")]
 
 
+class hstu_attn_delta_args(ctypes.Structure):
+    _fields_ = [("cand_offsets", _vp), ("cache_offsets", _vp), ("cache_tokens", ctypes.c_int64)] + \
+        [(n, _vp) for n in ("cand_timestamps", "cache_timestamps", "rab_pos", "rab_time", "q", "k", "v", "u",
+                            "k_cache", "v_cache", "o", "y", "ln_mean", "ln_rstd")]
+
+
 EXPORTED = ("hstu_attn_workspace_size", "hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_debug_plan",
             "hstu_get_device_error", "hstu_status_string", "hstu_last_launch_count",
             "hstu_time_next_attention_kernel", "hstu_last_error_detail", "hstu_attn_fwd_noalloc",
-            "hstu_layer_workspace_size", "hstu_layer_fwd", "hstu_layer_bwd")
+            "hstu_layer_workspace_size", "hstu_layer_fwd", "hstu_layer_bwd", "hstu_attn_fwd_delta")
 
 _lib = None
 
@@ -97,8 +103,10 @@ def load(build_if_missing: bool = True):
     L.hstu_layer_workspace_size.argtypes = [P(hstu_attn_desc), P(ctypes.c_size_t), P(ctypes.c_size_t)]
     L.hstu_layer_fwd.argtypes = [P(hstu_attn_desc), P(hstu_layer_fwd_args), _vp, ctypes.c_size_t, _vp]
     L.hstu_layer_bwd.argtypes = [P(hstu_attn_desc), P(hstu_layer_bwd_args), _vp, ctypes.c_size_t, _vp]
+    L.hstu_attn_fwd_delta.argtypes = [P(hstu_attn_desc), P(hstu_attn_delta_args), _vp, ctypes.c_size_t, _vp]
     for name in ("hstu_attn_workspace_size", "hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_debug_plan",
-                 "hstu_get_device_error", "hstu_layer_workspace_size", "hstu_layer_fwd", "hstu_layer_bwd"):
+                 "hstu_get_device_error", "hstu_layer_workspace_size", "hstu_layer_fwd", "hstu_layer_bwd",
+                 "hstu_attn_fwd_delta"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -173,6 +181,11 @@ def hstu_attn_fwd_noalloc(desc, args, stream: int, want_device_error: bool = Tru
                                         ctypes.byref(code) if want_device_error else None),
            "hstu_attn_fwd_noalloc")
     return int(code.value) if want_device_error else None
+
+
+def hstu_attn_fwd_delta(desc, args, workspace: int, workspace_bytes: int, stream: int):
+    _check(load().hstu_attn_fwd_delta(ctypes.byref(desc), ctypes.byref(args), workspace, workspace_bytes,
+                                      stream), "hstu_attn_fwd_delta")
 
 
 def hstu_layer_workspace_size(desc: hstu_attn_desc):

@@ -122,7 +122,7 @@ PlanParams plan_params(const hstu_attn_desc* d, const int64_t* off, const int32_
   p.B = d->B; p.T = d->total_tokens; p.max_n = d->max_seq_len;
   if (!tc) {
     p.BM = p.BN = kSimtTile;
-  } else if (pass == 0) {
+  } else if (pass == 0 || pass == 2) {
     p.BM = p.BN = kTcTile;
   } else {
     p.BM = kTcBwdQTile;  // the tensor-core backward walks 64-row query tiles per 128-row key block
@@ -344,6 +344,66 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
   ++g_launches;
   if (!dq_direct) {
     HSTU_CUDA_TRY(launch_convert_f32(dq_acc, a->dq, (int64_t)(rows * d->d_qk), d->out_dtype, st));
+    ++g_launches;
+  }
+  return HSTU_OK;
+}
+
+hstu_status_t hstu_attn_fwd_delta(const hstu_attn_desc* d, const hstu_attn_delta_args* a, void* workspace,
+                                  size_t workspace_bytes, hstu_stream_t stream) {
+  hstu_status_t s = check_desc(d);
+  if (s != HSTU_OK) return s;
+  if (!a || !a->cand_offsets || !a->cache_offsets || a->cache_tokens < 0) return HSTU_ERR_INVALID_ARG;
+  if (d->total_tokens > 0 && (!a->q || !a->k || !a->v || !a->o)) return HSTU_ERR_INVALID_ARG;
+  if (d->total_tokens > 0 && a->cache_tokens > 0 && (!a->k_cache || !a->v_cache)) return HSTU_ERR_INVALID_ARG;
+  if (a->cache_tokens > 0 && (a->cand_timestamps == nullptr) != (a->cache_timestamps == nullptr))
+    return HSTU_ERR_INVALID_ARG;
+  for (const void* ptr : {a->q, a->k, a->v, a->u, a->k_cache, a->v_cache, (const void*)a->o, (const void*)a->y})
+    if (ptr && !aligned16(ptr)) return HSTU_ERR_INVALID_ARG;
+  // tensor-core path only: 128-row TMA boxes over both token tensors
+  if ((d->flags & HSTU_FLAG_FORCE_SIMT) || dev_info().cc != 103 || !tc_fwd_supported(d->dtype, d->d_qk, d->d_v) ||
+      tc_fwd_smem_bytes(d->d_qk, d->H, d->num_pos_buckets, d->num_time_buckets) > kMaxSmemPerCta ||
+      (d->total_tokens > 0 && d->total_tokens < kTcTile) || (a->cache_tokens > 0 && a->cache_tokens < kTcTile) ||
+      a->cache_tokens > (int64_t)0x7fffffff)
+    return HSTU_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(d, false);
+  if ((s = check_ws(workspace, workspace_bytes, L.total)) != HSTU_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  g_launches = 0;
+  clear_detail();
+
+  PlanParams pp = plan_params(d, a->cand_offsets, nullptr, nullptr, a->cand_timestamps, 2, true, ws, L);
+  pp.off2 = a->cache_offsets;
+  pp.T2 = a->cache_tokens;
+  HSTU_CUDA_TRY(launch_plan(pp, st));
+  ++g_launches;
+  if (d->total_tokens == 0) return HSTU_OK;
+
+  AttnParams p{};
+  p.off = a->cand_offsets; p.nt = nullptr; p.nc = nullptr;
+  p.ts = a->cand_timestamps; p.rab_pos = a->rab_pos;
+  p.rab_time = a->cand_timestamps ? a->rab_time : nullptr;
+  p.q = a->q; p.k = a->k; p.v = a->v; p.o = a->o;
+  p.off2 = a->cache_offsets; p.ts2 = a->cache_timestamps; p.k2 = a->k_cache; p.v2 = a->v_cache;
+  p.T2 = a->cache_tokens;
+  p.hdr = pp.hdr; p.hdr_rw = pp.hdr; p.blocks = pp.blocks;
+  p.B = d->B; p.H = d->H; p.dqk = d->d_qk; p.dv_dim = d->d_v; p.T = d->total_tokens;
+  p.dtype = d->dtype; p.out_dtype = d->out_dtype;
+  p.alpha = d->alpha; p.inv_n = 1.0f / (float)d->max_seq_len;
+  p.P = d->num_pos_buckets; p.Tb = d->num_time_buckets; p.flags = d->flags;
+  p.num_sms = dev_info().sms;
+  {
+    KernelTimer timer(st);
+    HSTU_CUDA_TRY(launch_tc_fwd_delta(p, st));
+  }
+  ++g_launches;
+  if (a->y || a->ln_mean || a->ln_rstd) {
+    NormParams np{};
+    np.dtype = (d->flags & HSTU_FLAG_U_FP32) ? HSTU_FP32 : d->dtype; np.out_dtype = d->out_dtype;
+    np.o = a->o; np.u = a->u; np.y = a->y; np.mean = a->ln_mean; np.rstd = a->ln_rstd;
+    np.T = d->total_tokens; np.F = d->H * d->d_v; np.norm = d->norm; np.eps = d->ln_eps;
+    HSTU_CUDA_TRY(launch_norm_gate_fwd(np, st));
     ++g_launches;
   }
   return HSTU_OK;

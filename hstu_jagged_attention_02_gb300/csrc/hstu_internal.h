@@ -16,7 +16,9 @@ struct PlanParams {
   int64_t T;
   int max_n;
   int BM, BN;       // tile edges of the path that will run
-  int pass;         // 0 forward (query blocks), 1 backward (key blocks)
+  int pass;         // 0 forward (query blocks), 1 backward (key blocks), 2 delta forward (candidate blocks)
+  const int64_t* off2;  // pass 2: cached-token offsets [B+1] (off: candidate offsets)
+  int64_t T2;           // pass 2: cached tokens
   int* hdr;         // workspace header
   int* seq_start;   // [B+1] scratch
   Block* tmp;       // [cap_blocks] scratch
@@ -51,6 +53,13 @@ struct AttnParams {
   const int* hdr;        // workspace header (block count)
   int* hdr_rw;           // same, writable (error word)
   const Block* blocks;
+  // delta forward (KV-cached candidates): cached-token offsets [B+1], times
+  // [T2] (or NULL) and K, V [T2, H, d]; q, k, v, o above are the candidates'
+  const int64_t* off2;
+  const int64_t* ts2;
+  const void* k2;
+  const void* v2;
+  int64_t T2;
   int B, H, dqk, dv_dim;
   int dtype, out_dtype;  // hstu_dtype_t of the inputs / of the outputs
   int64_t T;
@@ -109,6 +118,8 @@ size_t tc_fwd_smem_bytes(int d, int H, int P, int Tb);
 constexpr size_t kMaxSmemPerCta = 227 * 1024;
 bool tc_bwd_supported(int dtype, int dqk, int dv);
 cudaError_t launch_tc_fwd(const AttnParams& p, cudaStream_t stream);
+// delta forward: candidate blocks against cached K/V (p.off2, p.ts2, p.k2, p.v2, p.T2)
+cudaError_t launch_tc_fwd_delta(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_tc_bwd(const AttnParams& p, cudaStream_t stream);
 
 }  // namespace hstu

@@ -44,9 +44,14 @@ __device__ int cta_exclusive_scan(int v, int* wsum, int* total) {
   return before + x - v;
 }
 
-__device__ int block_cost(const SeqInfo& s, int blk, int pass, int BM, int BN) {
+// Tiles of one block.  Pass 2 (delta forward): a block of up to BM
+// candidates sees every cached key tile of its sequence plus one tile of its
+// own keys (the diagonal); cached_len is that sequence's cached-token count.
+__device__ int block_cost(const SeqInfo& s, int blk, int pass, int BM, int BN, int cached_len) {
   int cost = 0;
-  if (pass == 0) {
+  if (pass == 2) {
+    cost = (cached_len + BN - 1) / BN + 1;
+  } else if (pass == 0) {
     const int q0 = blk * BM;
     const int nkb = fwd_kv_blocks(q0, s.n, s.c, BM, BN);
     for (int kb = 0; kb < nkb; ++kb) cost += tile_class(q0, kb * BN, BM, BN, s.n, s.c, s.h_end) != 0;
@@ -93,10 +98,13 @@ plan_kernel(PlanParams p) {
 
   // 1. validation
   if (t == 0 && (p.off[0] != 0 || p.off[p.B] != p.T)) atomicExch(&sh_bad, 1);
+  if (t == 0 && p.pass == 2 && (p.off2[0] != 0 || p.off2[p.B] != p.T2)) atomicExch(&sh_bad, 1);
   for (int b = t; b < p.B; b += kPlanThreads) {
     const int64_t n = off[b + 1] - off[b];
     const int64_t m = p.nt ? p.nt[b] : 0, c = p.nc ? p.nc[b] : 0;
-    if (n < 0 || n > p.max_n || m < 0 || c < 0 || m + c > n) {
+    // pass 2: n candidates after L cached tokens, n + L <= N
+    const int64_t L = p.pass == 2 ? p.off2[b + 1] - p.off2[b] : 0;
+    if (n < 0 || L < 0 || n + L > p.max_n || m < 0 || c < 0 || m + c > n) {
       if (atomicExch(&sh_bad, 1) == 0) sh_bad_b = b;
     }
   }
@@ -111,7 +119,7 @@ plan_kernel(PlanParams p) {
 
   // 2. blocks per sequence -> exclusive prefix (start[b]), one chunk of
   // kPlanThreads sequences at a time
-  const int BR = p.pass == 0 ? p.BM : p.BN;  // rows per block of this pass
+  const int BR = p.pass == 1 ? p.BN : p.BM;  // rows per block of this pass
   int carry = 0;
   for (int base = 0; base < p.B; base += kPlanThreads) {
     const int b = base + t;
@@ -144,7 +152,8 @@ plan_kernel(PlanParams p) {
     s.c = p.nc ? p.nc[b] : 0;
     s.h_end = s.n - (p.nt ? p.nt[b] : 0);
     const int blk = idx - start[b];
-    const int cost = block_cost(s, blk, p.pass, p.BM, p.BN);
+    const int cached_len = p.pass == 2 ? (int)(p.off2[b + 1] - p.off2[b]) : 0;
+    const int cost = block_cost(s, blk, p.pass, p.BM, p.BN, cached_len);
     Block r;
     r.b = b; r.blk = blk; r.cost = cost; r.pad = 0;
     rec[idx] = r;

@@ -62,7 +62,9 @@ struct __align__(16) ItemSlot {
   int valid;      // 0: no more work
   int h, q0, n, c, h_end;
   int wide;       // some query time of the item is 2^30 s or more from tbase
-  int pad;
+  int L;          // delta forward: cached tokens of the sequence
+  int64_t cs0;    // delta forward: first cached token of the sequence
+  int64_t pad;
 };
 
 template <int D>
@@ -117,8 +119,10 @@ struct RowCtx {
 // Scores of 32 consecutive key columns jb.. of one row -> P_hi, P_lo packed
 // pairs.  FAST_POS: every column is a history/context token at or before the
 // row (position gap = pos_i - j >= 0).  WIDE: 64-bit timestamp gaps.
-// PARTIAL: evaluate the mask per element.
-template <bool FAST_POS, bool WIDE, bool PARTIAL>
+// PARTIAL: evaluate the mask per element.  MODE (delta forward, candidate
+// rows only): 1 = cached keys j < L (position gap L - j, rc.h_end = L), 2 =
+// the candidates' own keys, where only the diagonal is allowed (gap 0).
+template <bool FAST_POS, bool WIDE, bool PARTIAL, int MODE = 0>
 __device__ __forceinline__ void score32(const uint32_t (&sv)[32], uint32_t (&hi)[16], uint32_t (&lo)[16],
                                         const RowCtx& rc, int jb, const int32_t* ts32, const int64_t* ts64) {
 #pragma unroll
@@ -128,7 +132,13 @@ __device__ __forceinline__ void score32(const uint32_t (&sv)[32], uint32_t (&hi)
     for (int c = 0; c < 16; ++c) {
       const int cc = half * 16 + c;
       int bp;
-      if (FAST_POS) {
+      if (MODE == 1) {
+        int dp = rc.pos_i - (jb + cc);
+        dp = dp < 0 ? 0 : dp;  // columns past the cache are masked below
+        bp = dp < rc.P - 1 ? dp : rc.P - 1;
+      } else if (MODE == 2) {
+        bp = 0;
+      } else if (FAST_POS) {
         const int dp = rc.pos_i - (jb + cc);
         bp = dp < rc.P - 1 ? dp : rc.P - 1;
       } else {
@@ -159,7 +169,11 @@ __device__ __forceinline__ void score32(const uint32_t (&sv)[32], uint32_t (&hi)
         const int cc = half * 16 + c + e;
         const float w = fmaf(rc.kA, __uint_as_float(sv[cc]), bias[c + e]);
         float a = (w * rc.kC) * rcp_approx(1.0f + ex2_approx(w));
-        if (PARTIAL) {
+        if (MODE == 1) {
+          a = (rc.row_ok && jb + cc < rc.h_end) ? a : 0.f;
+        } else if (MODE == 2) {
+          a = (rc.row_ok && jb + cc == rc.i) ? a : 0.f;
+        } else if (PARTIAL) {
           const int j = jb + cc;
           const bool valid = rc.row_ok && j < rc.n && allowed(rc.i, j, rc.cx, rc.h_end);
           a = valid ? a : 0.f;
@@ -175,10 +189,15 @@ __device__ __forceinline__ void score32(const uint32_t (&sv)[32], uint32_t (&hi)
 
 // Registers go to a block in groups of 4 warps: 18 warps are charged as 20,
 // and 20 x 32 threads x 96 registers = 61440 <= 65536.
-template <int D, typename TO>
+// DELTA: the delta forward (KV-cached candidates): work items are blocks of
+// up to 128 candidates; their key tiles are every tile of the sequence's
+// cached K/V (tmk2, tmv2, offsets p.off2, times p.ts2) and then one tile of
+// the candidates' own K/V (tmk, tmv) for the diagonal.
+template <int D, typename TO, bool DELTA>
 __global__ void __maxnreg__(96)
 hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmq,
-                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                   const __grid_constant__ CUtensorMap tmk2, const __grid_constant__ CUtensorMap tmv2) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -238,6 +257,10 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     tma_prefetch_desc(&tmq);
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
+    if (DELTA) {
+      tma_prefetch_desc(&tmk2);
+      tma_prefetch_desc(&tmv2);
+    }
   }
   fence_before_sync();
   __syncthreads();
@@ -264,13 +287,18 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       if (lane == 0) idx = atomicAdd(p.hdr_rw + WS_NEXT, 1);
       idx = __shfl_sync(0xffffffffu, idx, 0);
       const bool valid = idx < nitems;
-      int h = 0, q0 = 0;
+      int h = 0, q0 = 0, L = 0;
+      int64_t cs0 = 0;
       SeqInfo sq{};
       if (valid) {
         const Block blk = p.blocks[idx / H];
         h = idx % H;
         q0 = blk.blk * BM;
         sq = seq_info(p.off, p.nt, p.nc, blk.b);
+        if (DELTA) {
+          cs0 = p.off2[blk.b];
+          L = (int)(p.off2[blk.b + 1] - cs0);
+        }
       }
       const int64_t tbase = (valid && p.ts) ? p.ts[sq.s0] : 0;
       // query-row timestamps: loads issued before waiting for the buffer
@@ -293,6 +321,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         ItemSlot& sl = slots[qb];
         sl.s0 = sq.s0; sl.tbase = tbase; sl.valid = valid ? 1 : 0;
         sl.h = h; sl.q0 = q0; sl.n = sq.n; sl.c = sq.c; sl.h_end = sq.h_end; sl.wide = item_wide ? 1 : 0;
+        sl.L = L; sl.cs0 = cs0;
       }
       __syncwarp();
       if (lane == 0) {
@@ -310,19 +339,21 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       ++q_it;
       if (!valid) break;
       const int n = sq.n;
-      const int nkb = fwd_kv_blocks(q0, n, sq.c, BM, BN);
+      const int nkb = DELTA ? (L + BN - 1) / BN + 1 : fwd_kv_blocks(q0, n, sq.c, BM, BN);
       // test only: the CTA that takes work item 0 withholds that item's first K/V load
       bool withhold_next = (p.flags & HSTU_FLAG_TEST_TIMEOUT) && idx == 0;
       for (int kb = 0; ok && kb < nkb; ++kb) {
-        const int k0 = kb * BN;
-        if (tile_class(q0, k0, BM, BN, n, sq.c, sq.h_end) == 0) continue;
+        const bool self = DELTA && kb == nkb - 1;   // delta: the candidates' own keys
+        const int k0 = self ? q0 : kb * BN;
+        if (!DELTA && tile_class(q0, k0, BM, BN, n, sq.c, sq.h_end) == 0) continue;
         const int stage = kv_it % kStages;
         // key timestamps: loads issued before waiting for the stage, stored after
         int64_t tv[BN / 32];
 #pragma unroll
         for (int x = 0; x < BN / 32; ++x) {
           const int row = k0 + lane + 32 * x;
-          tv[x] = (p.ts && row < n) ? p.ts[sq.s0 + row] : tbase;
+          if (DELTA && !self) tv[x] = (p.ts2 && row < L) ? p.ts2[cs0 + row] : tbase;
+          else tv[x] = (p.ts && row < n) ? p.ts[sq.s0 + row] : tbase;
         }
         ok = mbar_wait(bar(BAR_KVEMPTY + stage), ((kv_it / kStages) & 1) ^ 1, wd, 2);
         if (!ok) break;
@@ -341,10 +372,13 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         if (lane == 0 && !withhold) {
           mbar_arrive_expect_tx(bar(BAR_KVFULL + stage), L::STAGE);
           const uint32_t dstK = sKV + stage * L::STAGE;
-          const int y = (int)(sq.s0 + k0);
+          const bool cached = DELTA && !self;
+          const CUtensorMap* mk = cached ? &tmk2 : &tmk;
+          const CUtensorMap* mv = cached ? &tmv2 : &tmv;
+          const int y = (int)(cached ? cs0 + k0 : sq.s0 + k0);
           for (int c = 0; c < L::NCH; ++c) {
-            tma_load_2d(dstK + c * L::BOX, &tmk, bar(BAR_KVFULL + stage), h * D + c * 64, y);
-            tma_load_2d(dstK + L::K_BYTES + c * L::BOX, &tmv, bar(BAR_KVFULL + stage), h * D + c * 64, y);
+            tma_load_2d(dstK + c * L::BOX, mk, bar(BAR_KVFULL + stage), h * D + c * 64, y);
+            tma_load_2d(dstK + L::K_BYTES + c * L::BOX, mv, bar(BAR_KVFULL + stage), h * D + c * 64, y);
           }
           armed[stage] += 1;
         }
@@ -381,7 +415,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         fence_after_sync();
         bool have_prev = false, first_pv = true;
         uint32_t prev_it = 0;
-        const int nkb = fwd_kv_blocks(sl.q0, sl.n, sl.c, BM, BN);
+        const int nkb = DELTA ? (sl.L + BN - 1) / BN + 1 : fwd_kv_blocks(sl.q0, sl.n, sl.c, BM, BN);
         // P of tile t: quarter k/2 of the S buffer, hi at [32 q, 32 q + 16), lo 16 columns later
         auto issue_pv = [&](uint32_t t) -> bool {
           const uint32_t sb = t & 1, stage = t % kStages;
@@ -401,7 +435,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         };
         for (int kb = 0; ok && kb < nkb; ++kb) {
           const int k0 = kb * BN;
-          if (tile_class(sl.q0, k0, BM, BN, sl.n, sl.c, sl.h_end) == 0) continue;
+          if (!DELTA && tile_class(sl.q0, k0, BM, BN, sl.n, sl.c, sl.h_end) == 0) continue;
           const uint32_t stage = kv_it % kStages, sb = kv_it & 1;
           ok = mbar_wait(bar(BAR_KVFULL + stage), (kv_it / kStages) & 1, wd, 6);
           if (!ok) break;
@@ -455,18 +489,19 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       const bool item_wide = sl.wide != 0;
       rc.n = sl.n;
       rc.cx = sl.c;
-      rc.h_end = sl.h_end;
+      rc.h_end = DELTA ? sl.L : sl.h_end;   // delta: the candidates' position is the cache length
       rc.i = q0 + row;
       rc.row_ok = rc.i < rc.n;
-      rc.pos_i = rc.i < rc.h_end ? rc.i : rc.h_end;
+      rc.pos_i = DELTA ? rc.h_end : (rc.i < rc.h_end ? rc.i : rc.h_end);
       rc.ti64 = qts_s[qb * BM + row];
       rc.ti32 = (int32_t)(rc.ti64 - sl.tbase);
       rc.tp = tab + hh * PT;
       rc.tt = rc.tp + P;
-      const int nkb = fwd_kv_blocks(q0, rc.n, rc.cx, BM, BN);
+      const int nkb = DELTA ? (rc.h_end + BN - 1) / BN + 1 : fwd_kv_blocks(q0, rc.n, rc.cx, BM, BN);
       for (int kb = 0; ok && kb < nkb; ++kb) {
-        const int k0 = kb * BN;
-        const int cls = tile_class(q0, k0, BM, BN, rc.n, rc.cx, rc.h_end);
+        const bool self = DELTA && kb == nkb - 1;
+        const int k0 = self ? q0 : kb * BN;
+        const int cls = DELTA ? 1 : tile_class(q0, k0, BM, BN, rc.n, rc.cx, rc.h_end);
         if (cls == 0) continue;
         const uint32_t stage = kv_it % kStages, sb = kv_it & 1;
         ok = mbar_wait(bar(BAR_KVFULL + stage), (kv_it / kStages) & 1, wd, 7) &&
@@ -482,7 +517,16 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         const int64_t* t64 = ts64_s + stage * BN + hq * 32;
         uint32_t hi[16], lo[16];
         const bool fast = cls == 2 && k0 + BN - 1 <= q0;
-        if (!item_wide && !stage_wide[stage]) {
+        const bool narrow = !item_wide && !stage_wide[stage];
+        if (DELTA) {
+          if (self) {
+            if (narrow) score32<false, false, false, 2>(sv, hi, lo, rc, jb, t32, t64);
+            else score32<false, true, false, 2>(sv, hi, lo, rc, jb, t32, t64);
+          } else {
+            if (narrow) score32<false, false, false, 1>(sv, hi, lo, rc, jb, t32, t64);
+            else score32<false, true, false, 1>(sv, hi, lo, rc, jb, t32, t64);
+          }
+        } else if (narrow) {
           if (fast) score32<true, false, false>(sv, hi, lo, rc, jb, t32, t64);
           else if (cls == 2) score32<false, false, false>(sv, hi, lo, rc, jb, t32, t64);
           else score32<false, false, true>(sv, hi, lo, rc, jb, t32, t64);
@@ -592,34 +636,47 @@ size_t tc_fwd_smem_bytes(int d, int H, int P, int Tb) {
   return (d == 64 ? Layout<64>::TAB_OFF : Layout<128>::TAB_OFF) + tab + 1024;
 }
 
-template <int D, typename TO>
+template <int D, typename TO, bool DELTA>
 static cudaError_t launch_fwd_t(const AttnParams& p, cudaStream_t st) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mk2, mv2;
   const int64_t cols = (int64_t)p.H * D;
   if (!make_tmap_bf16(&mq, p.q, p.T, cols, BM) || !make_tmap_bf16(&mk, p.k, p.T, cols, BN) ||
       !make_tmap_bf16(&mv, p.v, p.T, cols, BN))
     return cudaErrorInvalidValue;
+  if (DELTA && p.T2 > 0) {
+    if (!make_tmap_bf16(&mk2, p.k2, p.T2, cols, BN) || !make_tmap_bf16(&mv2, p.v2, p.T2, cols, BN))
+      return cudaErrorInvalidValue;
+  } else {
+    mk2 = mk;  // unused: no cached tiles
+    mv2 = mv;
+  }
   const size_t smem = tc_fwd_smem_bytes(D, p.H, p.P, p.Tb);
-  const void* fn = reinterpret_cast<const void*>(hstu_fwd_tc_kernel<D, TO>);
-  cudaError_t e = cudaFuncSetAttribute(hstu_fwd_tc_kernel<D, TO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  const void* fn = reinterpret_cast<const void*>(hstu_fwd_tc_kernel<D, TO, DELTA>);
+  cudaError_t e = cudaFuncSetAttribute(hstu_fwd_tc_kernel<D, TO, DELTA>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) {
     set_launch_detail(e, "hstu_fwd_tc_kernel (smem attribute)", fn, kThreads, smem);
     return e;
   }
   const int64_t max_items = ((p.T + BM - 1) / BM + p.B) * (int64_t)p.H;
   const int grid = (int)(max_items < p.num_sms ? max_items : p.num_sms);
-  hstu_fwd_tc_kernel<D, TO><<<grid, kThreads, smem, st>>>(p, mq, mk, mv);
+  hstu_fwd_tc_kernel<D, TO, DELTA><<<grid, kThreads, smem, st>>>(p, mq, mk, mv, mk2, mv2);
   e = cudaGetLastError();
   if (e != cudaSuccess) set_launch_detail(e, "hstu_fwd_tc_kernel", fn, kThreads, smem);
   return e;
 }
 
-cudaError_t launch_tc_fwd(const AttnParams& p, cudaStream_t st) {
+template <bool DELTA>
+static cudaError_t launch_any(const AttnParams& p, cudaStream_t st) {
   const bool f32 = p.out_dtype == HSTU_FP32;
-  if (p.dqk == 128) return f32 ? launch_fwd_t<128, float>(p, st) : launch_fwd_t<128, __nv_bfloat16>(p, st);
-  if (p.dqk == 64) return f32 ? launch_fwd_t<64, float>(p, st) : launch_fwd_t<64, __nv_bfloat16>(p, st);
+  if (p.dqk == 128)
+    return f32 ? launch_fwd_t<128, float, DELTA>(p, st) : launch_fwd_t<128, __nv_bfloat16, DELTA>(p, st);
+  if (p.dqk == 64)
+    return f32 ? launch_fwd_t<64, float, DELTA>(p, st) : launch_fwd_t<64, __nv_bfloat16, DELTA>(p, st);
   return cudaErrorInvalidValue;
 }
+
+cudaError_t launch_tc_fwd(const AttnParams& p, cudaStream_t st) { return launch_any<false>(p, st); }
+cudaError_t launch_tc_fwd_delta(const AttnParams& p, cudaStream_t st) { return launch_any<true>(p, st); }
 
 }  // namespace hstu

@@ -282,6 +282,50 @@ hstu_status_t hstu_layer_fwd(const hstu_attn_desc* desc, const hstu_layer_fwd_ar
 hstu_status_t hstu_layer_bwd(const hstu_attn_desc* desc, const hstu_layer_bwd_args* args,
                              void* workspace, size_t workspace_bytes, hstu_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Delta forward: KV-cached, candidate-only inference (P2 "HSTU acceleration
+ * operator" paragraph: variable-length sequences with a KV cache; P1 section
+ * 2.1.2: the ranking task scores all candidates of a request in one pass).
+ *
+ * Sequence b has L_b cached tokens (its context and history, already
+ * processed: their K and V are kept) and m_b new candidates.  The call
+ * computes, for the candidates only, exactly the candidate rows of
+ * hstu_attn_fwd on the whole sequence (n = L_b + m_b, num_targets = m_b):
+ * candidate r attends every cached token j < L_b (position bucket
+ * min(L_b - j, P - 1)) and itself (position bucket 0), never another
+ * candidate; o and y as in hstu_attn_fwd.  num_contexts play no part (a
+ * candidate sees all cached tokens either way).
+ *
+ * The descriptor is hstu_attn_fwd's with total_tokens = T_cand (candidates
+ * in the batch); max_seq_len = N must bound every L_b + m_b.  Workspace: the
+ * forward size from hstu_attn_workspace_size.  Tensor-core path only: BF16,
+ * d_qk = d_v in {64, 128}, T_cand >= 128 and T_cache == 0 or >= 128, else
+ * HSTU_ERR_UNSUPPORTED.  Offsets inconsistent with the counts are reported
+ * through the workspace error word (HSTU_ERR_DEVICE_CHECK).
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  const int64_t* cand_offsets;      /* [B+1] candidates of each sequence, packed; [B] == T_cand */
+  const int64_t* cache_offsets;     /* [B+1] cached tokens of each sequence, packed; [B] == cache_tokens */
+  int64_t cache_tokens;             /* T_cache */
+  const int64_t* cand_timestamps;   /* [T_cand] or NULL (no time bias) */
+  const int64_t* cache_timestamps;  /* [T_cache]; NULL iff cand_timestamps is NULL (when T_cache > 0) */
+  const float* rab_pos;             /* [H, P] or NULL */
+  const float* rab_time;            /* [H, Tb] or NULL */
+  const void* q;                    /* [T_cand, H, d] candidates */
+  const void* k;                    /* [T_cand, H, d] candidates' own keys */
+  const void* v;                    /* [T_cand, H, d] */
+  const void* u;                    /* [T_cand, H*d] gate or NULL */
+  const void* k_cache;              /* [T_cache, H, d] */
+  const void* v_cache;              /* [T_cache, H, d] */
+  void* o;                          /* out [T_cand, H, d] */
+  void* y;                          /* out [T_cand, H*d] or NULL */
+  float* ln_mean;                   /* out [T_cand] or NULL */
+  float* ln_rstd;                   /* out [T_cand] or NULL */
+} hstu_attn_delta_args;
+
+hstu_status_t hstu_attn_fwd_delta(const hstu_attn_desc* desc, const hstu_attn_delta_args* args,
+                                  void* workspace, size_t workspace_bytes, hstu_stream_t stream);
+
 /* Reads the device error word of the last call that used this workspace
  * (HSTU_OK when none).  Synchronises the stream. */
 hstu_status_t hstu_get_device_error(const void* workspace, hstu_stream_t stream, int32_t* code);

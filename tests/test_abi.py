@@ -135,3 +135,16 @@ def test_layer_rejects_missing_pointers_before_any_launch():
     with pytest.raises(C.HSTUError) as e:
         C.hstu_layer_bwd(d, bargs, 256, 1 << 30, None)
     assert e.value.status == C.HSTU_ERR_INVALID_ARG
+
+
+def test_delta_rejects_missing_pointers_before_any_launch():
+    d = _desc(out_dtype="fp32", total_tokens=256)
+    args = C.hstu_attn_delta_args()          # every pointer NULL
+    with pytest.raises(C.HSTUError) as e:
+        C.hstu_attn_fwd_delta(d, args, 256, 1 << 30, None)
+    assert e.value.status == C.HSTU_ERR_INVALID_ARG
+    args.cand_offsets = args.cache_offsets = 256   # offsets present, token tensors missing
+    args.cache_tokens = -1
+    with pytest.raises(C.HSTUError) as e:
+        C.hstu_attn_fwd_delta(d, args, 256, 1 << 30, None)
+    assert e.value.status == C.HSTU_ERR_INVALID_ARG
