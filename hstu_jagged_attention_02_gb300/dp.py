@@ -2,9 +2,9 @@
 
 The attention path shards by sequence with no exchange inside it: each rank
 runs whole sequences.  A data-parallel training step needs one exchange, the
-sum of the d_rab table gradients (H x (P + Tb) floats) over ranks; the
-benchmark needs the step time (max over ranks) and the work done (sum over
-ranks).  Everything here is host logic plus torch.distributed collectives on
+sum over ranks of the gradients of the shared parameters: the d_rab tables
+(H x (P + Tb) floats) and, for the full layer, dW1 and dW2; the benchmark
+needs the step time (max over ranks) and the work done (sum over ranks).  Everything here is host logic plus torch.distributed collectives on
 whatever backend the process group uses (NCCL on GPUs, gloo on CPUs).
 """
 from __future__ import annotations
@@ -43,7 +43,7 @@ def lpt_shard(costs: Sequence[int], world: int) -> List[List[int]]:
 
 def gather_sequences(batch, idx: Sequence[int]):
     """A new jagged batch holding the sequences idx of batch (same N, alpha,
-    tables): data movement only."""
+    tables and, for a layer batch, the same weights): data movement only."""
     idx = list(idx)
     off = batch.offsets
     rows = np.concatenate([np.arange(off[i], off[i + 1]) for i in idx]) if idx else np.zeros(0, np.int64)
@@ -57,7 +57,7 @@ def gather_sequences(batch, idx: Sequence[int]):
         timestamps=take(batch.timestamps), q=batch.q[rows], k=batch.k[rows], v=batch.v[rows],
         u=take(batch.u), dy=take(batch.dy), rab_pos=batch.rab_pos, rab_time=batch.rab_time,
         alpha=batch.alpha, max_seq_len=batch.max_seq_len, norm=batch.norm, eps=batch.eps,
-        backward=batch.backward)
+        backward=batch.backward, x=take(batch.x), w1=batch.w1, w2=batch.w2, dout=take(batch.dout))
 
 
 def allreduce_sum_(tensors, group=None):

@@ -75,3 +75,57 @@ def test_two_gloo_ranks_match_single_process():
         np.testing.assert_allclose(r[3], full["d_rab_time"], rtol=1e-10, atol=1e-12)
         assert r[4] == 11.0                                   # max over ranks
         assert r[5] == float(dp.sequence_costs(b).sum())      # summed work
+
+
+def _layer_batch():
+    r = np.random.default_rng(77)
+    H, d = 2, 4
+    D = H * d
+    hist = np.array([5, 9, 14, 3, 11])
+    nt = np.array([2, 3, 1, 2, 4], np.int32)
+    lengths = hist + nt
+    off = synth.offsets_from_lengths(lengths)
+    T = int(off[-1])
+    ts = np.concatenate([np.sort(r.integers(0, 4000, size=n)) for n in lengths]).astype(np.int64)
+    empty = np.zeros((T, H, 0))
+    return synth.Batch(name="layer", seed=77, dtype="fp32", B=5, H=H, d_qk=d, d_v=d, lengths=lengths,
+                       offsets=off, num_targets=nt, num_contexts=None, timestamps=ts, q=empty, k=empty, v=empty,
+                       u=None, dy=None, rab_pos=r.normal(0, 0.2, (H, 128)), rab_time=r.normal(0, 0.2, (H, 64)),
+                       alpha=0.5, max_seq_len=int(lengths.max()), x=r.standard_normal((T, D)),
+                       w1=r.normal(0, 0.3, (D, 4 * D)), w2=r.normal(0, 0.3, (D, D)),
+                       dout=r.standard_normal((T, D)))
+
+
+def _layer_worker(rank, world, port, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from oracle import oracle as O
+        b = _layer_batch()
+        shards = dp.lpt_shard(dp.sequence_costs(b), world)
+        g = O.layer_backward(dp.gather_sequences(b, shards[rank]))
+        grads = [torch.from_numpy(np.ascontiguousarray(g[k])) for k in ("dw1", "dw2", "d_rab_pos", "d_rab_time")]
+        dp.allreduce_sum_(grads)
+        q.put((rank, [t.numpy() for t in grads]))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_layer_gradients_all_reduced_over_two_ranks_match_single_process():
+    from oracle import oracle as O
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_layer_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=300) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    full = O.layer_backward(_layer_batch())
+    for _, grads in res:
+        for got, key in zip(grads, ("dw1", "dw2", "d_rab_pos", "d_rab_time")):
+            np.testing.assert_allclose(got, full[key], rtol=1e-9, atol=1e-12)
