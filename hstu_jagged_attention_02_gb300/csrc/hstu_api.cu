@@ -35,7 +35,7 @@ size_t align_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
 size_t esize(int dtype) { return dtype == HSTU_BF16 ? 2 : 4; }
 
 struct WsLayout {
-  size_t seq_start, tmp, blocks, plan_end, dO, dq_acc, drab_part, drab_part_bytes, total;
+  size_t seq_start, tmp, blocks, items, plan_end, dO, dq_acc, drab_part, drab_part_bytes, total;
   int cap_blocks;
 };
 
@@ -47,6 +47,7 @@ WsLayout ws_layout(const hstu_attn_desc* d, bool bwd) {
   L.seq_start = off; off = align_up(off + sizeof(int) * (size_t)(d->B + 1));
   L.tmp = off;       off = align_up(off + sizeof(Block) * (size_t)cap);
   L.blocks = off;    off = align_up(off + sizeof(Block) * (size_t)cap);
+  L.items = off;     off = align_up(off + sizeof(PlanItem) * (size_t)cap);
   L.plan_end = off;
   if (bwd) {
     const size_t rows = (size_t)d->total_tokens * (size_t)d->H;
@@ -133,6 +134,7 @@ PlanParams plan_params(const hstu_attn_desc* d, const int64_t* off, const int32_
   p.seq_start = reinterpret_cast<int*>(ws + L.seq_start);
   p.tmp = reinterpret_cast<Block*>(ws + L.tmp);
   p.blocks = reinterpret_cast<Block*>(ws + L.blocks);
+  p.items = reinterpret_cast<PlanItem*>(ws + L.items);
   p.cap_blocks = L.cap_blocks;
   return p;
 }
@@ -233,7 +235,7 @@ hstu_status_t hstu_attn_fwd(const hstu_attn_desc* d, const hstu_attn_fwd_args* a
   p.off = a->seq_offsets; p.nt = a->num_targets; p.nc = a->num_contexts;
   p.ts = a->timestamps; p.rab_pos = a->rab_pos; p.rab_time = a->timestamps ? a->rab_time : nullptr;
   p.q = a->q; p.k = a->k; p.v = a->v; p.o = a->o;
-  p.hdr = pp.hdr; p.hdr_rw = pp.hdr; p.blocks = pp.blocks;
+  p.hdr = pp.hdr; p.hdr_rw = pp.hdr; p.blocks = pp.blocks; p.items = pp.items;
   p.B = d->B; p.H = d->H; p.dqk = d->d_qk; p.dv_dim = d->d_v; p.T = d->total_tokens;
   p.dtype = d->dtype; p.out_dtype = d->out_dtype;
   p.alpha = d->alpha; p.inv_n = 1.0f / (float)d->max_seq_len;
@@ -326,7 +328,7 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
   p.d_rab_pos = has_rp ? a->d_rab_pos : nullptr;
   p.d_rab_time = has_rt ? a->d_rab_time : nullptr;
   p.drab_partial = drab_partial;
-  p.hdr = pp.hdr; p.hdr_rw = pp.hdr; p.blocks = pp.blocks;
+  p.hdr = pp.hdr; p.hdr_rw = pp.hdr; p.blocks = pp.blocks; p.items = pp.items;
   p.B = d->B; p.H = d->H; p.dqk = d->d_qk; p.dv_dim = d->d_v; p.T = d->total_tokens;
   p.dtype = d->dtype; p.out_dtype = d->out_dtype;
   p.alpha = d->alpha; p.inv_n = 1.0f / (float)d->max_seq_len;
@@ -387,7 +389,7 @@ hstu_status_t hstu_attn_fwd_delta(const hstu_attn_desc* d, const hstu_attn_delta
   p.q = a->q; p.k = a->k; p.v = a->v; p.o = a->o;
   p.off2 = a->cache_offsets; p.ts2 = a->cache_timestamps; p.k2 = a->k_cache; p.v2 = a->v_cache;
   p.T2 = a->cache_tokens;
-  p.hdr = pp.hdr; p.hdr_rw = pp.hdr; p.blocks = pp.blocks;
+  p.hdr = pp.hdr; p.hdr_rw = pp.hdr; p.blocks = pp.blocks; p.items = pp.items;
   p.B = d->B; p.H = d->H; p.dqk = d->d_qk; p.dv_dim = d->d_v; p.T = d->total_tokens;
   p.dtype = d->dtype; p.out_dtype = d->out_dtype;
   p.alpha = d->alpha; p.inv_n = 1.0f / (float)d->max_seq_len;

@@ -44,6 +44,19 @@ struct __align__(16) Block {
   int pad;
 };
 
+// The work-item record the planner writes for the tensor-core kernels, in
+// longest-first order: everything a producer needs about an item in one
+// 48-byte load (the sequence's first token and its timestamp, the counts,
+// and for the delta forward the sequence's cached tokens).
+struct __align__(16) PlanItem {
+  int64_t s0;     // first token of the sequence (candidates' first token for the delta forward)
+  int64_t tbase;  // timestamp of that token, 0 without timestamps
+  int64_t cs0;    // delta forward: first cached token of the sequence
+  int b, blk;     // sequence, block index within it
+  int n, c, h_end;
+  int L;          // delta forward: cached tokens of the sequence
+};
+
 __device__ __forceinline__ void set_error(int* hdr, int code, int info) {
   if (atomicCAS(hdr + WS_ERR, 0, code) == 0) hdr[WS_ERR_INFO] = info;
 }

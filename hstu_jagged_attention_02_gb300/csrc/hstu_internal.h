@@ -23,6 +23,7 @@ struct PlanParams {
   int* seq_start;   // [B+1] scratch
   Block* tmp;       // [cap_blocks] scratch
   Block* blocks;    // [cap_blocks] result, longest first
+  PlanItem* items;  // [cap_blocks] the same blocks as full item records (tensor-core kernels)
   int cap_blocks;
   int stage_off;    // set by launch_plan: offsets and block starts staged in shared memory
   int stage_rec;    // set by launch_plan: block records staged in shared memory
@@ -53,6 +54,7 @@ struct AttnParams {
   const int* hdr;        // workspace header (block count)
   int* hdr_rw;           // same, writable (error word)
   const Block* blocks;
+  const PlanItem* items;  // the planner's item records, same order as blocks
   // delta forward (KV-cached candidates): cached-token offsets [B+1], times
   // [T2] (or NULL) and K, V [T2, H, d]; q, k, v, o above are the candidates'
   const int64_t* off2;

@@ -183,11 +183,23 @@ plan_kernel(PlanParams p) {
   }
   __syncthreads();
 
-  // 5. scatter into longest-first order
+  // 5. scatter into longest-first order, as block records and as full item
+  // records (one load per item for the tensor-core kernels' producers)
   for (int idx = t; idx < nblk; idx += kPlanThreads) {
     const Block r = rec[idx];
     const int pos = atomicAdd(&sh_hist[r.cost < kCostBins ? r.cost : kCostBins - 1], 1);
     p.blocks[pos] = r;
+    PlanItem it;
+    it.b = r.b;
+    it.blk = r.blk;
+    it.s0 = off[r.b];
+    it.n = (int)(off[r.b + 1] - it.s0);
+    it.c = p.nc ? p.nc[r.b] : 0;
+    it.h_end = it.n - (p.nt ? p.nt[r.b] : 0);
+    it.tbase = (p.ts && it.n > 0) ? p.ts[it.s0] : 0;
+    it.cs0 = p.pass == 2 ? p.off2[r.b] : 0;
+    it.L = p.pass == 2 ? (int)(p.off2[r.b + 1] - it.cs0) : 0;
+    p.items[pos] = it;
   }
   if (t == 0) p.hdr[WS_NBLK] = nblk;
 }

@@ -115,6 +115,8 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 struct KeyCtx {
   int j, n, cx, h_end, pos_j, P, Tb;
   bool j_ok, want_rp, want_rt;
+  // the queries allowed to see this key under the compound mask: lo <= i <= hi
+  int lo, hi;
   int32_t tj32;
   int64_t tj64;
   const float* tp;   // position table of the head (times -log2 e)
@@ -179,7 +181,7 @@ __device__ __forceinline__ void grad_cols(const uint32_t (&sv)[NC], const uint32
       const float sg = rcp_approx(1.0f + ex2_approx(w));
       const float z = w * kc.kZ;
       const int i = ib + c + e;
-      const bool valid = kc.j_ok && i < kc.n && allowed(i, kc.j, kc.cx, kc.h_end);
+      const bool valid = i >= kc.lo && i <= kc.hi;
       const float a = valid ? (w * kc.kC) * sg : 0.f;
       const float dz = valid ? __uint_as_float(dav[c + e]) * sg * fmaf(z, 1.f - sg, 1.f) * kc.inv_n : 0.f;
       av[e] = a;
@@ -295,27 +297,24 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     bool kv_copy = false;                 // the last KVFULL phase carries a copy
     uint32_t armed[kQStages] = {0, 0};
     bool ok = true;
+    // The next work item is claimed only once the current one's loads are all
+    // issued (claiming earlier pairs items up statically and loses the
+    // longest-first balance); its planner record is one 48-byte load.
     while (ok) {
       int idx = 0;
       if (lane == 0) idx = atomicAdd(p.hdr_rw + WS_NEXT, 1);
       idx = __shfl_sync(0xffffffffu, idx, 0);
       const bool valid = idx < nitems;
-      int h = 0, k0 = 0;
-      SeqInfo sq{};
-      if (valid) {
-        const Block blk = p.blocks[idx / H];
-        h = idx % H;
-        k0 = blk.blk * BK;
-        sq = seq_info(p.off, p.nt, p.nc, blk.b);
-      }
-      const int n = sq.n;
-      const int64_t tbase = (valid && p.ts) ? p.ts[sq.s0] : 0;
+      PlanItem it{};
+      if (valid) it = p.items[idx / H];
+      const int h = idx % H, k0 = it.blk * BK, n = it.n;
+      const int64_t tbase = it.tbase, s0 = it.s0;
       // key-row timestamps of the item: loads issued before waiting
       int64_t kv[BK / 32];
 #pragma unroll
       for (int x = 0; x < BK / 32; ++x) {
         const int row = k0 + lane + 32 * x;
-        kv[x] = (valid && p.ts && row < n) ? p.ts[sq.s0 + row] : tbase;
+        kv[x] = (valid && p.ts && row < n) ? p.ts[s0 + row] : tbase;
       }
       bool kw = false;
 #pragma unroll
@@ -327,15 +326,15 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
 #pragma unroll
       for (int x = 0; x < BK / 32; ++x) kts_s[lane + 32 * x] = kv[x];
       if (lane == 0) {
-        slot->s0 = sq.s0; slot->tbase = tbase; slot->valid = valid ? 1 : 0;
-        slot->h = h; slot->k0 = k0; slot->n = n; slot->c = sq.c; slot->h_end = sq.h_end;
+        slot->s0 = s0; slot->tbase = tbase; slot->valid = valid ? 1 : 0;
+        slot->h = h; slot->k0 = k0; slot->n = n; slot->c = it.c; slot->h_end = it.h_end;
         slot->wide = item_wide ? 1 : 0;
       }
       __syncwarp();
       if (lane == 0) {
         if (valid) {
           mbar_arrive_expect_tx(bar(BAR_KVFULL), 4 * Lay::KBOX);
-          const int y = (int)(sq.s0 + k0);
+          const int y = (int)(s0 + k0);
           for (int c = 0; c < 2; ++c) {
             tma_load_2d(sK + c * Lay::KBOX, &tmk, bar(BAR_KVFULL), h * D + c * 64, y);
             tma_load_2d(sV + c * Lay::KBOX, &tmv, bar(BAR_KVFULL), h * D + c * 64, y);
@@ -349,16 +348,16 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       ++item_it;
       if (!valid) break;
       const int nqt = (n + BQ - 1) / BQ;
-      for (int qt = bwd_q_begin(k0, sq.c, BQ); ok && qt < nqt; ++qt) {
+      for (int qt = bwd_q_begin(k0, it.c, BQ); ok && qt < nqt; ++qt) {
         const int q0 = qt * BQ;
-        if (tile_class(q0, k0, BQ, BK, n, sq.c, sq.h_end) == 0) continue;
+        if (tile_class(q0, k0, BQ, BK, n, it.c, it.h_end) == 0) continue;
         const int stage = qt_it % kQStages;
         // query timestamps: loads issued before waiting for the stage, stored after
         int64_t tv[BQ / 32];
 #pragma unroll
         for (int x = 0; x < BQ / 32; ++x) {
           const int row = q0 + lane + 32 * x;
-          tv[x] = (p.ts && row < n) ? p.ts[sq.s0 + row] : tbase;
+          tv[x] = (p.ts && row < n) ? p.ts[s0 + row] : tbase;
         }
         ok = mbar_wait(bar(BAR_QEMPTY + stage), ((qt_it / kQStages) & 1) ^ 1, wd, 22);
         if (!ok) break;
@@ -376,7 +375,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           const uint32_t full = bar(BAR_QFULL + stage);
           mbar_arrive_expect_tx(full, Lay::QSTAGE);
           const uint32_t dst = sQS + stage * Lay::QSTAGE;
-          const int y = (int)(sq.s0 + q0);
+          const int y = (int)(s0 + q0);
           for (int c = 0; c < 2; ++c) {
             tma_load_2d(dst + c * Lay::QBOX, &tmq, full, h * D + c * 64, y);
             tma_load_2d(dst + Lay::Q_BYTES + c * Lay::QBOX, &tmdh, full, h * D + c * 64, y);
@@ -540,6 +539,10 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       kc.j = k0 + lrow;
       kc.j_ok = kc.j < kc.n;
       kc.pos_j = kc.j < kc.h_end ? kc.j : kc.h_end;
+      // queries that see this key: a context key is seen by every row, a
+      // history key by the rows at or after it, a candidate key by itself only
+      kc.lo = !kc.j_ok ? 1 : (kc.j >= kc.h_end ? kc.j : (kc.j < kc.cx ? 0 : kc.j));
+      kc.hi = !kc.j_ok ? 0 : (kc.j >= kc.h_end ? kc.j : kc.n - 1);
       kc.tj64 = kts_s[lrow];
       kc.tj32 = (int32_t)(kc.tj64 - sl.tbase);
       kc.tp = tab + hh * PT;

@@ -109,6 +109,9 @@ __device__ __forceinline__ float rcp_approx(float x) {
 struct RowCtx {
   int i, n, cx, h_end, pos_i, P, Tb;
   bool row_ok;
+  // the row's allowed keys under the compound mask: j <= hi, and j == dg
+  // (a candidate's own key); hi = -1, dg = -1 for rows past the sequence
+  int hi, dg;
   int32_t ti32;      // timestamp relative to the sequence's first token
   int64_t ti64;      // absolute timestamp
   const float* tp;   // position table of the head (pre-scaled)
@@ -175,7 +178,7 @@ __device__ __forceinline__ void score32(const uint32_t (&sv)[32], uint32_t (&hi)
           a = (rc.row_ok && jb + cc == rc.i) ? a : 0.f;
         } else if (PARTIAL) {
           const int j = jb + cc;
-          const bool valid = rc.row_ok && j < rc.n && allowed(rc.i, j, rc.cx, rc.h_end);
+          const bool valid = j <= rc.hi || j == rc.dg;
           a = valid ? a : 0.f;
         }
         a2[e] = a;
@@ -277,36 +280,29 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     uint32_t kv_it = 0, q_it = 0;
-    uint32_t armed[kStages] = {0, 0};   // phases armed per KV stage
+    uint32_t armed[kStages] = {0, 0};    // phases armed per stage
     uint32_t q_phases[kQBufs] = {0, 0};  // phases used per Q buffer (a copy or the final no-work arrive)
     bool q_copy[kQBufs] = {false, false}; // the buffer's last phase carries a copy
     bool ok = true;
+    // The next work item is claimed only once the current one's loads are all
+    // issued (claiming earlier pairs items up statically and loses the
+    // longest-first balance); its planner record is one 48-byte load.
     while (ok) {
       const int qb = (int)(q_it % kQBufs);
       int idx = 0;
       if (lane == 0) idx = atomicAdd(p.hdr_rw + WS_NEXT, 1);
       idx = __shfl_sync(0xffffffffu, idx, 0);
       const bool valid = idx < nitems;
-      int h = 0, q0 = 0, L = 0;
-      int64_t cs0 = 0;
-      SeqInfo sq{};
-      if (valid) {
-        const Block blk = p.blocks[idx / H];
-        h = idx % H;
-        q0 = blk.blk * BM;
-        sq = seq_info(p.off, p.nt, p.nc, blk.b);
-        if (DELTA) {
-          cs0 = p.off2[blk.b];
-          L = (int)(p.off2[blk.b + 1] - cs0);
-        }
-      }
-      const int64_t tbase = (valid && p.ts) ? p.ts[sq.s0] : 0;
+      PlanItem it{};
+      if (valid) it = p.items[idx / H];
+      const int h = idx % H, q0 = it.blk * BM, n = it.n, L = it.L;
+      const int64_t tbase = it.tbase, s0 = it.s0, cs0 = it.cs0;
       // query-row timestamps: loads issued before waiting for the buffer
       int64_t qv[BM / 32];
 #pragma unroll
       for (int x = 0; x < BM / 32; ++x) {
         const int row = q0 + lane + 32 * x;
-        qv[x] = (valid && p.ts && row < sq.n) ? p.ts[sq.s0 + row] : tbase;
+        qv[x] = (valid && p.ts && row < n) ? p.ts[s0 + row] : tbase;
       }
       bool qw = false;
 #pragma unroll
@@ -319,8 +315,8 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       for (int x = 0; x < BM / 32; ++x) qts_s[qb * BM + lane + 32 * x] = qv[x];
       if (lane == 0) {
         ItemSlot& sl = slots[qb];
-        sl.s0 = sq.s0; sl.tbase = tbase; sl.valid = valid ? 1 : 0;
-        sl.h = h; sl.q0 = q0; sl.n = sq.n; sl.c = sq.c; sl.h_end = sq.h_end; sl.wide = item_wide ? 1 : 0;
+        sl.s0 = s0; sl.tbase = tbase; sl.valid = valid ? 1 : 0;
+        sl.h = h; sl.q0 = q0; sl.n = n; sl.c = it.c; sl.h_end = it.h_end; sl.wide = item_wide ? 1 : 0;
         sl.L = L; sl.cs0 = cs0;
       }
       __syncwarp();
@@ -329,7 +325,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           mbar_arrive_expect_tx(bar(BAR_QFULL + qb), L::Q_BYTES);
           for (int c = 0; c < L::NCH; ++c)
             tma_load_2d(sQ0 + qb * L::Q_BYTES + c * L::BOX, &tmq, bar(BAR_QFULL + qb), h * D + c * 64,
-                        (int)(sq.s0 + q0));
+                        (int)(s0 + q0));
         } else {
           mbar_arrive(bar(BAR_QFULL + qb));  // the slot says: no more work
         }
@@ -338,14 +334,13 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       }
       ++q_it;
       if (!valid) break;
-      const int n = sq.n;
-      const int nkb = DELTA ? (L + BN - 1) / BN + 1 : fwd_kv_blocks(q0, n, sq.c, BM, BN);
+      const int nkb = DELTA ? (L + BN - 1) / BN + 1 : fwd_kv_blocks(q0, n, it.c, BM, BN);
       // test only: the CTA that takes work item 0 withholds that item's first K/V load
       bool withhold_next = (p.flags & HSTU_FLAG_TEST_TIMEOUT) && idx == 0;
       for (int kb = 0; ok && kb < nkb; ++kb) {
         const bool self = DELTA && kb == nkb - 1;   // delta: the candidates' own keys
         const int k0 = self ? q0 : kb * BN;
-        if (!DELTA && tile_class(q0, k0, BM, BN, n, sq.c, sq.h_end) == 0) continue;
+        if (!DELTA && tile_class(q0, k0, BM, BN, n, it.c, it.h_end) == 0) continue;
         const int stage = kv_it % kStages;
         // key timestamps: loads issued before waiting for the stage, stored after
         int64_t tv[BN / 32];
@@ -353,7 +348,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         for (int x = 0; x < BN / 32; ++x) {
           const int row = k0 + lane + 32 * x;
           if (DELTA && !self) tv[x] = (p.ts2 && row < L) ? p.ts2[cs0 + row] : tbase;
-          else tv[x] = (p.ts && row < n) ? p.ts[sq.s0 + row] : tbase;
+          else tv[x] = (p.ts && row < n) ? p.ts[s0 + row] : tbase;
         }
         ok = mbar_wait(bar(BAR_KVEMPTY + stage), ((kv_it / kStages) & 1) ^ 1, wd, 2);
         if (!ok) break;
@@ -375,7 +370,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           const bool cached = DELTA && !self;
           const CUtensorMap* mk = cached ? &tmk2 : &tmk;
           const CUtensorMap* mv = cached ? &tmv2 : &tmv;
-          const int y = (int)(cached ? cs0 + k0 : sq.s0 + k0);
+          const int y = (int)(cached ? cs0 + k0 : s0 + k0);
           for (int c = 0; c < L::NCH; ++c) {
             tma_load_2d(dstK + c * L::BOX, mk, bar(BAR_KVFULL + stage), h * D + c * 64, y);
             tma_load_2d(dstK + L::K_BYTES + c * L::BOX, mv, bar(BAR_KVFULL + stage), h * D + c * 64, y);
@@ -493,6 +488,10 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       rc.i = q0 + row;
       rc.row_ok = rc.i < rc.n;
       rc.pos_i = DELTA ? rc.h_end : (rc.i < rc.h_end ? rc.i : rc.h_end);
+      // allowed keys of this row: history/context rows see j <= i (context rows
+      // the whole context), candidates see all of history/context and themselves
+      rc.hi = !rc.row_ok ? -1 : (rc.i < rc.h_end ? (rc.i < rc.cx ? rc.cx - 1 : rc.i) : rc.h_end - 1);
+      rc.dg = (rc.row_ok && rc.i >= rc.h_end) ? rc.i : -1;
       rc.ti64 = qts_s[qb * BM + row];
       rc.ti32 = (int32_t)(rc.ti64 - sl.tbase);
       rc.tp = tab + hh * PT;

@@ -181,9 +181,9 @@ hstu_status_t hstu_attn_debug_plan(const hstu_attn_desc* desc, const int64_t* se
  * passes every input and output buffer.  The scratch comes from a 1 MiB
  * buffer built into the library (every GPU that loads the library holds it
  * until the process exits).  The plan of T tokens in B sequences needs
- * 256 + 4 (B + 1) + 32 (ceil(T / 32) + B) bytes (each part rounded up to
- * 256), roughly T + 36 B + 1 KiB, which must fit in 1 MiB: e.g. 500,000
- * tokens in 10,000 sequences.  Larger problems return HSTU_ERR_WORKSPACE
+ * 256 + 4 (B + 1) + 80 (ceil(T / 32) + B) bytes (each part rounded up to
+ * 256), roughly 2.5 T + 84 B + 1 KiB, which must fit in 1 MiB: e.g. 250,000
+ * tokens in 4,000 sequences.  Larger problems return HSTU_ERR_WORKSPACE
  * (hstu_last_error_detail says how much was needed) without launching.
  *
  * The first call on each device looks up the buffer's device address with
