@@ -82,6 +82,14 @@ hstu_status_t check_desc(const hstu_attn_desc* d) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// Score constants of the tensor-core epilogues (w = -log2(e) z form).
+void set_score_constants(AttnParams& p) {
+  const float log2e = 1.4426950408889634f;
+  p.kA = -log2e * p.alpha;
+  p.kC = -p.inv_n / log2e;
+  p.kZ = -1.0f / log2e;
+}
+
 hstu_status_t check_ws(void* ws, size_t bytes, size_t need) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kWsAlign - 1)) != 0) return HSTU_ERR_WORKSPACE;
   if (bytes < need) return HSTU_ERR_WORKSPACE;
@@ -239,6 +247,7 @@ hstu_status_t hstu_attn_fwd(const hstu_attn_desc* d, const hstu_attn_fwd_args* a
   p.B = d->B; p.H = d->H; p.dqk = d->d_qk; p.dv_dim = d->d_v; p.T = d->total_tokens;
   p.dtype = d->dtype; p.out_dtype = d->out_dtype;
   p.alpha = d->alpha; p.inv_n = 1.0f / (float)d->max_seq_len;
+  set_score_constants(p);
   p.P = d->num_pos_buckets; p.Tb = d->num_time_buckets; p.flags = d->flags;
   p.num_sms = dev_info().sms;
   if (d->total_tokens > 0) {
@@ -332,6 +341,7 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
   p.B = d->B; p.H = d->H; p.dqk = d->d_qk; p.dv_dim = d->d_v; p.T = d->total_tokens;
   p.dtype = d->dtype; p.out_dtype = d->out_dtype;
   p.alpha = d->alpha; p.inv_n = 1.0f / (float)d->max_seq_len;
+  set_score_constants(p);
   p.P = d->num_pos_buckets; p.Tb = d->num_time_buckets; p.flags = d->flags;
   p.num_sms = dev_info().sms;
   {
@@ -393,6 +403,7 @@ hstu_status_t hstu_attn_fwd_delta(const hstu_attn_desc* d, const hstu_attn_delta
   p.B = d->B; p.H = d->H; p.dqk = d->d_qk; p.dv_dim = d->d_v; p.T = d->total_tokens;
   p.dtype = d->dtype; p.out_dtype = d->out_dtype;
   p.alpha = d->alpha; p.inv_n = 1.0f / (float)d->max_seq_len;
+  set_score_constants(p);
   p.P = d->num_pos_buckets; p.Tb = d->num_time_buckets; p.flags = d->flags;
   p.num_sms = dev_info().sms;
   {

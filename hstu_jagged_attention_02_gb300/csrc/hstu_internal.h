@@ -66,6 +66,9 @@ struct AttnParams {
   int dtype, out_dtype;  // hstu_dtype_t of the inputs / of the outputs
   int64_t T;
   float alpha, inv_n;
+  // score constants of the tensor-core epilogues (w = -log2(e) z):
+  // kA = -log2(e) alpha, kC = -1 / (log2(e) N), kZ = -1 / log2(e)
+  float kA, kC, kZ;
   int P, Tb;
   uint32_t flags;
   int num_sms;

@@ -113,17 +113,14 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 
 // Per-thread context of the epilogue: one key row j of the item.
 struct KeyCtx {
-  int j, n, cx, h_end, pos_j, P, Tb;
-  bool j_ok, want_rp, want_rt;
+  int j, h_end, pos_j;
+  bool want_rp, want_rt;
   // the queries allowed to see this key under the compound mask: lo <= i <= hi
   int lo, hi;
   int32_t tj32;
   int64_t tj64;
-  const float* tp;   // position table of the head (times -log2 e)
-  const float* tt;   // time table of the head (times -log2 e)
-  float* drp;        // this CTA's d_rab partial sums of the head (global, private to the CTA)
-  float* drt;
-  float kA, kC, kZ, inv_n;  // -log2(e) alpha, -1/(log2(e) N), -1/log2(e), 1/N
+  const float* tp;   // bias tables of the head, times -log2 e: position [0, P), time [P, P + Tb)
+  float* drp;        // this CTA's d_rab partial sums of the head: position [0, P), time [P, P + Tb)
 };
 
 // d_rab partial sums one epilogue thread carries.  A thread owns one key row
@@ -144,7 +141,7 @@ struct RabAcc {
 // that skip the mask on full tiles cost more in instruction fetch than they
 // save on heavy-tailed batches, where tile classes alternate.)
 template <int NC, bool WIDE>
-__device__ __forceinline__ void grad_cols(const uint32_t (&sv)[NC], const uint32_t (&dav)[NC],
+__device__ __forceinline__ void grad_cols(const AttnParams& p, const uint32_t (&sv)[NC], const uint32_t (&dav)[NC],
                                           uint32_t (&ahi)[NC / 2], uint32_t (&alo)[NC / 2], uint32_t (&zhi)[NC / 2],
                                           uint32_t (&zlo)[NC / 2], const KeyCtx& kc, int ib, const int32_t* ts32,
                                           const int64_t* ts64, RabAcc& acc) {
@@ -156,7 +153,7 @@ __device__ __forceinline__ void grad_cols(const uint32_t (&sv)[NC], const uint32
     const int pi = i < kc.h_end ? i : kc.h_end;
     int dp = pi - kc.pos_j;
     dp = dp < 0 ? -dp : dp;
-    const int bp = dp < kc.P - 1 ? dp : kc.P - 1;
+    const int bp = dp < p.P - 1 ? dp : p.P - 1;
     int bt;
     if (WIDE) {
       const int64_t ti = ts64[c];
@@ -167,34 +164,34 @@ __device__ __forceinline__ void grad_cols(const uint32_t (&sv)[NC], const uint32
       d = d < 0 ? -d : d;
       bt = 32 - __clz(d);
     }
-    bt = bt < kc.Tb - 1 ? bt : kc.Tb - 1;
+    bt = bt < p.Tb - 1 ? bt : p.Tb - 1;
     bps[c] = bp;
     bts[c] = bt;
-    bias[c] = kc.tp[bp] + kc.tt[bt];
+    bias[c] = kc.tp[bp] + kc.tp[p.P + bt];
   }
 #pragma unroll
   for (int c = 0; c < NC; c += 2) {
     float av[2], zv[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const float w = fmaf(kc.kA, __uint_as_float(sv[c + e]), bias[c + e]);
+      const float w = fmaf(p.kA, __uint_as_float(sv[c + e]), bias[c + e]);
       const float sg = rcp_approx(1.0f + ex2_approx(w));
-      const float z = w * kc.kZ;
+      const float z = w * p.kZ;
       const int i = ib + c + e;
       const bool valid = i >= kc.lo && i <= kc.hi;
-      const float a = valid ? (w * kc.kC) * sg : 0.f;
-      const float dz = valid ? __uint_as_float(dav[c + e]) * sg * fmaf(z, 1.f - sg, 1.f) * kc.inv_n : 0.f;
+      const float a = valid ? (w * p.kC) * sg : 0.f;
+      const float dz = valid ? __uint_as_float(dav[c + e]) * sg * fmaf(z, 1.f - sg, 1.f) * p.inv_n : 0.f;
       av[e] = a;
       zv[e] = dz;
       if (kc.want_rp && valid) {
-        if (bps[c + e] == kc.P - 1) acc.rp_far += dz;
+        if (bps[c + e] == p.P - 1) acc.rp_far += dz;
         else red_add(kc.drp + bps[c + e], dz, true);
       }
       if (kc.want_rt && valid) {
         if (bts[c + e] == acc.rt_cur) {
           acc.rt_run += dz;
         } else {
-          red_add(kc.drt + acc.rt_cur, acc.rt_run, acc.rt_cur >= 0);
+          red_add(kc.drp + p.P + acc.rt_cur, acc.rt_run, acc.rt_cur >= 0);
           acc.rt_cur = bts[c + e];
           acc.rt_run = dz;
         }
@@ -496,14 +493,9 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     uint32_t item_it = 0, qt_it = 0;
     bool ok = true;
     KeyCtx kc;
-    kc.P = P;
-    kc.Tb = Tb;
+    int n_seq = 0;  // tokens of the current item's sequence
     kc.want_rp = want_rp;
     kc.want_rt = want_rt;
-    kc.kA = -kLog2e * p.alpha;
-    kc.kC = -p.inv_n / kLog2e;
-    kc.kZ = -1.0f / kLog2e;
-    kc.inv_n = p.inv_n;
     // the dQ^T of the previous query tile, drained in the middle of the next
     auto drain_dq = [&](uint32_t g, int qb0, int64_t s0, int hh) -> bool {
       if (!mbar_wait(bar(BAR_DQFULL), g & 1, wd, 30)) return false;
@@ -520,7 +512,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       const float alpha = p.alpha;
 #pragma unroll
       for (int c = 0; c < 16; ++c)
-        if (ib + c < kc.n) atomicAdd(dst + c * ld, alpha * __uint_as_float(qv[c]));
+        if (ib + c < n_seq) atomicAdd(dst + c * ld, alpha * __uint_as_float(qv[c]));
       return true;
     };
     while (ok) {
@@ -533,31 +525,29 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       const int64_t s0 = sl.s0;
       const int hh = sl.h, k0 = sl.k0;
       const bool item_wide = sl.wide != 0;
-      kc.n = sl.n;
-      kc.cx = sl.c;
+      n_seq = sl.n;
+      const int cx = sl.c;
       kc.h_end = sl.h_end;
       kc.j = k0 + lrow;
-      kc.j_ok = kc.j < kc.n;
+      const bool j_ok = kc.j < n_seq;
       kc.pos_j = kc.j < kc.h_end ? kc.j : kc.h_end;
       // queries that see this key: a context key is seen by every row, a
       // history key by the rows at or after it, a candidate key by itself only
-      kc.lo = !kc.j_ok ? 1 : (kc.j >= kc.h_end ? kc.j : (kc.j < kc.cx ? 0 : kc.j));
-      kc.hi = !kc.j_ok ? 0 : (kc.j >= kc.h_end ? kc.j : kc.n - 1);
+      kc.lo = !j_ok ? 1 : (kc.j >= kc.h_end ? kc.j : (kc.j < cx ? 0 : kc.j));
+      kc.hi = !j_ok ? 0 : (kc.j >= kc.h_end ? kc.j : n_seq - 1);
       kc.tj64 = kts_s[lrow];
       kc.tj32 = (int32_t)(kc.tj64 - sl.tbase);
       kc.tp = tab + hh * PT;
-      kc.tt = kc.tp + P;
       kc.drp = drab + hh * PT;
-      kc.drt = kc.drp + P;
       RabAcc racc;
       racc.rp_far = racc.rt_run = 0.f;
       racc.rt_cur = -1;
       bool pend = false;    // a dQ^T of this item waits to be drained
       int pend_q0 = 0;
-      const int nqt = (kc.n + BQ - 1) / BQ;
-      for (int qt = bwd_q_begin(k0, kc.cx, BQ); ok && qt < nqt; ++qt) {
+      const int nqt = (n_seq + BQ - 1) / BQ;
+      for (int qt = bwd_q_begin(k0, cx, BQ); ok && qt < nqt; ++qt) {
         const int q0 = qt * BQ;
-        const int cls = tile_class(q0, k0, BQ, BK, kc.n, kc.cx, kc.h_end);
+        const int cls = tile_class(q0, k0, BQ, BK, n_seq, cx, kc.h_end);
         if (cls == 0) continue;
         const uint32_t stage = qt_it % kQStages;
         ok = mbar_wait(bar(BAR_QFULL + stage), (qt_it / kQStages) & 1, wd, 28) &&
@@ -585,8 +575,8 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           const int32_t* t32 = ts32_s + stage * BQ + c0;
           const int64_t* t64 = ts64_s + stage * BQ + c0;
           uint32_t ahi[4], alo[4], zhi[4], zlo[4];
-          if (!item_wide && !stage_wide[stage]) grad_cols<8, false>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc);
-          else grad_cols<8, true>(sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc);
+          if (!item_wide && !stage_wide[stage]) grad_cols<8, false>(p, sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc);
+          else grad_cols<8, true>(p, sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc);
           if (half == 0 && pend) {
             // the previous tile's gradient MMAs are complete once its dQ^T is:
             // the A buffer and the dZ^T staging are free again
@@ -621,7 +611,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         if (!ok) break;
       }
       // the item's remaining d_rab partial sums
-      red_add(kc.drt + racc.rt_cur, racc.rt_run, want_rt && racc.rt_cur >= 0);
+      red_add(kc.drp + P + racc.rt_cur, racc.rt_run, want_rt && racc.rt_cur >= 0);
       if (want_rp) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) racc.rp_far += __shfl_xor_sync(0xffffffffu, racc.rp_far, o);
@@ -638,7 +628,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_DKVEMPTY));
-      if (kc.j_ok) {
+      if (j_ok) {
         const size_t g = ((size_t)(s0 + kc.j) * H + hh) * D + hq * 32;
         TO* dvp = static_cast<TO*>(p.dv) + g;
         TO* dkp = static_cast<TO*>(p.dk) + g;

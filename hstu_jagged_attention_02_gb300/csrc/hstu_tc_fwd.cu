@@ -107,16 +107,14 @@ __device__ __forceinline__ float rcp_approx(float x) {
 
 // Per-thread row context of the epilogue (one query row i of the item).
 struct RowCtx {
-  int i, n, cx, h_end, pos_i, P, Tb;
+  int i, h_end, pos_i;
   bool row_ok;
   // the row's allowed keys under the compound mask: j <= hi, and j == dg
   // (a candidate's own key); hi = -1, dg = -1 for rows past the sequence
   int hi, dg;
   int32_t ti32;      // timestamp relative to the sequence's first token
   int64_t ti64;      // absolute timestamp
-  const float* tp;   // position table of the head (pre-scaled)
-  const float* tt;   // time table of the head (pre-scaled)
-  float kA, kC;      // -log2(e) alpha, -1 / (log2(e) N)
+  const float* tp;   // bias tables of the head, pre-scaled: position [0, P), time [P, P + Tb)
 };
 
 // Scores of 32 consecutive key columns jb.. of one row -> P_hi, P_lo packed
@@ -126,8 +124,9 @@ struct RowCtx {
 // rows only): 1 = cached keys j < L (position gap L - j, rc.h_end = L), 2 =
 // the candidates' own keys, where only the diagonal is allowed (gap 0).
 template <bool FAST_POS, bool WIDE, bool PARTIAL, int MODE = 0>
-__device__ __forceinline__ void score32(const uint32_t (&sv)[32], uint32_t (&hi)[16], uint32_t (&lo)[16],
-                                        const RowCtx& rc, int jb, const int32_t* ts32, const int64_t* ts64) {
+__device__ __forceinline__ void score32(const AttnParams& p, const uint32_t (&sv)[32], uint32_t (&hi)[16],
+                                        uint32_t (&lo)[16], const RowCtx& rc, int jb, const int32_t* ts32,
+                                        const int64_t* ts64) {
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     float bias[16];
@@ -138,18 +137,18 @@ __device__ __forceinline__ void score32(const uint32_t (&sv)[32], uint32_t (&hi)
       if (MODE == 1) {
         int dp = rc.pos_i - (jb + cc);
         dp = dp < 0 ? 0 : dp;  // columns past the cache are masked below
-        bp = dp < rc.P - 1 ? dp : rc.P - 1;
+        bp = dp < p.P - 1 ? dp : p.P - 1;
       } else if (MODE == 2) {
         bp = 0;
       } else if (FAST_POS) {
         const int dp = rc.pos_i - (jb + cc);
-        bp = dp < rc.P - 1 ? dp : rc.P - 1;
+        bp = dp < p.P - 1 ? dp : p.P - 1;
       } else {
         const int j = jb + cc;
         const int pj = j < rc.h_end ? j : rc.h_end;
         int dp = rc.pos_i - pj;
         dp = dp < 0 ? -dp : dp;
-        bp = dp < rc.P - 1 ? dp : rc.P - 1;
+        bp = dp < p.P - 1 ? dp : p.P - 1;
       }
       int bt;
       if (WIDE) {
@@ -161,8 +160,8 @@ __device__ __forceinline__ void score32(const uint32_t (&sv)[32], uint32_t (&hi)
         d = d < 0 ? -d : d;
         bt = 32 - __clz(d);
       }
-      bt = bt < rc.Tb - 1 ? bt : rc.Tb - 1;
-      bias[c] = rc.tp[bp] + rc.tt[bt];
+      bt = bt < p.Tb - 1 ? bt : p.Tb - 1;
+      bias[c] = rc.tp[bp] + rc.tp[p.P + bt];
     }
 #pragma unroll
     for (int c = 0; c < 16; c += 2) {
@@ -170,8 +169,8 @@ __device__ __forceinline__ void score32(const uint32_t (&sv)[32], uint32_t (&hi)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int cc = half * 16 + c + e;
-        const float w = fmaf(rc.kA, __uint_as_float(sv[cc]), bias[c + e]);
-        float a = (w * rc.kC) * rcp_approx(1.0f + ex2_approx(w));
+        const float w = fmaf(p.kA, __uint_as_float(sv[cc]), bias[c + e]);
+        float a = (w * p.kC) * rcp_approx(1.0f + ex2_approx(w));
         if (MODE == 1) {
           a = (rc.row_ok && jb + cc < rc.h_end) ? a : 0.f;
         } else if (MODE == 2) {
@@ -467,10 +466,6 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     uint32_t kv_it = 0, o_it = 0, q_it = 0;
     bool ok = true;
     RowCtx rc;
-    rc.P = P;
-    rc.Tb = Tb;
-    rc.kA = -kLog2e * p.alpha;
-    rc.kC = -p.inv_n / kLog2e;
     while (ok) {
       const uint32_t qb = q_it % kQBufs;
       ok = mbar_wait(bar(BAR_QFULL + qb), (q_it / kQBufs) & 1, wd, 10);
@@ -482,25 +477,23 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       const int64_t s0 = sl.s0;
       const int hh = sl.h, q0 = sl.q0;
       const bool item_wide = sl.wide != 0;
-      rc.n = sl.n;
-      rc.cx = sl.c;
+      const int n_seq = sl.n, cx = sl.c;
       rc.h_end = DELTA ? sl.L : sl.h_end;   // delta: the candidates' position is the cache length
       rc.i = q0 + row;
-      rc.row_ok = rc.i < rc.n;
+      rc.row_ok = rc.i < n_seq;
       rc.pos_i = DELTA ? rc.h_end : (rc.i < rc.h_end ? rc.i : rc.h_end);
       // allowed keys of this row: history/context rows see j <= i (context rows
       // the whole context), candidates see all of history/context and themselves
-      rc.hi = !rc.row_ok ? -1 : (rc.i < rc.h_end ? (rc.i < rc.cx ? rc.cx - 1 : rc.i) : rc.h_end - 1);
+      rc.hi = !rc.row_ok ? -1 : (rc.i < rc.h_end ? (rc.i < cx ? cx - 1 : rc.i) : rc.h_end - 1);
       rc.dg = (rc.row_ok && rc.i >= rc.h_end) ? rc.i : -1;
       rc.ti64 = qts_s[qb * BM + row];
       rc.ti32 = (int32_t)(rc.ti64 - sl.tbase);
       rc.tp = tab + hh * PT;
-      rc.tt = rc.tp + P;
-      const int nkb = DELTA ? (rc.h_end + BN - 1) / BN + 1 : fwd_kv_blocks(q0, rc.n, rc.cx, BM, BN);
+      const int nkb = DELTA ? (rc.h_end + BN - 1) / BN + 1 : fwd_kv_blocks(q0, n_seq, cx, BM, BN);
       for (int kb = 0; ok && kb < nkb; ++kb) {
         const bool self = DELTA && kb == nkb - 1;
         const int k0 = self ? q0 : kb * BN;
-        const int cls = DELTA ? 1 : tile_class(q0, k0, BM, BN, rc.n, rc.cx, rc.h_end);
+        const int cls = DELTA ? 1 : tile_class(q0, k0, BM, BN, n_seq, cx, rc.h_end);
         if (cls == 0) continue;
         const uint32_t stage = kv_it % kStages, sb = kv_it & 1;
         ok = mbar_wait(bar(BAR_KVFULL + stage), (kv_it / kStages) & 1, wd, 7) &&
@@ -519,19 +512,19 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         const bool narrow = !item_wide && !stage_wide[stage];
         if (DELTA) {
           if (self) {
-            if (narrow) score32<false, false, false, 2>(sv, hi, lo, rc, jb, t32, t64);
-            else score32<false, true, false, 2>(sv, hi, lo, rc, jb, t32, t64);
+            if (narrow) score32<false, false, false, 2>(p, sv, hi, lo, rc, jb, t32, t64);
+            else score32<false, true, false, 2>(p, sv, hi, lo, rc, jb, t32, t64);
           } else {
-            if (narrow) score32<false, false, false, 1>(sv, hi, lo, rc, jb, t32, t64);
-            else score32<false, true, false, 1>(sv, hi, lo, rc, jb, t32, t64);
+            if (narrow) score32<false, false, false, 1>(p, sv, hi, lo, rc, jb, t32, t64);
+            else score32<false, true, false, 1>(p, sv, hi, lo, rc, jb, t32, t64);
           }
         } else if (narrow) {
-          if (fast) score32<true, false, false>(sv, hi, lo, rc, jb, t32, t64);
-          else if (cls == 2) score32<false, false, false>(sv, hi, lo, rc, jb, t32, t64);
-          else score32<false, false, true>(sv, hi, lo, rc, jb, t32, t64);
+          if (fast) score32<true, false, false>(p, sv, hi, lo, rc, jb, t32, t64);
+          else if (cls == 2) score32<false, false, false>(p, sv, hi, lo, rc, jb, t32, t64);
+          else score32<false, false, true>(p, sv, hi, lo, rc, jb, t32, t64);
         } else {
-          if (cls == 2) score32<false, true, false>(sv, hi, lo, rc, jb, t32, t64);
-          else score32<false, true, true>(sv, hi, lo, rc, jb, t32, t64);
+          if (cls == 2) score32<false, true, false>(p, sv, hi, lo, rc, jb, t32, t64);
+          else score32<false, true, true>(p, sv, hi, lo, rc, jb, t32, t64);
         }
         // P_hi of this quarter at [32 hq, 32 hq + 16), P_lo at [32 hq + 16, 32 hq + 32)
         tmem_st16(scol, hi);
