@@ -183,6 +183,10 @@ void set_launch_detail(cudaError_t e, const char* kernel, const void* func, int 
 
 }  // namespace hstu
 
+namespace hstu {
+void note_launches(int32_t n) { g_launches += n; }
+}  // namespace hstu
+
 extern "C" {
 
 const char* hstu_last_error_detail(void) { return g_detail; }

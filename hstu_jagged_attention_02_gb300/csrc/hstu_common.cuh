@@ -25,6 +25,8 @@ enum : int {
   WS_NTILES = 3,    // debug-plan tile counter
   WS_FLAGS = 4,     // reserved (zero)
   WS_NEXT = 5,      // next work item of the tensor-core kernels (dynamic scheduling)
+  WS_LAYER_ERR = 6, // layer input projection: first device error code (raised into WS_ERR later)
+  WS_LAYER_INFO = 7,
 };
 // Timestamps are staged relative to their sequence's first token; a tile
 // whose relative times all lie within +-2^30 s computes its gaps in 32 bits,

@@ -97,6 +97,8 @@ struct NormParams {
 void set_error_detail(cudaError_t e, const char* where);
 void set_launch_detail(cudaError_t e, const char* kernel, const void* func, int threads, size_t smem);
 void set_detail_message(const char* msg);
+// adds n kernels of a composite call (the layer) to hstu_last_launch_count
+void note_launches(int32_t n);
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 cudaError_t launch_debug_tiles(const PlanParams& p, int32_t* rec, int64_t cap, cudaStream_t stream);
@@ -126,5 +128,28 @@ cudaError_t launch_tc_fwd(const AttnParams& p, cudaStream_t stream);
 // delta forward: candidate blocks against cached K/V (p.off2, p.ts2, p.k2, p.v2, p.T2)
 cudaError_t launch_tc_fwd_delta(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_tc_bwd(const AttnParams& p, cudaStream_t stream);
+
+// Tensor-core GEMMs of the layer with fused epilogues (BF16 operands, FP32
+// accumulation).  A [M, K] row-major, B [K, N] row-major; K % 64 == 0,
+// N % 128 == 0, D % 128 == 0.
+struct GemmParams {
+  int64_t M;
+  int N, K, D;
+  int npass;            // 1: A = X; 2: A = y_hi, then y_lo, into one accumulator
+  int* err;             // first error code (HSTU_ERR_TIMEOUT) and its wait site
+  int* err_info;
+  const int* carry_err; // f2 only: error words of f1, raised into err at launch (or NULL)
+  float* z1;            // f1: [M, 4D] FP32
+  float* u;             // f1: [M, D] FP32
+  __nv_bfloat16* vqk;   // f1: [3][M][D] BF16 (V, Q, K)
+  const __nv_bfloat16* x; // f2: [M, D] BF16 residual
+  float* out;           // f2: [M, D] FP32
+};
+bool gemm_tc_supported(int D);
+// f1: z1 = X W1; u = SiLU(z1[:, :D]); V | Q | K = BF16(SiLU(z1[:, D:]))
+cudaError_t launch_gemm_f1(const GemmParams& p, const void* x, const void* w1, int num_sms, cudaStream_t st);
+// f2: out = X + y_hi W2 + y_lo W2
+cudaError_t launch_gemm_f2(const GemmParams& p, const void* y_hi, const void* y_lo, const void* w2, int num_sms,
+                           cudaStream_t st);
 
 }  // namespace hstu

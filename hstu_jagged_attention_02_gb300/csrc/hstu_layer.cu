@@ -4,14 +4,17 @@
 // two linear layers, no stored sub-layer activations beyond what the
 // backward needs):
 //
-//   Z1 = X W1                      [T, 4D]   cuBLAS, BF16 x BF16 -> FP32
-//   U | V | Q | K = SiLU(Z1)       U FP32 [T, D]; V, Q, K BF16 3 x [T, D]
-//   o, y = attention(Q, K, V, U)   hstu_attn_fwd (norm and gate per desc)
-//   out = X + y W2                 [T, D]    residual copy + cuBLAS (beta = 1)
+//   Z1 = X W1; U | V | Q | K = SiLU(Z1)   one tensor-core GEMM (hstu_gemm_tc.cu)
+//                                         whose epilogue writes z1 [T, 4D] FP32,
+//                                         U FP32 [T, D] and V, Q, K BF16 3 x [T, D]
+//   o, y = attention(Q, K, V, U)          hstu_attn_fwd (norm and gate per desc)
+//   out = X + y W2                        one tensor-core GEMM, residual in its epilogue
 //
-// and its backward.  The dense GEMMs are plain library GEMMs (cuBLAS, with
-// its workspace taken from the caller's workspace); the element-wise steps
-// (SiLU + split, residual, SiLU', BF16 pairs) are this file's kernels.
+// and its backward, whose four dense GEMMs are plain library GEMMs (cuBLAS,
+// with its workspace taken from the caller's workspace) around this file's
+// element-wise kernels (SiLU', BF16 pairs).  Where D is not a multiple of
+// 128 the forward takes the same library route: cuBLAS, then the SiLU split
+// and the residual as separate kernels.
 //
 // Precision: V, Q, K are BF16 (the attention's MMA operands); the gate U and
 // every accumulation stay FP32.  The computed GEMM operands y and dZ1 enter
@@ -253,14 +256,34 @@ hstu_status_t hstu_layer_fwd(const hstu_attn_desc* d, const hstu_layer_fwd_args*
   const int D = d->H * d->d_v;
   const size_t TD = (size_t)T * D;
   if (T == 0) return HSTU_OK;
-  cublasHandle_t h = prepare_cublas(st, ws + L.cublas);
-  if (!h) { set_detail_message("cuBLAS handle set-up failed"); return HSTU_ERR_CUDA; }
+  const bool fused = gemm_tc_supported(D);
+  cublasHandle_t h = nullptr;
+  if (!fused) {
+    h = prepare_cublas(st, ws + L.cublas);
+    if (!h) { set_detail_message("cuBLAS handle set-up failed"); return HSTU_ERR_CUDA; }
+  }
 
-  // Z1 = X W1 ; U | V | Q | K = SiLU(Z1)
-  LAYER_CUBLAS(gemm_rm(h, false, false, T, 4 * D, D, a->x, D, a->w1, 4 * D, 0.f, a->z1, 4 * D));
+  // Z1 = X W1 ; U | V | Q | K = SiLU(Z1): one tensor-core GEMM whose epilogue
+  // writes z1, U and V, Q, K (D % 128 == 0), else cuBLAS + the split kernel
   __nv_bfloat16* vqk = static_cast<__nv_bfloat16*>(a->vqk);
-  silu_split_kernel<<<grid_for(TD), 256, 0, st>>>(a->z1, a->u, vqk, T, D);
-  LAYER_CUDA(cudaGetLastError());
+  int32_t* hdr = reinterpret_cast<int32_t*>(ws + L.attn);
+  GemmParams gp{};
+  gp.M = T; gp.D = D; gp.K = D;
+  int sms = 0;
+  if (fused) {
+    int dev = 0;
+    LAYER_CUDA(cudaGetDevice(&dev));
+    LAYER_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    LAYER_CUDA(cudaMemsetAsync(hdr + WS_LAYER_ERR, 0, 2 * sizeof(int32_t), st));
+    gp.N = 4 * D; gp.npass = 1;
+    gp.err = hdr + WS_LAYER_ERR; gp.err_info = hdr + WS_LAYER_INFO;
+    gp.z1 = a->z1; gp.u = a->u; gp.vqk = vqk;
+    LAYER_CUDA(launch_gemm_f1(gp, a->x, a->w1, sms, st));
+  } else {
+    LAYER_CUBLAS(gemm_rm(h, false, false, T, 4 * D, D, a->x, D, a->w1, 4 * D, 0.f, a->z1, 4 * D));
+    silu_split_kernel<<<grid_for(TD), 256, 0, st>>>(a->z1, a->u, vqk, T, D);
+    LAYER_CUDA(cudaGetLastError());
+  }
 
   // attention: o, y
   hstu_attn_fwd_args fa{};
@@ -278,11 +301,23 @@ hstu_status_t hstu_layer_fwd(const hstu_attn_desc* d, const hstu_layer_fwd_args*
   f32_to_bf16_pair_kernel<<<grid_for(TD / 4), 256, 0, st>>>(static_cast<const float*>(a->y), y_hi, y_lo,
                                                            (int64_t)(TD / 4));
   LAYER_CUDA(cudaGetLastError());
+  if (fused) {
+    // one tensor-core GEMM over both halves of the pair, the residual added in its epilogue;
+    // an error of the first GEMM is raised into the workspace's error word here
+    gp.N = D; gp.npass = 2;
+    gp.err = hdr + WS_ERR; gp.err_info = hdr + WS_ERR_INFO; gp.carry_err = hdr + WS_LAYER_ERR;
+    gp.z1 = nullptr; gp.u = nullptr; gp.vqk = nullptr;
+    gp.x = static_cast<const __nv_bfloat16*>(a->x); gp.out = static_cast<float*>(a->out);
+    LAYER_CUDA(launch_gemm_f2(gp, y_hi, y_lo, a->w2, sms, st));
+    note_launches(3);  // f1, the y pair, f2
+    return HSTU_OK;
+  }
   bf16_to_f32_kernel<<<grid_for(TD), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(a->x),
                                                     static_cast<float*>(a->out), (int64_t)TD);
   LAYER_CUDA(cudaGetLastError());
   LAYER_CUBLAS(gemm_rm(h, false, false, T, D, D, y_hi, D, a->w2, D, 1.f, static_cast<float*>(a->out), D));
   LAYER_CUBLAS(gemm_rm(h, false, false, T, D, D, y_lo, D, a->w2, D, 1.f, static_cast<float*>(a->out), D));
+  note_launches(3);  // SiLU split, the y pair, the residual copy (cuBLAS's own kernels not counted)
   return HSTU_OK;
 }
 
@@ -354,6 +389,7 @@ hstu_status_t hstu_layer_bwd(const hstu_attn_desc* d, const hstu_layer_bwd_args*
   float* dx = static_cast<float*>(a->dx);
   LAYER_CUBLAS(gemm_rm(h, false, true, T, D, 4 * D, dz1_hi, 4 * D, a->w1, 4 * D, 1.f, dx, D));
   LAYER_CUBLAS(gemm_rm(h, false, true, T, D, 4 * D, dz1_lo, 4 * D, a->w1, 4 * D, 1.f, dx, D));
+  note_launches(3);  // the y pair, dout to BF16, SiLU' (cuBLAS's own kernels not counted)
   return HSTU_OK;
 }
 

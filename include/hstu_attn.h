@@ -218,12 +218,15 @@ hstu_status_t hstu_attn_fwd_noalloc(const hstu_attn_desc* desc, const hstu_attn_
  * out, dx and all gradients are FP32.  The descriptor is the
  * attention's and must have dtype BF16, out_dtype FP32, d_qk == d_v.
  *
- * The four dense GEMMs (and their four backward counterparts) are plain
- * cuBLAS GEMMs (BF16 x BF16 -> FP32); the SiLU split, residual and SiLU'
- * steps and the attention are this library's kernels.  cuBLAS's scratch
- * comes from the caller's workspace, but the first call on each (host
- * thread, device) creates a cuBLAS handle, which allocates cuBLAS's own
- * small state: make that first call outside any stream capture.
+ * When D is a multiple of 128 the forward's two projections are this
+ * library's tensor-core GEMMs: Z1 = X W1 with the SiLU split in its epilogue
+ * (z1, U, V, Q, K written once), and out = X + y_hi W2 + y_lo W2 with the
+ * residual in its epilogue.  Otherwise, and for the backward's GEMMs, they
+ * are plain cuBLAS GEMMs (BF16 x BF16 -> FP32) around this library's
+ * element-wise kernels.  cuBLAS's scratch comes from the caller's
+ * workspace, but the first call on each (host thread, device) that uses
+ * cuBLAS creates a cuBLAS handle, which allocates cuBLAS's own small state:
+ * make that first call outside any stream capture.
  * ------------------------------------------------------------------------ */
 typedef struct {
   const int64_t* seq_offsets;  /* as hstu_attn_fwd_args */
@@ -272,8 +275,9 @@ typedef struct {
 hstu_status_t hstu_layer_workspace_size(const hstu_attn_desc* desc, size_t* fwd_bytes, size_t* bwd_bytes);
 
 /* Layer forward (above).  All pointers device, 16-byte aligned; outputs are
- * overwritten.  Device-side problems land in the attention's error word at
- * the start of the workspace (hstu_get_device_error). */
+ * overwritten.  Device-side problems (the attention's, or a tensor-core
+ * projection's wait that ran out: HSTU_ERR_TIMEOUT) land in the error word
+ * at the start of the workspace (hstu_get_device_error). */
 hstu_status_t hstu_layer_fwd(const hstu_attn_desc* desc, const hstu_layer_fwd_args* args,
                              void* workspace, size_t workspace_bytes, hstu_stream_t stream);
 
@@ -340,8 +344,10 @@ const char* hstu_status_string(hstu_status_t status);
  * on this thread. */
 const char* hstu_last_error_detail(void);
 
-/* Number of kernels the last successful hstu_attn_fwd / hstu_attn_bwd call on
- * this thread launched (for launch accounting). */
+/* Number of this library's kernels that the last successful hstu_attn_fwd,
+ * hstu_attn_bwd, hstu_attn_fwd_delta, hstu_layer_fwd or hstu_layer_bwd call
+ * on this thread launched (for launch accounting; cuBLAS's kernels inside
+ * the layer calls are not counted). */
 int32_t hstu_last_launch_count(void);
 
 /* Measurement hook.  start_event and stop_event are cudaEvent_t handles (or

@@ -65,30 +65,42 @@ def _close(name, got, want, tol=TOL):
     assert err <= tol * rms, f"{name}: max abs err {err:.3e} > {tol:g} x rms {rms:.3e}"
 
 
-@pytest.mark.parametrize("case", ["ragged", "contexts", "d128"])
+def _check_projection(pr, f, T, D, sel=None):
+    """z1 = X W1 and its SiLU split U | V | Q | K on the rows sel (bool [T])."""
+    sel = np.ones(T, bool) if sel is None else sel
+    idx = torch.from_numpy(np.nonzero(sel)[0]).to(pr.z1.device)
+    _close("z1", _np(pr.z1[idx]), f["z1"][sel], 1e-4)
+    _close("u", _np(pr.u[idx]), f["u"][sel], 1e-4)
+    vqk = _np(pr.vqk[:, idx])
+    for i, key in enumerate(("v", "q", "k")):
+        # both sides round SiLU(z1) to bf16; a z1 within the GEMM's FP32
+        # accumulation error (about 1e-4 of the RMS at most here) of a rounding
+        # boundary lands one bf16 step (at most 2^-7 relative) away
+        want = f[key].reshape(T, D)[sel]
+        rms = math.sqrt(float(np.mean(want * want)))
+        bound = 2.0 ** -7 * np.abs(want) + 1e-4 * rms
+        assert np.all(np.abs(vqk[i] - want) <= bound), key
+
+
+# D = 128 and 256 take the tensor-core projections (f1 over 512 / 1024
+# output columns, f2 over 128 / 256, a ragged last row block); D = 64 the
+# library route (cuBLAS and separate element-wise kernels).
+@pytest.mark.parametrize("case", ["ragged", "contexts", "d128", "d64_library"])
 def test_layer_parity_small(case):
     if case == "ragged":
         b = _small_layer(40, [300, 131, 77, 1, 520])
     elif case == "contexts":
         b = _small_layer(41, [260, 400, 95], contexts=[5, 37, 0])
-    else:
+    elif case == "d128":
         b = _small_layer(42, [384, 129, 250], H=2, d=128, nt=32)
+    else:
+        b = _small_layer(43, [200, 77, 310], H=1, d=64)
     pr = _run(b)
     f = O.layer_forward(b, act_dtype="bf16")
     g = O.layer_backward(b, f, act_dtype="bf16")
     T, D = b.T, b.H * b.d_v
     x, dout = b.x.astype(np.float64), b.dout.astype(np.float64)
-    _close("z1", _np(pr.z1), f["z1"], 1e-4)
-    _close("u", _np(pr.u), f["u"], 1e-4)
-    vqk = _np(pr.vqk)
-    for i, key in enumerate(("v", "q", "k")):
-        # both sides round SiLU(z1) to bf16; a z1 within the GEMM's FP32
-        # accumulation error (about 1e-4 of the RMS at most here) of a rounding
-        # boundary lands one bf16 step (at most 2^-7 relative) away
-        want = f[key].reshape(T, D)
-        rms = math.sqrt(float(np.mean(want * want)))
-        bound = 2.0 ** -7 * np.abs(want) + 1e-4 * rms
-        assert np.all(np.abs(vqk[i] - want) <= bound), key
+    _check_projection(pr, f, T, D)
     _close("o", _np(pr.o), f["o"].reshape(T, D))
     _close("y", _np(pr.y), f["y"])
     _close("out - x", _np(pr.out) - x, f["out"] - x)
@@ -110,13 +122,16 @@ def _sample_rows(b):
 def test_layer_full_size_sampled_rows():
     """8 sequences of U[8192, 32768] history + 128 candidates, D = 512: every
     candidate row and the last history row of each sequence (whose keys only
-    queries of the same set attend), plus dW2 = Y^T dOut for the returned Y."""
+    queries of the same set attend), plus dW2 = Y^T dOut for the returned Y
+    and the input projection on a stride of rows."""
     b = synth.layer(0)
     pr = _run(b)
     rows = _sample_rows(b)
     f = O.layer_forward(b, rows=rows, act_dtype="bf16")
     g = O.layer_backward(b, f, act_dtype="bf16", rows=rows)
     D = b.H * b.d_v
+    # the projection on the sampled rows and every 37th row (every row block)
+    _check_projection(pr, f, b.T, D, rows | (np.arange(b.T) % 37 == 0))
     x, dout = b.x.astype(np.float64)[rows], b.dout.astype(np.float64)[rows]
     _close("o[rows]", _np(pr.o)[rows], f["o"].reshape(b.T, D)[rows])
     _close("y[rows]", _np(pr.y)[rows], f["y"][rows])
