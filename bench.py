@@ -127,12 +127,18 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def kernel_sources_sha():
+# the translation unit of each timed attention kernel plus the headers it includes
+KERNEL_SOURCES = {
+    "fwd": ("hstu_tc_fwd.cu", "tc_ptx.cuh", "hstu_common.cuh", "hstu_internal.h"),
+    "bwd": ("hstu_tc_bwd.cu", "tc_ptx.cuh", "hstu_common.cuh", "hstu_internal.h"),
+}
+
+
+def kernel_sources_sha(role: str):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "hstu_jagged_attention_02_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, fn), "rb").read())
+    for fn in KERNEL_SOURCES[role] + ("../../include/hstu_attn.h",):
+        h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -145,7 +151,7 @@ def traffic_record(kernel_role: str):
     try:
         d = json.load(open(path))
         rec = d.get(kernel_role)
-        if rec and rec.get("sources_sha") == kernel_sources_sha():
+        if rec and rec.get("sources_sha") == kernel_sources_sha(kernel_role.split(":")[1]):
             return rec
     except Exception:
         pass

@@ -12,10 +12,17 @@
 // X, y_hi, y_lo: [M, K] BF16 row-major (K-major A operands); W1 [K, 4D] and
 // W2 [K, D] BF16 row-major (MN-major B operands).  Tiles of 128 rows x BN
 // columns (BN = 256, or 128 for narrow outputs), k-blocks of 64 through a
-// 4-stage TMA ring, tcgen05.mma (M = 128, N = BN, K = 16) into one of two
+// 3-stage TMA ring, tcgen05.mma (M = 128, N = BN, K = 16) into one of two
 // FP32 TMEM accumulators, so the next tile's MMAs overlap this tile's
-// epilogue.  Persistent CTAs walk the tiles row-block-major, so consecutive
-// tiles of a CTA share their X rows in L2.
+// epilogue.  Persistent CTAs walk the tiles row-block-major, so the CTAs in
+// flight share their X rows in L2.
+//
+// The epilogue is store-bound (z1 alone is 16 bytes per output column of a
+// token): each warp stages its 32 x 32 chunks in 128-byte- (FP32) or
+// 64-byte-swizzled (BF16) shared memory, conflict-free, and writes them with
+// TMA tile stores, whole lines per row; the stores clip the ragged last row
+// block.  Two staging buffers per warp, each reused once the bulk group that
+// last read it is done.
 //
 // Roles (320 threads): warps 0-7 epilogue (TMEM lane quarter warp % 4,
 // column half warp / 4), warp 8 TMA producer, warp 9 MMA issuer and TMEM
@@ -31,7 +38,7 @@ namespace {
 using namespace tc;
 
 constexpr int GBM = 128, GBK = 64;
-constexpr int kGStages = 4;
+constexpr int kGStages = 3;
 constexpr int kGEpiWarps = 8;
 constexpr int kGProducerWarp = 8, kGMmaWarp = 9;
 constexpr int kGThreads = 10 * 32;
@@ -46,12 +53,34 @@ struct GLayout {
   static constexpr int B_BOX = GBK * 64 * 2;           // 8 KB: 64 k-rows x 64 n-columns
   static constexpr int B_BYTES = (BN / 64) * B_BOX;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int BAR_OFF = kGStages * STAGE;
+  static constexpr int STG_WARP = 2 * 4096;             // two 32 x 32 FP32 staging buffers per epilogue warp
+  static constexpr int STG_OFF = kGStages * STAGE;
+  static constexpr int BAR_OFF = STG_OFF + kGEpiWarps * STG_WARP;
   static constexpr int MISC_OFF = BAR_OFF + GB_COUNT * 8;  // tmem slot, abort flag
   static constexpr int BYTES = MISC_OFF + 16;
 };
 
-__device__ __forceinline__ float sigmoid_f(float z) { return 1.0f / (1.0f + expf(-z)); }
+// SiLU(z) = z / (1 + e^-z) with the fast exponential and division
+// intrinsics (relative error about 1e-6; z below about -87 gives 0)
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// FP32 row `lane` (32 values) of a 32 x 32 staging buffer, 128-byte swizzle:
+// 16-byte chunk c of row r at chunk c ^ (r % 8) of the row's 128 bytes
+__device__ __forceinline__ void stage_f32(uint8_t* buf, int lane, const float* a) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<float4*>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+        make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
+}
+// BF16 row `lane` (32 values, 64 bytes) of a 32 x 32 staging buffer, 64-byte
+// swizzle: 16-byte chunk c of row r at chunk c ^ ((r / 2) % 4)
+__device__ __forceinline__ void stage_bf16(uint8_t* buf, int lane, const float* a) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+        make_uint4(pack_bf16(a[8 * c], a[8 * c + 1]), pack_bf16(a[8 * c + 2], a[8 * c + 3]),
+                   pack_bf16(a[8 * c + 4], a[8 * c + 5]), pack_bf16(a[8 * c + 6], a[8 * c + 7]));
+}
 
 __device__ __forceinline__ void drain_wait_g(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
@@ -64,7 +93,9 @@ __device__ __forceinline__ void drain_wait_g(uint32_t bar, uint32_t parity) {
 template <int MODE, int BN>
 __global__ void __launch_bounds__(kGThreads, 1)
 hstu_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tma0,
-                    const __grid_constant__ CUtensorMap tma1, const __grid_constant__ CUtensorMap tmb) {
+                    const __grid_constant__ CUtensorMap tma1, const __grid_constant__ CUtensorMap tmb,
+                    const __grid_constant__ CUtensorMap tms0, const __grid_constant__ CUtensorMap tms1,
+                    const __grid_constant__ CUtensorMap tms2) {
   using L = GLayout<BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -120,7 +151,7 @@ hstu_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t it = 0;
-      uint32_t armed[kGStages] = {0, 0, 0, 0};
+      uint32_t armed[kGStages] = {};
       bool ok = true;
       for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
         const int mb = t / nblocks, nb = t % nblocks;
@@ -180,9 +211,12 @@ hstu_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // tms0: z1 (f1) or out (f2), FP32 [M, N]; tms1: u FP32 [M, D]; tms2: V | Q | K BF16 [3, M, D]
     const int wq = warp & 3, ch = warp >> 2;   // TMEM lane quarter, column half of the tile
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
-    uint32_t tc_it = 0;
+    uint8_t* stg = base + L::STG_OFF + warp * L::STG_WARP;
+    const uint32_t stg_u32 = base_u32 + L::STG_OFF + warp * L::STG_WARP;
+    uint32_t tc_it = 0, sc = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
       const int mb = t / nblocks, nb = t % nblocks;
@@ -190,55 +224,76 @@ hstu_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
       ok = mbar_wait(bar(GB_AFULL + ab), (tc_it >> 1) & 1, wd, 44);
       if (!ok) break;
       fence_after_sync();
-      const int row = mb * GBM + wq * 32 + lane;
-      const bool row_ok = row < p.M;
+      const int row0 = mb * GBM + wq * 32;
+      const int row = row0 + lane;
+      const bool in_rows = row0 < p.M;   // else the warp's 32 rows all lie past M: no store is issued
 #pragma unroll 1
       for (int cc = 0; cc < BN / 64; ++cc) {
         const int col = ch * (BN / 2) + cc * 32;     // within the tile
+        const int n = nb * BN + col;                 // output column
         uint32_t v[32];
         tmem_ld32(lane_base + ab * 256 + col, v);
         tmem_wait_ld();
-        if (!row_ok) continue;
-        const int n = nb * BN + col;                 // output column
+        float a[32];
         if (MODE == 0) {
-          float4* zdst = reinterpret_cast<float4*>(p.z1 + (size_t)row * p.N + n);
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            zdst[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                  __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
-          const int part = n / p.D, f = n % p.D;     // 32 columns never straddle a part
-          float a[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float z = __uint_as_float(v[e]);
-            a[e] = z * sigmoid_f(z);
+          for (int e = 0; e < 32; ++e) a[e] = __uint_as_float(v[e]);
+          // z1 chunk into buffer 0, once the store that last read it is done
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          stage_f32(stg, lane, a);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (in_rows) tma_store_2d(&tms0, stg_u32, n, row0);
+            bulk_commit();
           }
-          if (part == 0) {
-            float4* udst = reinterpret_cast<float4*>(p.u + (size_t)row * p.D + f);
+          // SiLU: U (FP32) or one of V, Q, K (BF16) into buffer 1; 32 columns never straddle a part
+          const int part = n / p.D, f = n - part * p.D;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) udst[e] = make_float4(a[4 * e], a[4 * e + 1], a[4 * e + 2], a[4 * e + 3]);
-          } else {
-            uint4* vdst = reinterpret_cast<uint4*>(p.vqk + (size_t)(part - 1) * p.M * p.D + (size_t)row * p.D + f);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              vdst[e] = make_uint4(pack_bf16(a[8 * e], a[8 * e + 1]), pack_bf16(a[8 * e + 2], a[8 * e + 3]),
-                                   pack_bf16(a[8 * e + 4], a[8 * e + 5]), pack_bf16(a[8 * e + 6], a[8 * e + 7]));
+          for (int e = 0; e < 32; ++e) a[e] = silu_f(a[e]);
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          if (part == 0) stage_f32(stg + 4096, lane, a);
+          else stage_bf16(stg + 4096, lane, a);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (in_rows && part == 0) tma_store_2d(&tms1, stg_u32 + 4096, f, row0);
+            if (in_rows && part != 0) tma_store_3d(&tms2, stg_u32 + 4096, f, row0, part - 1);
+            bulk_commit();
           }
         } else {
-          const uint4* xs = reinterpret_cast<const uint4*>(p.x + (size_t)row * p.N + n);
-          float4* odst = reinterpret_cast<float4*>(p.out + (size_t)row * p.N + n);
+          // out = X + acc, X read as BF16 (rows past M read nothing and are not stored)
+          uint4 xv[4] = {};
+          if (row < p.M) {
+            const uint4* xs = reinterpret_cast<const uint4*>(p.x + (size_t)row * p.N + n);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) xv[e] = xs[e];
+          }
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const uint4 xv = xs[e];
-            odst[2 * e] = make_float4(__uint_as_float(v[8 * e]) + bf16_lo_f(xv.x),
-                                      __uint_as_float(v[8 * e + 1]) + bf16_hi_f(xv.x),
-                                      __uint_as_float(v[8 * e + 2]) + bf16_lo_f(xv.y),
-                                      __uint_as_float(v[8 * e + 3]) + bf16_hi_f(xv.y));
-            odst[2 * e + 1] = make_float4(__uint_as_float(v[8 * e + 4]) + bf16_lo_f(xv.z),
-                                          __uint_as_float(v[8 * e + 5]) + bf16_hi_f(xv.z),
-                                          __uint_as_float(v[8 * e + 6]) + bf16_lo_f(xv.w),
-                                          __uint_as_float(v[8 * e + 7]) + bf16_hi_f(xv.w));
+            a[8 * e] = __uint_as_float(v[8 * e]) + bf16_lo_f(xv[e].x);
+            a[8 * e + 1] = __uint_as_float(v[8 * e + 1]) + bf16_hi_f(xv[e].x);
+            a[8 * e + 2] = __uint_as_float(v[8 * e + 2]) + bf16_lo_f(xv[e].y);
+            a[8 * e + 3] = __uint_as_float(v[8 * e + 3]) + bf16_hi_f(xv[e].y);
+            a[8 * e + 4] = __uint_as_float(v[8 * e + 4]) + bf16_lo_f(xv[e].z);
+            a[8 * e + 5] = __uint_as_float(v[8 * e + 5]) + bf16_hi_f(xv[e].z);
+            a[8 * e + 6] = __uint_as_float(v[8 * e + 6]) + bf16_lo_f(xv[e].w);
+            a[8 * e + 7] = __uint_as_float(v[8 * e + 7]) + bf16_hi_f(xv[e].w);
           }
+          // alternate the two buffers
+          const uint32_t off = (sc & 1) * 4096;
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          stage_f32(stg + off, lane, a);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (in_rows) tma_store_2d(&tms0, stg_u32 + off, n, row0);
+            bulk_commit();
+          }
+          ++sc;
         }
       }
       fence_before_sync();
@@ -246,6 +301,8 @@ hstu_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
       if (lane == 0) mbar_arrive(bar(GB_AEMPTY + ab));
       ++tc_it;
     }
+    if (lane == 0) bulk_wait_all();   // the staging buffers stay in use until every store is done
+    __syncwarp();
   }
 
   fence_before_sync();
@@ -254,17 +311,38 @@ hstu_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
   if (warp == kGMmaWarp) tmem_dealloc(tmem, kGTmemCols);
 }
 
-// 2-D BF16 tensor map over [rows, cols] (row-major) with a 64-column box of
-// box_rows rows, 128-byte swizzle (the layer's operands).
+// 32 x 32 FP32 store box over a row-major [rows, cols] FP32 array, 128-byte swizzle
+bool tmap_store_f32(CUtensorMap* m, const float* ptr, int64_t rows, int64_t cols) {
+  const uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows}, strides[1] = {(uint64_t)cols * 4};
+  const uint32_t box[2] = {32, 32};
+  return make_tmap_tile(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Operand maps: A boxes of 64 k-columns x 128 rows, B boxes of 64
+// n-columns x 64 k-rows (both 128-byte swizzle).  Store maps: f1 z1, u and
+// V | Q | K as [3, M, D] (each part clipped at row M); f2 out.
 template <int MODE, int BN>
 cudaError_t launch_gemm_t(const GemmParams& p, const void* a0, const void* a1, const void* b, int num_sms,
                           cudaStream_t st) {
-  CUtensorMap m0, m1, mb;
+  CUtensorMap m0, m1, mb, s0, s1, s2;
   if (!make_tmap_bf16(&m0, a0, p.M, p.K, GBM) || !make_tmap_bf16(&mb, b, p.K, p.N, GBK)) return cudaErrorInvalidValue;
   if (p.npass > 1) {
     if (!make_tmap_bf16(&m1, a1, p.M, p.K, GBM)) return cudaErrorInvalidValue;
   } else {
     m1 = m0;
+  }
+  if (MODE == 0) {
+    const uint64_t dims[3] = {(uint64_t)p.D, (uint64_t)p.M, 3};
+    const uint64_t strides[2] = {(uint64_t)p.D * 2, (uint64_t)p.M * p.D * 2};
+    const uint32_t box[3] = {32, 32, 1};
+    if (!tmap_store_f32(&s0, p.z1, p.M, p.N) || !tmap_store_f32(&s1, p.u, p.M, p.D) ||
+        !make_tmap_tile(&s2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.vqk, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!tmap_store_f32(&s0, p.out, p.M, p.N)) return cudaErrorInvalidValue;
+    s1 = s0;
+    s2 = s0;
   }
   const size_t smem = GLayout<BN>::BYTES + 1024;
   const void* fn = reinterpret_cast<const void*>(hstu_gemm_tc_kernel<MODE, BN>);
@@ -277,7 +355,7 @@ cudaError_t launch_gemm_t(const GemmParams& p, const void* a0, const void* a1, c
   const int ntiles = ((p.M + GBM - 1) / GBM) * (p.N / BN);
   const int grid = ntiles < num_sms ? ntiles : num_sms;
   if (grid <= 0) return cudaSuccess;
-  hstu_gemm_tc_kernel<MODE, BN><<<grid, kGThreads, smem, st>>>(p, m0, m1, mb);
+  hstu_gemm_tc_kernel<MODE, BN><<<grid, kGThreads, smem, st>>>(p, m0, m1, mb, s0, s1, s2);
   e = cudaGetLastError();
   if (e != cudaSuccess) set_launch_detail(e, "hstu_gemm_tc_kernel", fn, kGThreads, smem);
   return e;

@@ -119,6 +119,8 @@ constexpr int kTcTile = 128;
 constexpr int kTcBwdQTile = 64;
 constexpr int kDrabMaxCtas = 256;  // tensor-core backward grid cap (one d_rab partial row each)
 bool make_tmap_bf16(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_rows);
+bool make_tmap_tile(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* ptr, const uint64_t* dims,
+                    const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw);
 size_t tc_bwd_smem_bytes(int H, int P, int Tb);
 bool tc_fwd_supported(int dtype, int dqk, int dv);
 size_t tc_fwd_smem_bytes(int d, int H, int P, int Tb);

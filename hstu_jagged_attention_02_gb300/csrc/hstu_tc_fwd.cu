@@ -82,7 +82,7 @@ struct Layout {
   static constexpr int SLOT_OFF = QTS_OFF + kQBufs * BM * 8;    // ItemSlot [kQBufs]
   static constexpr int BAR_OFF = SLOT_OFF + kQBufs * (int)sizeof(ItemSlot);
   static constexpr int MISC_OFF = BAR_OFF + BAR_COUNT * 8;      // tmem slot, abort flag, per-stage wide flags
-  static constexpr int TAB_OFF = MISC_OFF + 16;                 // float [H][P + Tb]
+  static constexpr int TAB_OFF = MISC_OFF + 16;                 // float [H][P + 2 kTimeSlots]
   static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
 };
 
@@ -114,16 +114,22 @@ struct RowCtx {
   int hi, dg;
   int32_t ti32;      // timestamp relative to the sequence's first token
   int64_t ti64;      // absolute timestamp
-  const float* tp;   // bias tables of the head, pre-scaled: position [0, P), time [P, P + Tb)
+  // bias tables of the head, pre-scaled by -log2(e): position [0, P); time by
+  // bit length of the gap [P, P + kTimeSlots), clamped to Tb - 1 inside the
+  // table; the same plus the last position entry [P + kTimeSlots, P + 2 kTimeSlots)
+  const float* tp;
 };
 
 // Scores of 32 consecutive key columns jb.. of one row -> P_hi, P_lo packed
-// pairs.  FAST_POS: every column is a history/context token at or before the
-// row (position gap = pos_i - j >= 0).  WIDE: 64-bit timestamp gaps.
-// PARTIAL: evaluate the mask per element.  MODE (delta forward, candidate
-// rows only): 1 = cached keys j < L (position gap L - j, rc.h_end = L), 2 =
-// the candidates' own keys, where only the diagonal is allowed (gap 0).
-template <bool FAST_POS, bool WIDE, bool PARTIAL, int MODE = 0>
+// pairs.  POS 1: every column is a history/context token at or before the
+// row (position gap = pos_i - j >= 0); POS 2: besides, every gap of the
+// warp's 32 x 32 block is at least P - 1 (one position bucket, folded into
+// the far time table); POS 0: the general gap |pos_i - min(j, h_end)|.
+// WIDE: 64-bit timestamp gaps.  PARTIAL: evaluate the mask per element.
+// MODE (delta forward, candidate rows only): 1 = cached keys j < L (position
+// gap L - j, rc.h_end = L), 2 = the candidates' own keys, where only the
+// diagonal is allowed (gap 0).
+template <int POS, bool WIDE, bool PARTIAL, int MODE = 0>
 __device__ __forceinline__ void score32(const AttnParams& p, const uint32_t (&sv)[32], uint32_t (&hi)[16],
                                         uint32_t (&lo)[16], const RowCtx& rc, int jb, const int32_t* ts32,
                                         const int64_t* ts64) {
@@ -133,14 +139,16 @@ __device__ __forceinline__ void score32(const AttnParams& p, const uint32_t (&sv
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const int cc = half * 16 + c;
-      int bp;
-      if (MODE == 1) {
+      int bp = 0;
+      if (MODE == 0 && POS == 2) {
+        // no position term of its own
+      } else if (MODE == 1) {
         int dp = rc.pos_i - (jb + cc);
         dp = dp < 0 ? 0 : dp;  // columns past the cache are masked below
         bp = dp < p.P - 1 ? dp : p.P - 1;
       } else if (MODE == 2) {
         bp = 0;
-      } else if (FAST_POS) {
+      } else if (POS == 1) {
         const int dp = rc.pos_i - (jb + cc);
         bp = dp < p.P - 1 ? dp : p.P - 1;
       } else {
@@ -150,7 +158,7 @@ __device__ __forceinline__ void score32(const AttnParams& p, const uint32_t (&sv
         dp = dp < 0 ? -dp : dp;
         bp = dp < p.P - 1 ? dp : p.P - 1;
       }
-      int bt;
+      int bt;   // bit length of the gap, in [0, 64] (narrow: [0, 31]); the tables clamp it
       if (WIDE) {
         const int64_t tj = ts64[cc];
         const uint64_t dt = rc.ti64 >= tj ? (uint64_t)(rc.ti64 - tj) : (uint64_t)(tj - rc.ti64);
@@ -160,8 +168,8 @@ __device__ __forceinline__ void score32(const AttnParams& p, const uint32_t (&sv
         d = d < 0 ? -d : d;
         bt = 32 - __clz(d);
       }
-      bt = bt < p.Tb - 1 ? bt : p.Tb - 1;
-      bias[c] = rc.tp[bp] + rc.tp[p.P + bt];
+      if (MODE == 0 && POS == 2) bias[c] = rc.tp[p.P + kTimeSlots + bt];
+      else bias[c] = rc.tp[bp] + rc.tp[p.P + bt];
     }
 #pragma unroll
     for (int c = 0; c < 16; c += 2) {
@@ -219,7 +227,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   float* tab = reinterpret_cast<float*>(base + L::TAB_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int H = p.H, P = p.P, Tb = p.Tb, PT = p.P + p.Tb;
+  const int H = p.H, P = p.P, Tb = p.Tb, PT = p.P + 2 * kTimeSlots;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQBufs; ++s) {
@@ -240,14 +248,18 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // bias tables of every head, times -log2(e): [h][0, P) position, [h][P, P+Tb) time
+  // bias tables of every head, times -log2(e): [h][0, P) position; [h][P, P +
+  // kTimeSlots) time by bit length, entries past Tb - 1 repeating the last
+  // bucket; [h][P + kTimeSlots, P + 2 kTimeSlots) the same plus position P - 1
   for (int x = threadIdx.x; x < H * PT; x += kThreads) {
     const int h = x / PT, e = x % PT;
     float v = 0.f;
     if (e < P) {
       if (p.rab_pos) v = p.rab_pos[h * P + e];
-    } else if (p.rab_time && p.ts) {
-      v = p.rab_time[h * Tb + (e - P)];
+    } else {
+      const int k = (e - P) % kTimeSlots;
+      if (p.rab_time && p.ts) v = p.rab_time[h * Tb + (k < Tb - 1 ? k : Tb - 1)];
+      if (e - P >= kTimeSlots && p.rab_pos) v += p.rab_pos[h * P + P - 1];
     }
     tab[x] = -kLog2e * v;
   }
@@ -509,22 +521,26 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         const int64_t* t64 = ts64_s + stage * BN + hq * 32;
         uint32_t hi[16], lo[16];
         const bool fast = cls == 2 && k0 + BN - 1 <= q0;
+        // the warp's rows start at position pos_lo (positions grow with the row)
+        const int pos_lo = q0 + wq * 32 < rc.h_end ? q0 + wq * 32 : rc.h_end;
+        const bool far = fast && pos_lo - (jb + 31) >= p.P - 1;
         const bool narrow = !item_wide && !stage_wide[stage];
         if (DELTA) {
           if (self) {
-            if (narrow) score32<false, false, false, 2>(p, sv, hi, lo, rc, jb, t32, t64);
-            else score32<false, true, false, 2>(p, sv, hi, lo, rc, jb, t32, t64);
+            if (narrow) score32<0, false, false, 2>(p, sv, hi, lo, rc, jb, t32, t64);
+            else score32<0, true, false, 2>(p, sv, hi, lo, rc, jb, t32, t64);
           } else {
-            if (narrow) score32<false, false, false, 1>(p, sv, hi, lo, rc, jb, t32, t64);
-            else score32<false, true, false, 1>(p, sv, hi, lo, rc, jb, t32, t64);
+            if (narrow) score32<0, false, false, 1>(p, sv, hi, lo, rc, jb, t32, t64);
+            else score32<0, true, false, 1>(p, sv, hi, lo, rc, jb, t32, t64);
           }
         } else if (narrow) {
-          if (fast) score32<true, false, false>(p, sv, hi, lo, rc, jb, t32, t64);
-          else if (cls == 2) score32<false, false, false>(p, sv, hi, lo, rc, jb, t32, t64);
-          else score32<false, false, true>(p, sv, hi, lo, rc, jb, t32, t64);
+          if (far) score32<2, false, false>(p, sv, hi, lo, rc, jb, t32, t64);
+          else if (fast) score32<1, false, false>(p, sv, hi, lo, rc, jb, t32, t64);
+          else if (cls == 2) score32<0, false, false>(p, sv, hi, lo, rc, jb, t32, t64);
+          else score32<0, false, true>(p, sv, hi, lo, rc, jb, t32, t64);
         } else {
-          if (cls == 2) score32<false, true, false>(p, sv, hi, lo, rc, jb, t32, t64);
-          else score32<false, true, true>(p, sv, hi, lo, rc, jb, t32, t64);
+          if (cls == 2) score32<0, true, false>(p, sv, hi, lo, rc, jb, t32, t64);
+          else score32<0, true, true>(p, sv, hi, lo, rc, jb, t32, t64);
         }
         // P_hi of this quarter at [32 hq, 32 hq + 16), P_lo at [32 hq + 16, 32 hq + 32)
         tmem_st16(scol, hi);
@@ -619,12 +635,26 @@ bool make_tmap_bf16(CUtensorMap* map, const void* ptr, int64_t rows, int64_t col
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map of rank 2 or 3 for tile stores: dims innermost first, strides
+// in bytes of dims 1..rank-1, the box, the swizzle; no L2 promotion.
+bool make_tmap_tile(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* ptr, const uint64_t* dims,
+                    const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rank < 2 || rank > 3) return false;
+  cuuint64_t d[3], st[2];
+  cuuint32_t b[3], e[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; }
+  for (int i = 0; i < rank - 1; ++i) st[i] = strides[i];
+  return fn(map, dt, rank, const_cast<void*>(ptr), d, st, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool tc_fwd_supported(int dtype, int dqk, int dv) {
   return dtype == HSTU_BF16 && dqk == dv && (dqk == 64 || dqk == 128);
 }
 
 size_t tc_fwd_smem_bytes(int d, int H, int P, int Tb) {
-  const size_t tab = sizeof(float) * (size_t)H * (P + Tb);
+  const size_t tab = sizeof(float) * (size_t)H * (P + 2 * kTimeSlots);
   return (d == 64 ? Layout<64>::TAB_OFF : Layout<128>::TAB_OFF) + tab + 1024;
 }
 
