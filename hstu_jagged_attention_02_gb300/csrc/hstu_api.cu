@@ -88,6 +88,7 @@ void set_score_constants(AttnParams& p) {
   p.kA = -log2e * p.alpha;
   p.kC = -p.inv_n / log2e;
   p.kZ = -1.0f / log2e;
+  p.kCi = 1.0f / p.kC;
 }
 
 hstu_status_t check_ws(void* ws, size_t bytes, size_t need) {

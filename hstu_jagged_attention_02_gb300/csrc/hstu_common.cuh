@@ -32,9 +32,6 @@ enum : int {
 // whose relative times all lie within +-2^30 s computes its gaps in 32 bits,
 // any other tile takes the 64-bit path.
 constexpr int64_t kNarrowTsSpan = (int64_t)1 << 30;
-// time-bias table slots per head in the tensor-core kernels: one per bit length
-// of a 64-bit gap, [0, 64]; slots past Tb - 1 repeat the last bucket
-constexpr int kTimeSlots = 65;
 __device__ __forceinline__ bool ts_wide(int64_t rel) { return rel >= kNarrowTsSpan || rel <= -kNarrowTsSpan; }
 constexpr size_t kWsHeaderBytes = 256;
 constexpr size_t kWsAlign = 256;

@@ -67,8 +67,8 @@ struct AttnParams {
   int64_t T;
   float alpha, inv_n;
   // score constants of the tensor-core epilogues (w = -log2(e) z):
-  // kA = -log2(e) alpha, kC = -1 / (log2(e) N), kZ = -1 / log2(e)
-  float kA, kC, kZ;
+  // kA = -log2(e) alpha, kC = -1 / (log2(e) N), kZ = -1 / log2(e), kCi = 1 / kC
+  float kA, kC, kZ, kCi;
   int P, Tb;
   uint32_t flags;
   int num_sms;

@@ -82,9 +82,17 @@ struct Layout {
   static constexpr int SLOT_OFF = QTS_OFF + kQBufs * BM * 8;    // ItemSlot [kQBufs]
   static constexpr int BAR_OFF = SLOT_OFF + kQBufs * (int)sizeof(ItemSlot);
   static constexpr int MISC_OFF = BAR_OFF + BAR_COUNT * 8;      // tmem slot, abort flag, per-stage wide flags
-  static constexpr int TAB_OFF = MISC_OFF + 16;                 // float [H][P + 2 kTimeSlots]
+  static constexpr int TAB_OFF = MISC_OFF + 16;                 // float [H][P + kTabTime]
   static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
 };
+
+// Time-bias slots of a head's table after its P position entries, indexed by
+// the count of leading zeros of the gap (bit length = width - clz), each
+// holding bucket min(bit length, Tb - 1):
+//   [0, 65)   64-bit gaps, clz in [0, 64]
+//   [65, 98)  32-bit gaps, clz in [0, 32]
+//   [98, 131) 32-bit gaps plus position bucket P - 1 (blocks far from the diagonal)
+constexpr int kTabWide = 0, kTabNarrow = 65, kTabFar = 98, kTabTime = 131;
 
 // waits for a phase, ignoring the abort flag (used to drain async copies)
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -114,9 +122,8 @@ struct RowCtx {
   int hi, dg;
   int32_t ti32;      // timestamp relative to the sequence's first token
   int64_t ti64;      // absolute timestamp
-  // bias tables of the head, pre-scaled by -log2(e): position [0, P); time by
-  // bit length of the gap [P, P + kTimeSlots), clamped to Tb - 1 inside the
-  // table; the same plus the last position entry [P + kTimeSlots, P + 2 kTimeSlots)
+  // bias tables of the head, pre-scaled by -log2(e): position [0, P), then the
+  // kTabTime time slots
   const float* tp;
 };
 
@@ -158,18 +165,18 @@ __device__ __forceinline__ void score32(const AttnParams& p, const uint32_t (&sv
         dp = dp < 0 ? -dp : dp;
         bp = dp < p.P - 1 ? dp : p.P - 1;
       }
-      int bt;   // bit length of the gap, in [0, 64] (narrow: [0, 31]); the tables clamp it
+      int st;   // time slot: leading zeros of the gap, the tables map it to a bucket
       if (WIDE) {
         const int64_t tj = ts64[cc];
         const uint64_t dt = rc.ti64 >= tj ? (uint64_t)(rc.ti64 - tj) : (uint64_t)(tj - rc.ti64);
-        bt = 64 - __clzll((long long)dt);
+        st = kTabWide + __clzll((long long)dt);
       } else {
         int d = rc.ti32 - ts32[cc];
         d = d < 0 ? -d : d;
-        bt = 32 - __clz(d);
+        st = (MODE == 0 && POS == 2 ? kTabFar : kTabNarrow) + __clz(d);
       }
-      if (MODE == 0 && POS == 2) bias[c] = rc.tp[p.P + kTimeSlots + bt];
-      else bias[c] = rc.tp[bp] + rc.tp[p.P + bt];
+      if (MODE == 0 && POS == 2) bias[c] = rc.tp[p.P + st];
+      else bias[c] = rc.tp[bp] + rc.tp[p.P + st];
     }
 #pragma unroll
     for (int c = 0; c < 16; c += 2) {
@@ -177,8 +184,9 @@ __device__ __forceinline__ void score32(const AttnParams& p, const uint32_t (&sv
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int cc = half * 16 + c + e;
+        // SiLU(z)/N = w kC / (1 + 2^w), as w / (kCi + kCi 2^w)
         const float w = fmaf(p.kA, __uint_as_float(sv[cc]), bias[c + e]);
-        float a = (w * p.kC) * rcp_approx(1.0f + ex2_approx(w));
+        float a = w * rcp_approx(fmaf(p.kCi, ex2_approx(w), p.kCi));
         if (MODE == 1) {
           a = (rc.row_ok && jb + cc < rc.h_end) ? a : 0.f;
         } else if (MODE == 2) {
@@ -227,7 +235,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   float* tab = reinterpret_cast<float*>(base + L::TAB_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int H = p.H, P = p.P, Tb = p.Tb, PT = p.P + 2 * kTimeSlots;
+  const int H = p.H, P = p.P, Tb = p.Tb, PT = p.P + kTabTime;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQBufs; ++s) {
@@ -248,18 +256,18 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // bias tables of every head, times -log2(e): [h][0, P) position; [h][P, P +
-  // kTimeSlots) time by bit length, entries past Tb - 1 repeating the last
-  // bucket; [h][P + kTimeSlots, P + 2 kTimeSlots) the same plus position P - 1
+  // bias tables of every head, times -log2(e): [h][0, P) position, then the
+  // kTabTime time slots (wide, narrow, narrow plus position bucket P - 1)
   for (int x = threadIdx.x; x < H * PT; x += kThreads) {
     const int h = x / PT, e = x % PT;
     float v = 0.f;
     if (e < P) {
       if (p.rab_pos) v = p.rab_pos[h * P + e];
     } else {
-      const int k = (e - P) % kTimeSlots;
-      if (p.rab_time && p.ts) v = p.rab_time[h * Tb + (k < Tb - 1 ? k : Tb - 1)];
-      if (e - P >= kTimeSlots && p.rab_pos) v += p.rab_pos[h * P + P - 1];
+      const int k = e - P;
+      const int bits = k < kTabNarrow ? 64 - (k - kTabWide) : (k < kTabFar ? 32 - (k - kTabNarrow) : 32 - (k - kTabFar));
+      if (p.rab_time && p.ts) v = p.rab_time[h * Tb + (bits < Tb - 1 ? bits : Tb - 1)];
+      if (k >= kTabFar && p.rab_pos) v += p.rab_pos[h * P + P - 1];
     }
     tab[x] = -kLog2e * v;
   }
@@ -654,7 +662,7 @@ bool tc_fwd_supported(int dtype, int dqk, int dv) {
 }
 
 size_t tc_fwd_smem_bytes(int d, int H, int P, int Tb) {
-  const size_t tab = sizeof(float) * (size_t)H * (P + 2 * kTimeSlots);
+  const size_t tab = sizeof(float) * (size_t)H * (P + kTabTime);
   return (d == 64 ? Layout<64>::TAB_OFF : Layout<128>::TAB_OFF) + tab + 1024;
 }
 
