@@ -309,16 +309,18 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
   float* dq_acc = dq_direct ? static_cast<float*>(a->dq) : reinterpret_cast<float*>(ws + L.dq_acc);
   const bool has_rp = a->rab_pos != nullptr;
   const bool has_rt = a->rab_time != nullptr && a->timestamps != nullptr;
-  // the tensor-core path's reduction writes every d_rab entry of a table that
-  // is present; the other outputs start from zero
-  const bool reduced_rp = tc && has_rp && d->total_tokens > 0;
-  const bool reduced_rt = tc && has_rt && d->total_tokens > 0;
-  if (a->d_rab_pos && !reduced_rp)
-    HSTU_CUDA_TRY(cudaMemsetAsync(a->d_rab_pos, 0, sizeof(float) * d->H * d->num_pos_buckets, st));
-  if (a->d_rab_time && !reduced_rt)
-    HSTU_CUDA_TRY(cudaMemsetAsync(a->d_rab_time, 0, sizeof(float) * d->H * d->num_time_buckets, st));
+  // d_rab outputs and the dq accumulator start from zero: on the tensor-core
+  // path the norm-gate backward kernel zeroes them on its way (the attention
+  // kernel then adds each CTA's d_rab partial sums), otherwise memsets do
+  const bool fused_zero = tc && d->total_tokens > 0;
+  if (!fused_zero) {
+    if (a->d_rab_pos)
+      HSTU_CUDA_TRY(cudaMemsetAsync(a->d_rab_pos, 0, sizeof(float) * d->H * d->num_pos_buckets, st));
+    if (a->d_rab_time)
+      HSTU_CUDA_TRY(cudaMemsetAsync(a->d_rab_time, 0, sizeof(float) * d->H * d->num_time_buckets, st));
+  }
   if (d->total_tokens == 0) return HSTU_OK;
-  HSTU_CUDA_TRY(cudaMemsetAsync(dq_acc, 0, sizeof(float) * rows * d->d_qk, st));
+  if (!fused_zero) HSTU_CUDA_TRY(cudaMemsetAsync(dq_acc, 0, sizeof(float) * rows * d->d_qk, st));
   // per-CTA d_rab partial sums: each tensor-core CTA zeroes its own row first
   float* drab_partial = reinterpret_cast<float*>(ws + L.drab_part);
 
@@ -330,6 +332,11 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
     np.split = tc ? 1 : 0;
     np.dO_lo = ws + L.dO + sizeof(__nv_bfloat16) * rows * (size_t)d->d_v;
     np.T = d->total_tokens; np.F = d->H * d->d_v; np.norm = d->norm; np.eps = d->ln_eps;
+    if (fused_zero) {  // d_qk == d_v and H * d_qk % 4 == 0 on this path
+      np.zero_rows = dq_acc; np.zero_F = d->H * d->d_qk;
+      np.zero_a = a->d_rab_pos; np.zero_a_n = a->d_rab_pos ? d->H * d->num_pos_buckets : 0;
+      np.zero_b = a->d_rab_time; np.zero_b_n = a->d_rab_time ? d->H * d->num_time_buckets : 0;
+    }
     HSTU_CUDA_TRY(launch_norm_gate_bwd(np, st));
     ++g_launches;
   }
@@ -352,7 +359,7 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
   {
     KernelTimer timer(st);
     if (tc) {
-      HSTU_CUDA_TRY(launch_tc_bwd(p, st));  // includes the d_rab partial-sum reduction
+      HSTU_CUDA_TRY(launch_tc_bwd(p, st));  // its CTAs add their d_rab partial sums at exit
     } else {
       const int max_items = ((int)((d->total_tokens + kSimtTile - 1) / kSimtTile) + d->B) * d->H;
       HSTU_CUDA_TRY(launch_simt_bwd(p, max_items, st));

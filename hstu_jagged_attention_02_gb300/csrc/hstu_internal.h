@@ -50,7 +50,7 @@ struct AttnParams {
   float* dq_acc;         // backward: FP32 accumulator [T,H,dqk], zeroed before
   float* d_rab_pos;      // backward: [H,P] accumulated (zeroed before), or NULL
   float* d_rab_time;
-  float* drab_partial;   // tensor-core backward: [kDrabMaxCtas][H][P+Tb] zeroed partial sums
+  float* drab_partial;   // tensor-core backward: [kDrabMaxCtas][H][P+Tb] per-CTA partial sums
   const int* hdr;        // workspace header (block count)
   int* hdr_rw;           // same, writable (error word)
   const Block* blocks;
@@ -86,6 +86,14 @@ struct NormParams {
   void* du;
   float* mean;
   float* rstd;
+  // backward only, or NULL: FP32 buffers the kernel zeroes on the way (the
+  // tensor-core backward's dq accumulator [T, zero_F], and the two d_rab tables)
+  float* zero_rows;
+  int zero_F;
+  float* zero_a;
+  int zero_a_n;
+  float* zero_b;
+  int zero_b_n;
   int64_t T;
   int F;           // H * d_v
   int norm;

@@ -123,10 +123,18 @@ __global__ void __launch_bounds__(kWarps * 32) norm_gate_fwd_kernel(NormParams p
 // du = xn * dy;  g = dy * u;  LayerNorm: dO = rstd * (g - mean(g) - xn * mean(g xn)); none: dO = g
 template <typename TI, typename TO, int VEC, int PER>
 __global__ void __launch_bounds__(kWarps * 32) norm_gate_bwd_kernel(NormParams p) {
+  if (blockIdx.x == 0) {
+    for (int x = threadIdx.x; x < p.zero_a_n; x += blockDim.x) p.zero_a[x] = 0.f;
+    for (int x = threadIdx.x; x < p.zero_b_n; x += blockDim.x) p.zero_b[x] = 0.f;
+  }
   const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (t >= p.T) return;
   const int lane = threadIdx.x & 31;
   const int F = p.F;
+  if (p.zero_rows) {  // zero_F % 4 == 0, 16-byte aligned rows
+    float4* zr = reinterpret_cast<float4*>(p.zero_rows + t * p.zero_F);
+    for (int f4 = lane; f4 < p.zero_F / 4; f4 += 32) zr[f4] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   const TO* o = static_cast<const TO*>(p.o) + t * F;
   const TI* u = p.u ? static_cast<const TI*>(p.u) + t * F : nullptr;
   const TO* dy = static_cast<const TO*>(p.dy) + t * F;

@@ -663,46 +663,19 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     }
   }
 
+  __threadfence();   // this CTA's partial-sum reductions are performed before they are read back
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
-}
-
-// d_rab_pos[h][b] / d_rab_time[h][b] = sum over CTAs of their partial sums.
-// A block owns 32 consecutive entries (one per lane, coalesced rows); its 8
-// warps split the CTA rows and combine their sums in shared memory.
-constexpr int kReduceWarps = 8;
-__global__ void __launch_bounds__(kReduceWarps * 32)
-drab_reduce_kernel(const float* __restrict__ partial, int nctas, int H, int P, int Tb, float* d_rab_pos,
-                   float* d_rab_time) {
-  __shared__ float part[kReduceWarps][32];
-  const int PT = P + Tb, n = H * PT;
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int x = blockIdx.x * 32 + lane;
-  float s = 0.f;
-  if (x < n) {
-    int c = w;
-    for (; c + 3 * kReduceWarps < nctas; c += 4 * kReduceWarps) {
-      const float a0 = partial[(size_t)c * n + x];
-      const float a1 = partial[(size_t)(c + kReduceWarps) * n + x];
-      const float a2 = partial[(size_t)(c + 2 * kReduceWarps) * n + x];
-      const float a3 = partial[(size_t)(c + 3 * kReduceWarps) * n + x];
-      s += (a0 + a1) + (a2 + a3);
+  // d_rab += this CTA's partial sums (the outputs were zeroed before the launch)
+  if (want_rp || want_rt) {
+    for (int x = threadIdx.x; x < H * PT; x += kThreads) {
+      const float v = __ldcg(drab + x);
+      const int h = x / PT, e = x % PT;
+      if (e < P) red_add(p.d_rab_pos + h * P + e, v, want_rp && v != 0.f);
+      else red_add(p.d_rab_time + h * Tb + (e - P), v, want_rt && v != 0.f);
     }
-    for (; c < nctas; c += kReduceWarps) s += partial[(size_t)c * n + x];
-  }
-  part[w][lane] = s;
-  __syncthreads();
-  if (w != 0 || x >= n) return;
-  float t = 0.f;
-#pragma unroll
-  for (int i = 0; i < kReduceWarps; ++i) t += part[i][lane];
-  const int h = x / PT, e = x % PT;
-  if (e < P) {
-    if (d_rab_pos) d_rab_pos[h * P + e] = t;
-  } else if (d_rab_time) {
-    d_rab_time[h * Tb + (e - P)] = t;
   }
 }
 
@@ -729,17 +702,7 @@ cudaError_t launch_t(const AttnParams& p, cudaStream_t st) {
   if (grid > kDrabMaxCtas) grid = kDrabMaxCtas;  // one d_rab partial row per CTA
   hstu_bwd_tc_kernel<TO><<<grid, kThreads, smem, st>>>(p, mq, mk, mv, mdh, mdl);
   e = cudaGetLastError();
-  if (e != cudaSuccess) {
-    set_launch_detail(e, "hstu_bwd_tc_kernel", fn, kThreads, smem);
-    return e;
-  }
-  // d_rab = sum of the CTAs' partial sums (overwrites the outputs)
-  const int entries = p.H * (p.P + p.Tb);
-  if (p.d_rab_pos || p.d_rab_time) {
-    drab_reduce_kernel<<<(entries + 31) / 32, kReduceWarps * 32, 0, st>>>(p.drab_partial, grid, p.H, p.P, p.Tb,
-                                                                         p.d_rab_pos, p.d_rab_time);
-    e = cudaGetLastError();
-  }
+  if (e != cudaSuccess) set_launch_detail(e, "hstu_bwd_tc_kernel", fn, kThreads, smem);
   return e;
 }
 
