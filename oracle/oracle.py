@@ -14,6 +14,10 @@ the C attention routines:
     [U | V | Q | K] = SiLU(X W1)           (split in that order, no bias)
     Y   = LayerNorm(attention(Q, K, V)) * U
     out = X + Y W2                         (no bias)
+
+The optional fused dropout on Y draws its keep decisions from Philox4x64-10
+(a counter-based generator, written out here from its published
+definition), so both sides derive the same mask from (seed, offset).
 """
 from __future__ import annotations
 
@@ -147,6 +151,88 @@ def norm_gate_bwd(o, u, dy, norm="layernorm", eps=1e-5, rows=None):
     return dx, du
 
 
+# ------------------------------------------------------------------ dropout
+# Dropout on y = Norm(o) * u, fused with the norm-gate (ai6s.net survey,
+# section 2.1.3, "memory optimisation": dropout fused with its neighbouring
+# operators).  The keep decision of element (t, f) of the [T, F] output comes
+# from the counter-based generator Philox4x64-10 (Salmon, Moraes, Dror, Shaw,
+# "Parallel random numbers: as easy as 1, 2, 3", SC 2011), so the backward
+# regenerates the forward's mask from (seed, offset) alone:
+#   e = t F + f;  (r0, r1, r2, r3) = Philox4x64-10(counter (e >> 3, offset, 0, 0), key (seed, 0))
+#   w = 32-bit word (e & 7) of r0..r3, low half of each 64-bit word first
+#   keep iff w >= floor(p 2^32);  kept elements are scaled by 1 / (1 - p)
+# p is the descriptor's float32 value.
+
+_M64 = np.uint64(0xFFFFFFFFFFFFFFFF)
+_LO32 = np.uint64(0xFFFFFFFF)
+_PHILOX_M0 = np.uint64(0xD2E7470EE14C6C93)   # round multipliers
+_PHILOX_M1 = np.uint64(0xCA5A826395121157)
+_PHILOX_W0 = np.uint64(0x9E3779B97F4A7C15)   # key schedule (Weyl) increments
+_PHILOX_W1 = np.uint64(0xBB67AE8584CAA73B)
+
+
+def _mulhilo64(a, b):
+    """(high, low) 64-bit halves of the 128-bit products a * b (uint64 arrays)."""
+    s32 = np.uint64(32)
+    al, ah = a & _LO32, a >> s32
+    bl, bh = b & _LO32, b >> s32
+    p0, p1, p2, p3 = al * bl, al * bh, ah * bl, ah * bh
+    mid = (p0 >> s32) + (p1 & _LO32) + (p2 & _LO32)
+    hi = p3 + (p1 >> s32) + (p2 >> s32) + (mid >> s32)
+    return hi, a * b
+
+
+def philox4x64_10(c0, c1, c2, c3, k0, k1):
+    """Philox4x64 with 10 rounds on uint64 arrays (broadcast): returns the four
+    output words.  A round multiplies c0 and c2 by the two round constants and
+    crosses the halves with c1, c3 and the key; the key advances by the Weyl
+    increments between rounds."""
+    with np.errstate(over="ignore"):
+        c = [np.asarray(x, np.uint64) for x in (c0, c1, c2, c3)]
+        k = [np.asarray(k0, np.uint64), np.asarray(k1, np.uint64)]
+        for r in range(10):
+            if r > 0:
+                k = [k[0] + _PHILOX_W0, k[1] + _PHILOX_W1]
+            hi0, lo0 = _mulhilo64(_PHILOX_M0, c[0])
+            hi1, lo1 = _mulhilo64(_PHILOX_M1, c[2])
+            c = [hi1 ^ c[1] ^ k[0], lo1, hi0 ^ c[3] ^ k[1], lo0]
+    return c
+
+
+def dropout_threshold(p) -> int:
+    """floor(p 2^32) for the float32 probability p (0 <= p < 1)."""
+    p32 = float(np.float32(p))
+    if not 0.0 <= p32 < 1.0:
+        raise ValueError("dropout probability must lie in [0, 1)")
+    return int(np.floor(p32 * 4294967296.0))
+
+
+def dropout_mask(T, F, p, seed, offset, rows=None):
+    """(keep bool [T, F], scale) of the fused dropout; rows (bool [T]) limits
+    the evaluation to those rows (the others are reported kept)."""
+    p32 = float(np.float32(p))
+    thr = dropout_threshold(p)
+    keep = np.ones((T, F), bool)
+    if p32 == 0.0 or T == 0:
+        return keep, 1.0
+    t_idx = np.arange(T, dtype=np.uint64) if rows is None else np.nonzero(np.asarray(rows, bool))[0].astype(np.uint64)
+    e = t_idx[:, None] * np.uint64(F) + np.arange(F, dtype=np.uint64)[None, :]
+    r = philox4x64_10(e >> np.uint64(3), np.uint64(offset), np.uint64(0), np.uint64(0),
+                      np.uint64(seed), np.uint64(0))
+    k = (e & np.uint64(7)).astype(np.int64)
+    word64 = np.choose(k >> 1, r)
+    w = (word64 >> (np.uint64(32) * (k & 1).astype(np.uint64))) & _LO32
+    keep[t_idx.astype(np.int64)] = w >= np.uint64(thr)
+    return keep, 1.0 / (1.0 - p32)
+
+
+def apply_dropout(y, p, seed, offset, rows=None):
+    """y [T, F] with the fused dropout applied (the identity when p == 0)."""
+    y = _f64(y)
+    keep, scale = dropout_mask(y.shape[0], y.shape[1], p, seed, offset, rows)
+    return np.where(keep, y * scale, 0.0)
+
+
 def attn_bwd(pb: Problem, dO, q_rows=None, kv_rows=None, want_rab=True):
     """dq, dk, dv [T, H, d] and d_rab_pos [H, P], d_rab_time [H, Tb] (None when
     the table is absent or rows are restricted)."""
@@ -166,21 +252,27 @@ def attn_bwd(pb: Problem, dO, q_rows=None, kv_rows=None, want_rab=True):
     return dq, dk, dv, drp, drt
 
 
-def forward(b, rows=None):
-    """Whole forward of a synth.Batch: dict with o [T,H,dv], y [T,F], mean, rstd."""
+def forward(b, rows=None, dropout=None):
+    """Whole forward of a synth.Batch: dict with o [T,H,dv], y [T,F], mean, rstd.
+    dropout = (p, seed, offset) applies the fused dropout to y."""
     pb = Problem.from_batch(b)
     o = attn_fwd(pb, rows)
     y, mean, rstd = norm_gate(o, b.u, b.norm, b.eps, rows)
+    if dropout is not None:
+        y = apply_dropout(y, *dropout, rows=rows)
     return {"o": o, "y": y, "mean": mean, "rstd": rstd}
 
 
-def backward(b, o=None):
+def backward(b, o=None, dropout=None):
     """Whole backward of a synth.Batch given its dy: dict with dq, dk, dv, du,
-    d_rab_pos, d_rab_time (and the forward's o, y)."""
+    d_rab_pos, d_rab_time (and the forward's o, y).  dropout = (p, seed,
+    offset): dy is the gradient w.r.t. the dropped-out y, so it passes the
+    forward's mask and scale before the norm-gate backward."""
     pb = Problem.from_batch(b)
     if o is None:
         o = attn_fwd(pb)
-    dO, du = norm_gate_bwd(o, b.u, b.dy, b.norm, b.eps)
+    dy = b.dy if dropout is None else apply_dropout(_f64(b.dy).reshape(pb.T, -1), *dropout)
+    dO, du = norm_gate_bwd(o, b.u, dy, b.norm, b.eps)
     dq, dk, dv, drp, drt = attn_bwd(pb, dO)
     return {"o": o, "dO": dO.reshape(pb.T, pb.H, pb.dv), "dq": dq, "dk": dk, "dv": dv, "du": du,
             "d_rab_pos": drp, "d_rab_time": drt}
