@@ -30,7 +30,9 @@ class Problem:
     workspace, with the C argument structs filled once."""
 
     def __init__(self, batch, device="cuda", flags: int = 0, want_y: bool = True,
-                 want_stats: bool = False, want_drab: bool = True, out_dtype: str = "fp32"):
+                 want_stats: bool = False, want_drab: bool = True, out_dtype: str = "fp32",
+                 dropout=None):
+        # dropout: None or (p, seed, offset) of the fused dropout on y
         self.batch = batch
         dev = torch.device(device)
         self.dev = dev
@@ -77,21 +79,23 @@ class Problem:
             max_seq_len=batch.max_seq_len, alpha=batch.alpha,
             num_pos_buckets=batch.rab_pos.shape[1] if batch.rab_pos is not None else 128,
             num_time_buckets=batch.rab_time.shape[1] if batch.rab_time is not None else 64,
-            norm=batch.norm, ln_eps=batch.eps, flags=flags)
+            norm=batch.norm, ln_eps=batch.eps, flags=flags,
+            dropout_p=0.0 if dropout is None else float(dropout[0]))
+        seed, offset = (0, 0) if dropout is None else (int(dropout[1]), int(dropout[2]))
         fwd_b, bwd_b = C.hstu_attn_workspace_size(self.desc)
         self.ws_bytes = max(fwd_b, bwd_b if self.backward_enabled else 0)
         self.ws = torch.empty(self.ws_bytes, device=dev, dtype=torch.uint8)
         self.fwd_args = C.hstu_attn_fwd_args(
             _ptr(self.offsets), _ptr(self.num_targets), _ptr(self.num_contexts), _ptr(self.timestamps),
             _ptr(self.rab_pos), _ptr(self.rab_time), _ptr(self.q), _ptr(self.k), _ptr(self.v),
-            _ptr(self.u), _ptr(self.o), _ptr(self.y), _ptr(self.mean), _ptr(self.rstd))
+            _ptr(self.u), _ptr(self.o), _ptr(self.y), _ptr(self.mean), _ptr(self.rstd), seed, offset)
         if self.backward_enabled:
             self.bwd_args = C.hstu_attn_bwd_args(
                 _ptr(self.offsets), _ptr(self.num_targets), _ptr(self.num_contexts),
                 _ptr(self.timestamps), _ptr(self.rab_pos), _ptr(self.rab_time), _ptr(self.q),
                 _ptr(self.k), _ptr(self.v), _ptr(self.u), _ptr(self.o), _ptr(self.dy),
                 _ptr(self.dq), _ptr(self.dk), _ptr(self.dvv), _ptr(self.du), _ptr(self.d_rab_pos),
-                _ptr(self.d_rab_time))
+                _ptr(self.d_rab_time), seed, offset)
 
     def forward(self, stream=None):
         C.hstu_attn_fwd(self.desc, self.fwd_args, self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
@@ -117,7 +121,7 @@ class HSTUAttnFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, u, rab_pos, rab_time, seq_offsets, num_targets, num_contexts,
                 timestamps, max_seq_len: int, alpha: float, norm: str = "layernorm",
-                eps: float = 1e-5):
+                eps: float = 1e-5, dropout_p: float = 0.0, dropout_seed: int = 0, dropout_offset: int = 0):
         T, H, dqk = q.shape
         dv = v.shape[2]
         dtype = "bf16" if q.dtype == torch.bfloat16 else "fp32"
@@ -125,7 +129,7 @@ class HSTUAttnFunction(torch.autograd.Function):
                            total_tokens=T, max_seq_len=max_seq_len, alpha=alpha,
                            num_pos_buckets=rab_pos.shape[1] if rab_pos is not None else 128,
                            num_time_buckets=rab_time.shape[1] if rab_time is not None else 64,
-                           norm=norm, ln_eps=eps)
+                           norm=norm, ln_eps=eps, dropout_p=dropout_p)
         fwd_b, bwd_b = C.hstu_attn_workspace_size(desc)
         ws = torch.empty(max(fwd_b, bwd_b), device=q.device, dtype=torch.uint8)
         o = torch.empty(T, H, dv, device=q.device, dtype=q.dtype)
@@ -134,11 +138,12 @@ class HSTUAttnFunction(torch.autograd.Function):
         u = u.contiguous() if u is not None else None
         args = C.hstu_attn_fwd_args(_ptr(seq_offsets), _ptr(num_targets), _ptr(num_contexts),
                                     _ptr(timestamps), _ptr(rab_pos), _ptr(rab_time), _ptr(q), _ptr(k),
-                                    _ptr(v), _ptr(u), _ptr(o), _ptr(y), None, None)
+                                    _ptr(v), _ptr(u), _ptr(o), _ptr(y), None, None, dropout_seed,
+                                    dropout_offset)
         C.hstu_attn_fwd(desc, args, ws.data_ptr(), ws.numel(), _stream_handle())
         ctx.save_for_backward(q, k, v, u, rab_pos, rab_time, seq_offsets, num_targets, num_contexts,
                               timestamps, o)
-        ctx.desc, ctx.ws = desc, ws
+        ctx.desc, ctx.ws, ctx.drop = desc, ws, (dropout_seed, dropout_offset)
         return y
 
     @staticmethod
@@ -151,13 +156,16 @@ class HSTUAttnFunction(torch.autograd.Function):
         drt = torch.empty_like(rab_time, dtype=torch.float32) if rab_time is not None else None
         args = C.hstu_attn_bwd_args(_ptr(off), _ptr(nt), _ptr(nc), _ptr(ts), _ptr(rab_pos), _ptr(rab_time),
                                     _ptr(q), _ptr(k), _ptr(v), _ptr(u), _ptr(o), _ptr(dy), _ptr(dq),
-                                    _ptr(dk), _ptr(dv), _ptr(du), _ptr(drp), _ptr(drt))
+                                    _ptr(dk), _ptr(dv), _ptr(du), _ptr(drp), _ptr(drt), *ctx.drop)
         C.hstu_attn_bwd(ctx.desc, args, ctx.ws.data_ptr(), ctx.ws.numel(), _stream_handle())
-        return (dq, dk, dv, du, drp, drt, None, None, None, None, None, None, None, None)
+        return (dq, dk, dv, du, drp, drt) + (None,) * 11
 
 
 def hstu_attention(q, k, v, u, seq_offsets, max_seq_len, alpha, *, num_targets=None, num_contexts=None,
-                   timestamps=None, rab_pos=None, rab_time=None, norm="layernorm", eps=1e-5):
-    """Differentiable HSTU jagged attention: returns y [T, H*d_v]."""
+                   timestamps=None, rab_pos=None, rab_time=None, norm="layernorm", eps=1e-5,
+                   dropout_p=0.0, dropout_seed=0, dropout_offset=0):
+    """Differentiable HSTU jagged attention: returns y [T, H*d_v] (with the
+    fused dropout when dropout_p > 0; the seed and offset select the mask)."""
     return HSTUAttnFunction.apply(q, k, v, u, rab_pos, rab_time, seq_offsets, num_targets, num_contexts,
-                                  timestamps, int(max_seq_len), float(alpha), norm, float(eps))
+                                  timestamps, int(max_seq_len), float(alpha), norm, float(eps),
+                                  float(dropout_p), int(dropout_seed), int(dropout_offset))

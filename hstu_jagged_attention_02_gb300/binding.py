@@ -32,30 +32,33 @@ class hstu_attn_desc(ctypes.Structure):
                 ("total_tokens", ctypes.c_int64), ("max_seq_len", ctypes.c_int32),
                 ("alpha", ctypes.c_float), ("num_pos_buckets", ctypes.c_int32),
                 ("num_time_buckets", ctypes.c_int32), ("norm", ctypes.c_int32),
-                ("ln_eps", ctypes.c_float), ("flags", ctypes.c_uint32)]
+                ("ln_eps", ctypes.c_float), ("flags", ctypes.c_uint32),
+                ("dropout_p", ctypes.c_float), ("reserved", ctypes.c_uint32)]
+
+_DROP = [("dropout_seed", ctypes.c_uint64), ("dropout_offset", ctypes.c_uint64)]
 
 
 class hstu_attn_fwd_args(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("seq_offsets", "num_targets", "num_contexts", "timestamps",
                                    "rab_pos", "rab_time", "q", "k", "v", "u", "o", "y",
-                                   "ln_mean", "ln_rstd")]
+                                   "ln_mean", "ln_rstd")] + _DROP
 
 
 class hstu_attn_bwd_args(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("seq_offsets", "num_targets", "num_contexts", "timestamps",
                                    "rab_pos", "rab_time", "q", "k", "v", "u", "o", "dy",
-                                   "dq", "dk", "dv", "du", "d_rab_pos", "d_rab_time")]
+                                   "dq", "dk", "dv", "du", "d_rab_pos", "d_rab_time")] + _DROP
 
 
 class hstu_layer_fwd_args(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("seq_offsets", "num_targets", "num_contexts", "timestamps",
-                                   "rab_pos", "rab_time", "x", "w1", "w2", "out", "z1", "u", "vqk", "o", "y")]
+                                   "rab_pos", "rab_time", "x", "w1", "w2", "out", "z1", "u", "vqk", "o", "y")] + _DROP
 
 
 class hstu_layer_bwd_args(ctypes.Structure):
     _fields_ = [(n, _vp) for n in ("seq_offsets", "num_targets", "num_contexts", "timestamps",
                                    "rab_pos", "rab_time", "x", "w1", "w2", "z1", "u", "vqk", "o", "y",
-                                   "dout", "dx", "dw1", "dw2", "d_rab_pos", "d_rab_time")]
+                                   "dout", "dx", "dw1", "dw2", "d_rab_pos", "d_rab_time")] + _DROP
 
 
 class hstu_attn_delta_args(ctypes.Structure):
@@ -137,7 +140,7 @@ def _check(status: int, where: str):
 def make_desc(*, dtype: str, out_dtype: Optional[str] = None, B: int, H: int, d_qk: int, d_v: int, total_tokens: int,
               max_seq_len: int, alpha: float, num_pos_buckets: int = 128,
               num_time_buckets: int = 64, norm: str = "layernorm", ln_eps: float = 1e-5,
-              flags: int = 0) -> hstu_attn_desc:
+              flags: int = 0, dropout_p: float = 0.0) -> hstu_attn_desc:
     d = hstu_attn_desc()
     d.struct_size = ctypes.sizeof(hstu_attn_desc)
     d.dtype = HSTU_BF16 if dtype == "bf16" else HSTU_FP32
@@ -150,6 +153,7 @@ def make_desc(*, dtype: str, out_dtype: Optional[str] = None, B: int, H: int, d_
     d.norm = HSTU_NORM_LAYERNORM if norm == "layernorm" else HSTU_NORM_NONE
     d.ln_eps = ln_eps
     d.flags = flags
+    d.dropout_p = dropout_p
     return d
 
 

@@ -70,6 +70,7 @@ hstu_status_t check_desc(const hstu_attn_desc* d) {
   if (d->norm != HSTU_NORM_NONE && d->norm != HSTU_NORM_LAYERNORM) return HSTU_ERR_INVALID_ARG;
   if (d->norm == HSTU_NORM_LAYERNORM && !(d->ln_eps > 0.f && std::isfinite(d->ln_eps))) return HSTU_ERR_INVALID_ARG;
   if (!std::isfinite(d->alpha)) return HSTU_ERR_INVALID_ARG;
+  if (!(d->dropout_p >= 0.f && d->dropout_p < 1.f) || d->reserved != 0) return HSTU_ERR_INVALID_ARG;
   if (d->flags & ~kKnownFlags) return HSTU_ERR_INVALID_ARG;
   if ((d->flags & HSTU_FLAG_U_FP32) && d->out_dtype != HSTU_FP32) return HSTU_ERR_UNSUPPORTED;
   if (d->d_qk != d->d_v || (d->d_qk != 32 && d->d_qk != 64 && d->d_qk != 128)) return HSTU_ERR_UNSUPPORTED;
@@ -81,6 +82,18 @@ hstu_status_t check_desc(const hstu_attn_desc* d) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Fused dropout constants of the norm-gate kernels: keep iff the element's
+// 32-bit generator word >= floor(p 2^32); kept values times 1 / (1 - p).
+void set_dropout(NormParams& np, const hstu_attn_desc* d, uint64_t seed, uint64_t offset) {
+  if (!(d->dropout_p > 0.f)) return;
+  const double p = (double)d->dropout_p;
+  np.drop = 1;
+  np.drop_thr = (uint32_t)std::floor(p * 4294967296.0);
+  np.drop_scale = (float)(1.0 / (1.0 - p));
+  np.drop_seed = seed;
+  np.drop_offset = offset;
+}
 
 // Score constants of the tensor-core epilogues (w = -log2(e) z form).
 void set_score_constants(AttnParams& p) {
@@ -271,6 +284,7 @@ hstu_status_t hstu_attn_fwd(const hstu_attn_desc* d, const hstu_attn_fwd_args* a
       np.dtype = (d->flags & HSTU_FLAG_U_FP32) ? HSTU_FP32 : d->dtype; np.out_dtype = d->out_dtype;
       np.o = a->o; np.u = a->u; np.y = a->y; np.mean = a->ln_mean; np.rstd = a->ln_rstd;
       np.T = d->total_tokens; np.F = d->H * d->d_v; np.norm = d->norm; np.eps = d->ln_eps;
+      set_dropout(np, d, a->dropout_seed, a->dropout_offset);
       HSTU_CUDA_TRY(launch_norm_gate_fwd(np, st));
       ++g_launches;
     }
@@ -332,6 +346,7 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
     np.split = tc ? 1 : 0;
     np.dO_lo = ws + L.dO + sizeof(__nv_bfloat16) * rows * (size_t)d->d_v;
     np.T = d->total_tokens; np.F = d->H * d->d_v; np.norm = d->norm; np.eps = d->ln_eps;
+    set_dropout(np, d, a->dropout_seed, a->dropout_offset);
     if (fused_zero) {  // d_qk == d_v and H * d_qk % 4 == 0 on this path
       np.zero_rows = dq_acc; np.zero_F = d->H * d->d_qk;
       np.zero_a = a->d_rab_pos; np.zero_a_n = a->d_rab_pos ? d->H * d->num_pos_buckets : 0;
@@ -378,6 +393,7 @@ hstu_status_t hstu_attn_fwd_delta(const hstu_attn_desc* d, const hstu_attn_delta
   hstu_status_t s = check_desc(d);
   if (s != HSTU_OK) return s;
   if (!a || !a->cand_offsets || !a->cache_offsets || a->cache_tokens < 0) return HSTU_ERR_INVALID_ARG;
+  if (d->dropout_p > 0.f) return HSTU_ERR_UNSUPPORTED;  // inference: no dropout
   if (d->total_tokens > 0 && (!a->q || !a->k || !a->v || !a->o)) return HSTU_ERR_INVALID_ARG;
   if (d->total_tokens > 0 && a->cache_tokens > 0 && (!a->k_cache || !a->v_cache)) return HSTU_ERR_INVALID_ARG;
   if (a->cache_tokens > 0 && (a->cand_timestamps == nullptr) != (a->cache_timestamps == nullptr))

@@ -94,6 +94,12 @@ struct NormParams {
   int zero_a_n;
   float* zero_b;
   int zero_b_n;
+  // fused dropout on y (forward) / dy (backward): keep iff the element's
+  // Philox4x64-10 word >= drop_thr, kept values times drop_scale
+  int drop;
+  uint32_t drop_thr;
+  float drop_scale;
+  uint64_t drop_seed, drop_offset;
   int64_t T;
   int F;           // H * d_v
   int norm;

@@ -291,6 +291,7 @@ hstu_status_t hstu_layer_fwd(const hstu_attn_desc* d, const hstu_layer_fwd_args*
   fa.timestamps = a->timestamps; fa.rab_pos = a->rab_pos; fa.rab_time = a->rab_time;
   fa.u = a->u; fa.v = vqk; fa.q = vqk + TD; fa.k = vqk + 2 * TD;
   fa.o = a->o; fa.y = a->y;
+  fa.dropout_seed = a->dropout_seed; fa.dropout_offset = a->dropout_offset;
   const hstu_attn_desc ad = attn_desc(d);
   s = hstu_attn_fwd(&ad, &fa, ws + L.attn, L.attn_bytes, stream);
   if (s != HSTU_OK) return s;
@@ -376,6 +377,7 @@ hstu_status_t hstu_layer_bwd(const hstu_attn_desc* d, const hstu_layer_bwd_args*
   ba.o = a->o; ba.dy = dy;
   ba.du = grads; ba.dv = grads + TD; ba.dq = grads + 2 * TD; ba.dk = grads + 3 * TD;
   ba.d_rab_pos = a->d_rab_pos; ba.d_rab_time = a->d_rab_time;
+  ba.dropout_seed = a->dropout_seed; ba.dropout_offset = a->dropout_offset;
   const hstu_attn_desc ad = attn_desc(d);
   s = hstu_attn_bwd(&ad, &ba, ws + L.attn, L.attn_bytes, stream);
   if (s != HSTU_OK) return s;

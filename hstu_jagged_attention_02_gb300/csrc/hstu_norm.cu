@@ -10,6 +10,12 @@
 // Lane l of the warp owns features (r * 32 + l) * VEC + [0, VEC) for
 // r < PER: with VEC = 4 every access is a 16-byte (FP32) or 8-byte (BF16)
 // vector and a warp touches 512 / 256 contiguous bytes per access.
+//
+// Fused dropout (ai6s.net survey, section 2.1.3: dropout fused with its
+// neighbouring operators): y = dropout(Norm(o) * u), and in the backward dy
+// passes the same mask and scale.  Element e = t F + f is kept iff 32-bit
+// word e & 7 of Philox4x64-10(counter (e >> 3, offset, 0, 0), key (seed, 0))
+// is at least floor(p 2^32); no mask is stored.
 #include "hstu_internal.h"
 
 namespace hstu {
@@ -50,6 +56,54 @@ template <> struct Vec<4> {
     *reinterpret_cast<uint2*>(p) = x;
   }
 };
+
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC 2011): ten rounds, each multiplying counter words 0
+// and 2 by the round constants (128-bit products) and crossing the halves
+// with words 1, 3 and the key; the key advances by the Weyl increments
+// between rounds.
+__device__ __forceinline__ void philox4x64_10(uint64_t (&c)[4], uint64_t k0, uint64_t k1) {
+  constexpr uint64_t kM0 = 0xD2E7470EE14C6C93ull, kM1 = 0xCA5A826395121157ull;
+  constexpr uint64_t kW0 = 0x9E3779B97F4A7C15ull, kW1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += kW0;
+      k1 += kW1;
+    }
+    const uint64_t hi0 = __umul64hi(kM0, c[0]), lo0 = kM0 * c[0];
+    const uint64_t hi1 = __umul64hi(kM1, c[2]), lo1 = kM1 * c[2];
+    const uint64_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+  }
+}
+
+// Dropout factors (scale or 0) of the VEC elements at flat indices e0 ..
+// e0 + VEC - 1; with VEC = 4, e0 % 4 == 0, so all four share one generator
+// block and take words (e0 & 4) .. (e0 & 4) + 3.
+template <int VEC>
+__device__ __forceinline__ void dropout_factors(const NormParams& p, uint64_t e0, float (&m)[VEC]) {
+  uint64_t c[4] = {e0 >> 3, p.drop_offset, 0ull, 0ull};
+  philox4x64_10(c, p.drop_seed, 0ull);
+  uint32_t w[VEC];
+  if constexpr (VEC == 4) {
+    const bool up = (e0 & 4) != 0;
+    const uint64_t a = up ? c[2] : c[0], b = up ? c[3] : c[1];
+    w[0] = (uint32_t)a;
+    w[1] = (uint32_t)(a >> 32);
+    w[2] = (uint32_t)b;
+    w[3] = (uint32_t)(b >> 32);
+  } else {
+    const int k = (int)(e0 & 7);
+    const uint64_t a = k < 2 ? c[0] : (k < 4 ? c[1] : (k < 6 ? c[2] : c[3]));
+    w[0] = (k & 1) ? (uint32_t)(a >> 32) : (uint32_t)a;
+  }
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) m[i] = w[i] >= p.drop_thr ? p.drop_scale : 0.f;
+}
 
 // feature index of element e of chunk r of this lane
 template <int VEC>
@@ -111,6 +165,12 @@ __global__ void __launch_bounds__(kWarps * 32) norm_gate_fwd_kernel(NormParams p
         for (int e = 0; e < VEC; ++e) g[e] = 1.f;
 #pragma unroll
       for (int e = 0; e < VEC; ++e) out[e] = (x[r][e] - mean) * rstd * g[e];
+      if (p.drop) {
+        float m[VEC];
+        dropout_factors<VEC>(p, (uint64_t)t * F + f, m);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) out[e] *= m[e];
+      }
       Vec<VEC>::store(y + f, out);
     }
   }
@@ -162,6 +222,12 @@ __global__ void __launch_bounds__(kWarps * 32) norm_gate_bwd_kernel(NormParams p
     }
     float d[VEC], uu[VEC], dun[VEC];
     Vec<VEC>::load(dy + f, d);
+    if (p.drop) {  // dy is the gradient of the dropped-out y
+      float m[VEC];
+      dropout_factors<VEC>(p, (uint64_t)t * F + f, m);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) d[e] *= m[e];
+    }
     if (u) Vec<VEC>::load(u + f, uu);
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {

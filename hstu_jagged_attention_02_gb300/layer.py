@@ -14,7 +14,8 @@ class LayerProblem:
     """Device copies of a synth.layer batch (x, w1, w2, dout, offsets,
     timestamps, bias tables) plus every output and the workspace."""
 
-    def __init__(self, batch, device="cuda", want_drab: bool = True):
+    def __init__(self, batch, device="cuda", want_drab: bool = True, dropout=None):
+        # dropout: None or (p, seed, offset) of the fused dropout on y
         self.batch = batch
         dev = torch.device(device)
         self.dev = dev
@@ -59,18 +60,20 @@ class LayerProblem:
             max_seq_len=batch.max_seq_len, alpha=batch.alpha,
             num_pos_buckets=batch.rab_pos.shape[1] if batch.rab_pos is not None else 128,
             num_time_buckets=batch.rab_time.shape[1] if batch.rab_time is not None else 64,
-            norm=batch.norm, ln_eps=batch.eps)
+            norm=batch.norm, ln_eps=batch.eps, dropout_p=0.0 if dropout is None else float(dropout[0]))
+        drop = (0, 0) if dropout is None else (int(dropout[1]), int(dropout[2]))
         fwd_b, bwd_b = C.hstu_layer_workspace_size(self.desc)
         self.ws_bytes = max(fwd_b, bwd_b if self.backward_enabled else 0)
         self.ws = torch.empty(self.ws_bytes, device=dev, dtype=torch.uint8)
         common = (_ptr(self.offsets), _ptr(self.num_targets), _ptr(self.num_contexts), _ptr(self.timestamps),
                   _ptr(self.rab_pos), _ptr(self.rab_time), _ptr(self.x), _ptr(self.w1), _ptr(self.w2))
         self.fwd_args = C.hstu_layer_fwd_args(*common, _ptr(self.out), _ptr(self.z1), _ptr(self.u),
-                                              _ptr(self.vqk), _ptr(self.o), _ptr(self.y))
+                                              _ptr(self.vqk), _ptr(self.o), _ptr(self.y), *drop)
         if self.backward_enabled:
             self.bwd_args = C.hstu_layer_bwd_args(
                 *common, _ptr(self.z1), _ptr(self.u), _ptr(self.vqk), _ptr(self.o), _ptr(self.y), _ptr(self.dout),
-                _ptr(self.dx), _ptr(self.dw1), _ptr(self.dw2), _ptr(self.d_rab_pos), _ptr(self.d_rab_time))
+                _ptr(self.dx), _ptr(self.dw1), _ptr(self.dw2), _ptr(self.d_rab_pos), _ptr(self.d_rab_time),
+                *drop)
 
     def forward(self, stream=None):
         C.hstu_layer_fwd(self.desc, self.fwd_args, self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))

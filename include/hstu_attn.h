@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define HSTU_ATTN_ABI_VERSION 1
+#define HSTU_ATTN_ABI_VERSION 2
 
 typedef struct CUstream_st* hstu_stream_t; /* same type as cudaStream_t; NULL = legacy default stream */
 
@@ -100,7 +100,25 @@ typedef struct {
   int32_t norm;             /* hstu_norm_t */
   float ln_eps;             /* LayerNorm epsilon (1e-5) */
   uint32_t flags;           /* HSTU_FLAG_* */
+  float dropout_p;          /* fused dropout on y, 0 <= p < 1 (0: none); see below */
+  uint32_t reserved;        /* must be 0 */
 } hstu_attn_desc;
+
+/* Fused dropout (ai6s.net survey, section 2.1.3, "memory optimisation":
+ * dropout fused with its neighbouring operators).  With dropout_p = p > 0
+ * the forward's y becomes dropout(Norm(o) * u) and the backward takes dy as
+ * the gradient of that dropped-out y.  The keep decision of element (t, f)
+ * of the [T, F] output (F = H * d_v) comes from the counter-based generator
+ * Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC 2011):
+ *
+ *   e = t F + f;  r = Philox4x64-10(counter (e >> 3, dropout_offset, 0, 0),
+ *                                   key (dropout_seed, 0))
+ *   w = 32-bit word (e & 7) of r[0..3] (low half of each 64-bit word first)
+ *   keep iff w >= floor(p 2^32); kept elements are multiplied by 1 / (1 - p)
+ *
+ * so the backward regenerates the forward's mask from the same seed and
+ * offset (a caller advances the offset, or changes the seed, per step).  The
+ * mask does not depend on the batch's split into sequences. */
 
 typedef struct {
   const int64_t* seq_offsets;  /* [B+1], non-decreasing, seq_offsets[0] == 0 */
@@ -117,6 +135,8 @@ typedef struct {
   void* y;                     /* out [T, H*d_v]: Norm(o) * u, or NULL (not produced) */
   float* ln_mean;              /* out [T] or NULL: per-token mean of o (LAYERNORM) */
   float* ln_rstd;              /* out [T] or NULL: per-token 1/sqrt(var + eps) (LAYERNORM) */
+  uint64_t dropout_seed;       /* fused dropout (desc->dropout_p > 0): generator key */
+  uint64_t dropout_offset;     /* and counter word 1 */
 } hstu_attn_fwd_args;
 
 typedef struct {
@@ -140,6 +160,8 @@ typedef struct {
   void* du;                    /* [T, H*d_v]; required iff u != NULL */
   float* d_rab_pos;            /* [H, P] or NULL (not wanted) */
   float* d_rab_time;           /* [H, Tb] or NULL */
+  uint64_t dropout_seed;       /* the forward's dropout seed and offset */
+  uint64_t dropout_offset;
 } hstu_attn_bwd_args;
 
 /* Workspace bytes the forward and the backward need for this descriptor
@@ -243,7 +265,9 @@ typedef struct {
   float* u;                    /* out [T, D] FP32: the gate U */
   void* vqk;                   /* out [3, T, D] BF16: V, Q, K, each [T, H, d] */
   void* o;                     /* out [T, D] FP32: A.V, kept for the backward */
-  void* y;                     /* out [T, D] FP32: Norm(o) * U */
+  void* y;                     /* out [T, D] FP32: Norm(o) * U (dropped out when desc->dropout_p > 0) */
+  uint64_t dropout_seed;       /* fused dropout on y, as hstu_attn_fwd_args */
+  uint64_t dropout_offset;
 } hstu_layer_fwd_args;
 
 typedef struct {
@@ -267,6 +291,8 @@ typedef struct {
   float* dw2;                  /* out [D, D]: y^T dout */
   float* d_rab_pos;            /* out [H, P] or NULL */
   float* d_rab_time;           /* out [H, Tb] or NULL */
+  uint64_t dropout_seed;       /* the forward's dropout seed and offset */
+  uint64_t dropout_offset;
 } hstu_layer_bwd_args;
 
 /* Workspace bytes of hstu_layer_fwd / hstu_layer_bwd (256-byte aligned
@@ -303,8 +329,8 @@ hstu_status_t hstu_layer_bwd(const hstu_attn_desc* desc, const hstu_layer_bwd_ar
  * The descriptor is hstu_attn_fwd's with total_tokens = T_cand (candidates
  * in the batch); max_seq_len = N must bound every L_b + m_b.  Workspace: the
  * forward size from hstu_attn_workspace_size.  Tensor-core path only: BF16,
- * d_qk = d_v in {64, 128}, T_cand >= 128 and T_cache == 0 or >= 128, else
- * HSTU_ERR_UNSUPPORTED.  Offsets inconsistent with the counts are reported
+ * d_qk = d_v in {64, 128}, T_cand >= 128 and T_cache == 0 or >= 128, and no
+ * dropout (inference), else HSTU_ERR_UNSUPPORTED.  Offsets inconsistent with the counts are reported
  * through the workspace error word (HSTU_ERR_DEVICE_CHECK).
  * ------------------------------------------------------------------------ */
 typedef struct {

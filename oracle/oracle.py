@@ -326,14 +326,15 @@ def bf16_round(a):
     return np.ldexp(np.round(m * 256.0) / 256.0, e)   # np.round: half to even
 
 
-def layer_forward(b, rows=None, act_dtype=None):
+def layer_forward(b, rows=None, act_dtype=None, dropout=None):
     """Full HSTU layer forward in float64: dict with z1, u, v, q, k, o, y, out.
 
     act_dtype="bf16" rounds the values a BF16 layer stores once: V, Q and
     K = SiLU(X W1) are rounded to bfloat16 before the attention.  The gate U
     and Y (which such a layer carries at about 16 bits) are not rounded.
     rows (bool [T]) restricts o, y and out to those rows (the others are
-    zero); z1 and the U/V/Q/K split are always complete."""
+    zero); z1 and the U/V/Q/K split are always complete.  dropout = (p, seed,
+    offset) applies the fused dropout to y (before y W2)."""
     rnd = bf16_round if act_dtype == "bf16" else (lambda a: a)
     x, w1, w2 = _f64(b.x), _f64(b.w1), _f64(b.w2)
     z1 = x @ w1
@@ -343,15 +344,18 @@ def layer_forward(b, rows=None, act_dtype=None):
                  b.timestamps, b.rab_pos, b.rab_time)
     o = attn_fwd(pb, rows)
     y, mean, rstd = norm_gate(o, u, "layernorm", b.eps, rows)
+    if dropout is not None:
+        y = apply_dropout(y, *dropout, rows=rows)
     y_op = y
     out = x + y_op @ w2
     if rows is not None:
         out[~np.asarray(rows, bool)] = 0.0
     return {"z1": z1, "u": u, "v": pb.v, "q": pb.q, "k": pb.k, "o": o, "y": y, "out": out,
-            "mean": mean, "rstd": rstd, "pb": pb, "y_op": y_op, "act_dtype": act_dtype, "rows": rows}
+            "mean": mean, "rstd": rstd, "pb": pb, "y_op": y_op, "act_dtype": act_dtype, "rows": rows,
+            "dropout": dropout}
 
 
-def layer_backward(b, fwd=None, act_dtype=None, rows=None):
+def layer_backward(b, fwd=None, act_dtype=None, rows=None, dropout=None):
     """Full HSTU layer backward given d(out) = b.dout: dict with dx, dw1, dw2
     and the attention intermediates dq, dk, dv, du, d_rab_pos, d_rab_time.
 
@@ -364,12 +368,14 @@ def layer_backward(b, fwd=None, act_dtype=None, rows=None):
     for every row whose key is attended only by queries inside rows (the
     candidate rows and the last history row of a sequence, when rows holds
     all the candidates of that sequence), because dO is formed on rows only."""
-    f = layer_forward(b, rows=rows, act_dtype=act_dtype) if fwd is None else fwd
+    f = layer_forward(b, rows=rows, act_dtype=act_dtype, dropout=dropout) if fwd is None else fwd
     rnd = bf16_round if act_dtype == "bf16" else (lambda a: a)
     x, w1, w2, dout = _f64(b.x), _f64(b.w1), _f64(b.w2), _f64(b.dout)
     dout_op = rnd(dout)
     dw2 = f["y_op"].T @ dout_op if rows is None else None
     dy = dout_op @ w2.T
+    if f.get("dropout") is not None:
+        dy = apply_dropout(dy, *f["dropout"], rows=rows)
     dO, du = norm_gate_bwd(f["o"], f["u"], dy, "layernorm", b.eps, rows)
     dq, dk, dv, drp, drt = attn_bwd(f["pb"], dO, q_rows=rows, kv_rows=rows)
     T = x.shape[0]

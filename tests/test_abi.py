@@ -65,6 +65,9 @@ def _desc(**kw):
     (dict(flags=1 << 20), C.HSTU_ERR_INVALID_ARG),
     (dict(num_pos_buckets=0), C.HSTU_ERR_INVALID_ARG),
     (dict(max_seq_len=10**7), C.HSTU_ERR_UNSUPPORTED),
+    (dict(dropout_p=1.0), C.HSTU_ERR_INVALID_ARG),
+    (dict(dropout_p=-0.25), C.HSTU_ERR_INVALID_ARG),
+    (dict(dropout_p=float("nan")), C.HSTU_ERR_INVALID_ARG),
 ])
 def test_descriptor_validation(kw, status):
     with pytest.raises(C.HSTUError) as e:
@@ -148,3 +151,27 @@ def test_delta_rejects_missing_pointers_before_any_launch():
     with pytest.raises(C.HSTUError) as e:
         C.hstu_attn_fwd_delta(d, args, 256, 1 << 30, None)
     assert e.value.status == C.HSTU_ERR_INVALID_ARG
+
+
+def test_dropout_descriptor_fields():
+    f0, b0 = C.hstu_attn_workspace_size(_desc())
+    assert C.hstu_attn_workspace_size(_desc(dropout_p=0.5)) == (f0, b0)   # no stored mask
+    d = _desc(dropout_p=0.1)
+    d.reserved = 1
+    with pytest.raises(C.HSTUError) as e:
+        C.hstu_attn_workspace_size(d)
+    assert e.value.status == C.HSTU_ERR_INVALID_ARG
+    # the seed and offset sit after the pointers of every argument struct
+    for cls in (C.hstu_attn_fwd_args, C.hstu_attn_bwd_args, C.hstu_layer_fwd_args, C.hstu_layer_bwd_args):
+        names = [n for n, _ in cls._fields_]
+        assert names[-2:] == ["dropout_seed", "dropout_offset"], cls
+        assert cls.dropout_seed.offset == 8 * (len(names) - 2)
+
+
+def test_delta_rejects_dropout():
+    d = _desc(out_dtype="fp32", total_tokens=256, dropout_p=0.1)
+    args = C.hstu_attn_delta_args()
+    args.cand_offsets = args.cache_offsets = 256
+    with pytest.raises(C.HSTUError) as e:
+        C.hstu_attn_fwd_delta(d, args, 256, 1 << 30, None)
+    assert e.value.status == C.HSTU_ERR_UNSUPPORTED

@@ -354,14 +354,15 @@ def _tiny_layer(seed=30):
                        dout=r.standard_normal((T, D)))
 
 
-def test_layer_backward_central_differences():
+@pytest.mark.parametrize("dropout", [None, (0.3, 12, 4)])
+def test_layer_backward_central_differences(dropout):
     b = _tiny_layer()
-    g = O.layer_backward(b)
+    g = O.layer_backward(b, dropout=dropout)
     r = np.random.default_rng(31)
     h = 1e-6
 
     def loss(bb):
-        return float((O.layer_forward(bb)["out"] * bb.dout).sum())
+        return float((O.layer_forward(bb, dropout=dropout)["out"] * bb.dout).sum())
 
     import copy
     for key, gk in (("x", "dx"), ("w1", "dw1"), ("w2", "dw2"), ("rab_pos", "d_rab_pos"),
