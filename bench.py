@@ -167,13 +167,17 @@ class AttentionWorkload:
     metric = METRIC
     description = WORKLOAD
     n_batches = N_SEEDS
+    dropout_p = 0.0   # --dropout: the fused dropout on y (fixed seed and offset)
+
+    def dropout(self):
+        return None if not self.dropout_p else (self.dropout_p, 20240601, 0)
 
     def batches(self, rank):
         return [synth.heavy_tailed(rank * N_SEEDS + s) for s in range(N_SEEDS)]
 
     def problem(self, b, dev):
         from hstu_jagged_attention_02_gb300.attention import Problem
-        return Problem(b, device=dev, out_dtype="fp32")
+        return Problem(b, device=dev, out_dtype="fp32", dropout=self.dropout())
 
     def flops(self, b):
         """(attention fwd, attention bwd, whole step) useful FLOPs."""
@@ -193,7 +197,8 @@ class AttentionWorkload:
 
     def oracle_step(self, b):
         from oracle import oracle as O
-        O.backward(b, o=O.forward(b)["o"])
+        d = self.dropout()
+        O.backward(b, o=O.forward(b, dropout=d)["o"], dropout=d)
 
     def cpu_samples(self, batches):
         return [sub_batch(b, 16) for b in batches], "fwd+bwd of the first 16 of the 64 sequences of a batch"
@@ -219,7 +224,7 @@ class LayerWorkload(AttentionWorkload):
 
     def problem(self, b, dev):
         from hstu_jagged_attention_02_gb300.layer import LayerProblem
-        return LayerProblem(b, device=dev)
+        return LayerProblem(b, device=dev, dropout=self.dropout())
 
     def flops(self, b):
         f, bw = useful_flops(b)
@@ -235,7 +240,7 @@ class LayerWorkload(AttentionWorkload):
 
     def oracle_step(self, b):
         from oracle import oracle as O
-        O.layer_backward(b)
+        O.layer_backward(b, dropout=self.dropout())
 
     def cpu_samples(self, batches):
         return ([synth.layer(100 + s, n_lo=1024, n_hi=1024, B=1) for s in range(2)],
@@ -483,6 +488,8 @@ def run_gpu(args, wl, rank, world, local_rank):
                "sample": f"{used} x {what}", "seconds": cdt}
     cfg = {"workload": wl.description}
     cfg.update(wl.config())
+    if wl.dropout_p:
+        cfg["dropout_p"] = wl.dropout_p
     cfg.update({"per_rank_batches": nb, "mean_tokens_per_batch": float(np.mean([b.T for b in batches]))})
     line = {"metric": wl.metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
@@ -553,8 +560,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="heavy_tailed", choices=sorted(WORKLOADS),
                     help="heavy_tailed attention (the default line) or the full layer")
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="fused dropout probability on y (heavy_tailed and layer workloads)")
     args = ap.parse_args()
     wl = WORKLOADS[args.workload]()
+    if args.dropout:
+        if not wl.has_backward:
+            ap.error("--dropout applies to training workloads only")
+        wl.dropout_p = args.dropout
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

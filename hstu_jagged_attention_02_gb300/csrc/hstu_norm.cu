@@ -105,6 +105,43 @@ __device__ __forceinline__ void dropout_factors(const NormParams& p, uint64_t e0
   for (int i = 0; i < VEC; ++i) m[i] = w[i] >= p.drop_thr ? p.drop_scale : 0.f;
 }
 
+// Dropout factors of every chunk of this lane's row t (the lane layout of
+// feat()).  With VEC = 4 the chunks r of lanes 2i and 2i + 1 share one
+// generator block (elements t F + 128 r + 8 i + [0, 8)); when PER is even,
+// lane 2i computes the blocks of the even chunks and lane 2i + 1 those of
+// the odd ones, and each hands its partner the partner's half: one
+// generator call per lane per two chunks.
+template <int VEC, int PER>
+__device__ __forceinline__ void dropout_row(const NormParams& p, int64_t t, int F, float (&m)[PER][VEC]) {
+  const int lane = threadIdx.x & 31;
+  if constexpr (VEC == 4 && PER % 2 == 0) {
+    const int q = lane & 1;
+#pragma unroll
+    for (int r = 0; r < PER; r += 2) {
+      uint64_t c[4] = {((uint64_t)t * F + (uint64_t)(r + q) * 128 + (uint64_t)(lane >> 1) * 8) >> 3,
+                       p.drop_offset, 0ull, 0ull};
+      philox4x64_10(c, p.drop_seed, 0ull);
+      // words 0..3 of the block serve the even lane, 4..7 the odd one
+      const uint64_t mine0 = q ? c[2] : c[0], mine1 = q ? c[3] : c[1];
+      const uint64_t give0 = q ? c[0] : c[2], give1 = q ? c[1] : c[3];
+      const uint64_t got0 = __shfl_xor_sync(0xffffffffu, give0, 1);
+      const uint64_t got1 = __shfl_xor_sync(0xffffffffu, give1, 1);
+      // own block is chunk r + q; the partner's is chunk r + 1 - q
+      const uint64_t w[2][2] = {{q ? got0 : mine0, q ? got1 : mine1}, {q ? mine0 : got0, q ? mine1 : got1}};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t x[4] = {(uint32_t)w[h][0], (uint32_t)(w[h][0] >> 32), (uint32_t)w[h][1],
+                               (uint32_t)(w[h][1] >> 32)};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m[r + h][i] = x[i] >= p.drop_thr ? p.drop_scale : 0.f;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int r = 0; r < PER; ++r) dropout_factors<VEC>(p, (uint64_t)t * F + (uint64_t)(r * 32 + lane) * VEC, m[r]);
+  }
+}
+
 // feature index of element e of chunk r of this lane
 template <int VEC>
 __device__ __forceinline__ int feat(int r, int lane) { return (r * 32 + lane) * VEC; }
@@ -154,6 +191,8 @@ __global__ void __launch_bounds__(kWarps * 32) norm_gate_fwd_kernel(NormParams p
   if (p.norm == HSTU_NORM_LAYERNORM) row_stats<VEC, PER>(x, F, p.eps, mean, rstd);
   if (p.y) {
     TO* y = static_cast<TO*>(p.y) + t * F;
+    float m[PER][VEC];
+    if (p.drop) dropout_row<VEC, PER>(p, t, F, m);
 #pragma unroll
     for (int r = 0; r < PER; ++r) {
       const int f = feat<VEC>(r, lane);
@@ -165,12 +204,9 @@ __global__ void __launch_bounds__(kWarps * 32) norm_gate_fwd_kernel(NormParams p
         for (int e = 0; e < VEC; ++e) g[e] = 1.f;
 #pragma unroll
       for (int e = 0; e < VEC; ++e) out[e] = (x[r][e] - mean) * rstd * g[e];
-      if (p.drop) {
-        float m[VEC];
-        dropout_factors<VEC>(p, (uint64_t)t * F + f, m);
+      if (p.drop)
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) out[e] *= m[e];
-      }
+        for (int e = 0; e < VEC; ++e) out[e] *= m[r][e];
       Vec<VEC>::store(y + f, out);
     }
   }
@@ -212,6 +248,8 @@ __global__ void __launch_bounds__(kWarps * 32) norm_gate_bwd_kernel(NormParams p
   if (ln) row_stats<VEC, PER>(x, F, p.eps, mean, rstd);
   float mg = 0.f, mgx = 0.f;
   TO* du = p.du ? static_cast<TO*>(p.du) + t * F : nullptr;
+  float m[PER][VEC];
+  if (p.drop) dropout_row<VEC, PER>(p, t, F, m);
 #pragma unroll
   for (int r = 0; r < PER; ++r) {
     const int f = feat<VEC>(r, lane);
@@ -222,12 +260,9 @@ __global__ void __launch_bounds__(kWarps * 32) norm_gate_bwd_kernel(NormParams p
     }
     float d[VEC], uu[VEC], dun[VEC];
     Vec<VEC>::load(dy + f, d);
-    if (p.drop) {  // dy is the gradient of the dropped-out y
-      float m[VEC];
-      dropout_factors<VEC>(p, (uint64_t)t * F + f, m);
+    if (p.drop)  // dy is the gradient of the dropped-out y
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) d[e] *= m[e];
-    }
+      for (int e = 0; e < VEC; ++e) d[e] *= m[r][e];
     if (u) Vec<VEC>::load(u + f, uu);
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
