@@ -414,6 +414,35 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, false, true);
       uint32_t kv_it = 0, q_it = 0, o_it = 0;
       bool ok = true;
+      // The P.V of the latest S tile is issued after the next S tile, of the
+      // same item or of the next one, so the tensor core computes S(t + 1)
+      // while the epilogue scores tile t, also across items.  The tile that
+      // closes an item commits the item's Q buffer and O buffer with it.
+      struct PendPV {
+        bool have, first, last;
+        uint32_t it, ocol, ob, qb;
+      };
+      PendPV pend{false, false, false, 0, 0, 0, 0};
+      // P of tile t: quarter k/2 of the S buffer, hi at [32 q, 32 q + 16), lo 16 columns later
+      auto issue_pv = [&](const PendPV& pv) -> bool {
+        const uint32_t sb = pv.it & 1, stage = pv.it % kStages;
+        if (!mbar_wait(bar(BAR_PREADY + sb), (pv.it >> 1) & 1, wd, 5)) return false;
+        fence_after_sync();
+        const uint32_t vbase = sKV + stage * L::STAGE + L::K_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint32_t a_hi = tmem + sb * kSColStride + 32u * (kk >> 1) + 8u * (kk & 1);
+          const uint64_t bd = sdesc_sw128(vbase + kk * 2048, L::BOX, 1024);
+          mma_ts(tmem + pv.ocol, a_hi, bd, IDESC_PV, (pv.first && kk == 0) ? 0u : 1u);
+          mma_ts(tmem + pv.ocol, a_hi + 16, bd, IDESC_PV, 1u);
+        }
+        mma_commit(bar(BAR_KVEMPTY + stage));
+        if (pv.last) {
+          mma_commit(bar(BAR_QEMPTY + pv.qb));
+          mma_commit(bar(BAR_OFULL + pv.ob));
+        }
+        return true;
+      };
       while (ok) {
         const uint32_t qb = q_it % kQBufs;
         ok = mbar_wait(bar(BAR_QFULL + qb), (q_it / kQBufs) & 1, wd, 3);
@@ -424,29 +453,8 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         const uint32_t sQ = sQ0 + qb * L::Q_BYTES;
         const uint32_t ob = o_it & 1;
         const uint32_t ocol = ob ? L::O_COL1 : L::O_COL0;
-        ok = mbar_wait(bar(BAR_OEMPTY + ob), ((o_it >> 1) & 1) ^ 1, wd, 4);
-        if (!ok) break;
-        fence_after_sync();
-        bool have_prev = false, first_pv = true;
-        uint32_t prev_it = 0;
+        bool first = true;
         const int nkb = DELTA ? (sl.L + BN - 1) / BN + 1 : fwd_kv_blocks(sl.q0, sl.n, sl.c, BM, BN);
-        // P of tile t: quarter k/2 of the S buffer, hi at [32 q, 32 q + 16), lo 16 columns later
-        auto issue_pv = [&](uint32_t t) -> bool {
-          const uint32_t sb = t & 1, stage = t % kStages;
-          if (!mbar_wait(bar(BAR_PREADY + sb), (t >> 1) & 1, wd, 5)) return false;
-          fence_after_sync();
-          const uint32_t vbase = sKV + stage * L::STAGE + L::K_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint32_t a_hi = tmem + sb * kSColStride + 32u * (kk >> 1) + 8u * (kk & 1);
-            const uint64_t bd = sdesc_sw128(vbase + kk * 2048, L::BOX, 1024);
-            mma_ts(tmem + ocol, a_hi, bd, IDESC_PV, (first_pv && kk == 0) ? 0u : 1u);
-            mma_ts(tmem + ocol, a_hi + 16, bd, IDESC_PV, 1u);
-          }
-          first_pv = false;
-          mma_commit(bar(BAR_KVEMPTY + stage));
-          return true;
-        };
         for (int kb = 0; ok && kb < nkb; ++kb) {
           const int k0 = kb * BN;
           if (!DELTA && tile_class(sl.q0, k0, BM, BN, sl.n, sl.c, sl.h_end) == 0) continue;
@@ -462,18 +470,32 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
                    IDESC_S, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(BAR_SFULL + sb));
-          if (have_prev) ok = issue_pv(prev_it);
-          have_prev = true;
-          prev_it = kv_it;
+          if (pend.have) {
+            ok = issue_pv(pend);
+            if (!ok) break;
+          }
+          if (first) {  // this item's P.V go into O buffer ob once the epilogue has written it out
+            ok = mbar_wait(bar(BAR_OEMPTY + ob), ((o_it >> 1) & 1) ^ 1, wd, 4);
+            if (!ok) break;
+            fence_after_sync();
+          }
+          pend = PendPV{true, first, false, kv_it, ocol, ob, qb};
+          first = false;
           ++kv_it;
         }
-        if (ok && have_prev) ok = issue_pv(prev_it);
         if (!ok) break;
-        mma_commit(bar(BAR_QEMPTY + qb));
-        mma_commit(bar(BAR_OFULL + ob));
+        if (first) {  // an item without tiles (none is planned): release its buffers as they are
+          ok = mbar_wait(bar(BAR_OEMPTY + ob), ((o_it >> 1) & 1) ^ 1, wd, 4);
+          if (!ok) break;
+          mma_commit(bar(BAR_QEMPTY + qb));
+          mma_commit(bar(BAR_OFULL + ob));
+        } else {
+          pend.last = true;
+        }
         ++q_it;
         ++o_it;
       }
+      if (ok && pend.have) ok = issue_pv(pend);   // the last tile of the last item
       // every MMA issued by this thread is complete before TMEM is released
       mma_commit(bar(BAR_DRAIN));
       drain_wait(bar(BAR_DRAIN), 0);
@@ -486,6 +508,53 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     uint32_t kv_it = 0, o_it = 0, q_it = 0;
     bool ok = true;
     RowCtx rc;
+    // An item's O is written out after the next item's first P is handed
+    // over (or when the work runs out), so the epilogue does not wait for the
+    // item's last P.V: what the write-out needs is kept here.
+    bool o_pend = false;
+    uint32_t po_it = 0;
+    int64_t po_row = 0;   // token of this thread's row, or -1
+    int po_h = 0;
+    auto write_o = [&]() -> bool {
+      const uint32_t ob = po_it & 1;
+      if (!mbar_wait(bar(BAR_OFULL + ob), (po_it >> 1) & 1, wd, 9)) return false;
+      fence_after_sync();
+      constexpr int QC = D / 4;  // columns per quarter
+      const uint32_t ocol = lane_base + (ob ? L::O_COL1 : L::O_COL0) + hq * QC;
+      uint32_t ov[32];
+      if constexpr (QC == 32) {
+        tmem_ld32(ocol, ov);
+      } else {
+        uint32_t o16[16];
+        tmem_ld16(ocol, o16);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ov[e] = o16[e];
+      }
+      tmem_wait_ld();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_OEMPTY + ob));
+      if (po_row >= 0) {
+        TO* orow = static_cast<TO*>(p.o) + ((size_t)po_row * H + po_h) * D + hq * QC;
+        if constexpr (sizeof(TO) == 4) {
+          float4* dst = reinterpret_cast<float4*>(orow);
+#pragma unroll
+          for (int e = 0; e < QC / 4; ++e)
+            dst[e] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                                 __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]));
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+          for (int e = 0; e < QC / 8; ++e)
+            dst[e] = make_uint4(pack_bf16(__uint_as_float(ov[8 * e]), __uint_as_float(ov[8 * e + 1])),
+                                pack_bf16(__uint_as_float(ov[8 * e + 2]), __uint_as_float(ov[8 * e + 3])),
+                                pack_bf16(__uint_as_float(ov[8 * e + 4]), __uint_as_float(ov[8 * e + 5])),
+                                pack_bf16(__uint_as_float(ov[8 * e + 6]), __uint_as_float(ov[8 * e + 7])));
+        }
+      }
+      o_pend = false;
+      return true;
+    };
     while (ok) {
       const uint32_t qb = q_it % kQBufs;
       ok = mbar_wait(bar(BAR_QFULL + qb), (q_it / kQBufs) & 1, wd, 10);
@@ -558,49 +627,24 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_PREADY + sb));
         ++kv_it;
-      }
-      if (!ok) break;
-      // O out: this warp's lane quarter, column quarter hq of d
-      const uint32_t ob = o_it & 1;
-      ok = mbar_wait(bar(BAR_OFULL + ob), (o_it >> 1) & 1, wd, 9);
-      if (!ok) break;
-      fence_after_sync();
-      constexpr int QC = D / 4;  // columns per quarter
-      const uint32_t ocol = lane_base + (ob ? L::O_COL1 : L::O_COL0) + hq * QC;
-      uint32_t ov[32];
-      if constexpr (QC == 32) {
-        tmem_ld32(ocol, ov);
-      } else {
-        uint32_t o16[16];
-        tmem_ld16(ocol, o16);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) ov[e] = o16[e];
-      }
-      tmem_wait_ld();
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_OEMPTY + ob));
-      if (rc.row_ok) {
-        TO* orow = static_cast<TO*>(p.o) + ((size_t)(s0 + rc.i) * H + hh) * D + hq * QC;
-        if constexpr (sizeof(TO) == 4) {
-          float4* dst = reinterpret_cast<float4*>(orow);
-#pragma unroll
-          for (int e = 0; e < QC / 4; ++e)
-            dst[e] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
-                                 __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]));
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-          for (int e = 0; e < QC / 8; ++e)
-            dst[e] = make_uint4(pack_bf16(__uint_as_float(ov[8 * e]), __uint_as_float(ov[8 * e + 1])),
-                                pack_bf16(__uint_as_float(ov[8 * e + 2]), __uint_as_float(ov[8 * e + 3])),
-                                pack_bf16(__uint_as_float(ov[8 * e + 4]), __uint_as_float(ov[8 * e + 5])),
-                                pack_bf16(__uint_as_float(ov[8 * e + 6]), __uint_as_float(ov[8 * e + 7])));
+        if (o_pend) {  // the previous item's O, now that this item's first P is out
+          ok = write_o();
+          if (!ok) break;
         }
       }
+      if (!ok) break;
+      if (o_pend) {  // an item without tiles (none is planned)
+        ok = write_o();
+        if (!ok) break;
+      }
+      o_pend = true;
+      po_it = o_it;
+      po_row = rc.row_ok ? s0 + rc.i : -1;
+      po_h = hh;
       ++o_it;
       ++q_it;
     }
+    if (ok && o_pend) ok = write_o();
   }
 
   fence_before_sync();
