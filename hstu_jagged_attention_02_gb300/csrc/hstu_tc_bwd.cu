@@ -396,8 +396,11 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       constexpr uint32_t IDESC_DQ = idesc_bf16(D, BQ, true, true);      // A = K^T, B = dZ^T, MN-major
       uint32_t item_it = 0, qt_it = 0;
       bool ok = true;
-      // dV += A^T dO, dK += dZ^T Q, dQ^T = K^T dZ^T of query tile g (stage st)
-      auto issue_grad = [&](uint32_t g, uint32_t st, bool first) -> bool {
+      // dQ^T = K^T dZ^T, dV += A^T dO, dK += dZ^T Q of query tile g (stage st).
+      // dQ^T goes first: it is the last reader of K, so on an item's last
+      // tile the K/V buffer is released before dV and dK, and the next item's
+      // K/V load overlaps them.  DQFULL still follows all of them.
+      auto issue_grad = [&](uint32_t g, uint32_t st, bool first, bool last) -> bool {
         if (!mbar_wait(bar(BAR_PREADY), g & 1, wd, 26) ||
             !mbar_wait(bar(BAR_DQEMPTY), (g & 1) ^ 1, wd, 27))
           return false;
@@ -405,6 +408,15 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         fence_after_sync();
         const uint32_t sQ = sQS + st * Lay::QSTAGE;
         const uint32_t sDh = sQ + Lay::Q_BYTES, sDl = sQ + 2 * Lay::Q_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {   // K = 128 keys: 8 steps of 16
+          const uint64_t ak = sdesc_sw128(sK + kk * 2048, Lay::KBOX, 1024);
+          mma_ss(tmem + DQ_COL, ak, sdesc_sw128(sDZ + kk * 2048, Lay::DZ_BYTES, 1024), IDESC_DQ,
+                 kk > 0 ? 1u : 0u);
+          mma_ss(tmem + DQ_COL, ak, sdesc_sw128(sDZ + Lay::DZ_BYTES + kk * 2048, Lay::DZ_BYTES, 1024),
+                 IDESC_DQ, 1u);
+        }
+        if (last) mma_commit(bar(BAR_KVEMPTY));   // K and V of this item are read by no later MMA
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {   // K = 64 queries: 4 steps of 16
           const uint32_t a_hi = tmem + A_COL + 16u * kk;
@@ -420,14 +432,8 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           mma_ss(tmem + DK_COL, zh, bq, IDESC_DVK, acc0);
           mma_ss(tmem + DK_COL, zl, bq, IDESC_DVK, 1u);
         }
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {   // K = 128 keys: 8 steps of 16
-          const uint64_t ak = sdesc_sw128(sK + kk * 2048, Lay::KBOX, 1024);
-          mma_ss(tmem + DQ_COL, ak, sdesc_sw128(sDZ + kk * 2048, Lay::DZ_BYTES, 1024), IDESC_DQ,
-                 kk > 0 ? 1u : 0u);
-          mma_ss(tmem + DQ_COL, ak, sdesc_sw128(sDZ + Lay::DZ_BYTES + kk * 2048, Lay::DZ_BYTES, 1024),
-                 IDESC_DQ, 1u);
-        }
+        // the epilogue takes DQFULL to mean every gradient MMA of the tile is
+        // done (A in TMEM and the dZ^T staging are free again)
         mma_commit(bar(BAR_DQFULL));
         mma_commit(bar(BAR_QEMPTY + st));
         return true;
@@ -468,7 +474,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           }
           mma_commit(bar(BAR_SFULL));
           if (have_prev) {
-            ok = issue_grad(prev, prev_st, first);
+            ok = issue_grad(prev, prev_st, first, false);
             first = false;
           }
           have_prev = true;
@@ -476,10 +482,10 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           prev_st = stage;
           ++qt_it;
         }
-        if (ok && have_prev) ok = issue_grad(prev, prev_st, first);
+        if (ok && have_prev) ok = issue_grad(prev, prev_st, first, true);
         if (!ok) break;
+        if (!have_prev) mma_commit(bar(BAR_KVEMPTY));   // an item without tiles (none is planned)
         mma_commit(bar(BAR_DKVFULL));
-        mma_commit(bar(BAR_KVEMPTY));
         ++item_it;
       }
       mma_commit(bar(BAR_DRAIN));
