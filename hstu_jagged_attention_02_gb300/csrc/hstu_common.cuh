@@ -59,6 +59,14 @@ struct __align__(16) PlanItem {
   int L;          // delta forward: cached tokens of the sequence
 };
 
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while its predecessor in the
+// stream still runs; pdl_wait() blocks until the predecessor has completed
+// and its memory is visible (it returns at once without such a predecessor).
+// pdl_launch_dependents() lets the dependent start before this grid ends.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void set_error(int* hdr, int code, int info) {
   if (atomicCAS(hdr + WS_ERR, 0, code) == 0) hdr[WS_ERR_INFO] = info;
 }

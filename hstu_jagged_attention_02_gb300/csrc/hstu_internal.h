@@ -3,6 +3,8 @@
 
 #include <cuda.h>
 
+#include <utility>
+
 #include "hstu_common.cuh"
 
 namespace hstu {
@@ -113,6 +115,26 @@ void set_launch_detail(cudaError_t e, const char* kernel, const void* func, int 
 void set_detail_message(const char* msg);
 // adds n kernels of a composite call (the layer) to hstu_last_launch_count
 void note_launches(int32_t n);
+
+// Launches kernel<<<grid, block, smem, st>>>(args...) with programmatic
+// stream serialization: it may start while the previous kernel in the stream
+// runs, and must call pdl_wait() before it reads that kernel's outputs or
+// writes what that kernel reads.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 cudaError_t launch_debug_tiles(const PlanParams& p, int32_t* rec, int64_t cap, cudaStream_t stream);

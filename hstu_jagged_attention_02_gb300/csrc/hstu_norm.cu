@@ -219,6 +219,11 @@ __global__ void __launch_bounds__(kWarps * 32) norm_gate_fwd_kernel(NormParams p
 // du = xn * dy;  g = dy * u;  LayerNorm: dO = rstd * (g - mean(g) - xn * mean(g xn)); none: dO = g
 template <typename TI, typename TO, int VEC, int PER>
 __global__ void __launch_bounds__(kWarps * 32) norm_gate_bwd_kernel(NormParams p) {
+  // Launched programmatically after the backward's planner, with which it
+  // shares no data: it runs alongside it.  One thread waits for the planner,
+  // so this grid completes only after it (the attention backward, launched
+  // normally after this kernel, reads the plan).
+  if (blockIdx.x == 0 && threadIdx.x == 0) pdl_wait();
   if (blockIdx.x == 0) {
     for (int x = threadIdx.x; x < p.zero_a_n; x += blockDim.x) p.zero_a[x] = 0.f;
     for (int x = threadIdx.x; x < p.zero_b_n; x += blockDim.x) p.zero_b[x] = 0.f;
@@ -312,10 +317,13 @@ __global__ void convert_kernel(const float* __restrict__ src, TO* __restrict__ d
 template <typename TI, typename TO, int VEC, int PER>
 cudaError_t launch_t(const NormParams& p, bool bwd, cudaStream_t st) {
   const int64_t grid = (p.T + kWarps - 1) / kWarps;
-  if (bwd)
-    norm_gate_bwd_kernel<TI, TO, VEC, PER><<<(unsigned)grid, kWarps * 32, 0, st>>>(p);
-  else
+  if (bwd) {
+    const cudaError_t e = launch_pdl(norm_gate_bwd_kernel<TI, TO, VEC, PER>, dim3((unsigned)grid), dim3(kWarps * 32),
+                                     0, st, p);
+    if (e != cudaSuccess) return e;
+  } else {
     norm_gate_fwd_kernel<TI, TO, VEC, PER><<<(unsigned)grid, kWarps * 32, 0, st>>>(p);
+  }
   return cudaGetLastError();
 }
 

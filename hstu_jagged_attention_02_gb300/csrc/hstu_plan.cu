@@ -80,6 +80,9 @@ plan_kernel(PlanParams p) {
   if (p.stage_off) { start = reinterpret_cast<int*>(cur); cur += sizeof(int) * ((p.B + 1 + 3) & ~3); }
   Block* rec = p.stage_rec ? reinterpret_cast<Block*>(cur) : p.tmp;
   const int t = threadIdx.x;
+  // the kernel that follows (launched programmatically) may start its own
+  // set-up now; it waits for this grid before it reads the plan
+  pdl_launch_dependents();
 
   if (t == 0) {
     p.hdr[WS_ERR] = 0;

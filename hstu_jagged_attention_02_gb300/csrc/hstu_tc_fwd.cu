@@ -288,6 +288,9 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // the set-up above reads inputs only; the planner's work list and work
+  // counter are read after it has completed (programmatic launch)
+  pdl_wait();
 
   Watchdog wd;
   wd.abort = abort_flag;
@@ -734,8 +737,9 @@ static cudaError_t launch_fwd_t(const AttnParams& p, cudaStream_t st) {
   }
   const int64_t max_items = ((p.T + BM - 1) / BM + p.B) * (int64_t)p.H;
   const int grid = (int)(max_items < p.num_sms ? max_items : p.num_sms);
-  hstu_fwd_tc_kernel<D, TO, DELTA><<<grid, kThreads, smem, st>>>(p, mq, mk, mv, mk2, mv2);
-  e = cudaGetLastError();
+  // launched programmatically after the planner: the set-up overlaps it
+  e = launch_pdl(hstu_fwd_tc_kernel<D, TO, DELTA>, dim3(grid), dim3(kThreads), smem, st, p, mq, mk, mv, mk2, mv2);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) set_launch_detail(e, "hstu_fwd_tc_kernel", fn, kThreads, smem);
   return e;
 }
