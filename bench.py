@@ -289,8 +289,10 @@ class DeltaWorkload(AttentionWorkload):
         return (4 * (b.T - m) + 10 * m) * b.H * b.d_qk
 
     def host_io(self, pr):
-        ins = [t for t in (pr.cand_offsets, pr.cache_offsets, pr.cand_ts, pr.cache_ts, pr.rab_pos, pr.rab_time,
-                           pr.q, pr.k, pr.v, pr.u, pr.k_cache, pr.v_cache) if t is not None]
+        # the KV cache (cached K, V and their timestamps) is resident device
+        # state between requests; a request uploads its candidates
+        ins = [t for t in (pr.cand_offsets, pr.cache_offsets, pr.cand_ts, pr.rab_pos, pr.rab_time,
+                           pr.q, pr.k, pr.v, pr.u) if t is not None]
         return ins, [pr.o, pr.y]
 
     def oracle_step(self, b):
@@ -506,7 +508,12 @@ def run_gpu(args, wl, rank, world, local_rank):
 def run_e2e(args, wl, probs, flops, stream, world):
     """Same metric through the public C ABI with pinned host buffers: each step
     copies its inputs host -> device, runs forward + backward and copies the
-    results back.  Returns the e2e dict."""
+    results back.  The copies run on two copy streams and overlap the compute
+    of the neighbouring steps, as a training loop's input prefetch and result
+    drain would (each batch has its own device buffers; a step's upload waits
+    until the download of the previous step that used those buffers is done,
+    and its compute waits for its upload).  The timed region runs from before
+    the first upload to after the last download.  Returns the e2e dict."""
     import torch
     nb = len(probs)
     hosts = []
@@ -517,17 +524,32 @@ def run_e2e(args, wl, probs, flops, stream, world):
         hosts.append((ins, h_in, outs, h_out))
     bi = sum(t.numel() * t.element_size() for t in hosts[0][1])
     bo = sum(t.numel() * t.element_size() for t in hosts[0][3])
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    drained = [None] * nb          # event: the last download from batch slot j is done
 
     def one(i):
-        pr = probs[i % nb]
-        ins, h_in, outs, h_out = hosts[i % nb]
-        for d, h in zip(ins, h_in):
-            d.copy_(h, non_blocking=True)
-        pr.forward()
+        j = i % nb
+        pr = probs[j]
+        ins, h_in, outs, h_out = hosts[j]
+        with torch.cuda.stream(up):
+            if drained[j] is not None:
+                up.wait_event(drained[j])
+            for d, h in zip(ins, h_in):
+                d.copy_(h, non_blocking=True)
+            uploaded = torch.cuda.Event()
+            uploaded.record(up)
+        stream.wait_event(uploaded)
+        pr.forward(stream)
         if wl.has_backward:
-            pr.backward()
-        for d, h in zip(outs, h_out):
-            h.copy_(d, non_blocking=True)
+            pr.backward(stream)
+        computed = torch.cuda.Event()
+        computed.record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(computed)
+            for d, h in zip(outs, h_out):
+                h.copy_(d, non_blocking=True)
+            drained[j] = torch.cuda.Event()
+            drained[j].record(down)
 
     for w in range(max(args.warmup, 1)):
         one(w)
@@ -536,8 +558,11 @@ def run_e2e(args, wl, probs, flops, stream, world):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
+    up.wait_stream(stream)
+    down.wait_stream(stream)
     for i in range(k):
         one(i)
+    stream.wait_stream(down)
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
