@@ -149,6 +149,38 @@ def test_wide_timestamp_gaps(dtype, d):
     check(got, run_oracle(b), TOL[dtype])
 
 
+def _with_tables(b, P, Tb, seed):
+    r = np.random.default_rng(seed)
+    b.rab_pos = r.normal(0, 0.02, (b.H, P)).astype(np.float32)
+    b.rab_time = r.normal(0, 0.02, (b.H, Tb)).astype(np.float32)
+    return b
+
+
+# Bias tables of other sizes than the workloads' 128 / 64: a small P puts
+# most 32 x 32 blocks of the forward past the saturated position bucket (its
+# far-from-diagonal table), a small Tb clamps 32-bit gaps inside the time
+# tables, and a Tb between 32 and 64 clamps only 64-bit ones.
+@pytest.mark.parametrize("P,Tb", [(16, 8), (40, 24), (128, 40), (300, 64)])
+def test_bucket_table_sizes(P, Tb):
+    b = synth.make_batch([900, 300, 64, 1500], H=4, d_qk=128, d_v=128, num_targets=[16, 4, 0, 32],
+                         num_contexts=[0, 5, 3, 0], seed=73)
+    _with_tables(b, P, Tb, 74)
+    _, got = run_gpu(b)
+    check(got, run_oracle(b), TOL["bf16"])
+
+
+@pytest.mark.parametrize("Tb", [8, 40])
+def test_wide_timestamp_gaps_small_time_table(Tb):
+    b = _ragged_batch("bf16", 128, seed=75, lengths=[700, 300, 129, 40])
+    ts, o = b.timestamps.copy(), b.offsets
+    ts[int(o[0]) + 400:int(o[1])] += np.int64(1) << 34
+    ts[int(o[3]) + 5] += np.int64(1) << 31
+    b.timestamps = ts
+    _with_tables(b, 64, Tb, 76)
+    _, got = run_gpu(b)
+    check(got, run_oracle(b), TOL["bf16"])
+
+
 @pytest.mark.parametrize("simt", [False, True])
 def test_fp32_gate_with_bf16_operands(simt):
     # HSTU_FLAG_U_FP32: u is read as FP32 while q, k, v stay BF16; the gate's
@@ -191,6 +223,39 @@ def test_edge_shapes():
                           num_contexts=np.array([7, 0, 130]), num_targets=np.array([0, 9, 0]), seed=61)
     _, got2 = run_gpu(b2)
     check(got2, run_oracle(b2), TOL["fp32"])
+
+
+def test_many_tiny_sequences():
+    # 9000 sequences of 0-3 tokens (+ candidates): the planner's offsets and
+    # block records no longer fit its shared-memory staging (2048 sequences,
+    # 8192 blocks) and it works from the workspace arrays
+    r = np.random.default_rng(63)
+    B = 9000
+    hist = r.integers(0, 4, size=B)
+    b = synth.make_batch(hist, H=2, d_qk=128, d_v=128, num_targets=r.integers(0, 2, size=B),
+                         num_contexts=r.integers(0, 2, size=B), seed=64)
+    _, got = run_gpu(b)
+    check(got, run_oracle(b), TOL["bf16"])
+
+
+@pytest.mark.parametrize("dropout", [None, (0.25, 5, 6)])
+def test_eight_heads(dropout):
+    # F = H d = 1024: eight 4-wide chunks per lane in the norm-gate kernels
+    from hstu_jagged_attention_02_gb300.attention import Problem
+    b = synth.make_batch([700, 130, 333], H=8, d_qk=128, d_v=128, num_targets=[8, 0, 20], seed=65)
+    pr = Problem(b, dropout=dropout)
+    pr.forward()
+    pr.backward()
+    torch.cuda.synchronize()
+    assert pr.device_error() == 0
+    got = {"o": pr.o, "y": pr.y, "dq": pr.dq, "dk": pr.dk, "dv": pr.dvv, "du": pr.du,
+           "d_rab_pos": pr.d_rab_pos, "d_rab_time": pr.d_rab_time}
+    got = {k: v.double().cpu().numpy() for k, v in got.items()}
+    f = O.forward(b, dropout=dropout)
+    g = O.backward(b, o=f["o"], dropout=dropout)
+    want = {"o": f["o"], "y": f["y"], "dq": g["dq"], "dk": g["dk"], "dv": g["dv"], "du": g["du"],
+            "d_rab_pos": g["d_rab_pos"], "d_rab_time": g["d_rab_time"]}
+    check(got, want, TOL["bf16"])
 
 
 def test_no_tokens():
