@@ -174,6 +174,7 @@ struct GemmParams {
   int64_t M;
   int N, K, D;
   int npass;            // 1: A = X; 2: A = y_hi, then y_lo, into one accumulator
+  int test_timeout;     // test only: CTA 0 never loads its first stage; waits give up after ~1 ms
   int* err;             // first error code (HSTU_ERR_TIMEOUT) and its wait site
   int* err_info;
   const int* carry_err; // f2 only: error words of f1, raised into err at launch (or NULL)

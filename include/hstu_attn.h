@@ -80,7 +80,9 @@ typedef enum { HSTU_NORM_NONE = 0, HSTU_NORM_LAYERNORM = 1 } hstu_norm_t;
 #define HSTU_FLAG_TEST_TIMEOUT (1u << 1) /* test only: the tensor-core forward withholds one load (the
                                             first K/V tile of work item 0) and its waits give up after about
                                             a millisecond, so the timeout path runs without a hang; the
-                                            result is HSTU_ERR_TIMEOUT */
+                                            result is HSTU_ERR_TIMEOUT.  In hstu_layer_fwd it applies to the
+                                            tensor-core input projection instead (its CTA 0 skips its first
+                                            load), and hstu_layer_bwd rejects it */
 #define HSTU_FLAG_U_FP32 (1u << 2)       /* u is FP32 whatever dtype is (requires out_dtype FP32).  The
                                             gate multiplies y element by element, so a BF16 rounding of u
                                             is never averaged out; q, k, v stay in dtype */

@@ -28,3 +28,27 @@ def test_forward_wait_times_out_and_context_survives():
     torch.cuda.synchronize()
     assert pr2.device_error() == 0
     assert torch.isfinite(pr2.o).all() and torch.isfinite(pr2.dq).all()
+
+
+def test_layer_projection_wait_times_out_and_context_survives():
+    # the layer's tensor-core input projection in its test mode: CTA 0 skips
+    # its first load, the MMA warp's wait runs out, every role exits, and the
+    # error (kept in the layer's own header word while the attention runs)
+    # is raised into the workspace error word by the output projection
+    from hstu_jagged_attention_02_gb300.layer import LayerProblem
+    from tests.test_gpu_layer import _small_layer
+    b = _small_layer(91, [300, 131, 260], H=2, d=64)
+    pr = LayerProblem(b)
+    pr.desc.flags |= C.HSTU_FLAG_TEST_TIMEOUT
+    pr.forward()
+    torch.cuda.synchronize()
+    assert pr.device_error() == C.HSTU_ERR_TIMEOUT
+    with pytest.raises(C.HSTUError) as e:   # a forward-only test mode
+        pr.backward()
+    assert e.value.status == C.HSTU_ERR_UNSUPPORTED
+    pr.desc.flags &= ~C.HSTU_FLAG_TEST_TIMEOUT
+    pr.forward()
+    pr.backward()
+    torch.cuda.synchronize()
+    assert pr.device_error() == 0
+    assert torch.isfinite(pr.out).all() and torch.isfinite(pr.dx).all()
