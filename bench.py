@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -129,16 +130,30 @@ class ClockSampler:
 
 # the translation unit of each timed attention kernel plus the headers it includes
 KERNEL_SOURCES = {
-    "fwd": ("hstu_tc_fwd.cu", "tc_ptx.cuh", "hstu_common.cuh", "hstu_internal.h"),
-    "bwd": ("hstu_tc_bwd.cu", "tc_ptx.cuh", "hstu_common.cuh", "hstu_internal.h"),
+    "fwd": ("hstu_tc_fwd.cu", "tc_ptx.cuh", "hstu_common.cuh"),
+    "bwd": ("hstu_tc_bwd.cu", "tc_ptx.cuh", "hstu_common.cuh"),
 }
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and blank lines."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_sources_sha(role: str):
+    """Hash of the code an attention kernel is compiled from: its translation
+    unit and device headers, the kernel parameter block of hstu_internal.h
+    and the public header's declarations (comments left out)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "hstu_jagged_attention_02_gb300", "csrc")
-    for fn in KERNEL_SOURCES[role] + ("../../include/hstu_attn.h",):
-        h.update(open(os.path.join(csrc, fn), "rb").read())
+    for fn in KERNEL_SOURCES[role]:
+        h.update(_code_only(open(os.path.join(csrc, fn)).read()).encode())
+    internal = open(os.path.join(csrc, "hstu_internal.h")).read()
+    i = internal.index("struct AttnParams {")
+    h.update(_code_only(internal[i:internal.index("};", i)]).encode())
+    h.update(_code_only(open(os.path.join(ROOT, "include", "hstu_attn.h")).read()).encode())
     return h.hexdigest()[:16]
 
 
