@@ -16,7 +16,11 @@ With --workload layer it measures the full HSTU layer instead (x W1, SiLU
 split, the same attention, LayerNorm gate, y W2 + x, forward + backward on 8
 sequences of 8K-32K tokens at D = 512), counting the projections' FLOPs too.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload layer]
+With --graph the K timed steps are captured once as a CUDA graph and the
+timed region replays it (the per-kernel events of the library's timing hook
+are part of the graph); by default they are launched one by one.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload layer] [--graph]
 """
 from __future__ import annotations
 
@@ -405,10 +409,7 @@ def run_gpu(args, wl, rank, world, local_rank):
             C.hstu_time_next_attention_kernel(ev[0].cuda_event, ev[1].cuda_event)
         pr.forward()
         n = C.hstu_last_launch_count()
-        if not wl.has_backward:
-            if ev is not None:  # no backward kernel: an empty interval
-                ev[2].record(stream)
-                ev[3].record(stream)
+        if not wl.has_backward:   # no backward kernel: its interval is reported as 0
             return n
         if ev is not None:
             C.hstu_time_next_attention_kernel(ev[2].cuda_event, ev[3].cuda_event)
@@ -426,6 +427,21 @@ def run_gpu(args, wl, rank, world, local_rank):
     for e4 in evs:   # torch only times events it has recorded once; the library re-records them
         for e in e4:
             e.record(stream)
+    # With --graph the K steps are captured once into a CUDA graph (the
+    # library's calls, their kernel-timing events and programmatic launch
+    # edges included) and the timed region replays it; by default they are
+    # launched one by one.
+    graph = None
+    launches = 0
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                for k in range(args.steps):
+                    launches += step(k, evs[k])
+        torch.cuda.synchronize()
     clock = ClockSampler(local_rank)
     if world > 1:
         dist.barrier()
@@ -433,10 +449,12 @@ def run_gpu(args, wl, rank, world, local_rank):
     clock.start()
     time.sleep(0.3)  # let the sampler start before the region
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches = 0
     start.record(stream)
-    for k in range(args.steps):
-        launches += step(k, evs[k])
+    if graph is not None:
+        graph.replay()
+    else:
+        for k in range(args.steps):
+            launches += step(k, evs[k])
     end.record(stream)
     torch.cuda.synchronize()
     clocks = clock.stop()
@@ -444,7 +462,7 @@ def run_gpu(args, wl, rank, world, local_rank):
         dist.barrier()
     elapsed_ms = start.elapsed_time(end)
     fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    bwd_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    bwd_ms = [e[2].elapsed_time(e[3]) if wl.has_backward else 0.0 for e in evs]
     step_flops = [flops[k % nb] for k in range(args.steps)]
     tot_flops = sum(f[2] for f in step_flops)
     for pr in probs:
@@ -505,6 +523,8 @@ def run_gpu(args, wl, rank, world, local_rank):
                "sample": f"{used} x {what}", "seconds": cdt}
     cfg = {"workload": wl.description}
     cfg.update(wl.config())
+    cfg["launch"] = ("the K timed steps captured once as a CUDA graph and replayed" if args.graph
+                     else "stream launches")
     if wl.dropout_p:
         cfg["dropout_p"] = wl.dropout_p
     cfg.update({"per_rank_batches": nb, "mean_tokens_per_batch": float(np.mean([b.T for b in batches]))})
@@ -600,6 +620,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="heavy_tailed", choices=sorted(WORKLOADS),
                     help="heavy_tailed attention (the default line) or the full layer")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the timed steps as a CUDA graph and time its replay")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="fused dropout probability on y (heavy_tailed and layer workloads)")
     args = ap.parse_args()

@@ -19,14 +19,25 @@ bool detail_is_set() { return g_detail[0] != 0; }
 void clear_detail() { g_detail[0] = 0; }
 
 // Records the measurement-hook events around one launch, then clears them.
+// Records the hook's events around one launch.  Under stream capture they
+// become external event-record nodes, so each replay of the graph
+// timestamps them; outside capture they are plain records.
+void record_hook_event(cudaEvent_t e, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, st);
+}
+
 struct KernelTimer {
   cudaStream_t st;
   cudaEvent_t a, b;
   explicit KernelTimer(cudaStream_t s) : st(s), a(g_ev_start), b(g_ev_stop) {
     g_ev_start = g_ev_stop = nullptr;
-    if (a) cudaEventRecord(a, st);
+    if (a) record_hook_event(a, st);
   }
-  ~KernelTimer() { if (b) cudaEventRecord(b, st); }
+  ~KernelTimer() { if (b) record_hook_event(b, st); }
 };
 
 constexpr uint32_t kKnownFlags = HSTU_FLAG_FORCE_SIMT | HSTU_FLAG_TEST_TIMEOUT | HSTU_FLAG_U_FP32;

@@ -381,7 +381,9 @@ int32_t hstu_last_launch_count(void);
 /* Measurement hook.  start_event and stop_event are cudaEvent_t handles (or
  * both NULL to clear).  The next hstu_attn_fwd or hstu_attn_bwd call on this
  * thread records start_event on its stream right before launching its
- * attention kernel and stop_event right after, then forgets them. */
+ * attention kernel and stop_event right after, then forgets them.  Under
+ * stream capture they are recorded as external event nodes, so each replay
+ * of the graph timestamps them. */
 hstu_status_t hstu_time_next_attention_kernel(void* start_event, void* stop_event);
 
 #ifdef __cplusplus
