@@ -75,7 +75,11 @@ struct Lay {
   static constexpr int SLOT_OFF = KTS_OFF + BK * 8;              // ItemSlot
   static constexpr int BAR_OFF = SLOT_OFF + (int)sizeof(ItemSlot);
   static constexpr int MISC_OFF = BAR_OFF + BAR_COUNT * 8;
-  static constexpr int TAB_OFF = MISC_OFF + 16;              // float [H][P+Tb] bias
+  // per epilogue warp: a 32-dim x 8-query FP32 block of dQ, the source of its
+  // bulk reduce-add into dq
+  static constexpr int DQS_OFF = (MISC_OFF + 16 + 127) / 128 * 128;
+  static constexpr int DQS_WARP = 32 * 8 * 4;
+  static constexpr int TAB_OFF = DQS_OFF + kEpiWarps * DQS_WARP;  // float [H][P+Tb] bias
 };
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -212,7 +216,8 @@ template <typename TO>
 __global__ void __maxnreg__(96)
 hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                   const __grid_constant__ CUtensorMap tmdh, const __grid_constant__ CUtensorMap tmdl) {
+                   const __grid_constant__ CUtensorMap tmdh, const __grid_constant__ CUtensorMap tmdl,
+                   const __grid_constant__ CUtensorMap tmdq) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
@@ -503,6 +508,14 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     kc.want_rp = want_rp;
     kc.want_rt = want_rt;
     // the dQ^T of the previous query tile, drained in the middle of the next
+    // dQ^T's columns are queries and its TMEM lanes dims: this warp holds dims
+    // [32 wq, 32 wq + 32) of the 16 queries [qb0 + 16 hq, + 16).  They go
+    // through the warp's staging block, 8 queries at a time, into one bulk
+    // reduce-add each (tensor map [T][H][D] FP32).  Queries past the
+    // sequence carry exact zeros (their dZ is masked), so the neighbouring
+    // sequence's rows they land on are unchanged; rows past T are clipped.
+    uint8_t* dqs = base + Lay::DQS_OFF + warp * Lay::DQS_WARP;
+    const uint32_t dqs_u32 = base_u32 + Lay::DQS_OFF + warp * Lay::DQS_WARP;
     auto drain_dq = [&](uint32_t g, int qb0, int64_t s0, int hh) -> bool {
       if (!mbar_wait(bar(BAR_DQFULL), g & 1, wd, 30)) return false;
       fence_after_sync();
@@ -512,13 +525,22 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_DQEMPTY));
-      const int ib = qb0 + hq * 16;
-      float* dst = p.dq_acc + ((size_t)(s0 + ib) * H + hh) * D + lrow;
-      const size_t ld = (size_t)H * D;
       const float alpha = p.alpha;
+      const int tok0 = (int)(s0 + qb0 + hq * 16);
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        if (ib + c < n_seq) atomicAdd(dst + c * ld, alpha * __uint_as_float(qv[c]));
+      for (int r = 0; r < 2; ++r) {
+        if (lane == 0) bulk_wait_read<0>();   // the block's previous reduce has read it
+        __syncwarp();
+        float* blk = reinterpret_cast<float*>(dqs) + lane;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) blk[c * 32] = alpha * __uint_as_float(qv[8 * r + c]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (tok0 + 8 * r < p.T) tma_reduce_add_3d(&tmdq, dqs_u32, wq * 32, hh, tok0 + 8 * r);
+          bulk_commit();
+        }
+      }
       return true;
     };
     while (ok) {
@@ -669,6 +691,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     }
   }
 
+  if (warp < kEpiWarps && lane == 0) bulk_wait_all();   // the dQ reduce-adds are complete
   __threadfence();   // this CTA's partial-sum reductions are performed before they are read back
   fence_before_sync();
   __syncthreads();
@@ -706,7 +729,17 @@ cudaError_t launch_t(const AttnParams& p, cudaStream_t st) {
   const int64_t max_items = ((p.T + BK - 1) / BK + p.B) * (int64_t)p.H;
   int grid = (int)(max_items < p.num_sms ? max_items : p.num_sms);
   if (grid > kDrabMaxCtas) grid = kDrabMaxCtas;  // one d_rab partial row per CTA
-  hstu_bwd_tc_kernel<TO><<<grid, kThreads, smem, st>>>(p, mq, mk, mv, mdh, mdl);
+  // dq accumulator [T][H][D] FP32, 32-dim x 8-query reduce-add blocks
+  CUtensorMap mdq;
+  {
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.H, (uint64_t)p.T};
+    const uint64_t strides[2] = {(uint64_t)D * 4, (uint64_t)p.H * D * 4};
+    const uint32_t box[3] = {32, 1, 8};
+    if (!make_tmap_tile(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.dq_acc, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  }
+  hstu_bwd_tc_kernel<TO><<<grid, kThreads, smem, st>>>(p, mq, mk, mv, mdh, mdl, mdq);
   e = cudaGetLastError();
   if (e != cudaSuccess) set_launch_detail(e, "hstu_bwd_tc_kernel", fn, kThreads, smem);
   return e;
