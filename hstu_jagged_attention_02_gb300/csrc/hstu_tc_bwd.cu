@@ -301,11 +301,17 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     bool ok = true;
     // The next work item is claimed only once the current one's loads are all
     // issued (claiming earlier pairs items up statically and loses the
-    // longest-first balance); its planner record is one 48-byte load.
+    // longest-first balance); its planner record is one 48-byte load.  The
+    // first item of CTA b is item b (no atomic on the way in); later claims
+    // count on from the grid size.
+    bool first_claim = true;
     while (ok) {
-      int idx = 0;
-      if (lane == 0) idx = atomicAdd(p.hdr_rw + WS_NEXT, 1);
-      idx = __shfl_sync(0xffffffffu, idx, 0);
+      int idx = (int)blockIdx.x;
+      if (!first_claim) {
+        if (lane == 0) idx = (int)gridDim.x + atomicAdd(p.hdr_rw + WS_NEXT, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+      }
+      first_claim = false;
       const bool valid = idx < nitems;
       PlanItem it{};
       if (valid) it = p.items[idx / H];
@@ -318,13 +324,23 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         const int row = k0 + lane + 32 * x;
         kv[x] = (valid && p.ts && row < n) ? p.ts[s0 + row] : tbase;
       }
+      if (lane == 0) ok = mbar_wait(bar(BAR_KVEMPTY), (item_it & 1) ^ 1, wd, 21);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      // the K/V copy starts before the key timestamps arrive; the phase
+      // completes with the copy and the arrive below, after they are staged
+      if (lane == 0 && valid) {
+        mbar_expect_tx(bar(BAR_KVFULL), 4 * Lay::KBOX);
+        const int y = (int)(s0 + k0);
+        for (int c = 0; c < 2; ++c) {
+          tma_load_2d(sK + c * Lay::KBOX, &tmk, bar(BAR_KVFULL), h * D + c * 64, y);
+          tma_load_2d(sV + c * Lay::KBOX, &tmv, bar(BAR_KVFULL), h * D + c * 64, y);
+        }
+      }
       bool kw = false;
 #pragma unroll
       for (int x = 0; x < BK / 32; ++x) kw |= ts_wide(kv[x] - tbase);
       const bool item_wide = __any_sync(0xffffffffu, kw);
-      if (lane == 0) ok = mbar_wait(bar(BAR_KVEMPTY), (item_it & 1) ^ 1, wd, 21);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
 #pragma unroll
       for (int x = 0; x < BK / 32; ++x) kts_s[lane + 32 * x] = kv[x];
       if (lane == 0) {
@@ -334,16 +350,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       }
       __syncwarp();
       if (lane == 0) {
-        if (valid) {
-          mbar_arrive_expect_tx(bar(BAR_KVFULL), 4 * Lay::KBOX);
-          const int y = (int)(s0 + k0);
-          for (int c = 0; c < 2; ++c) {
-            tma_load_2d(sK + c * Lay::KBOX, &tmk, bar(BAR_KVFULL), h * D + c * 64, y);
-            tma_load_2d(sV + c * Lay::KBOX, &tmv, bar(BAR_KVFULL), h * D + c * 64, y);
-          }
-        } else {
-          mbar_arrive(bar(BAR_KVFULL));  // the slot says: no more work
-        }
+        mbar_arrive(bar(BAR_KVFULL));  // without a copy the slot says: no more work
         kv_phases += 1;
         kv_copy = valid;
       }
@@ -363,6 +370,17 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         }
         ok = mbar_wait(bar(BAR_QEMPTY + stage), ((qt_it / kQStages) & 1) ^ 1, wd, 22);
         if (!ok) break;
+        const uint32_t full = bar(BAR_QFULL + stage);
+        if (lane == 0) {   // the copies start before the query timestamps arrive
+          mbar_expect_tx(full, Lay::QSTAGE);
+          const uint32_t dst = sQS + stage * Lay::QSTAGE;
+          const int y = (int)(s0 + q0);
+          for (int c = 0; c < 2; ++c) {
+            tma_load_2d(dst + c * Lay::QBOX, &tmq, full, h * D + c * 64, y);
+            tma_load_2d(dst + Lay::Q_BYTES + c * Lay::QBOX, &tmdh, full, h * D + c * 64, y);
+            tma_load_2d(dst + 2 * Lay::Q_BYTES + c * Lay::QBOX, &tmdl, full, h * D + c * 64, y);
+          }
+        }
         bool qw = false;
 #pragma unroll
         for (int x = 0; x < BQ / 32; ++x) {
@@ -374,15 +392,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         if (lane == 0) stage_wide[stage] = qw ? 1 : 0;
         __syncwarp();
         if (lane == 0) {
-          const uint32_t full = bar(BAR_QFULL + stage);
-          mbar_arrive_expect_tx(full, Lay::QSTAGE);
-          const uint32_t dst = sQS + stage * Lay::QSTAGE;
-          const int y = (int)(s0 + q0);
-          for (int c = 0; c < 2; ++c) {
-            tma_load_2d(dst + c * Lay::QBOX, &tmq, full, h * D + c * 64, y);
-            tma_load_2d(dst + Lay::Q_BYTES + c * Lay::QBOX, &tmdh, full, h * D + c * 64, y);
-            tma_load_2d(dst + 2 * Lay::Q_BYTES + c * Lay::QBOX, &tmdl, full, h * D + c * 64, y);
-          }
+          mbar_arrive(full);
           armed[stage] += 1;
         }
         ++qt_it;

@@ -308,12 +308,18 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     bool ok = true;
     // The next work item is claimed only once the current one's loads are all
     // issued (claiming earlier pairs items up statically and loses the
-    // longest-first balance); its planner record is one 48-byte load.
+    // longest-first balance); its planner record is one 48-byte load.  The
+    // first item of CTA b is item b (no atomic on the way in); later claims
+    // count on from the grid size.
+    bool first_claim = true;
     while (ok) {
       const int qb = (int)(q_it % kQBufs);
-      int idx = 0;
-      if (lane == 0) idx = atomicAdd(p.hdr_rw + WS_NEXT, 1);
-      idx = __shfl_sync(0xffffffffu, idx, 0);
+      int idx = (int)blockIdx.x;
+      if (!first_claim) {
+        if (lane == 0) idx = (int)gridDim.x + atomicAdd(p.hdr_rw + WS_NEXT, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+      }
+      first_claim = false;
       const bool valid = idx < nitems;
       PlanItem it{};
       if (valid) it = p.items[idx / H];
@@ -326,13 +332,20 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         const int row = q0 + lane + 32 * x;
         qv[x] = (valid && p.ts && row < n) ? p.ts[s0 + row] : tbase;
       }
+      if (lane == 0) ok = mbar_wait(bar(BAR_QEMPTY + qb), ((q_it / kQBufs) & 1) ^ 1, wd, 1);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      // the Q copy starts before the timestamps arrive; the buffer's phase
+      // completes with the copy and the arrive below, after they are staged
+      if (lane == 0 && valid) {
+        mbar_expect_tx(bar(BAR_QFULL + qb), L::Q_BYTES);
+        for (int c = 0; c < L::NCH; ++c)
+          tma_load_2d(sQ0 + qb * L::Q_BYTES + c * L::BOX, &tmq, bar(BAR_QFULL + qb), h * D + c * 64, (int)(s0 + q0));
+      }
       bool qw = false;
 #pragma unroll
       for (int x = 0; x < BM / 32; ++x) qw |= ts_wide(qv[x] - tbase);
       const bool item_wide = __any_sync(0xffffffffu, qw);
-      if (lane == 0) ok = mbar_wait(bar(BAR_QEMPTY + qb), ((q_it / kQBufs) & 1) ^ 1, wd, 1);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
 #pragma unroll
       for (int x = 0; x < BM / 32; ++x) qts_s[qb * BM + lane + 32 * x] = qv[x];
       if (lane == 0) {
@@ -343,14 +356,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       }
       __syncwarp();
       if (lane == 0) {
-        if (valid) {
-          mbar_arrive_expect_tx(bar(BAR_QFULL + qb), L::Q_BYTES);
-          for (int c = 0; c < L::NCH; ++c)
-            tma_load_2d(sQ0 + qb * L::Q_BYTES + c * L::BOX, &tmq, bar(BAR_QFULL + qb), h * D + c * 64,
-                        (int)(s0 + q0));
-        } else {
-          mbar_arrive(bar(BAR_QFULL + qb));  // the slot says: no more work
-        }
+        mbar_arrive(bar(BAR_QFULL + qb));  // without a copy the slot says: no more work
         q_phases[qb] += 1;
         q_copy[qb] = valid;
       }
@@ -374,6 +380,21 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         }
         ok = mbar_wait(bar(BAR_KVEMPTY + stage), ((kv_it / kStages) & 1) ^ 1, wd, 2);
         if (!ok) break;
+        const bool withhold = withhold_next;
+        withhold_next = false;
+        // the K/V copy starts before the key timestamps arrive (as for Q)
+        if (lane == 0 && !withhold) {
+          mbar_expect_tx(bar(BAR_KVFULL + stage), L::STAGE);
+          const uint32_t dstK = sKV + stage * L::STAGE;
+          const bool cached = DELTA && !self;
+          const CUtensorMap* mk = cached ? &tmk2 : &tmk;
+          const CUtensorMap* mv = cached ? &tmv2 : &tmv;
+          const int y = (int)(cached ? cs0 + k0 : s0 + k0);
+          for (int c = 0; c < L::NCH; ++c) {
+            tma_load_2d(dstK + c * L::BOX, mk, bar(BAR_KVFULL + stage), h * D + c * 64, y);
+            tma_load_2d(dstK + L::K_BYTES + c * L::BOX, mv, bar(BAR_KVFULL + stage), h * D + c * 64, y);
+          }
+        }
         bool kw = false;
 #pragma unroll
         for (int x = 0; x < BN / 32; ++x) {
@@ -384,19 +405,8 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         kw = __any_sync(0xffffffffu, kw);
         if (lane == 0) stage_wide[stage] = kw ? 1 : 0;
         __syncwarp();
-        const bool withhold = withhold_next;
-        withhold_next = false;
-        if (lane == 0 && !withhold) {
-          mbar_arrive_expect_tx(bar(BAR_KVFULL + stage), L::STAGE);
-          const uint32_t dstK = sKV + stage * L::STAGE;
-          const bool cached = DELTA && !self;
-          const CUtensorMap* mk = cached ? &tmk2 : &tmk;
-          const CUtensorMap* mv = cached ? &tmv2 : &tmv;
-          const int y = (int)(cached ? cs0 + k0 : s0 + k0);
-          for (int c = 0; c < L::NCH; ++c) {
-            tma_load_2d(dstK + c * L::BOX, mk, bar(BAR_KVFULL + stage), h * D + c * 64, y);
-            tma_load_2d(dstK + L::K_BYTES + c * L::BOX, mv, bar(BAR_KVFULL + stage), h * D + c * 64, y);
-          }
+        if (lane == 0 && !withhold) {   // withheld (test only): neither copy nor arrive
+          mbar_arrive(bar(BAR_KVFULL + stage));
           armed[stage] += 1;
         }
         ++kv_it;
