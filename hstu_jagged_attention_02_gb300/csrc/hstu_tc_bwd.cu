@@ -149,7 +149,6 @@ __device__ __forceinline__ void grad_cols(const AttnParams& p, const uint32_t (&
                                           uint32_t (&ahi)[NC / 2], uint32_t (&alo)[NC / 2], uint32_t (&zhi)[NC / 2],
                                           uint32_t (&zlo)[NC / 2], const KeyCtx& kc, int ib, const int32_t* ts32,
                                           const int64_t* ts64, RabAcc& acc) {
-  float bias[NC];
   int bps[NC], bts[NC];
 #pragma unroll
   for (int c = 0; c < NC; ++c) {
@@ -171,20 +170,31 @@ __device__ __forceinline__ void grad_cols(const AttnParams& p, const uint32_t (&
     bt = bt < p.Tb - 1 ? bt : p.Tb - 1;
     bps[c] = bp;
     bts[c] = bt;
-    bias[c] = kc.tp[bp] + kc.tp[p.P + bt];
   }
+  // Paired FP32 arithmetic (fma/mul/add on float2, one instruction for two
+  // elements); each lane of a pair rounds exactly like the scalar operation,
+  // and the products keep the scalar association.
+  const float2 one2 = make_float2(1.f, 1.f);
 #pragma unroll
   for (int c = 0; c < NC; c += 2) {
+    const float2 b2 = __fadd2_rn(make_float2(kc.tp[bps[c]], kc.tp[bps[c + 1]]),
+                                 make_float2(kc.tp[p.P + bts[c]], kc.tp[p.P + bts[c + 1]]));
+    const float2 w2 = __ffma2_rn(make_float2(p.kA, p.kA), make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), b2);
+    const float2 d2 = __fadd2_rn(one2, make_float2(ex2_approx(w2.x), ex2_approx(w2.y)));
+    const float2 sg2 = make_float2(rcp_approx(d2.x), rcp_approx(d2.y));
+    const float2 z2 = make_float2(w2.x * p.kZ, w2.y * p.kZ);
+    const float2 a2 = __fmul2_rn(make_float2(w2.x * p.kC, w2.y * p.kC), sg2);
+    const float2 f2 = __ffma2_rn(z2, fsub2(one2, sg2), one2);  // 1 + z (1 - sg)
+    const float2 h2 = __fmul2_rn(__fmul2_rn(make_float2(__uint_as_float(dav[c]), __uint_as_float(dav[c + 1])), sg2), f2);
+    const float2 g2 = make_float2(h2.x * p.inv_n, h2.y * p.inv_n);
+    const float aa[2] = {a2.x, a2.y}, gg[2] = {g2.x, g2.y};
     float av[2], zv[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const float w = fmaf(p.kA, __uint_as_float(sv[c + e]), bias[c + e]);
-      const float sg = rcp_approx(1.0f + ex2_approx(w));
-      const float z = w * p.kZ;
       const int i = ib + c + e;
       const bool valid = i >= kc.lo && i <= kc.hi;
-      const float a = valid ? (w * p.kC) * sg : 0.f;
-      const float dz = valid ? __uint_as_float(dav[c + e]) * sg * fmaf(z, 1.f - sg, 1.f) * p.inv_n : 0.f;
+      const float a = valid ? aa[e] : 0.f;
+      const float dz = valid ? gg[e] : 0.f;
       av[e] = a;
       zv[e] = dz;
       if (kc.want_rp && valid) {
@@ -204,9 +214,11 @@ __device__ __forceinline__ void grad_cols(const AttnParams& p, const uint32_t (&
     const uint32_t ah = pack_bf16(av[0], av[1]);
     const uint32_t zh = pack_bf16(zv[0], zv[1]);
     ahi[c >> 1] = ah;
-    alo[c >> 1] = pack_bf16(av[0] - bf16_lo_f(ah), av[1] - bf16_hi_f(ah));
     zhi[c >> 1] = zh;
-    zlo[c >> 1] = pack_bf16(zv[0] - bf16_lo_f(zh), zv[1] - bf16_hi_f(zh));
+    const float2 al = bf16_residual2(make_float2(av[0], av[1]), ah);
+    const float2 zl = bf16_residual2(make_float2(zv[0], zv[1]), zh);
+    alo[c >> 1] = pack_bf16(al.x, al.y);
+    zlo[c >> 1] = pack_bf16(zl.x, zl.y);
   }
 }
 

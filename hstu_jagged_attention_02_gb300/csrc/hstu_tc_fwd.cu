@@ -140,9 +140,13 @@ template <int POS, bool WIDE, bool PARTIAL, int MODE = 0>
 __device__ __forceinline__ void score32(const AttnParams& p, const uint32_t (&sv)[32], uint32_t (&hi)[16],
                                         uint32_t (&lo)[16], const RowCtx& rc, int jb, const int32_t* ts32,
                                         const int64_t* ts64) {
+  // Paired FP32 arithmetic (fma/mul/add on float2, one instruction for two
+  // elements); each lane of a pair rounds exactly like the scalar operation.
+  const float2 kA2 = make_float2(p.kA, p.kA), kCi2 = make_float2(p.kCi, p.kCi);
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     float bias[16];
+    int bps[16];
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const int cc = half * 16 + c;
@@ -175,18 +179,27 @@ __device__ __forceinline__ void score32(const AttnParams& p, const uint32_t (&sv
         d = d < 0 ? -d : d;
         st = (MODE == 0 && POS == 2 ? kTabFar : kTabNarrow) + __clz(d);
       }
-      if (MODE == 0 && POS == 2) bias[c] = rc.tp[p.P + st];
-      else bias[c] = rc.tp[bp] + rc.tp[p.P + st];
+      if (MODE == 0 && POS == 2) {
+        bias[c] = rc.tp[p.P + st];
+      } else {
+        bps[c] = bp;
+        bias[c] = rc.tp[p.P + st];
+      }
     }
 #pragma unroll
     for (int c = 0; c < 16; c += 2) {
-      float a2[2];
+      const int c0 = half * 16 + c;
+      float2 b2 = make_float2(bias[c], bias[c + 1]);
+      if (!(MODE == 0 && POS == 2)) b2 = __fadd2_rn(make_float2(rc.tp[bps[c]], rc.tp[bps[c + 1]]), b2);
+      // SiLU(z)/N = w kC / (1 + 2^w), as w / (kCi + kCi 2^w)
+      const float2 w2 = __ffma2_rn(kA2, make_float2(__uint_as_float(sv[c0]), __uint_as_float(sv[c0 + 1])), b2);
+      const float2 den = __ffma2_rn(kCi2, make_float2(ex2_approx(w2.x), ex2_approx(w2.y)), kCi2);
+      const float2 r2 = __fmul2_rn(w2, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
+      float a2[2] = {r2.x, r2.y};
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int cc = half * 16 + c + e;
-        // SiLU(z)/N = w kC / (1 + 2^w), as w / (kCi + kCi 2^w)
-        const float w = fmaf(p.kA, __uint_as_float(sv[cc]), bias[c + e]);
-        float a = w * rcp_approx(fmaf(p.kCi, ex2_approx(w), p.kCi));
+        const int cc = c0 + e;
+        float a = a2[e];
         if (MODE == 1) {
           a = (rc.row_ok && jb + cc < rc.h_end) ? a : 0.f;
         } else if (MODE == 2) {
@@ -199,8 +212,9 @@ __device__ __forceinline__ void score32(const AttnParams& p, const uint32_t (&sv
         a2[e] = a;
       }
       const uint32_t h2 = pack_bf16(a2[0], a2[1]);
-      hi[(half * 16 + c) >> 1] = h2;
-      lo[(half * 16 + c) >> 1] = pack_bf16(a2[0] - bf16_lo_f(h2), a2[1] - bf16_hi_f(h2));
+      hi[c0 >> 1] = h2;
+      const float2 l2 = bf16_residual2(make_float2(a2[0], a2[1]), h2);
+      lo[c0 >> 1] = pack_bf16(l2.x, l2.y);
     }
   }
 }

@@ -250,6 +250,21 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo_f(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi_f(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// x - y on two FP32 lanes in one instruction (PTX sub.f32x2, sm_100 family);
+// each lane rounds like the scalar subtraction.
+__device__ __forceinline__ float2 fsub2(float2 x, float2 y) {
+  float2 d;
+  asm("{\n\t.reg .b64 a, b, c;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "sub.rn.f32x2 c, a, b;\n\tmov.b64 {%0, %1}, c;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(x.x), "f"(x.y), "f"(y.x), "f"(y.y));
+  return d;
+}
+// x - bf16 pair v (low half first) on two lanes: the residual of a BF16 split
+__device__ __forceinline__ float2 bf16_residual2(float2 x, uint32_t v) {
+  return fsub2(x, make_float2(bf16_lo_f(v), bf16_hi_f(v)));
+}
+
 __device__ __forceinline__ float tanh_approx(float x) {
   float y;
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
