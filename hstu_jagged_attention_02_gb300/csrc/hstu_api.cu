@@ -113,6 +113,11 @@ void set_score_constants(AttnParams& p) {
   p.kC = -p.inv_n / log2e;
   p.kZ = -1.0f / log2e;
   p.kCi = 1.0f / p.kC;
+  p.kA2 = make_float2(p.kA, p.kA);
+  p.kC2 = make_float2(p.kC, p.kC);
+  p.kZ2 = make_float2(p.kZ, p.kZ);
+  p.kCi2 = make_float2(p.kCi, p.kCi);
+  p.inv_n2 = make_float2(p.inv_n, p.inv_n);
 }
 
 hstu_status_t check_ws(void* ws, size_t bytes, size_t need) {

@@ -74,6 +74,8 @@ struct AttnParams {
   int P, Tb;
   uint32_t flags;
   int num_sms;
+  // the same constants as lane pairs, for paired (f32x2) arithmetic
+  float2 kA2, kC2, kZ2, kCi2, inv_n2;
 };
 
 struct NormParams {

@@ -179,14 +179,14 @@ __device__ __forceinline__ void grad_cols(const AttnParams& p, const uint32_t (&
   for (int c = 0; c < NC; c += 2) {
     const float2 b2 = __fadd2_rn(make_float2(kc.tp[bps[c]], kc.tp[bps[c + 1]]),
                                  make_float2(kc.tp[p.P + bts[c]], kc.tp[p.P + bts[c + 1]]));
-    const float2 w2 = __ffma2_rn(make_float2(p.kA, p.kA), make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), b2);
+    const float2 w2 = __ffma2_rn(p.kA2, make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), b2);
     const float2 d2 = __fadd2_rn(one2, make_float2(ex2_approx(w2.x), ex2_approx(w2.y)));
     const float2 sg2 = make_float2(rcp_approx(d2.x), rcp_approx(d2.y));
     const float2 z2 = make_float2(w2.x * p.kZ, w2.y * p.kZ);
     const float2 a2 = __fmul2_rn(make_float2(w2.x * p.kC, w2.y * p.kC), sg2);
     const float2 f2 = __ffma2_rn(z2, fsub2(one2, sg2), one2);  // 1 + z (1 - sg)
     const float2 h2 = __fmul2_rn(__fmul2_rn(make_float2(__uint_as_float(dav[c]), __uint_as_float(dav[c + 1])), sg2), f2);
-    const float2 g2 = make_float2(h2.x * p.inv_n, h2.y * p.inv_n);
+    const float2 g2 = __fmul2_rn(h2, p.inv_n2);
     const float aa[2] = {a2.x, a2.y}, gg[2] = {g2.x, g2.y};
     float av[2], zv[2];
 #pragma unroll
