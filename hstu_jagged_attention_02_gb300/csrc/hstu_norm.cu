@@ -172,6 +172,10 @@ __device__ __forceinline__ void row_stats(const float (&x)[PER][VEC], int F, flo
 
 template <typename TI, typename TO, int VEC, int PER>
 __global__ void __launch_bounds__(kWarps * 32) norm_gate_fwd_kernel(NormParams p) {
+  // Launched programmatically after the attention forward that writes o: the
+  // launch overlaps that kernel's tail, and every thread waits for it to
+  // complete before reading.
+  pdl_wait();
   const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (t >= p.T) return;
   const int lane = threadIdx.x & 31;
@@ -322,7 +326,9 @@ cudaError_t launch_t(const NormParams& p, bool bwd, cudaStream_t st) {
                                      0, st, p);
     if (e != cudaSuccess) return e;
   } else {
-    norm_gate_fwd_kernel<TI, TO, VEC, PER><<<(unsigned)grid, kWarps * 32, 0, st>>>(p);
+    const cudaError_t e = launch_pdl(norm_gate_fwd_kernel<TI, TO, VEC, PER>, dim3((unsigned)grid), dim3(kWarps * 32),
+                                     0, st, p);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
