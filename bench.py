@@ -222,6 +222,18 @@ class AttentionWorkload:
     def cpu_samples(self, batches):
         return [sub_batch(b, 16) for b in batches], "fwd+bwd of the first 16 of the 64 sequences of a batch"
 
+    def shrink_samples(self, samples, frac, what):
+        """Each sample cut to its longest prefix of sequences with at most frac
+        of its useful FLOPs (at least one sequence)."""
+        out = []
+        for b in samples:
+            full, keep = self.flops(b)[2], 1
+            for n in range(2, b.B + 1):
+                if self.flops(sub_batch(b, n))[2] <= frac * full:
+                    keep = n
+            out.append(sub_batch(b, keep))
+        return out, f"{what}, each cut to the prefix of sequences with <= {frac:.2f} of its FLOPs (time budget)"
+
     def config(self):
         return {"batches": N_SEEDS, "seeds": f"0..{N_SEEDS - 1} (+rank*{N_SEEDS})",
                 "l2": "inputs larger than L2: 16 distinct resident batches taken in turn"}
@@ -264,6 +276,9 @@ class LayerWorkload(AttentionWorkload):
     def cpu_samples(self, batches):
         return ([synth.layer(100 + s, n_lo=1024, n_hi=1024, B=1) for s in range(2)],
                 "layer fwd+bwd of one sequence of 1024 history + 128 candidates at D=512")
+
+    def shrink_samples(self, samples, frac, what):
+        return samples, what   # one sequence per sample already
 
     def config(self):
         return {"batches": 2, "seeds": "0..1 (+rank*2)",
@@ -363,12 +378,26 @@ def sub_batch(b, n_seq):
         alpha=b.alpha, max_seq_len=b.max_seq_len, norm=b.norm, eps=b.eps)
 
 
+REFERENCE_BUDGET_S = 150.0   # the whole --impl reference run, warm-up included
+
+
 def run_reference(args, wl, rank, world):
     if rank != 0:
         return
     from oracle import oracle as O
     samples, what = wl.cpu_samples(wl.batches(0))
-    for w in range(args.warmup):
+    # The first warm-up step times the sample; if K + W steps of it would
+    # overrun the budget, every step takes a smaller sample (fewer sequences,
+    # sized by allowed pairs, which the oracle's time follows).
+    n_steps = args.steps + max(args.warmup, 1)
+    t0 = time.perf_counter()
+    wl.oracle_step(samples[0])
+    t_first = time.perf_counter() - t0
+    cost = [wl.flops(b)[2] for b in samples]
+    est = t_first / cost[0] * sum(cost[k % len(samples)] for k in range(n_steps))
+    if est > REFERENCE_BUDGET_S:
+        samples, what = wl.shrink_samples(samples, REFERENCE_BUDGET_S / est, what)
+    for w in range(1, args.warmup):
         wl.oracle_step(samples[w % len(samples)])
     flops, t0 = 0, time.perf_counter()
     for k in range(args.steps):
