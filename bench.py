@@ -501,16 +501,21 @@ def run_gpu(args, wl, rank, world, local_rank):
     # the other attention kernel: one untimed pass over the resident batches
     # with its events (the forward of a training step; none for the delta
     # forward, which has no backward)
+    # The same pass gives the per-batch spread: events at each step's
+    # boundaries (between steps, where no programmatic edge is crossed).
     other_ms = [0.0]
+    oev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nb)]
+    sev = [torch.cuda.Event(enable_timing=True) for _ in range(nb + 1)]
+    for e in [x for e4 in oev for x in e4] + sev:
+        e.record(stream)
+    sev[0].record(stream)
+    for k in range(nb):
+        step(k, oev[k], roles=("fwd",) if wl.has_backward else ())
+        sev[k + 1].record(stream)
+    torch.cuda.synchronize()
     if wl.has_backward:
-        oev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nb)]
-        for e4 in oev:
-            for e in e4:
-                e.record(stream)
-        for k in range(nb):
-            step(k, oev[k], roles=("fwd",))
-        torch.cuda.synchronize()
         other_ms = [e[0].elapsed_time(e[1]) for e in oev]
+    per_batch = sorted(flops[k][2] / (sev[k].elapsed_time(sev[k + 1]) * 1e-3) / 1e12 for k in range(nb))
     step_flops = [flops[k % nb] for k in range(args.steps)]
     tot_flops = sum(f[2] for f in step_flops)
     for pr in probs:
@@ -584,6 +589,9 @@ def run_gpu(args, wl, rank, world, local_rank):
             "kernel_times": (f"{dom}: events around every launch in the timed region; "
                              + ("fwd: a separate untimed pass over the resident batches" if dom == "bwd"
                                 else "no backward kernel")),
+            "per_batch": {"unit": UNIT, "min": per_batch[0], "median": statistics.median(per_batch),
+                          "max": per_batch[-1],
+                          "note": "each resident batch once, in a separate untimed pass with step-boundary events"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clocks}
     print(json.dumps(line), flush=True)
