@@ -8,6 +8,7 @@ ranking task; wmrh.cn RecSDK page, compound causal + context/target mask).
 bench.py takes the count from a closed form per sequence; here it is the sum
 of an explicit [n, n] visibility matrix built from whole-matrix pieces.
 """
+import json
 import types
 
 import numpy as np
@@ -74,3 +75,23 @@ def test_delta_forward_counts_candidate_rows_only():
     assert bw == 0 and tot == f
     assert f == _dense_pairs(b, rows="candidates") * 2 * (128 + 128)
 
+
+
+def test_source_hash_ignores_comments_only():
+    code = "int a = 1;  // one\n/* block\n comment */\nint b = a;\n\n"
+    assert bench._code_only(code) == bench._code_only("int a = 1;\nint b = a;")
+    assert bench._code_only(code) != bench._code_only("int a = 2;\nint b = a;")
+
+
+def test_traffic_record_is_used_only_on_the_sources_it_was_taken_on(monkeypatch, tmp_path):
+    # a DRAM-traffic record counts only while the kernel's code hashes to the
+    # value stored with the capture; any other code gives no record (null)
+    (tmp_path / "profiles").mkdir()
+    rec = {"dram_bytes_per_token": 1.0, "sources_sha": "abc", "profile": "p"}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"w:bwd": rec}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_sources_sha", lambda role: "abc" if role == "bwd" else "zzz")
+    assert bench.traffic_record("w:bwd") == rec
+    monkeypatch.setattr(bench, "kernel_sources_sha", lambda role: "def")
+    assert bench.traffic_record("w:bwd") is None
+    assert bench.traffic_record("w:fwd") is None
