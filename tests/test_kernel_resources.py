@@ -1,0 +1,64 @@
+"""Register budget of the tensor-core attention kernels, read from the
+compiler's resource report (ptxas -v) on the CPU.
+
+Both kernels run 18 warps per CTA under a 96-register cap (20 warps are
+charged: 20 x 32 x 96 = 61,440 of the SM's 65,536 registers), so every
+spill is a local-memory round trip inside the per-score epilogue.  The
+backward compiles spill-free; the forward variant the benchmark runs
+(d = 128, FP32 outputs) spills 8 bytes.  A change
+that adds spills shows here before it is timed.
+"""
+import os
+import re
+import shutil
+import subprocess
+import tempfile
+
+import pytest
+
+from hstu_jagged_attention_02_gb300 import build as B
+
+NVCC = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+pytestmark = pytest.mark.skipif(not os.path.exists(NVCC), reason="needs nvcc")
+
+
+def _resources(src):
+    with tempfile.TemporaryDirectory() as d:
+        cmd = [NVCC, "-Xptxas=-v", *B.ARCH, *B.FLAGS, "-c", os.path.join(B.CSRC, src), "-o",
+               os.path.join(d, "k.o")]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-2000:]
+    out, name = {}, None
+    for line in r.stderr.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            name = m.group(1)
+            continue
+        if name is None:
+            continue
+        m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
+        if m:
+            out.setdefault(name, {})["spill"] = int(m.group(1)) + int(m.group(2))
+        m = re.search(r"Used (\d+) registers", line)
+        if m:
+            out.setdefault(name, {})["regs"] = int(m.group(1))
+    return out
+
+
+def test_backward_kernel_is_spill_free_at_96_registers():
+    res = {k: v for k, v in _resources("hstu_tc_bwd.cu").items() if "hstu_bwd_tc_kernel" in k}
+    assert res, "backward kernel not found in the resource report"
+    for name, r in res.items():
+        assert r["regs"] <= 96, name
+        assert r["spill"] == 0, (name, r)
+
+
+def test_forward_kernel_spill_stays_within_its_budget():
+    res = {k: v for k, v in _resources("hstu_tc_fwd.cu").items() if "hstu_fwd_tc_kernel" in k}
+    assert res, "forward kernel not found in the resource report"
+    for r in res.values():
+        assert r["regs"] <= 96
+    # the benchmarked variant: d = 128, FP32 outputs, not the delta forward
+    bench = [r for k, r in res.items() if "hstu_fwd_tc_kernelILi128EfLb0E" in k]
+    assert len(bench) == 1
+    assert bench[0]["spill"] <= 16, bench[0]     # 8 stores + 8 loads
