@@ -3,7 +3,7 @@ compiler's resource report (ptxas -v) on the CPU.
 
 Both kernels run 18 warps per CTA under a 96-register cap (20 warps are
 charged: 20 x 32 x 96 = 61,440 of the SM's 65,536 registers); a spill
-costs local-memory round trips, and added spills measured as slower steps
+costs local-memory round trips, and added spills measured slower or no faster
 every time they appeared.  The backward compiles spill-free; the forward
 variant the benchmark runs (d = 128, FP32 outputs) spills 8 bytes.  A
 change that adds spills shows here before it is timed.
