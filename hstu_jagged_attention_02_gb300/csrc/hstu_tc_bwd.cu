@@ -11,7 +11,7 @@
 //   dZ   = mask ? dA SiLU'(z) / N : 0,    SiLU'(z) = s (1 + z (1 - s))
 //   dV  += A^T dO                         (A from its own TMEM buffer, hi/lo)
 //   dK  += dZ^T Q                         (dZ^T staged in SMEM, hi/lo)
-//   dQ^T = K^T dZ^T                       (both MN-major in SMEM) -> FP32 red
+//   dQ^T = K^T dZ^T                       (both MN-major in SMEM) -> TMA reduce-add into FP32 dq
 //   d_rab[bucket] += dZ                   (per-CTA partial sums, summed after)
 // S^T and dA^T are released as soon as the epilogue has loaded them, so the
 // next tile's S^T and dA^T are computed while this tile's A and dZ are; the
@@ -22,9 +22,10 @@
 //
 // Roles (576 threads): warps 0-15 epilogue (TMEM lane quarter warp%4, column
 // quarter warp/4), warp 16 TMA producer, warp 17 MMA issuer and TMEM owner.
-// The planner lists the key blocks longest-first and the producer takes the
-// next work item from a global counter (greedy LPT), passing it to the other
-// roles in a shared-memory slot with the item's key timestamps.
+// The planner lists the key blocks longest-first and the producer takes its
+// block index as its first work item and every later one from a global
+// counter (greedy LPT), passing it to the other roles in a shared-memory slot
+// with the item's key timestamps.
 #include "hstu_internal.h"
 #include "tc_ptx.cuh"
 

@@ -26,8 +26,8 @@
 // TMEM columns: S/P buffers at 0 and 128, O buffers at 256 and 256 + d.
 //
 // Scheduling: the planner lists the query blocks longest-first; the producer
-// of each CTA takes the next work item from a global counter (greedy LPT,
-// dynamic), and passes it to the other roles through a shared-memory slot
+// of each CTA takes its block index as its first work item and every later
+// one from a global counter (greedy LPT, dynamic), and passes it to the other roles through a shared-memory slot
 // that travels with one of two Q buffers, so the next item's Q and first K/V
 // are loading while the current item's last tiles are computed.
 #include "hstu_internal.h"
