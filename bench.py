@@ -96,7 +96,7 @@ class ClockSampler:
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
-        except Exception:
+        except OSError:   # no nvidia-smi: the line says so
             self.proc = None
 
     def stop(self):
@@ -106,8 +106,8 @@ class ClockSampler:
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
+        except subprocess.TimeoutExpired:
+            self.proc.kill()   # the sampler this object started
         self.f.flush()
         self.f.seek(0)
         rows = [ln.strip().split(",") for ln in self.f.read().splitlines() if ln.strip()]
@@ -168,12 +168,13 @@ def traffic_record(kernel_role: str):
     if not os.path.exists(path):
         return None
     try:
-        d = json.load(open(path))
-        rec = d.get(kernel_role)
-        if rec and rec.get("sources_sha") == kernel_sources_sha(kernel_role.split(":")[1]):
-            return rec
-    except Exception:
-        pass
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):   # unreadable or malformed record: no traffic figure
+        return None
+    rec = d.get(kernel_role)
+    if rec and rec.get("sources_sha") == kernel_sources_sha(kernel_role.split(":")[1]):
+        return rec
     return None
 
 
