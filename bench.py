@@ -550,7 +550,8 @@ def run_gpu(args, wl, rank, world, local_rank):
     mean_tokens = float(np.mean([batches[k % nb].T for k in range(args.steps)]))
     traffic = tr["dram_bytes_per_token"] * mean_tokens if tr else None
     common = {"traffic": traffic, "kernel": f"attention {dom} kernel",
-              "traffic_source": (f"{tr['profile']} (per-token DRAM bytes x {mean_tokens:.0f} tokens)" if tr else
+              "traffic_source": (f"ncu capture `{tr['capture']}` of {tr['capture_tokens']} tokens, sources "
+                                 f"{tr['sources_sha']} (per-token DRAM bytes x {mean_tokens:.0f} tokens)" if tr else
                                  "no capture on the current kernel sources"),
               "avg_launch_ms": sum(dom_ms) / len(dom_ms), "share_of_step": sum(dom_ms) / elapsed_ms,
               "algorithmic_bytes_per_launch": sum(dom_bytes) / len(dom_bytes),

@@ -11,23 +11,17 @@
 // The buffer is a file-scope __device__ array of kScratchBytes; every GPU that
 // loads the library holds it until the process exits.  Host code cannot hand
 // the array's name to a kernel (on the host it is only a stand-in, not a
-// device address), so the first call on each device looks its device address
-// up with cudaGetSymbolAddress while that device is current.
+// device address), so every call looks its device address up with
+// cudaGetSymbolAddress while the stream's device is current.  The lookup is a
+// host call and is not cached: a cached address would outlive a device reset
+// (cudaDeviceReset) or a new context and then point at freed memory.
 #include <cstdio>
-#include <mutex>
 
 #include "hstu_internal.h"
 
 static constexpr size_t kScratchBytes = size_t(1) << 20;  // 1 MiB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
-
-namespace {
-
-std::mutex g_scratch_mu;
-void* g_scratch_addr[64] = {};  // per device
-
-}  // namespace
 
 extern "C" hstu_status_t hstu_attn_fwd_noalloc(const hstu_attn_desc* desc, const hstu_attn_fwd_args* args,
                                                hstu_stream_t stream, int32_t* host_device_error) {
@@ -41,25 +35,26 @@ extern "C" hstu_status_t hstu_attn_fwd_noalloc(const hstu_attn_desc* desc, const
     hstu::set_detail_message(msg);
     return HSTU_ERR_WORKSPACE;
   }
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+  // the scratch belongs to the current device: a stream of another device
+  // would run the kernels against memory of the wrong GPU
+  int dev = -1, stream_dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaStreamGetDevice(reinterpret_cast<cudaStream_t>(stream), &stream_dev);
+  if (e != cudaSuccess) {
     (void)cudaGetLastError();
+    hstu::set_error_detail(e, "cudaGetDevice / cudaStreamGetDevice before the built-in forward scratch");
     return HSTU_ERR_CUDA;
   }
+  if (stream_dev != dev) {
+    hstu::set_detail_message("the stream belongs to another device than the current one");
+    return HSTU_ERR_INVALID_ARG;
+  }
   void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-      void* ptr = nullptr;
-      const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-      if (e != cudaSuccess || ptr == nullptr) {
-        (void)cudaGetLastError();
-        hstu::set_error_detail(e, "cudaGetSymbolAddress of the built-in forward scratch");
-        return HSTU_ERR_CUDA;
-      }
-      g_scratch_addr[dev] = ptr;
-    }
-    scratch = g_scratch_addr[dev];
+  e = cudaGetSymbolAddress(&scratch, g_noalloc_scratch);
+  if (e != cudaSuccess || scratch == nullptr) {
+    (void)cudaGetLastError();
+    hstu::set_error_detail(e, "cudaGetSymbolAddress of the built-in forward scratch");
+    return HSTU_ERR_CUDA;
   }
   // The planner rewrites the whole plan region, header first, on every call,
   // so nothing left by an earlier call is read.

@@ -38,7 +38,10 @@
  *  - Every pointer is a device pointer except the host_* outputs of
  *    hstu_attn_debug_plan and hstu_get_device_error.  The caller owns every
  *    buffer, including the workspace; the library never allocates device
- *    memory and keeps no state between calls.
+ *    memory and keeps no state between calls.  The one exception is
+ *    hstu_attn_fwd_noalloc: it uses a fixed buffer built into the library
+ *    in place of a workspace, shared by all its calls on a device (its own
+ *    comment gives the size limit and the race between overlapping calls).
  *  - Calls are stream-ordered and return without synchronising, except
  *    hstu_attn_debug_plan and hstu_get_device_error, which synchronise the
  *    given stream.  Concurrent calls must use distinct workspaces.
@@ -210,12 +213,15 @@ hstu_status_t hstu_attn_debug_plan(const hstu_attn_desc* desc, const int64_t* se
  * tokens in 4,000 sequences.  Larger problems return HSTU_ERR_WORKSPACE
  * (hstu_last_error_detail says how much was needed) without launching.
  *
- * The first call on each device looks up the buffer's device address with
- * that device current, so make that first call before any stream capture.
- * Every call shares the one buffer: calls that may overlap on the GPU (other
- * streams, other host threads) race and must be serialised by the caller.
- * The buffer keeps the last call's contents; the planner rewrites everything
- * it reads on every call.
+ * Each call looks up the buffer's device address (cudaGetSymbolAddress) with
+ * the current device, which must be the stream's device (else
+ * HSTU_ERR_INVALID_ARG).  The address is not cached, so a device reset
+ * between calls does not leave a stale pointer behind.  The first call on a
+ * device may load the library's device code, so make that first call before
+ * any stream capture.  Every call shares the one buffer: calls that may
+ * overlap on the GPU (other streams, other host threads) race and must be
+ * serialised by the caller.  The buffer keeps the last call's contents; the
+ * planner rewrites everything it reads on every call.
  *
  * host_device_error: NULL, or a host int32 that receives the call's device
  * error code (as hstu_get_device_error reports it); non-NULL makes the call

@@ -87,7 +87,7 @@ def test_traffic_record_is_used_only_on_the_sources_it_was_taken_on(monkeypatch,
     # a DRAM-traffic record counts only while the kernel's code hashes to the
     # value stored with the capture; any other code gives no record (null)
     (tmp_path / "profiles").mkdir()
-    rec = {"dram_bytes_per_token": 1.0, "sources_sha": "abc", "profile": "p"}
+    rec = {"dram_bytes_per_token": 1.0, "sources_sha": "abc", "capture": "ncu ...", "capture_tokens": 10}
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"w:bwd": rec}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "kernel_sources_sha", lambda role: "abc" if role == "bwd" else "zzz")
