@@ -72,7 +72,8 @@ struct Lay {
   static constexpr int DZ_BYTES = BK * 128;
   static constexpr int TS64_OFF = DZ_OFF + 2 * DZ_BYTES;     // int64 [kQStages][BQ] absolute
   static constexpr int TS32_OFF = TS64_OFF + kQStages * BQ * 8;  // int32 [kQStages][BQ] relative
-  static constexpr int KTS_OFF = TS32_OFF + kQStages * BQ * 4;   // int64 [BK] key times of the item
+  static constexpr int CMM_OFF = TS32_OFF + kQStages * BQ * 4;   // int32 [kQStages][4 chunks][min, max] relative
+  static constexpr int KTS_OFF = CMM_OFF + kQStages * 8 * 4;     // int64 [BK] key times of the item
   static constexpr int SLOT_OFF = KTS_OFF + BK * 8;              // ItemSlot
   static constexpr int BAR_OFF = SLOT_OFF + (int)sizeof(ItemSlot);
   static constexpr int MISC_OFF = BAR_OFF + BAR_COUNT * 8;
@@ -223,8 +224,41 @@ __device__ __forceinline__ void grad_cols(const AttnParams& p, const uint32_t (&
   }
 }
 
-// Registers go to a block in groups of 4 warps: 18 warps are charged as 20,
-// and 20 x 32 threads x 96 registers = 61440 <= 65536.
+// All 16 query columns of this thread's key row are allowed and see one
+// bias value rb (scaled by -log2 e): the position bucket is saturated and the
+// time bucket is the same for every column.  A and dZ as packed BF16 hi/lo
+// pairs; returns the sum of the 16 dZ (their one d_rab bucket each).
+// kC and inv_n are the score constants, or 0 for a key row past the
+// sequence, which then yields exact zeros.
+__device__ __forceinline__ float grad_fast16(const AttnParams& p, const uint32_t (&sv)[16], const uint32_t (&dav)[16],
+                                             float rb, float kC, float inv_n, uint32_t (&ahi)[8], uint32_t (&alo)[8],
+                                             uint32_t (&zhi)[8], uint32_t (&zlo)[8]) {
+  const float2 b2 = make_float2(rb, rb), one2 = make_float2(1.f, 1.f), inv_n2 = make_float2(inv_n, inv_n);
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < 16; c += 2) {
+    const float2 w2 = __ffma2_rn(p.kA2, make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), b2);
+    const float2 d2 = __fadd2_rn(one2, make_float2(ex2_approx(w2.x), ex2_approx(w2.y)));
+    const float2 sg2 = make_float2(rcp_approx(d2.x), rcp_approx(d2.y));
+    const float2 z2 = make_float2(w2.x * p.kZ, w2.y * p.kZ);
+    const float2 a2 = __fmul2_rn(make_float2(w2.x * kC, w2.y * kC), sg2);
+    const float2 f2 = __ffma2_rn(z2, fsub2(one2, sg2), one2);  // 1 + z (1 - sg)
+    const float2 h2 = __fmul2_rn(__fmul2_rn(make_float2(__uint_as_float(dav[c]), __uint_as_float(dav[c + 1])), sg2), f2);
+    const float2 g2 = __fmul2_rn(h2, inv_n2);
+    acc = __fadd2_rn(acc, g2);
+    const uint32_t ah = pack_bf16(a2.x, a2.y), zh = pack_bf16(g2.x, g2.y);
+    ahi[c >> 1] = ah;
+    zhi[c >> 1] = zh;
+    const float2 al = bf16_residual2(a2, ah), zl = bf16_residual2(g2, zh);
+    alo[c >> 1] = pack_bf16(al.x, al.y);
+    zlo[c >> 1] = pack_bf16(zl.x, zl.y);
+  }
+  return acc.x + acc.y;
+}
+
+// Warps are spread over the four SM sub-partitions, each with a quarter of the
+// register file: with 18 warps two sub-partitions hold five,
+// and 5 x 32 threads x 96 registers = 15360 <= 16384.
 template <typename TO>
 __global__ void __maxnreg__(96)
 hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmq,
@@ -239,6 +273,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   const uint32_t sQS = base_u32 + Lay::QS_OFF, sDZ = base_u32 + Lay::DZ_OFF;
   int64_t* ts64_s = reinterpret_cast<int64_t*>(base + Lay::TS64_OFF);
   int32_t* ts32_s = reinterpret_cast<int32_t*>(base + Lay::TS32_OFF);
+  int32_t* cmm_s = reinterpret_cast<int32_t*>(base + Lay::CMM_OFF);
   int64_t* kts_s = reinterpret_cast<int64_t*>(base + Lay::KTS_OFF);
   ItemSlot* slot = reinterpret_cast<ItemSlot*>(base + Lay::SLOT_OFF);
   const uint32_t bar0 = base_u32 + Lay::BAR_OFF;
@@ -393,13 +428,35 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
             tma_load_2d(dst + Lay::Q_BYTES + c * Lay::QBOX, &tmdh, full, h * D + c * 64, y);
             tma_load_2d(dst + 2 * Lay::Q_BYTES + c * Lay::QBOX, &tmdl, full, h * D + c * 64, y);
           }
+          // the query tile two ahead into L2, so its loads do not wait on HBM
+          if (qt + 2 < nqt) {
+            for (int c = 0; c < 2; ++c) {
+              tma_prefetch_l2_2d(&tmq, h * D + c * 64, y + 2 * BQ);
+              tma_prefetch_l2_2d(&tmdh, h * D + c * 64, y + 2 * BQ);
+              tma_prefetch_l2_2d(&tmdl, h * D + c * 64, y + 2 * BQ);
+            }
+          }
         }
         bool qw = false;
 #pragma unroll
         for (int x = 0; x < BQ / 32; ++x) {
+          const int32_t r = (int32_t)(tv[x] - tbase);
           ts64_s[stage * BQ + lane + 32 * x] = tv[x];
-          ts32_s[stage * BQ + lane + 32 * x] = (int32_t)(tv[x] - tbase);
+          ts32_s[stage * BQ + lane + 32 * x] = r;
           qw |= ts_wide(tv[x] - tbase);
+          // min and max relative time of each 16-query chunk (lanes 0-15
+          // and 16-31 of this 32-query half), for the epilogue's test for a
+          // time bucket that is the same across a chunk
+          int mn = r, mx = r;
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) {
+            mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          }
+          if ((lane & 15) == 0) {
+            cmm_s[stage * 8 + (2 * x + (lane >> 4)) * 2] = mn;
+            cmm_s[stage * 8 + (2 * x + (lane >> 4)) * 2 + 1] = mx;
+          }
         }
         qw = __any_sync(0xffffffffu, qw);
         if (lane == 0) stage_wide[stage] = qw ? 1 : 0;
@@ -424,46 +481,47 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       constexpr uint32_t IDESC_DQ = idesc_bf16(D, BQ, true, true);      // A = K^T, B = dZ^T, MN-major
       uint32_t item_it = 0, qt_it = 0;
       bool ok = true;
-      // dQ^T = K^T dZ^T, dV += A^T dO, dK += dZ^T Q of query tile g (stage st).
-      // dQ^T goes first: it is the last reader of K, so on an item's last
-      // tile the K/V buffer is released before dV and dK, and the next item's
-      // K/V load overlaps them.  DQFULL still follows all of them.
+      // Shared-memory descriptors, built once; every MMA below moves a start
+      // address by a constant (one add on the low descriptor word).
+      //  K-major operands (rows of 128 bytes): K, V, and per stage Q, dO_hi, dO_lo
+      //  MN-major operands: K^T (dQ), dO_hi/lo (dV), Q (dK B), dZ^T (dQ B)
+      const SDesc k_km = sdesc_w(sK, 16, 1024), v_km = sdesc_w(sV, 16, 1024);
+      const SDesc q_km = sdesc_w(sQS, 16, 1024);
+      const SDesc k_mn = sdesc_w(sK, Lay::KBOX, 1024);
+      const SDesc q_mn = sdesc_w(sQS, Lay::QBOX, 1024);
+      const SDesc zh_mn = sdesc_w(sDZ, Lay::DZ_BYTES, 1024), zl_mn = sdesc_w(sDZ + Lay::DZ_BYTES, Lay::DZ_BYTES, 1024);
+      const SDesc zh_km = sdesc_w(sDZ, 16, 1024), zl_km = sdesc_w(sDZ + Lay::DZ_BYTES, 16, 1024);
+      // dV += A^T dO (3 products: A_hi dO_hi, A_lo dO_hi, A_hi dO_lo) and
+      // dK += dZ^T Q (2) of query tile g, which read the Q stage st; then
+      // the stage is released, and dQ^T = K^T dZ^T (2) follows.  DQFULL
+      // comes after all of them (A in TMEM and the dZ^T staging are free
+      // again); on an item's last tile K/V is released after dQ^T.
       auto issue_grad = [&](uint32_t g, uint32_t st, bool first, bool last) -> bool {
-        if (!mbar_wait(bar(BAR_PREADY), g & 1, wd, 26) ||
-            !mbar_wait(bar(BAR_DQEMPTY), (g & 1) ^ 1, wd, 27))
-          return false;
+        if (!mbar_wait(bar(BAR_PREADY), g & 1, wd, 26)) return false;
         if (first && !mbar_wait(bar(BAR_DKVEMPTY), (item_it & 1) ^ 1, wd, 24)) return false;
         fence_after_sync();
-        const uint32_t sQ = sQS + st * Lay::QSTAGE;
-        const uint32_t sDh = sQ + Lay::Q_BYTES, sDl = sQ + 2 * Lay::Q_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {   // K = 128 keys: 8 steps of 16
-          const uint64_t ak = sdesc_sw128(sK + kk * 2048, Lay::KBOX, 1024);
-          mma_ss(tmem + DQ_COL, ak, sdesc_sw128(sDZ + kk * 2048, Lay::DZ_BYTES, 1024), IDESC_DQ,
-                 kk > 0 ? 1u : 0u);
-          mma_ss(tmem + DQ_COL, ak, sdesc_sw128(sDZ + Lay::DZ_BYTES + kk * 2048, Lay::DZ_BYTES, 1024),
-                 IDESC_DQ, 1u);
-        }
-        if (last) mma_commit(bar(BAR_KVEMPTY));   // K and V of this item are read by no later MMA
+        const uint32_t so = st * Lay::QSTAGE;
+        const SDesc q_s = q_mn + so, dh_s = q_mn + (so + Lay::Q_BYTES), dl_s = q_mn + (so + 2 * Lay::Q_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {   // K = 64 queries: 4 steps of 16
           const uint32_t a_hi = tmem + A_COL + 16u * kk;
-          const uint64_t bdh = sdesc_sw128(sDh + kk * 2048, Lay::QBOX, 1024);
-          const uint64_t bdl = sdesc_sw128(sDl + kk * 2048, Lay::QBOX, 1024);
-          const uint64_t bq = sdesc_sw128(sQ + kk * 2048, Lay::QBOX, 1024);
-          const uint64_t zh = sdesc_sw128(sDZ + kk * 32, 16, 1024);
-          const uint64_t zl = sdesc_sw128(sDZ + Lay::DZ_BYTES + kk * 32, 16, 1024);
           const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
-          mma_ts(tmem + DV_COL, a_hi, bdh, IDESC_DVK, acc0);
-          mma_ts(tmem + DV_COL, a_hi + 8, bdh, IDESC_DVK, 1u);
-          mma_ts(tmem + DV_COL, a_hi, bdl, IDESC_DVK, 1u);
-          mma_ss(tmem + DK_COL, zh, bq, IDESC_DVK, acc0);
-          mma_ss(tmem + DK_COL, zl, bq, IDESC_DVK, 1u);
+          mma_ts_w(tmem + DV_COL, a_hi, dh_s + kk * 2048, IDESC_DVK, acc0);
+          mma_ts_w(tmem + DV_COL, a_hi + 8, dh_s + kk * 2048, IDESC_DVK, 1u);
+          mma_ts_w(tmem + DV_COL, a_hi, dl_s + kk * 2048, IDESC_DVK, 1u);
+          mma_ss_w(tmem + DK_COL, zh_km + kk * 32, q_s + kk * 2048, IDESC_DVK, acc0);
+          mma_ss_w(tmem + DK_COL, zl_km + kk * 32, q_s + kk * 2048, IDESC_DVK, 1u);
         }
-        // the epilogue takes DQFULL to mean every gradient MMA of the tile is
-        // done (A in TMEM and the dZ^T staging are free again)
+        mma_commit(bar(BAR_QEMPTY + st));   // the Q / dO stage is read by no later MMA
+        if (!mbar_wait(bar(BAR_DQEMPTY), (g & 1) ^ 1, wd, 27)) return false;
+        fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {   // K = 128 keys: 8 steps of 16
+          mma_ss_w(tmem + DQ_COL, k_mn + kk * 2048, zh_mn + kk * 2048, IDESC_DQ, kk > 0 ? 1u : 0u);
+          mma_ss_w(tmem + DQ_COL, k_mn + kk * 2048, zl_mn + kk * 2048, IDESC_DQ, 1u);
+        }
+        if (last) mma_commit(bar(BAR_KVEMPTY));   // K and V of this item are read by no later MMA
         mma_commit(bar(BAR_DQFULL));
-        mma_commit(bar(BAR_QEMPTY + st));
         return true;
       };
       while (ok) {
@@ -482,23 +540,21 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
                mbar_wait(bar(BAR_SEMPTY), (qt_it & 1) ^ 1, wd, 28);
           if (!ok) break;
           fence_after_sync();
-          const uint32_t sQ = sQS + stage * Lay::QSTAGE;
-          const uint32_t sDh = sQ + Lay::Q_BYTES, sDl = sQ + 2 * Lay::Q_BYTES;
+          const uint32_t so = stage * Lay::QSTAGE;
+          const SDesc q_s = q_km + so, dh_s = q_km + (so + Lay::Q_BYTES), dl_s = q_km + (so + 2 * Lay::Q_BYTES);
           // S^T = K Q^T ; dA^T = V dO_hi^T + V dO_lo^T
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ka = (kk >> 2) * Lay::KBOX + (kk & 3) * 32;
             const uint32_t qb = (kk >> 2) * Lay::QBOX + (kk & 3) * 32;
-            mma_ss(tmem + S_COL, sdesc_sw128(sK + ka, 16, 1024), sdesc_sw128(sQ + qb, 16, 1024), IDESC_S,
-                   kk > 0 ? 1u : 0u);
+            mma_ss_w(tmem + S_COL, k_km + ka, q_s + qb, IDESC_S, kk > 0 ? 1u : 0u);
           }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ka = (kk >> 2) * Lay::KBOX + (kk & 3) * 32;
             const uint32_t qb = (kk >> 2) * Lay::QBOX + (kk & 3) * 32;
-            const uint64_t av = sdesc_sw128(sV + ka, 16, 1024);
-            mma_ss(tmem + DA_COL, av, sdesc_sw128(sDh + qb, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
-            mma_ss(tmem + DA_COL, av, sdesc_sw128(sDl + qb, 16, 1024), IDESC_S, 1u);
+            mma_ss_w(tmem + DA_COL, v_km + ka, dh_s + qb, IDESC_S, kk > 0 ? 1u : 0u);
+            mma_ss_w(tmem + DA_COL, v_km + ka, dl_s + qb, IDESC_S, 1u);
           }
           mma_commit(bar(BAR_SFULL));
           if (have_prev) {
@@ -612,39 +668,106 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_SEMPTY));   // S^T, dA^T may be overwritten now
-        // computed and written out in two halves of 8 query columns
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int c0 = hq * 16 + half * 8;    // first query column of this half within the tile
-          uint32_t sv[8], dav[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            sv[e] = svq[half * 8 + e];
-            dav[e] = daq[half * 8 + e];
+        const int c0 = hq * 16;   // first query column of this thread within the tile
+        const int ib = q0 + c0;
+        const bool narrow = !item_wide && !stage_wide[stage];
+        // Constant-bias test for this thread's 16 columns: all allowed, the
+        // position bucket saturated for all (checked at both ends, positions
+        // grow with the column), and the time bucket the same for all (the
+        // chunk's times all on one side of t_j, and the bucket of the
+        // nearest and of the farthest gap equal: buckets grow with the gap).
+        bool fast = narrow && ib >= kc.lo && ib + 15 <= kc.hi;
+        int btc = 0;
+        if (fast && has_rp) {
+          const int pa = ib < kc.h_end ? ib : kc.h_end;
+          const int pb = ib + 15 < kc.h_end ? ib + 15 : kc.h_end;
+          fast = pa - kc.pos_j >= P - 1 || kc.pos_j - pb >= P - 1;
+        }
+        if (fast && has_rt) {
+          const int32_t cmin = cmm_s[stage * 8 + hq * 2], cmax = cmm_s[stage * 8 + hq * 2 + 1];
+          int32_t dlo, dhi;
+          if (kc.tj32 <= cmin) {
+            dlo = cmin - kc.tj32;
+            dhi = cmax - kc.tj32;
+          } else if (kc.tj32 >= cmax) {
+            dlo = kc.tj32 - cmax;
+            dhi = kc.tj32 - cmin;
+          } else {
+            dlo = 0;
+            dhi = 1;   // gaps of both signs: buckets differ
+            fast = false;
           }
-          const int ib = q0 + c0;
-          const int32_t* t32 = ts32_s + stage * BQ + c0;
-          const int64_t* t64 = ts64_s + stage * BQ + c0;
-          uint32_t ahi[4], alo[4], zhi[4], zlo[4];
-          if (!item_wide && !stage_wide[stage]) grad_cols<8, false>(p, sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc);
-          else grad_cols<8, true>(p, sv, dav, ahi, alo, zhi, zlo, kc, ib, t32, t64, racc);
-          if (half == 0 && pend) {
+          const int blo = min(32 - __clz(dlo), Tb - 1), bhi = min(32 - __clz(dhi), Tb - 1);
+          fast = fast && blo == bhi;
+          btc = blo;
+        }
+        // a key row past the sequence takes the same path with zero
+        // constants: its A and dZ (which the dQ products read) are exact zeros
+        if (__all_sync(0xffffffffu, fast || !j_ok)) {
+          uint32_t ahi[8], alo[8], zhi[8], zlo[8];
+          const float rb = kc.tp[P - 1] + kc.tp[P + btc];
+          const float sum = grad_fast16(p, svq, daq, rb, j_ok ? p.kC : 0.f, j_ok ? p.inv_n : 0.f, ahi, alo, zhi, zlo);
+          if (want_rp) racc.rp_far += sum;
+          if (want_rt) {
+            if (btc == racc.rt_cur) {
+              racc.rt_run += sum;
+            } else {
+              red_add(kc.drp + P + racc.rt_cur, racc.rt_run, racc.rt_cur >= 0);
+              racc.rt_cur = btc;
+              racc.rt_run = sum;
+            }
+          }
+          if (pend) {
             // the previous tile's gradient MMAs are complete once its dQ^T is:
             // the A buffer and the dZ^T staging are free again
             ok = drain_dq(qt_it - 1, pend_q0, s0, hh);
             if (!ok) break;
             pend = false;
           }
-          // A into its TMEM buffer.  Quarter hq owns columns [16 hq, 16 hq + 16):
-          // hi pairs in the first 8, lo pairs in the last 8; this half's 8
-          // queries are 4 packed columns of each.
-          tmem_st4(lane_base + A_COL + hq * 16 + half * 4, ahi);
-          tmem_st4(lane_base + A_COL + hq * 16 + 8 + half * 4, alo);
-          // dZ^T into SMEM (row = key, 64 queries = 128 B, 128-byte swizzle) for the dK and dQ MMAs
+          tmem_st8(lane_base + A_COL + hq * 16, ahi);
+          tmem_st8(lane_base + A_COL + hq * 16 + 8, alo);
           const uint32_t rowh = sDZ + (uint32_t)lrow * 128u, rowl = rowh + Lay::DZ_BYTES;
-          const uint32_t chunk = (uint32_t)((hq * 2 + half) ^ (lrow & 7));
-          st_shared_v4(rowh + chunk * 16, zhi[0], zhi[1], zhi[2], zhi[3]);
-          st_shared_v4(rowl + chunk * 16, zlo[0], zlo[1], zlo[2], zlo[3]);
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t chunk = (uint32_t)((hq * 2 + half) ^ (lrow & 7));
+            st_shared_v4(rowh + chunk * 16, zhi[4 * half], zhi[4 * half + 1], zhi[4 * half + 2], zhi[4 * half + 3]);
+            st_shared_v4(rowl + chunk * 16, zlo[4 * half], zlo[4 * half + 1], zlo[4 * half + 2], zlo[4 * half + 3]);
+          }
+        } else {
+          // computed and written out in two halves of 8 query columns
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int hc0 = c0 + half * 8;    // first query column of this half within the tile
+            uint32_t sv[8], dav[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              sv[e] = svq[half * 8 + e];
+              dav[e] = daq[half * 8 + e];
+            }
+            const int hib = q0 + hc0;
+            const int32_t* t32 = ts32_s + stage * BQ + hc0;
+            const int64_t* t64 = ts64_s + stage * BQ + hc0;
+            uint32_t ahi[4], alo[4], zhi[4], zlo[4];
+            if (narrow) grad_cols<8, false>(p, sv, dav, ahi, alo, zhi, zlo, kc, hib, t32, t64, racc);
+            else grad_cols<8, true>(p, sv, dav, ahi, alo, zhi, zlo, kc, hib, t32, t64, racc);
+            if (half == 0 && pend) {
+              // the previous tile's gradient MMAs are complete once its dQ^T is:
+              // the A buffer and the dZ^T staging are free again
+              ok = drain_dq(qt_it - 1, pend_q0, s0, hh);
+              if (!ok) break;
+              pend = false;
+            }
+            // A into its TMEM buffer.  Quarter hq owns columns [16 hq, 16 hq + 16):
+            // hi pairs in the first 8, lo pairs in the last 8; this half's 8
+            // queries are 4 packed columns of each.
+            tmem_st4(lane_base + A_COL + hq * 16 + half * 4, ahi);
+            tmem_st4(lane_base + A_COL + hq * 16 + 8 + half * 4, alo);
+            // dZ^T into SMEM (row = key, 64 queries = 128 B, 128-byte swizzle) for the dK and dQ MMAs
+            const uint32_t rowh = sDZ + (uint32_t)lrow * 128u, rowl = rowh + Lay::DZ_BYTES;
+            const uint32_t chunk = (uint32_t)((hq * 2 + half) ^ (lrow & 7));
+            st_shared_v4(rowh + chunk * 16, zhi[0], zhi[1], zhi[2], zhi[3]);
+            st_shared_v4(rowl + chunk * 16, zlo[0], zlo[1], zlo[2], zlo[3]);
+          }
         }
         if (!ok) break;
         fence_async_smem();

@@ -20,9 +20,13 @@
 // c = -1 / (log2(e) N); the bias tables are stored pre-multiplied by
 // -log2(e) so one FFMA gives w.
 //
-// Roles (576 threads): warps 0-15 epilogue (warp w reads TMEM lanes
+// Roles (608 threads): warps 0-15 epilogue (warp w reads TMEM lanes
 // 32*(w%4).. and the 32-column quarter w/4 of each tile), warp 16 TMA
-// producer (plus timestamps), warp 17 MMA issuer and TMEM owner.
+// producer of Q and K (plus the key timestamps), warp 17 MMA issuer and TMEM
+// owner, warp 18 TMA producer of V.  K and V have rings of their own: a K
+// stage is free once its S = Q K^T is done, so the next tiles' K loads and
+// S products never wait for the P V of the tile before, which is what a
+// shared K/V stage made them do.
 // TMEM columns: S/P buffers at 0 and 128, O buffers at 256 and 256 + d.
 //
 // Scheduling: the planner lists the query blocks longest-first; the producer
@@ -41,18 +45,20 @@ using namespace tc;
 
 constexpr int BM = kTcTile, BN = kTcTile;
 constexpr int kEpiWarps = 16;
-constexpr int kProducerWarp = 16, kMmaWarp = 17;
-constexpr int kThreads = 18 * 32;
-constexpr int kStages = 2;
+constexpr int kProducerWarp = 16, kMmaWarp = 17, kVProducerWarp = 18;
+constexpr int kThreads = 19 * 32;
+constexpr int kStages = 2;      // K ring and V ring, each
+constexpr int kTsSlots = 4;     // key-timestamp slots, released by the epilogue
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSColStride = 128;  // S/P buffer sb starts at column sb * 128
 constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr int kQBufs = 2;
 
-enum : int { BAR_QFULL = 0, BAR_QEMPTY = BAR_QFULL + kQBufs, BAR_KVFULL = BAR_QEMPTY + kQBufs,
-             BAR_KVEMPTY = BAR_KVFULL + kStages,
-             BAR_SFULL = BAR_KVEMPTY + kStages, BAR_PREADY = BAR_SFULL + 2, BAR_OFULL = BAR_PREADY + 2,
+enum : int { BAR_QFULL = 0, BAR_QEMPTY = BAR_QFULL + kQBufs, BAR_KFULL = BAR_QEMPTY + kQBufs,
+             BAR_KEMPTY = BAR_KFULL + kStages, BAR_VFULL = BAR_KEMPTY + kStages, BAR_VEMPTY = BAR_VFULL + kStages,
+             BAR_TSFULL = BAR_VEMPTY + kStages, BAR_TSEMPTY = BAR_TSFULL + kTsSlots,
+             BAR_SFULL = BAR_TSEMPTY + kTsSlots, BAR_PREADY = BAR_SFULL + 2, BAR_OFULL = BAR_PREADY + 2,
              BAR_OEMPTY = BAR_OFULL + 2, BAR_DRAIN = BAR_OEMPTY + 2, BAR_COUNT };
 
 // A work item as the producer hands it to the other roles (one per Q buffer).
@@ -73,16 +79,17 @@ struct Layout {
   static constexpr int BOX = 128 * 128;         // one TMA box: 128 rows x 64 bf16 = 16 KB
   static constexpr int Q_BYTES = NCH * BOX;
   static constexpr int Q_OFF = 0;               // kQBufs Q buffers
-  static constexpr int K_BYTES = NCH * BOX;
-  static constexpr int STAGE = 2 * K_BYTES;     // K then V
-  static constexpr int KV_OFF = Q_OFF + kQBufs * Q_BYTES;
-  static constexpr int TS64_OFF = KV_OFF + kStages * STAGE;     // int64 [kStages][BN] key times, absolute
-  static constexpr int TS32_OFF = TS64_OFF + kStages * BN * 8;  // int32 [kStages][BN] relative
-  static constexpr int QTS_OFF = TS32_OFF + kStages * BN * 4;   // int64 [kQBufs][BM] query times
+  static constexpr int K_BYTES = NCH * BOX;     // one K or V stage
+  static constexpr int K_OFF = Q_OFF + kQBufs * Q_BYTES;        // K ring
+  static constexpr int V_OFF = K_OFF + kStages * K_BYTES;       // V ring
+  static constexpr int TS64_OFF = V_OFF + kStages * K_BYTES;    // int64 [kTsSlots][BN] key times, absolute
+  static constexpr int TS32_OFF = TS64_OFF + kTsSlots * BN * 8; // int32 [kTsSlots][BN] relative
+  static constexpr int CMM_OFF = TS32_OFF + kTsSlots * BN * 4;  // int32 [kTsSlots][4 chunks][min, max] relative
+  static constexpr int QTS_OFF = CMM_OFF + kTsSlots * 8 * 4;    // int64 [kQBufs][BM] query times
   static constexpr int SLOT_OFF = QTS_OFF + kQBufs * BM * 8;    // ItemSlot [kQBufs]
   static constexpr int BAR_OFF = SLOT_OFF + kQBufs * (int)sizeof(ItemSlot);
-  static constexpr int MISC_OFF = BAR_OFF + BAR_COUNT * 8;      // tmem slot, abort flag, per-stage wide flags
-  static constexpr int TAB_OFF = MISC_OFF + 16;                 // float [H][P + kTabTime]
+  static constexpr int MISC_OFF = BAR_OFF + BAR_COUNT * 8;      // tmem slot, abort flag, per-slot wide flags
+  static constexpr int TAB_OFF = MISC_OFF + 32;                 // float [H][P + kTabTime]
   static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
 };
 
@@ -219,8 +226,55 @@ __device__ __forceinline__ void score32(const AttnParams& p, const uint32_t (&sv
   }
 }
 
-// Registers go to a block in groups of 4 warps: 18 warps are charged as 20,
-// and 20 x 32 threads x 96 registers = 61440 <= 65536.
+// Scores of 32 key columns that are all allowed and share one bias value rb
+// (scaled by -log2 e): position bucket saturated, one time bucket.  With so
+// little else to do per score, the special-function unit (ex2 and rcp, two
+// per score) would set the pace; so 7 of every 8 reciprocals are taken by
+// Newton-Raphson on the FMA pipe instead (w is clamped at 64 there, where
+// SiLU(z) / N has long been zero to within its rounding, so 1 + 2^w stays
+// finite).  S is read and P written 16 columns at a time, which keeps few
+// registers live: P_hi of columns [0, 16) goes to scol + [0, 8) and P_lo to
+// scol + [16, 24), the columns of the second half's S, so that store waits
+// until the second half is loaded.
+__device__ __forceinline__ void score16_const(const AttnParams& p, const uint32_t (&sv)[16], uint32_t (&hi)[8],
+                                              uint32_t (&lo)[8], float rb) {
+  const float2 kA2 = make_float2(p.kA, p.kA), kC2 = make_float2(p.kC, p.kC), b2 = make_float2(rb, rb);
+  const float2 one2 = make_float2(1.f, 1.f);
+#pragma unroll
+  for (int c = 0; c < 16; c += 2) {
+    const float2 w2 = __ffma2_rn(kA2, make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), b2);
+    float2 r2;
+    if (c == 0) {
+      const float2 den = __fadd2_rn(make_float2(ex2_approx(w2.x), ex2_approx(w2.y)), one2);
+      r2 = __fmul2_rn(__fmul2_rn(w2, kC2), make_float2(rcp_approx(den.x), rcp_approx(den.y)));
+    } else {
+      const float2 den = __fadd2_rn(make_float2(ex2_approx(fminf(w2.x, 64.f)), ex2_approx(fminf(w2.y, 64.f))), one2);
+      r2 = __fmul2_rn(__fmul2_rn(w2, kC2), rcp2_newton(den));
+    }
+    const uint32_t h2 = pack_bf16(r2.x, r2.y);
+    hi[c >> 1] = h2;
+    const float2 l2 = bf16_residual2(r2, h2);
+    lo[c >> 1] = pack_bf16(l2.x, l2.y);
+  }
+}
+__device__ __forceinline__ void score32_const(const AttnParams& p, uint32_t scol, float rb) {
+  uint32_t sv[16], hi[8], lo0[8];
+  tmem_ld16(scol, sv);
+  tmem_wait_ld();
+  score16_const(p, sv, hi, lo0, rb);
+  tmem_st8(scol, hi);
+  tmem_ld16(scol + 16, sv);
+  tmem_wait_ld();
+  tmem_st8(scol + 16, lo0);
+  uint32_t lo[8];
+  score16_const(p, sv, hi, lo, rb);
+  tmem_st8(scol + 8, hi);
+  tmem_st8(scol + 24, lo);
+}
+
+// Warps are spread over the four SM sub-partitions, each with a quarter of the
+// register file: with 19 warps three sub-partitions hold five,
+// and 5 x 32 threads x 96 registers = 15360 <= 16384.
 // DELTA: the delta forward (KV-cached candidates): work items are blocks of
 // up to 128 candidates; their key tiles are every tile of the sequence's
 // cached K/V (tmk2, tmv2, offsets p.off2, times p.ts2) and then one tile of
@@ -236,16 +290,17 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
   const uint32_t sQ0 = base_u32 + L::Q_OFF;
-  const uint32_t sKV = base_u32 + L::KV_OFF;
+  const uint32_t sK0 = base_u32 + L::K_OFF, sV0 = base_u32 + L::V_OFF;
   int64_t* ts64_s = reinterpret_cast<int64_t*>(base + L::TS64_OFF);
   int32_t* ts32_s = reinterpret_cast<int32_t*>(base + L::TS32_OFF);
+  int32_t* cmm_s = reinterpret_cast<int32_t*>(base + L::CMM_OFF);
   int64_t* qts_s = reinterpret_cast<int64_t*>(base + L::QTS_OFF);
   ItemSlot* slots = reinterpret_cast<ItemSlot*>(base + L::SLOT_OFF);
   const uint32_t bar0 = base_u32 + L::BAR_OFF;
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L::MISC_OFF + 4);
-  int* stage_wide = reinterpret_cast<int*>(base + L::MISC_OFF + 8);  // [kStages]: key times need 64 bits
+  int* slot_wide = reinterpret_cast<int*>(base + L::MISC_OFF + 8);  // [kTsSlots]: key times need 64 bits
   float* tab = reinterpret_cast<float*>(base + L::TAB_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -257,8 +312,14 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       mbar_init(bar(BAR_QEMPTY + s), 1);
     }
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(BAR_KVFULL + s), 1);
-      mbar_init(bar(BAR_KVEMPTY + s), 1);
+      mbar_init(bar(BAR_KFULL + s), 1);
+      mbar_init(bar(BAR_KEMPTY + s), 1);
+      mbar_init(bar(BAR_VFULL + s), 1);
+      mbar_init(bar(BAR_VEMPTY + s), 1);
+    }
+    for (int s = 0; s < kTsSlots; ++s) {
+      mbar_init(bar(BAR_TSFULL + s), 1);
+      mbar_init(bar(BAR_TSEMPTY + s), kEpiWarps);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(BAR_SFULL + s), 1);
@@ -292,11 +353,11 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmq);
     tma_prefetch_desc(&tmk);
+    if (DELTA) tma_prefetch_desc(&tmk2);
+  }
+  if (warp == kVProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmv);
-    if (DELTA) {
-      tma_prefetch_desc(&tmk2);
-      tma_prefetch_desc(&tmv2);
-    }
+    if (DELTA) tma_prefetch_desc(&tmv2);
   }
   fence_before_sync();
   __syncthreads();
@@ -314,9 +375,9 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   const int nitems = p.hdr[WS_NBLK] * H;
 
   if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------- producer: Q, K, times
     uint32_t kv_it = 0, q_it = 0;
-    uint32_t armed[kStages] = {0, 0};    // phases armed per stage
+    uint32_t armed[kStages] = {0, 0};    // K phases armed per stage
     uint32_t q_phases[kQBufs] = {0, 0};  // phases used per Q buffer (a copy or the final no-work arrive)
     bool q_copy[kQBufs] = {false, false}; // the buffer's last phase carries a copy
     bool ok = true;
@@ -377,14 +438,14 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       ++q_it;
       if (!valid) break;
       const int nkb = DELTA ? (L + BN - 1) / BN + 1 : fwd_kv_blocks(q0, n, it.c, BM, BN);
-      // test only: the CTA that takes work item 0 withholds that item's first K/V load
+      // test only: the CTA that takes work item 0 withholds that item's first K load
       bool withhold_next = (p.flags & HSTU_FLAG_TEST_TIMEOUT) && idx == 0;
       for (int kb = 0; ok && kb < nkb; ++kb) {
         const bool self = DELTA && kb == nkb - 1;   // delta: the candidates' own keys
         const int k0 = self ? q0 : kb * BN;
         if (!DELTA && tile_class(q0, k0, BM, BN, n, it.c, it.h_end) == 0) continue;
-        const int stage = kv_it % kStages;
-        // key timestamps: loads issued before waiting for the stage, stored after
+        const int stage = kv_it % kStages, ts = kv_it % kTsSlots;
+        // key timestamps: loads issued before waiting, stored after
         int64_t tv[BN / 32];
 #pragma unroll
         for (int x = 0; x < BN / 32; ++x) {
@@ -392,53 +453,110 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           if (DELTA && !self) tv[x] = (p.ts2 && row < L) ? p.ts2[cs0 + row] : tbase;
           else tv[x] = (p.ts && row < n) ? p.ts[s0 + row] : tbase;
         }
-        ok = mbar_wait(bar(BAR_KVEMPTY + stage), ((kv_it / kStages) & 1) ^ 1, wd, 2);
+        ok = mbar_wait(bar(BAR_KEMPTY + stage), ((kv_it / kStages) & 1) ^ 1, wd, 2);
         if (!ok) break;
         const bool withhold = withhold_next;
         withhold_next = false;
-        // the K/V copy starts before the key timestamps arrive (as for Q)
-        if (lane == 0 && !withhold) {
-          mbar_expect_tx(bar(BAR_KVFULL + stage), L::STAGE);
-          const uint32_t dstK = sKV + stage * L::STAGE;
+        if (lane == 0 && !withhold) {   // withheld (test only): neither copy nor arrive
           const bool cached = DELTA && !self;
-          const CUtensorMap* mk = cached ? &tmk2 : &tmk;
-          const CUtensorMap* mv = cached ? &tmv2 : &tmv;
+          mbar_arrive_expect_tx(bar(BAR_KFULL + stage), L::K_BYTES);
           const int y = (int)(cached ? cs0 + k0 : s0 + k0);
-          for (int c = 0; c < L::NCH; ++c) {
-            tma_load_2d(dstK + c * L::BOX, mk, bar(BAR_KVFULL + stage), h * D + c * 64, y);
-            tma_load_2d(dstK + L::K_BYTES + c * L::BOX, mv, bar(BAR_KVFULL + stage), h * D + c * 64, y);
+          for (int c = 0; c < L::NCH; ++c)
+            tma_load_2d(sK0 + stage * L::K_BYTES + c * L::BOX, cached ? &tmk2 : &tmk, bar(BAR_KFULL + stage),
+                        h * D + c * 64, y);
+          armed[stage] += 1;
+          // K and V two tiles ahead into L2, so their loads, issued once a
+          // stage frees up, do not wait on HBM
+          if (kb + 2 < nkb) {
+            const bool self2 = DELTA && kb + 2 == nkb - 1, cached2 = DELTA && !self2;
+            const int y2 = (int)(cached2 ? cs0 + (kb + 2) * BN : s0 + (self2 ? q0 : (kb + 2) * BN));
+            for (int c = 0; c < L::NCH; ++c) {
+              tma_prefetch_l2_2d(cached2 ? &tmk2 : &tmk, h * D + c * 64, y2);
+              tma_prefetch_l2_2d(cached2 ? &tmv2 : &tmv, h * D + c * 64, y2);
+            }
           }
         }
+        ok = mbar_wait(bar(BAR_TSEMPTY + ts), ((kv_it / kTsSlots) & 1) ^ 1, wd, 11);
+        if (!ok) break;
         bool kw = false;
 #pragma unroll
         for (int x = 0; x < BN / 32; ++x) {
-          ts64_s[stage * BN + lane + 32 * x] = tv[x];
-          ts32_s[stage * BN + lane + 32 * x] = (int32_t)(tv[x] - tbase);
+          const int32_t r = (int32_t)(tv[x] - tbase);
+          ts64_s[ts * BN + lane + 32 * x] = tv[x];
+          ts32_s[ts * BN + lane + 32 * x] = r;
           kw |= ts_wide(tv[x] - tbase);
+          // min and max relative time of the 32-key chunk x, for the
+          // epilogue's test for a time bucket that is the same across it
+          int mn = r, mx = r;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          }
+          if (lane == 0) {
+            cmm_s[ts * 8 + 2 * x] = mn;
+            cmm_s[ts * 8 + 2 * x + 1] = mx;
+          }
         }
         kw = __any_sync(0xffffffffu, kw);
-        if (lane == 0) stage_wide[stage] = kw ? 1 : 0;
+        if (lane == 0) slot_wide[ts] = kw ? 1 : 0;
         __syncwarp();
-        if (lane == 0 && !withhold) {   // withheld (test only): neither copy nor arrive
-          mbar_arrive(bar(BAR_KVFULL + stage));
-          armed[stage] += 1;
-        }
+        if (lane == 0) mbar_arrive(bar(BAR_TSFULL + ts));
         ++kv_it;
       }
     }
     // make sure no copy is still landing in shared memory when the CTA ends
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s)
-        if (armed[s]) drain_wait(bar(BAR_KVFULL + s), (armed[s] - 1) & 1);
+        if (armed[s]) drain_wait(bar(BAR_KFULL + s), (armed[s] - 1) & 1);
       // an earlier phase of a Q buffer completed before the buffer was reused
       for (int s = 0; s < kQBufs; ++s)
         if (q_copy[s]) drain_wait(bar(BAR_QFULL + s), (q_phases[s] - 1) & 1);
+    }
+  } else if (warp == kVProducerWarp) {
+    // ------------------------------------------------------- producer: V
+    // walks the items the Q/K producer publishes (each Q buffer's phase), so
+    // it issues V loads as soon as a V stage is free, independently of K
+    if (lane == 0) {
+      uint32_t kv_it = 0, q_it = 0;
+      uint32_t armed[kStages] = {0, 0};
+      bool ok = true;
+      while (ok) {
+        const uint32_t qb = q_it % kQBufs;
+        ok = mbar_wait(bar(BAR_QFULL + qb), (q_it / kQBufs) & 1, wd, 12);
+        if (!ok) break;
+        const ItemSlot sl = slots[qb];
+        if (!sl.valid) break;
+        const int nkb = DELTA ? (sl.L + BN - 1) / BN + 1 : fwd_kv_blocks(sl.q0, sl.n, sl.c, BM, BN);
+        for (int kb = 0; ok && kb < nkb; ++kb) {
+          const bool self = DELTA && kb == nkb - 1;
+          const int k0 = self ? sl.q0 : kb * BN;
+          if (!DELTA && tile_class(sl.q0, k0, BM, BN, sl.n, sl.c, sl.h_end) == 0) continue;
+          const int stage = kv_it % kStages;
+          ok = mbar_wait(bar(BAR_VEMPTY + stage), ((kv_it / kStages) & 1) ^ 1, wd, 13);
+          if (!ok) break;
+          const bool cached = DELTA && !self;
+          mbar_arrive_expect_tx(bar(BAR_VFULL + stage), L::K_BYTES);
+          const int y = (int)(cached ? sl.cs0 + k0 : sl.s0 + k0);
+          for (int c = 0; c < L::NCH; ++c)
+            tma_load_2d(sV0 + stage * L::K_BYTES + c * L::BOX, cached ? &tmv2 : &tmv, bar(BAR_VFULL + stage),
+                        sl.h * D + c * 64, y);
+          armed[stage] += 1;
+          ++kv_it;
+        }
+        ++q_it;
+      }
+      for (int s = 0; s < kStages; ++s)
+        if (armed[s]) drain_wait(bar(BAR_VFULL + s), (armed[s] - 1) & 1);
     }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false, false);
       constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, false, true);
+      // descriptors built once; each MMA moves a start address by a constant
+      const SDesc q_km = sdesc_w(sQ0, 16, 1024), k_km = sdesc_w(sK0, 16, 1024);
+      const SDesc v_mn = sdesc_w(sV0, L::BOX, 1024);
       uint32_t kv_it = 0, q_it = 0, o_it = 0;
       bool ok = true;
       // The P.V of the latest S tile is issued after the next S tile, of the
@@ -453,17 +571,18 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       // P of tile t: quarter k/2 of the S buffer, hi at [32 q, 32 q + 16), lo 16 columns later
       auto issue_pv = [&](const PendPV& pv) -> bool {
         const uint32_t sb = pv.it & 1, stage = pv.it % kStages;
-        if (!mbar_wait(bar(BAR_PREADY + sb), (pv.it >> 1) & 1, wd, 5)) return false;
+        if (!mbar_wait(bar(BAR_PREADY + sb), (pv.it >> 1) & 1, wd, 5) ||
+            !mbar_wait(bar(BAR_VFULL + stage), (pv.it / kStages) & 1, wd, 14))
+          return false;
         fence_after_sync();
-        const uint32_t vbase = sKV + stage * L::STAGE + L::K_BYTES;
+        const SDesc v_s = v_mn + stage * L::K_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint32_t a_hi = tmem + sb * kSColStride + 32u * (kk >> 1) + 8u * (kk & 1);
-          const uint64_t bd = sdesc_sw128(vbase + kk * 2048, L::BOX, 1024);
-          mma_ts(tmem + pv.ocol, a_hi, bd, IDESC_PV, (pv.first && kk == 0) ? 0u : 1u);
-          mma_ts(tmem + pv.ocol, a_hi + 16, bd, IDESC_PV, 1u);
+          mma_ts_w(tmem + pv.ocol, a_hi, v_s + kk * 2048, IDESC_PV, (pv.first && kk == 0) ? 0u : 1u);
+          mma_ts_w(tmem + pv.ocol, a_hi + 16, v_s + kk * 2048, IDESC_PV, 1u);
         }
-        mma_commit(bar(BAR_KVEMPTY + stage));
+        mma_commit(bar(BAR_VEMPTY + stage));
         if (pv.last) {
           mma_commit(bar(BAR_QEMPTY + pv.qb));
           mma_commit(bar(BAR_OFULL + pv.ob));
@@ -477,7 +596,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         fence_after_sync();
         const ItemSlot sl = slots[qb];
         if (!sl.valid) break;
-        const uint32_t sQ = sQ0 + qb * L::Q_BYTES;
+        const SDesc q_s = q_km + qb * L::Q_BYTES;
         const uint32_t ob = o_it & 1;
         const uint32_t ocol = ob ? L::O_COL1 : L::O_COL0;
         bool first = true;
@@ -486,17 +605,17 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           const int k0 = kb * BN;
           if (!DELTA && tile_class(sl.q0, k0, BM, BN, sl.n, sl.c, sl.h_end) == 0) continue;
           const uint32_t stage = kv_it % kStages, sb = kv_it & 1;
-          ok = mbar_wait(bar(BAR_KVFULL + stage), (kv_it / kStages) & 1, wd, 6);
+          ok = mbar_wait(bar(BAR_KFULL + stage), (kv_it / kStages) & 1, wd, 6);
           if (!ok) break;
           fence_after_sync();
-          const uint32_t kbase = sKV + stage * L::STAGE;
+          const SDesc k_s = k_km + stage * L::K_BYTES;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * L::BOX + (kk & 3) * 32;
-            mma_ss(tmem + sb * kSColStride, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                   IDESC_S, kk > 0 ? 1u : 0u);
+            mma_ss_w(tmem + sb * kSColStride, q_s + off, k_s + off, IDESC_S, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(BAR_SFULL + sb));
+          mma_commit(bar(BAR_KEMPTY + stage));   // K is read by no later MMA
           if (pend.have) {
             ok = issue_pv(pend);
             if (!ok) break;
@@ -527,7 +646,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       mma_commit(bar(BAR_DRAIN));
       drain_wait(bar(BAR_DRAIN), 0);
     }
-  } else {
+  } else if (warp < kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int wq = warp & 3, hq = warp >> 2;      // TMEM lane quarter, column quarter
     const int row = wq * 32 + lane;
@@ -611,25 +730,33 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         const int k0 = self ? q0 : kb * BN;
         const int cls = DELTA ? 1 : tile_class(q0, k0, BM, BN, n_seq, cx, rc.h_end);
         if (cls == 0) continue;
-        const uint32_t stage = kv_it % kStages, sb = kv_it & 1;
-        ok = mbar_wait(bar(BAR_KVFULL + stage), (kv_it / kStages) & 1, wd, 7) &&
+        const uint32_t ts = kv_it % kTsSlots, sb = kv_it & 1;
+        ok = mbar_wait(bar(BAR_TSFULL + ts), (kv_it / kTsSlots) & 1, wd, 7) &&
              mbar_wait(bar(BAR_SFULL + sb), (kv_it >> 1) & 1, wd, 8);
         if (!ok) break;
         fence_after_sync();
         const uint32_t scol = lane_base + sb * kSColStride + hq * 32;
-        uint32_t sv[32];
-        tmem_ld32(scol, sv);
-        tmem_wait_ld();
         const int jb = k0 + hq * 32;
-        const int32_t* t32 = ts32_s + stage * BN + hq * 32;
-        const int64_t* t64 = ts64_s + stage * BN + hq * 32;
-        uint32_t hi[16], lo[16];
-        const bool fast = cls == 2 && k0 + BN - 1 <= q0;
+        const int32_t* t32 = ts32_s + ts * BN + hq * 32;
+        const int64_t* t64 = ts64_s + ts * BN + hq * 32;
+        uint32_t sv[32], hi[16], lo[16];
+        bool stored = false;   // the constant-bias path loads S and stores P itself
+        // Class of the warp's block (32 rows from r0, 32 keys from jb).  Rows
+        // past the sequence only feed rows of O that are never written out,
+        // so they do not limit it: the block is full when every key is a
+        // history or context token that every row may see, i.e. all keys lie
+        // at or before the first row, or all rows are candidates (which see
+        // the whole history).  That holds on the ragged last block of a
+        // sequence too, whose tiles are partial only by their missing rows.
+        const int r0 = q0 + wq * 32, kend = jb + 31;
+        const bool fast = kend < rc.h_end && (kend <= r0 || r0 >= rc.h_end);
         // the warp's rows start at position pos_lo (positions grow with the row)
-        const int pos_lo = q0 + wq * 32 < rc.h_end ? q0 + wq * 32 : rc.h_end;
-        const bool far = fast && pos_lo - (jb + 31) >= p.P - 1;
-        const bool narrow = !item_wide && !stage_wide[stage];
+        const int pos_lo = r0 < rc.h_end ? r0 : rc.h_end;
+        const bool far = fast && pos_lo - kend >= p.P - 1;
+        const bool narrow = !item_wide && !slot_wide[ts];
         if (DELTA) {
+          tmem_ld32(scol, sv);
+          tmem_wait_ld();
           if (self) {
             if (narrow) score32<0, false, false, 2>(p, sv, hi, lo, rc, jb, t32, t64);
             else score32<0, true, false, 2>(p, sv, hi, lo, rc, jb, t32, t64);
@@ -638,21 +765,49 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
             else score32<0, true, false, 1>(p, sv, hi, lo, rc, jb, t32, t64);
           }
         } else if (narrow) {
-          if (far) score32<2, false, false>(p, sv, hi, lo, rc, jb, t32, t64);
-          else if (fast) score32<1, false, false>(p, sv, hi, lo, rc, jb, t32, t64);
-          else if (cls == 2) score32<0, false, false>(p, sv, hi, lo, rc, jb, t32, t64);
-          else score32<0, false, true>(p, sv, hi, lo, rc, jb, t32, t64);
+          // far blocks whose time bucket is also the same across the row's 32
+          // keys (the keys' times all on one side of t_i, and the bucket of
+          // the nearest and of the farthest gap equal): one bias per row
+          bool cst = far;
+          int slot = kTabFar;
+          if (far && p.ts) {
+            // gaps to the latest and the earliest key time of the chunk: of
+            // one sign when t_i is not inside the chunk's time range, and then
+            // the gaps of all its keys lie between them
+            const int32_t d1 = rc.ti32 - cmm_s[ts * 8 + 2 * hq + 1], d2 = rc.ti32 - cmm_s[ts * 8 + 2 * hq];
+            const int z1 = __clz(abs(d1)), z2 = __clz(abs(d2));
+            cst = ((d1 ^ d2) >= 0 && min(32 - z1, Tb - 1) == min(32 - z2, Tb - 1)) || !rc.row_ok;
+            slot = kTabFar + z1;   // a row past the sequence takes any bias
+          }
+          if (__all_sync(0xffffffffu, cst)) {
+            score32_const(p, scol, rc.tp[P + slot]);
+            stored = true;
+          } else {
+            tmem_ld32(scol, sv);
+            tmem_wait_ld();
+            if (far) score32<2, false, false>(p, sv, hi, lo, rc, jb, t32, t64);
+            else if (fast) score32<1, false, false>(p, sv, hi, lo, rc, jb, t32, t64);
+            else if (cls == 2) score32<0, false, false>(p, sv, hi, lo, rc, jb, t32, t64);
+            else score32<0, false, true>(p, sv, hi, lo, rc, jb, t32, t64);
+          }
         } else {
+          tmem_ld32(scol, sv);
+          tmem_wait_ld();
           if (cls == 2) score32<0, true, false>(p, sv, hi, lo, rc, jb, t32, t64);
           else score32<0, true, true>(p, sv, hi, lo, rc, jb, t32, t64);
         }
         // P_hi of this quarter at [32 hq, 32 hq + 16), P_lo at [32 hq + 16, 32 hq + 32)
-        tmem_st16(scol, hi);
-        tmem_st16(scol + 16, lo);
+        if (!stored) {
+          tmem_st16(scol, hi);
+          tmem_st16(scol + 16, lo);
+        }
         tmem_wait_st();
         fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_PREADY + sb));
+        if (lane == 0) {
+          mbar_arrive(bar(BAR_PREADY + sb));
+          mbar_arrive(bar(BAR_TSEMPTY + ts));
+        }
         ++kv_it;
         if (o_pend) {  // the previous item's O, now that this item's first P is out
           ok = write_o();

@@ -95,6 +95,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// L2 prefetch of a 2-D tile (no shared-memory destination, no completion
+// to wait for): a later TMA load of the same box then finds it in L2.
+// Same coordinate rules as the loads.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // Tile stores from shared memory, completed through bulk groups.  Elements
 // of the box outside the tensor are not written.  x must be a multiple of
 // 16 bytes and no coordinate may be negative.
@@ -229,6 +238,37 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// A shared-memory descriptor kept as its two 32-bit words.  The low word
+// holds the start address >> 4 in bits 0-13 (and the leading byte offset in
+// bits 16-29), so moving the start address by a multiple of 16 bytes is one
+// 32-bit add on the low word: the 14-bit field cannot carry out for
+// addresses below 256 KB, which covers all of a CTA's shared memory.
+struct SDesc {
+  uint32_t lo, hi;
+  __device__ __forceinline__ SDesc operator+(uint32_t bytes) const { return SDesc{lo + (bytes >> 4), hi}; }
+};
+__device__ __forceinline__ SDesc sdesc_w(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  const uint64_t d = sdesc_sw128(saddr, lbo, sbo);
+  return SDesc{(uint32_t)d, (uint32_t)(d >> 32)};
+}
+// D[tmem] (+)= A[smem] x B[smem] with word-pair descriptors
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tmov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] x B[smem] with a word-pair descriptor
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, SDesc b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\tmov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Instruction descriptor, kind::f16 with BF16 A and B, FP32 accumulator.
 // b_mn_major: B stored with N contiguous (else K contiguous).
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
@@ -263,6 +303,20 @@ __device__ __forceinline__ float2 fsub2(float2 x, float2 y) {
 // x - bf16 pair v (low half first) on two lanes: the residual of a BF16 split
 __device__ __forceinline__ float2 bf16_residual2(float2 x, uint32_t v) {
   return fsub2(x, make_float2(bf16_lo_f(v), bf16_hi_f(v)));
+}
+
+// 1 / d on two lanes for 1 <= d < 2^126, on the FMA pipe instead of the
+// special-function unit: the exponent-negating bit-pattern estimate
+// C - bits(d), with C = 0x7EF311C0 chosen here to minimise the estimate's
+// worst relative error over a binade (5.05e-2), refined by two Newton-Raphson
+// steps r <- r + r (1 - d r), each squaring the relative error (6.5e-6).
+__device__ __forceinline__ float2 rcp2_newton(float2 d) {
+  float2 r = make_float2(__int_as_float(0x7EF311C0 - __float_as_int(d.x)),
+                         __int_as_float(0x7EF311C0 - __float_as_int(d.y)));
+  const float2 one = make_float2(1.f, 1.f), nd = make_float2(-d.x, -d.y);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) r = __ffma2_rn(r, __ffma2_rn(nd, r, one), r);
+  return r;
 }
 
 __device__ __forceinline__ float tanh_approx(float x) {

@@ -1,12 +1,14 @@
 """Register budget of the tensor-core attention kernels, read from the
 compiler's resource report (ptxas -v) on the CPU.
 
-Both kernels run 18 warps per CTA under a 96-register cap (20 warps are
-charged: 20 x 32 x 96 = 61,440 of the SM's 65,536 registers); a spill
-costs local-memory round trips, and added spills measured slower or no faster
-every time they appeared.  The backward compiles spill-free; the forward
-variant the benchmark runs (d = 128, FP32 outputs) spills 8 bytes.  A
-change that adds spills shows here before it is timed.
+The backward runs 18 warps per CTA and the forward 19 under a 96-register
+cap: warps are spread over the SM's four sub-partitions, each with a quarter
+of the 65,536 registers, so the sub-partitions holding five warps need
+5 x 32 x 96 = 15,360 <= 16,384.  A spill costs local-memory round trips, and
+added spills measured slower or no faster every time they appeared.  The
+backward compiles spill-free; the forward variant the benchmark runs
+(d = 128, FP32 outputs) spills 8 bytes each way.  A change that adds spills
+shows here before it is timed.
 """
 import os
 import re
