@@ -31,8 +31,10 @@ class Problem:
 
     def __init__(self, batch, device="cuda", flags: int = 0, want_y: bool = True,
                  want_stats: bool = False, want_drab: bool = True, out_dtype: str = "fp32",
-                 dropout=None):
-        # dropout: None or (p, seed, offset) of the fused dropout on y
+                 dropout=None, bwd_flags: int = 0):
+        # dropout: None or (p, seed, offset) of the fused dropout on y;
+        # bwd_flags: flags added for the backward call only (e.g.
+        # HSTU_FLAG_FORCE_SIMT for a BF16 backward without a tensor-core kernel)
         self.batch = batch
         dev = torch.device(device)
         self.dev = dev
@@ -81,6 +83,7 @@ class Problem:
             num_time_buckets=batch.rab_time.shape[1] if batch.rab_time is not None else 64,
             norm=batch.norm, ln_eps=batch.eps, flags=flags,
             dropout_p=0.0 if dropout is None else float(dropout[0]))
+        self.bwd_flags = bwd_flags
         seed, offset = (0, 0) if dropout is None else (int(dropout[1]), int(dropout[2]))
         fwd_b, bwd_b = C.hstu_attn_workspace_size(self.desc)
         self.ws_bytes = max(fwd_b, bwd_b if self.backward_enabled else 0)
@@ -101,7 +104,9 @@ class Problem:
         C.hstu_attn_fwd(self.desc, self.fwd_args, self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
 
     def backward(self, stream=None):
-        C.hstu_attn_bwd(self.desc, self.bwd_args, self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
+        d = C.hstu_attn_desc.from_buffer_copy(self.desc)
+        d.flags |= self.bwd_flags
+        C.hstu_attn_bwd(d, self.bwd_args, self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
 
     def device_error(self, stream=None) -> int:
         return C.hstu_get_device_error(self.ws.data_ptr(), _stream_handle(stream))
@@ -116,24 +121,35 @@ class Problem:
 
 class HSTUAttnFunction(torch.autograd.Function):
     """y = Norm(A V) * u with A = SiLU(alpha Q K^T + rab) / N under the
-    compound mask; gradients for q, k, v, u, rab_pos, rab_time."""
+    compound mask; gradients for q, k, v, u, rab_pos, rab_time.
+
+    The library computes o, y and every gradient in out_dtype ("fp32", the
+    default, or "bf16"; FP32 inputs always give FP32).  An FP32 u with BF16
+    q, k, v is read as FP32 (HSTU_FLAG_U_FP32).  Autograd hands each gradient
+    back in the dtype of its input, so BF16 q, k, v receive the FP32 results
+    rounded once to BF16."""
 
     @staticmethod
     def forward(ctx, q, k, v, u, rab_pos, rab_time, seq_offsets, num_targets, num_contexts,
                 timestamps, max_seq_len: int, alpha: float, norm: str = "layernorm",
-                eps: float = 1e-5, dropout_p: float = 0.0, dropout_seed: int = 0, dropout_offset: int = 0):
+                eps: float = 1e-5, dropout_p: float = 0.0, dropout_seed: int = 0, dropout_offset: int = 0,
+                out_dtype: Optional[str] = None, flags: int = 0):
         T, H, dqk = q.shape
         dv = v.shape[2]
         dtype = "bf16" if q.dtype == torch.bfloat16 else "fp32"
-        desc = C.make_desc(dtype=dtype, B=seq_offsets.numel() - 1, H=H, d_qk=dqk, d_v=dv,
+        out_dtype = "fp32" if (dtype == "fp32" or out_dtype is None) else out_dtype
+        if dtype == "bf16" and u is not None and u.dtype == torch.float32:
+            flags |= C.HSTU_FLAG_U_FP32
+        to = torch_dtype(out_dtype)
+        desc = C.make_desc(dtype=dtype, out_dtype=out_dtype, B=seq_offsets.numel() - 1, H=H, d_qk=dqk, d_v=dv,
                            total_tokens=T, max_seq_len=max_seq_len, alpha=alpha,
                            num_pos_buckets=rab_pos.shape[1] if rab_pos is not None else 128,
                            num_time_buckets=rab_time.shape[1] if rab_time is not None else 64,
-                           norm=norm, ln_eps=eps, dropout_p=dropout_p)
+                           norm=norm, ln_eps=eps, flags=flags, dropout_p=dropout_p)
         fwd_b, bwd_b = C.hstu_attn_workspace_size(desc)
         ws = torch.empty(max(fwd_b, bwd_b), device=q.device, dtype=torch.uint8)
-        o = torch.empty(T, H, dv, device=q.device, dtype=q.dtype)
-        y = torch.empty(T, H * dv, device=q.device, dtype=q.dtype)
+        o = torch.empty(T, H, dv, device=q.device, dtype=to)
+        y = torch.empty(T, H * dv, device=q.device, dtype=to)
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
         u = u.contiguous() if u is not None else None
         args = C.hstu_attn_fwd_args(_ptr(seq_offsets), _ptr(num_targets), _ptr(num_contexts),
@@ -143,29 +159,34 @@ class HSTUAttnFunction(torch.autograd.Function):
         C.hstu_attn_fwd(desc, args, ws.data_ptr(), ws.numel(), _stream_handle())
         ctx.save_for_backward(q, k, v, u, rab_pos, rab_time, seq_offsets, num_targets, num_contexts,
                               timestamps, o)
-        ctx.desc, ctx.ws, ctx.drop = desc, ws, (dropout_seed, dropout_offset)
+        ctx.desc, ctx.ws, ctx.drop, ctx.to = desc, ws, (dropout_seed, dropout_offset), to
         return y
 
     @staticmethod
     def backward(ctx, dy):
         q, k, v, u, rab_pos, rab_time, off, nt, nc, ts, o = ctx.saved_tensors
-        dy = dy.contiguous().to(q.dtype)
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        du = torch.empty_like(u) if u is not None else None
+        to = ctx.to
+        dy = dy.contiguous().to(to)
+        dq = torch.empty(q.shape, device=q.device, dtype=to)
+        dk = torch.empty(k.shape, device=k.device, dtype=to)
+        dv = torch.empty(v.shape, device=v.device, dtype=to)
+        du = torch.empty(u.shape, device=u.device, dtype=to) if u is not None else None
         drp = torch.empty_like(rab_pos, dtype=torch.float32) if rab_pos is not None else None
         drt = torch.empty_like(rab_time, dtype=torch.float32) if rab_time is not None else None
         args = C.hstu_attn_bwd_args(_ptr(off), _ptr(nt), _ptr(nc), _ptr(ts), _ptr(rab_pos), _ptr(rab_time),
                                     _ptr(q), _ptr(k), _ptr(v), _ptr(u), _ptr(o), _ptr(dy), _ptr(dq),
                                     _ptr(dk), _ptr(dv), _ptr(du), _ptr(drp), _ptr(drt), *ctx.drop)
         C.hstu_attn_bwd(ctx.desc, args, ctx.ws.data_ptr(), ctx.ws.numel(), _stream_handle())
-        return (dq, dk, dv, du, drp, drt) + (None,) * 11
+        return (dq, dk, dv, du, drp, drt) + (None,) * 13
 
 
 def hstu_attention(q, k, v, u, seq_offsets, max_seq_len, alpha, *, num_targets=None, num_contexts=None,
                    timestamps=None, rab_pos=None, rab_time=None, norm="layernorm", eps=1e-5,
-                   dropout_p=0.0, dropout_seed=0, dropout_offset=0):
+                   dropout_p=0.0, dropout_seed=0, dropout_offset=0, out_dtype=None, flags=0):
     """Differentiable HSTU jagged attention: returns y [T, H*d_v] (with the
-    fused dropout when dropout_p > 0; the seed and offset select the mask)."""
+    fused dropout when dropout_p > 0; the seed and offset select the mask).
+    out_dtype: "fp32" (default) or "bf16" for o, y and the library's
+    gradients; flags: HSTU_FLAG_* bits (e.g. HSTU_FLAG_FORCE_SIMT)."""
     return HSTUAttnFunction.apply(q, k, v, u, rab_pos, rab_time, seq_offsets, num_targets, num_contexts,
                                   timestamps, int(max_seq_len), float(alpha), norm, float(eps),
-                                  float(dropout_p), int(dropout_seed), int(dropout_offset))
+                                  float(dropout_p), int(dropout_seed), int(dropout_offset), out_dtype, int(flags))

@@ -154,6 +154,26 @@ bool use_tc(const hstu_attn_desc* d, bool bwd) {
          tc_fwd_smem_bytes(d->d_qk, d->H, d->num_pos_buckets, d->num_time_buckets) <= kMaxSmemPerCta;
 }
 
+// BF16 work the tensor-core kernels do not take (head sizes other than 128,
+// or 64 in the forward; bias tables too large for shared memory) would run
+// on the CUDA-core kernels, some thirty times slower.  That happens only when
+// the caller asks for it with HSTU_FLAG_FORCE_SIMT; otherwise the call is
+// refused.  Problems under 128 tokens take the CUDA-core kernels either way
+// (they last microseconds).
+hstu_status_t check_tc_shape(const hstu_attn_desc* d, bool bwd) {
+  if (d->dtype != HSTU_BF16 || (d->flags & HSTU_FLAG_FORCE_SIMT)) return HSTU_OK;
+  const bool ok = bwd ? tc_bwd_supported(d->dtype, d->d_qk, d->d_v) &&
+                            tc_bwd_smem_bytes(d->H, d->num_pos_buckets, d->num_time_buckets) <= kMaxSmemPerCta
+                      : tc_fwd_supported(d->dtype, d->d_qk, d->d_v) &&
+                            tc_fwd_smem_bytes(d->d_qk, d->H, d->num_pos_buckets, d->num_time_buckets) <= kMaxSmemPerCta;
+  if (ok) return HSTU_OK;
+  set_detail_message(bwd ? "BF16 backward without a tensor-core kernel for this shape (d = 128 only); "
+                           "HSTU_FLAG_FORCE_SIMT runs it on the CUDA-core kernels"
+                         : "BF16 forward without a tensor-core kernel for this shape (d = 64 or 128); "
+                           "HSTU_FLAG_FORCE_SIMT runs it on the CUDA-core kernels");
+  return HSTU_ERR_UNSUPPORTED;
+}
+
 PlanParams plan_params(const hstu_attn_desc* d, const int64_t* off, const int32_t* nt, const int32_t* nc,
                        const int64_t* ts, int pass, bool tc, char* ws, const WsLayout& L) {
   PlanParams p{};
@@ -260,12 +280,13 @@ hstu_status_t hstu_attn_fwd(const hstu_attn_desc* d, const hstu_attn_fwd_args* a
     return HSTU_ERR_INVALID_ARG;
   for (const void* ptr : {a->q, a->k, a->v, (const void*)a->o, a->u, (const void*)a->y})
     if (ptr && !aligned16(ptr)) return HSTU_ERR_INVALID_ARG;
+  clear_detail();
+  if ((s = check_tc_shape(d, false)) != HSTU_OK) return s;
   const WsLayout L = ws_layout(d, false);
   if ((s = check_ws(workspace, workspace_bytes, L.total)) != HSTU_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   g_launches = 0;
-  clear_detail();
 
   const bool tc = use_tc(d, false);
   const PlanParams pp =
@@ -319,12 +340,13 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
   for (const void* ptr : {a->q, a->k, a->v, a->o, a->u, a->dy, (const void*)a->dq, (const void*)a->dk,
                           (const void*)a->dv, (const void*)a->du})
     if (ptr && !aligned16(ptr)) return HSTU_ERR_INVALID_ARG;
+  clear_detail();
+  if ((s = check_tc_shape(d, true)) != HSTU_OK) return s;
   const WsLayout L = ws_layout(d, true);
   if ((s = check_ws(workspace, workspace_bytes, L.total)) != HSTU_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   g_launches = 0;
-  clear_detail();
 
   const bool tc = use_tc(d, true);
   const PlanParams pp =

@@ -14,8 +14,10 @@ class LayerProblem:
     """Device copies of a synth.layer batch (x, w1, w2, dout, offsets,
     timestamps, bias tables) plus every output and the workspace."""
 
-    def __init__(self, batch, device="cuda", want_drab: bool = True, dropout=None):
-        # dropout: None or (p, seed, offset) of the fused dropout on y
+    def __init__(self, batch, device="cuda", want_drab: bool = True, dropout=None, bwd_flags: int = 0):
+        # dropout: None or (p, seed, offset) of the fused dropout on y;
+        # bwd_flags: flags added for the backward call only (HSTU_FLAG_FORCE_SIMT
+        # runs an attention backward without a tensor-core kernel, d != 128)
         self.batch = batch
         dev = torch.device(device)
         self.dev = dev
@@ -61,6 +63,7 @@ class LayerProblem:
             num_pos_buckets=batch.rab_pos.shape[1] if batch.rab_pos is not None else 128,
             num_time_buckets=batch.rab_time.shape[1] if batch.rab_time is not None else 64,
             norm=batch.norm, ln_eps=batch.eps, dropout_p=0.0 if dropout is None else float(dropout[0]))
+        self.bwd_flags = bwd_flags
         drop = (0, 0) if dropout is None else (int(dropout[1]), int(dropout[2]))
         fwd_b, bwd_b = C.hstu_layer_workspace_size(self.desc)
         self.ws_bytes = max(fwd_b, bwd_b if self.backward_enabled else 0)
@@ -79,7 +82,9 @@ class LayerProblem:
         C.hstu_layer_fwd(self.desc, self.fwd_args, self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
 
     def backward(self, stream=None):
-        C.hstu_layer_bwd(self.desc, self.bwd_args, self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
+        d = C.hstu_attn_desc.from_buffer_copy(self.desc)
+        d.flags |= self.bwd_flags
+        C.hstu_layer_bwd(d, self.bwd_args, self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
 
     def device_error(self, stream=None) -> int:
         return C.hstu_get_device_error(self.ws.data_ptr(), _stream_handle(stream))

@@ -79,7 +79,10 @@ typedef enum { HSTU_BF16 = 0, HSTU_FP32 = 1 } hstu_dtype_t;
 typedef enum { HSTU_NORM_NONE = 0, HSTU_NORM_LAYERNORM = 1 } hstu_norm_t;
 
 /* Flags */
-#define HSTU_FLAG_FORCE_SIMT (1u << 0)   /* use the CUDA-core kernels even where the tensor-core path applies */
+#define HSTU_FLAG_FORCE_SIMT (1u << 0)   /* use the CUDA-core kernels even where the tensor-core path applies;
+                                            BF16 work the tensor-core kernels do not take (the backward
+                                            needs d = 128, the forward d = 64 or 128) runs only with this
+                                            flag, else the call returns HSTU_ERR_UNSUPPORTED */
 #define HSTU_FLAG_TEST_TIMEOUT (1u << 1) /* test only: the tensor-core forward withholds one load (the
                                             first K/V tile of work item 0) and its waits give up after about
                                             a millisecond, so the timeout path runs without a hang; the

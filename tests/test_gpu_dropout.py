@@ -90,11 +90,10 @@ def test_dropout_heavy_tailed_config():
 
 
 def test_layer_with_dropout():
-    from tests.test_gpu_layer import _close, _np, _small_layer
-    from hstu_jagged_attention_02_gb300.layer import LayerProblem
+    from tests.test_gpu_layer import _close, _np, _small_layer, layer_problem
     b = _small_layer(44, [300, 131, 77, 1, 260])
     drop = (0.2, 555, 9)
-    pr = LayerProblem(b, dropout=drop)
+    pr = layer_problem(b, dropout=drop)
     pr.forward()
     pr.backward()
     torch.cuda.synchronize()

@@ -35,10 +35,9 @@ def test_layer_projection_wait_times_out_and_context_survives():
     # its first load, the MMA warp's wait runs out, every role exits, and the
     # error (kept in the layer's own header word while the attention runs)
     # is raised into the workspace error word by the output projection
-    from hstu_jagged_attention_02_gb300.layer import LayerProblem
-    from tests.test_gpu_layer import _small_layer
+    from tests.test_gpu_layer import _small_layer, layer_problem
     b = _small_layer(91, [300, 131, 260], H=2, d=64)
-    pr = LayerProblem(b)
+    pr = layer_problem(b)
     pr.desc.flags |= C.HSTU_FLAG_TEST_TIMEOUT
     pr.forward()
     torch.cuda.synchronize()
