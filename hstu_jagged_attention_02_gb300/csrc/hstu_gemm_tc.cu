@@ -90,13 +90,26 @@ __device__ __forceinline__ void drain_wait_g(uint32_t bar, uint32_t parity) {
   }
 }
 
-// MODE 0: f1 epilogue (z1, U, V|Q|K).  MODE 1: f2 epilogue (out = X + acc).
-template <int MODE, int BN>
+// Epilogue modes.  0: f1 (z1, U, V|Q|K); 1: out = X + acc (BF16 residual);
+// 2: out = acc; 3: out += acc (TMA reduce-add: split-K partial sums);
+// 4: out = res + acc (FP32 residual).
+enum : int { GM_F1 = 0, GM_RES_BF16 = 1, GM_STORE = 2, GM_REDUCE = 3, GM_RES_F32 = 4 };
+
+// Operand layouts.  A_MN: A is the transpose of a row-major [K, M] array,
+// loaded as two 64-column x 64-row boxes per k-block (M contiguous);
+// otherwise a row-major [M, K] array, one 64 x 128 box.  B_KM: B is the
+// transpose of a row-major [N, K] array, one 64-column x BN-row box
+// (K contiguous); otherwise a row-major [K, N] array, BN / 64 boxes of
+// 64 x 64.  Every box is 128-byte swizzled.
+//
+// Work items are (row block, column block, K range): the K range is all of
+// K unless p.ksplit > 1, which only the reduce epilogue uses.
+template <int MODE, int BN, bool A_MN, bool B_KM>
 __global__ void __launch_bounds__(kGThreads, 1)
 hstu_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tma0,
-                    const __grid_constant__ CUtensorMap tma1, const __grid_constant__ CUtensorMap tmb,
-                    const __grid_constant__ CUtensorMap tms0, const __grid_constant__ CUtensorMap tms1,
-                    const __grid_constant__ CUtensorMap tms2) {
+                    const __grid_constant__ CUtensorMap tma1, const __grid_constant__ CUtensorMap tmb0,
+                    const __grid_constant__ CUtensorMap tmb1, const __grid_constant__ CUtensorMap tms0,
+                    const __grid_constant__ CUtensorMap tms1, const __grid_constant__ CUtensorMap tms2) {
   using L = GLayout<BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -127,8 +140,11 @@ hstu_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
   }
   if (warp == kGProducerWarp && lane == 0) {
     tma_prefetch_desc(&tma0);
-    if (p.npass > 1) tma_prefetch_desc(&tma1);
-    tma_prefetch_desc(&tmb);
+    tma_prefetch_desc(&tmb0);
+    if (p.npass > 1) {
+      if (p.pair_b) tma_prefetch_desc(&tmb1);
+      else tma_prefetch_desc(&tma1);
+    }
   }
   fence_before_sync();
   __syncthreads();
@@ -139,14 +155,24 @@ hstu_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
   wd.abort = abort_flag;
   wd.err = p.err;
   wd.err_info = p.err_info;
-  if (MODE == 1 && blockIdx.x == 0 && threadIdx.x == 0 && p.carry_err) {
+  if (MODE != GM_F1 && blockIdx.x == 0 && threadIdx.x == 0 && p.carry_err) {
     const int code = p.carry_err[0];
     if (code != 0 && atomicCAS(p.err, 0, code) == 0) *p.err_info = p.carry_err[1];
   }
   wd.limit_ns = p.test_timeout ? 1000000ull : 2000000000ull;
-  const int mblocks = (p.M + GBM - 1) / GBM, nblocks = p.N / BN;
+  const int mblocks = (int)((p.M + GBM - 1) / GBM), nblocks = p.N / BN;
   const int ntiles = mblocks * nblocks;
-  const int kblocks = p.K / GBK;
+  const int kbt = (int)((p.K + GBK - 1) / GBK);          // 64-blocks of K (the last one zero-filled)
+  const int kper = (kbt + p.ksplit - 1) / p.ksplit;      // 64-blocks per K range
+  const int nitems = ntiles * p.ksplit;
+  // work item t: tile t % ntiles, K range t / ntiles, 64-blocks [kb0, kb1)
+  auto item = [&](int t, int& mb, int& nb, int& kb0, int& kb1) {
+    const int tile = t % ntiles, ks = t / ntiles;
+    mb = tile / nblocks;
+    nb = tile % nblocks;
+    kb0 = ks * kper;
+    kb1 = min(kbt, kb0 + kper);
+  };
 
   if (warp == kGProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -155,11 +181,13 @@ hstu_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
       uint32_t armed[kGStages] = {};
       bool ok = true;
       const bool withhold = p.test_timeout && blockIdx.x == 0;   // test only
-      for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-        const int mb = t / nblocks, nb = t % nblocks;
+      for (int t = blockIdx.x; ok && t < nitems; t += gridDim.x) {
+        int mb, nb, kb0, kb1;
+        item(t, mb, nb, kb0, kb1);
         for (int pass = 0; ok && pass < p.npass; ++pass) {
-          const CUtensorMap* ma = pass == 0 ? &tma0 : &tma1;
-          for (int kb = 0; kb < kblocks; ++kb) {
+          const CUtensorMap* ma = (pass == 0 || p.pair_b) ? &tma0 : &tma1;
+          const CUtensorMap* mbm = (pass == 0 || !p.pair_b) ? &tmb0 : &tmb1;
+          for (int kb = kb0; kb < kb1; ++kb) {
             const int stage = (int)(it % kGStages);
             ok = mbar_wait(bar(GB_EMPTY + stage), ((it / kGStages) & 1) ^ 1, wd, 41);
             if (!ok) break;
@@ -169,9 +197,17 @@ hstu_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
             }
             const uint32_t sA = base_u32 + stage * L::STAGE, sB = sA + L::A_BYTES;
             mbar_arrive_expect_tx(bar(GB_FULL + stage), L::STAGE);
-            tma_load_2d(sA, ma, bar(GB_FULL + stage), kb * GBK, mb * GBM);
-            for (int c = 0; c < BN / 64; ++c)
-              tma_load_2d(sB + c * L::B_BOX, &tmb, bar(GB_FULL + stage), nb * BN + c * 64, kb * GBK);
+            if (A_MN) {
+              for (int c = 0; c < 2; ++c) tma_load_2d(sA + c * L::B_BOX, ma, bar(GB_FULL + stage), mb * GBM + c * 64, kb * GBK);
+            } else {
+              tma_load_2d(sA, ma, bar(GB_FULL + stage), kb * GBK, mb * GBM);
+            }
+            if (B_KM) {
+              tma_load_2d(sB, mbm, bar(GB_FULL + stage), kb * GBK, nb * BN);
+            } else {
+              for (int c = 0; c < BN / 64; ++c)
+                tma_load_2d(sB + c * L::B_BOX, mbm, bar(GB_FULL + stage), nb * BN + c * 64, kb * GBK);
+            }
             armed[stage] += 1;
             ++it;
           }
@@ -183,26 +219,34 @@ hstu_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
   } else if (warp == kGMmaWarp) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t IDESC = idesc_bf16(GBM, BN, false, true);
+      constexpr uint32_t IDESC = idesc_bf16(GBM, BN, A_MN, !B_KM);
       uint32_t it = 0, tc_it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+      for (int t = blockIdx.x; ok && t < nitems; t += gridDim.x) {
+        int mb, nb, kb0, kb1;
+        item(t, mb, nb, kb0, kb1);
+        if (kb0 >= kb1) continue;   // an empty K range (the last split of a short K)
         const uint32_t ab = tc_it & 1;
         ok = mbar_wait(bar(GB_AEMPTY + ab), ((tc_it >> 1) & 1) ^ 1, wd, 42);
         if (!ok) break;
         fence_after_sync();
         bool first = true;
         for (int pass = 0; ok && pass < p.npass; ++pass) {
-          for (int kb = 0; kb < kblocks; ++kb) {
+          for (int kb = kb0; kb < kb1; ++kb) {
             const int stage = (int)(it % kGStages);
             ok = mbar_wait(bar(GB_FULL + stage), (it / kGStages) & 1, wd, 43);
             if (!ok) break;
             fence_after_sync();
             const uint32_t sA = base_u32 + stage * L::STAGE, sB = sA + L::A_BYTES;
+            // K-major operands step 32 bytes (16 k) along their 128-byte rows;
+            // MN-major ones step 16 rows of 128 bytes, their 64-wide column
+            // chunks one box (8 KB) apart
+            const SDesc da = A_MN ? sdesc_w(sA, L::B_BOX, 1024) : sdesc_w(sA, 16, 1024);
+            const SDesc db = B_KM ? sdesc_w(sB, 16, 1024) : sdesc_w(sB, L::B_BOX, 1024);
 #pragma unroll
             for (int kk = 0; kk < GBK / 16; ++kk)
-              mma_ss(tmem + ab * 256, sdesc_sw128(sA + kk * 32, 16, 1024),
-                     sdesc_sw128(sB + kk * 2048, L::B_BOX, 1024), IDESC, (first && kk == 0) ? 0u : 1u);
+              mma_ss_w(tmem + ab * 256, da + (A_MN ? kk * 2048 : kk * 32), db + (B_KM ? kk * 32 : kk * 2048), IDESC,
+                       (first && kk == 0) ? 0u : 1u);
             first = false;
             mma_commit(bar(GB_EMPTY + stage));
             ++it;
@@ -217,15 +261,17 @@ hstu_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // tms0: z1 (f1) or out (f2), FP32 [M, N]; tms1: u FP32 [M, D]; tms2: V | Q | K BF16 [3, M, D]
+    // tms0: z1 (f1) or out, FP32 [M, N]; tms1: u FP32 [M, D]; tms2: V | Q | K BF16 [3, M, D]
     const int wq = warp & 3, ch = warp >> 2;   // TMEM lane quarter, column half of the tile
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
     uint8_t* stg = base + L::STG_OFF + warp * L::STG_WARP;
     const uint32_t stg_u32 = base_u32 + L::STG_OFF + warp * L::STG_WARP;
     uint32_t tc_it = 0, sc = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
-      const int mb = t / nblocks, nb = t % nblocks;
+    for (int t = blockIdx.x; ok && t < nitems; t += gridDim.x) {
+      int mb, nb, kb0, kb1;
+      item(t, mb, nb, kb0, kb1);
+      if (kb0 >= kb1) continue;   // no MMA ran for an empty K range: nothing to add
       const uint32_t ab = tc_it & 1;
       ok = mbar_wait(bar(GB_AFULL + ab), (tc_it >> 1) & 1, wd, 44);
       if (!ok) break;
@@ -241,7 +287,7 @@ hstu_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
         tmem_ld32(lane_base + ab * 256 + col, v);
         tmem_wait_ld();
         float a[32];
-        if (MODE == 0) {
+        if (MODE == GM_F1) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) a[e] = __uint_as_float(v[e]);
           // z1 chunk into buffer 0, once the store that last read it is done
@@ -270,23 +316,43 @@ hstu_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
             bulk_commit();
           }
         } else {
-          // out = X + acc, X read as BF16 (rows past M read nothing and are not stored)
-          uint4 xv[4] = {};
-          if (row < p.M) {
-            const uint4* xs = reinterpret_cast<const uint4*>(p.x + (size_t)row * p.N + n);
+          if (MODE == GM_RES_BF16) {
+            // out = X + acc, X read as BF16 (rows past M read nothing and are not stored)
+            uint4 xv[4] = {};
+            if (row < p.M) {
+              const uint4* xs = reinterpret_cast<const uint4*>(p.x + (size_t)row * p.N + n);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) xv[e] = xs[e];
-          }
+              for (int e = 0; e < 4; ++e) xv[e] = xs[e];
+            }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            a[8 * e] = __uint_as_float(v[8 * e]) + bf16_lo_f(xv[e].x);
-            a[8 * e + 1] = __uint_as_float(v[8 * e + 1]) + bf16_hi_f(xv[e].x);
-            a[8 * e + 2] = __uint_as_float(v[8 * e + 2]) + bf16_lo_f(xv[e].y);
-            a[8 * e + 3] = __uint_as_float(v[8 * e + 3]) + bf16_hi_f(xv[e].y);
-            a[8 * e + 4] = __uint_as_float(v[8 * e + 4]) + bf16_lo_f(xv[e].z);
-            a[8 * e + 5] = __uint_as_float(v[8 * e + 5]) + bf16_hi_f(xv[e].z);
-            a[8 * e + 6] = __uint_as_float(v[8 * e + 6]) + bf16_lo_f(xv[e].w);
-            a[8 * e + 7] = __uint_as_float(v[8 * e + 7]) + bf16_hi_f(xv[e].w);
+            for (int e = 0; e < 4; ++e) {
+              a[8 * e] = __uint_as_float(v[8 * e]) + bf16_lo_f(xv[e].x);
+              a[8 * e + 1] = __uint_as_float(v[8 * e + 1]) + bf16_hi_f(xv[e].x);
+              a[8 * e + 2] = __uint_as_float(v[8 * e + 2]) + bf16_lo_f(xv[e].y);
+              a[8 * e + 3] = __uint_as_float(v[8 * e + 3]) + bf16_hi_f(xv[e].y);
+              a[8 * e + 4] = __uint_as_float(v[8 * e + 4]) + bf16_lo_f(xv[e].z);
+              a[8 * e + 5] = __uint_as_float(v[8 * e + 5]) + bf16_hi_f(xv[e].z);
+              a[8 * e + 6] = __uint_as_float(v[8 * e + 6]) + bf16_lo_f(xv[e].w);
+              a[8 * e + 7] = __uint_as_float(v[8 * e + 7]) + bf16_hi_f(xv[e].w);
+            }
+          } else if (MODE == GM_RES_F32) {
+            // out = res + acc, res read as FP32 (rows past M read nothing)
+            float4 rv[8] = {};
+            if (row < p.M) {
+              const float4* rs = reinterpret_cast<const float4*>(p.res + (size_t)row * p.N + n);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) rv[e] = rs[e];
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              a[4 * e] = __uint_as_float(v[4 * e]) + rv[e].x;
+              a[4 * e + 1] = __uint_as_float(v[4 * e + 1]) + rv[e].y;
+              a[4 * e + 2] = __uint_as_float(v[4 * e + 2]) + rv[e].z;
+              a[4 * e + 3] = __uint_as_float(v[4 * e + 3]) + rv[e].w;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) a[e] = __uint_as_float(v[e]);
           }
           // alternate the two buffers
           const uint32_t off = (sc & 1) * 4096;
@@ -296,7 +362,10 @@ hstu_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant_
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if (in_rows) tma_store_2d(&tms0, stg_u32 + off, n, row0);
+            if (in_rows) {
+              if (MODE == GM_REDUCE) tma_reduce_add_2d(&tms0, stg_u32 + off, n, row0);
+              else tma_store_2d(&tms0, stg_u32 + off, n, row0);
+            }
             bulk_commit();
           }
           ++sc;
@@ -324,20 +393,29 @@ bool tmap_store_f32(CUtensorMap* m, const float* ptr, int64_t rows, int64_t cols
   return make_tmap_tile(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// Operand maps: A boxes of 64 k-columns x 128 rows, B boxes of 64
-// n-columns x 64 k-rows (both 128-byte swizzle).  Store maps: f1 z1, u and
-// V | Q | K as [3, M, D] (each part clipped at row M); f2 out.
-template <int MODE, int BN>
-cudaError_t launch_gemm_t(const GemmParams& p, const void* a0, const void* a1, const void* b, int num_sms,
-                          cudaStream_t st) {
-  CUtensorMap m0, m1, mb, s0, s1, s2;
-  if (!make_tmap_bf16(&m0, a0, p.M, p.K, GBM) || !make_tmap_bf16(&mb, b, p.K, p.N, GBK)) return cudaErrorInvalidValue;
+// The kernel's seven maps.  A: 64 k-columns x 128 rows of a row-major
+// [M, K] array, or 64 x 64 boxes of a row-major [K, M] array (A_MN).  B: 64
+// n-columns x 64 k-rows of a row-major [K, N] array, or 64 k-columns x BN
+// rows of a row-major [N, K] array (B_KM).  Every box 128-byte swizzled.
+// Store maps: f1 z1, u and V | Q | K as [3, M, D] (each part clipped at row
+// M); the other modes out only.
+template <int MODE, int BN, bool A_MN, bool B_KM>
+cudaError_t launch_gemm_t(const GemmParams& p, const void* a0, const void* a1, const void* b0, const void* b1,
+                          int num_sms, cudaStream_t st) {
+  CUtensorMap ma0, ma1, mb0, mb1, s0, s1, s2;
+  auto map_a = [&](CUtensorMap* m, const void* a) {
+    return A_MN ? make_tmap_bf16(m, a, p.K, p.M, GBK) : make_tmap_bf16(m, a, p.M, p.K, GBM);
+  };
+  auto map_b = [&](CUtensorMap* m, const void* b) {
+    return B_KM ? make_tmap_bf16(m, b, p.N, p.K, BN) : make_tmap_bf16(m, b, p.K, p.N, GBK);
+  };
+  if (!map_a(&ma0, a0) || !map_b(&mb0, b0)) return cudaErrorInvalidValue;
+  ma1 = ma0;
+  mb1 = mb0;
   if (p.npass > 1) {
-    if (!make_tmap_bf16(&m1, a1, p.M, p.K, GBM)) return cudaErrorInvalidValue;
-  } else {
-    m1 = m0;
+    if (p.pair_b ? !map_b(&mb1, b1) : !map_a(&ma1, a1)) return cudaErrorInvalidValue;
   }
-  if (MODE == 0) {
+  if (MODE == GM_F1) {
     const uint64_t dims[3] = {(uint64_t)p.D, (uint64_t)p.M, 3};
     const uint64_t strides[2] = {(uint64_t)p.D * 2, (uint64_t)p.M * p.D * 2};
     const uint32_t box[3] = {32, 32, 1};
@@ -351,17 +429,17 @@ cudaError_t launch_gemm_t(const GemmParams& p, const void* a0, const void* a1, c
     s2 = s0;
   }
   const size_t smem = GLayout<BN>::BYTES + 1024;
-  const void* fn = reinterpret_cast<const void*>(hstu_gemm_tc_kernel<MODE, BN>);
-  cudaError_t e = cudaFuncSetAttribute(hstu_gemm_tc_kernel<MODE, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  auto kern = hstu_gemm_tc_kernel<MODE, BN, A_MN, B_KM>;
+  const void* fn = reinterpret_cast<const void*>(kern);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) {
     set_launch_detail(e, "hstu_gemm_tc_kernel (smem attribute)", fn, kGThreads, smem);
     return e;
   }
-  const int ntiles = ((p.M + GBM - 1) / GBM) * (p.N / BN);
-  const int grid = ntiles < num_sms ? ntiles : num_sms;
+  const int64_t nitems = ((p.M + GBM - 1) / GBM) * (int64_t)(p.N / BN) * p.ksplit;
+  const int grid = (int)(nitems < num_sms ? nitems : num_sms);
   if (grid <= 0) return cudaSuccess;
-  hstu_gemm_tc_kernel<MODE, BN><<<grid, kGThreads, smem, st>>>(p, m0, m1, mb, s0, s1, s2);
+  kern<<<grid, kGThreads, smem, st>>>(p, ma0, ma1, mb0, mb1, s0, s1, s2);
   e = cudaGetLastError();
   if (e != cudaSuccess) set_launch_detail(e, "hstu_gemm_tc_kernel", fn, kGThreads, smem);
   return e;
@@ -372,14 +450,62 @@ cudaError_t launch_gemm_t(const GemmParams& p, const void* a0, const void* a1, c
 bool gemm_tc_supported(int D) { return D > 0 && D % 128 == 0; }
 
 cudaError_t launch_gemm_f1(const GemmParams& p, const void* x, const void* w1, int num_sms, cudaStream_t st) {
-  return p.N % 256 == 0 ? launch_gemm_t<0, 256>(p, x, nullptr, w1, num_sms, st)
-                        : launch_gemm_t<0, 128>(p, x, nullptr, w1, num_sms, st);
+  GemmParams q = p;
+  q.npass = 1; q.pair_b = 0; q.ksplit = 1;
+  return q.N % 256 == 0 ? launch_gemm_t<GM_F1, 256, false, false>(q, x, nullptr, w1, nullptr, num_sms, st)
+                        : launch_gemm_t<GM_F1, 128, false, false>(q, x, nullptr, w1, nullptr, num_sms, st);
 }
 
 cudaError_t launch_gemm_f2(const GemmParams& p, const void* y_hi, const void* y_lo, const void* w2, int num_sms,
                            cudaStream_t st) {
-  return p.N % 256 == 0 ? launch_gemm_t<1, 256>(p, y_hi, y_lo, w2, num_sms, st)
-                        : launch_gemm_t<1, 128>(p, y_hi, y_lo, w2, num_sms, st);
+  GemmParams q = p;
+  q.npass = 2; q.pair_b = 0; q.ksplit = 1;
+  return q.N % 256 == 0 ? launch_gemm_t<GM_RES_BF16, 256, false, false>(q, y_hi, y_lo, w2, nullptr, num_sms, st)
+                        : launch_gemm_t<GM_RES_BF16, 128, false, false>(q, y_hi, y_lo, w2, nullptr, num_sms, st);
+}
+
+// out = [res +] sum over the passes of A_p W^T: A_p [M, K] row-major BF16
+// (a1 the second half of a pair, or null for one pass), W [N, K] row-major
+// BF16, out [M, N] FP32, res [M, N] FP32 or null
+cudaError_t launch_gemm_nt(const GemmParams& p, const void* a0, const void* a1, const void* w, int num_sms,
+                           cudaStream_t st) {
+  GemmParams q = p;
+  q.npass = a1 ? 2 : 1; q.pair_b = 0; q.ksplit = 1;
+  if (q.res) {
+    return q.N % 256 == 0 ? launch_gemm_t<GM_RES_F32, 256, false, true>(q, a0, a1, w, nullptr, num_sms, st)
+                          : launch_gemm_t<GM_RES_F32, 128, false, true>(q, a0, a1, w, nullptr, num_sms, st);
+  }
+  return q.N % 256 == 0 ? launch_gemm_t<GM_STORE, 256, false, true>(q, a0, a1, w, nullptr, num_sms, st)
+                        : launch_gemm_t<GM_STORE, 128, false, true>(q, a0, a1, w, nullptr, num_sms, st);
+}
+
+// out += sum over the passes of L_p^T R_p: L_p [K, M] and R_p [K, N]
+// row-major BF16, out [M, N] FP32 already holding its start value (zero).
+// One of l1, r1 may name the second half of a pair.  K is cut into ranges so
+// that the work items about fill the GPU once; each range's partial sum is
+// added into out by TMA reduce-add (FP32, in no fixed order).
+cudaError_t launch_gemm_tn_reduce(const GemmParams& p, const void* l0, const void* l1, const void* r0, const void* r1,
+                                  int num_sms, cudaStream_t st) {
+  GemmParams q = p;
+  q.npass = (l1 || r1) ? 2 : 1;
+  q.pair_b = r1 ? 1 : 0;
+  const bool wide = q.N % 256 == 0;
+  const int64_t tiles = ((q.M + GBM - 1) / GBM) * (int64_t)(q.N / (wide ? 256 : 128));
+  const int64_t kbt = (q.K + GBK - 1) / GBK;
+  // the split that minimises the busiest CTA's work: waves of items x (64-blocks per
+  // item + about two 64-blocks' worth for an item's start and its reduce)
+  int64_t best_ks = 1, best_cost = -1;
+  const int64_t sms = num_sms > 0 ? num_sms : 1;
+  for (int64_t ks = 1; ks <= kbt && ks <= 64; ++ks) {
+    const int64_t kper = (kbt + ks - 1) / ks;
+    const int64_t used = (kbt + kper - 1) / kper;      // non-empty ranges
+    const int64_t waves = (tiles * used + sms - 1) / sms;
+    const int64_t cost = waves * (kper + 2);
+    if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_ks = ks; }
+  }
+  q.ksplit = (int)best_ks;
+  return wide ? launch_gemm_t<GM_REDUCE, 256, true, false>(q, l0, l1, r0, r1, num_sms, st)
+              : launch_gemm_t<GM_REDUCE, 128, true, false>(q, l0, l1, r0, r1, num_sms, st);
 }
 
 }  // namespace hstu

@@ -170,21 +170,30 @@ cudaError_t launch_tc_fwd_delta(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_tc_bwd(const AttnParams& p, cudaStream_t stream);
 
 // Tensor-core GEMMs of the layer with fused epilogues (BF16 operands, FP32
-// accumulation).  A [M, K] row-major, B [K, N] row-major; K % 64 == 0,
-// N % 128 == 0, D % 128 == 0.
+// accumulation).  C [M, N] = sum over passes of A_p B_p, A [M, K], B [K, N];
+// A is read K-major (a row-major [M, K] array) or MN-major (a row-major
+// [K, M] array, i.e. the transpose of a stored matrix), B MN-major (row-major
+// [K, N]) or K-major (row-major [N, K]).  M % 128 == 0 unless the output rows
+// are clipped (row-major outputs), N % 128 == 0; K needs no alignment (the
+// last 64-block is zero-filled).
 struct GemmParams {
   int64_t M;
-  int N, K, D;
-  int npass;            // 1: A = X; 2: A = y_hi, then y_lo, into one accumulator
+  int N;
+  int64_t K;
+  int D;
+  int npass;            // passes over K into one accumulator: the two halves of a BF16 operand pair
+  int pair_b;           // 0: pass p reads A_p (and B_0); 1: pass p reads B_p (and A_0)
+  int ksplit;           // K cut into ksplit ranges of whole 64-blocks, one work item each (reduce epilogue)
   int test_timeout;     // test only: CTA 0 never loads its first stage; waits give up after ~1 ms
   int* err;             // first error code (HSTU_ERR_TIMEOUT) and its wait site
   int* err_info;
-  const int* carry_err; // f2 only: error words of f1, raised into err at launch (or NULL)
+  const int* carry_err; // error words of an earlier GEMM, raised into err at launch (or NULL)
   float* z1;            // f1: [M, 4D] FP32
   float* u;             // f1: [M, D] FP32
   __nv_bfloat16* vqk;   // f1: [3][M][D] BF16 (V, Q, K)
-  const __nv_bfloat16* x; // f2: [M, D] BF16 residual
-  float* out;           // f2: [M, D] FP32
+  const __nv_bfloat16* x; // f2: [M, N] BF16 residual
+  const float* res;     // FP32 residual [M, N] (dX = dOut + dZ1 W1^T)
+  float* out;           // [M, N] FP32 output (stored, residual-added or reduce-added)
 };
 bool gemm_tc_supported(int D);
 // f1: z1 = X W1; u = SiLU(z1[:, :D]); V | Q | K = BF16(SiLU(z1[:, D:]))
@@ -192,5 +201,14 @@ cudaError_t launch_gemm_f1(const GemmParams& p, const void* x, const void* w1, i
 // f2: out = X + y_hi W2 + y_lo W2
 cudaError_t launch_gemm_f2(const GemmParams& p, const void* y_hi, const void* y_lo, const void* w2, int num_sms,
                            cudaStream_t st);
+// out = A W^T with A [M, K] row-major and W [N, K] row-major (dy = dOut W2^T);
+// with res: out = res + sum_p A_p W^T (dX = dOut + dZ1_hi W1^T + dZ1_lo W1^T)
+cudaError_t launch_gemm_nt(const GemmParams& p, const void* a0, const void* a1, const void* w, int num_sms,
+                           cudaStream_t st);
+// out += sum_p L_p^T R_p over K = rows of L and R (L [K, M], R [K, N] row-major),
+// split over K: the weight gradients dW2 = y^T dOut and dW1 = X^T dZ1.  out
+// must hold its initial value (zero) before the launch.
+cudaError_t launch_gemm_tn_reduce(const GemmParams& p, const void* l0, const void* l1, const void* r0,
+                                  const void* r1, int num_sms, cudaStream_t st);
 
 }  // namespace hstu

@@ -335,7 +335,7 @@ hstu_status_t hstu_layer_bwd(const hstu_attn_desc* d, const hstu_layer_bwd_args*
                                !a->dx || !a->dw1 || !a->dw2)))
     return HSTU_ERR_INVALID_ARG;
   for (const void* p : {a->x, a->w1, a->w2, (const void*)a->z1, (const void*)a->u, a->vqk, a->o, a->y, (const void*)a->dout,
-                        (const void*)a->dx})
+                        (const void*)a->dx, (const void*)a->dw1, (const void*)a->dw2})
     if (p && !aligned16(p)) return HSTU_ERR_INVALID_ARG;
   const LayerWs L = layer_ws(d, true);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kWsAlign - 1)) || workspace_bytes < L.total)
@@ -352,8 +352,23 @@ hstu_status_t hstu_layer_bwd(const hstu_attn_desc* d, const hstu_layer_bwd_args*
     if (a->d_rab_time) LAYER_CUDA(cudaMemsetAsync(a->d_rab_time, 0, sizeof(float) * d->H * d->num_time_buckets, st));
     return HSTU_OK;
   }
-  cublasHandle_t h = prepare_cublas(st, ws + L.cublas);
-  if (!h) { set_detail_message("cuBLAS handle set-up failed"); return HSTU_ERR_CUDA; }
+  // the four GEMMs run on the tensor-core kernel when D % 128 == 0, else on cuBLAS
+  const bool fused = gemm_tc_supported(D);
+  cublasHandle_t h = nullptr;
+  int32_t* hdr = reinterpret_cast<int32_t*>(ws + L.attn);
+  int sms = 0;
+  if (fused) {
+    int dev = 0;
+    LAYER_CUDA(cudaGetDevice(&dev));
+    LAYER_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    LAYER_CUDA(cudaMemsetAsync(hdr + WS_LAYER_ERR, 0, 2 * sizeof(int32_t), st));
+    // the weight gradients are reduce-added over ranges of tokens: start from zero
+    LAYER_CUDA(cudaMemsetAsync(a->dw1, 0, sizeof(float) * (size_t)D * 4 * D, st));
+    LAYER_CUDA(cudaMemsetAsync(a->dw2, 0, sizeof(float) * (size_t)D * D, st));
+  } else {
+    h = prepare_cublas(st, ws + L.cublas);
+    if (!h) { set_detail_message("cuBLAS handle set-up failed"); return HSTU_ERR_CUDA; }
+  }
   const __nv_bfloat16* vqk = static_cast<const __nv_bfloat16*>(a->vqk);
   __nv_bfloat16* y_hi = reinterpret_cast<__nv_bfloat16*>(ws + L.y_hi);
   __nv_bfloat16* y_lo = reinterpret_cast<__nv_bfloat16*>(ws + L.y_lo);
@@ -369,9 +384,19 @@ hstu_status_t hstu_layer_bwd(const hstu_attn_desc* d, const hstu_layer_bwd_args*
   LAYER_CUDA(cudaGetLastError());
   f32_to_bf16_kernel<<<grid_for(TD), 256, 0, st>>>(static_cast<const float*>(a->dout), doutbf, (int64_t)TD);
   LAYER_CUDA(cudaGetLastError());
-  LAYER_CUBLAS(gemm_rm(h, true, false, D, D, T, y_hi, D, doutbf, D, 0.f, a->dw2, D));
-  LAYER_CUBLAS(gemm_rm(h, true, false, D, D, T, y_lo, D, doutbf, D, 1.f, a->dw2, D));
-  LAYER_CUBLAS(gemm_rm(h, false, true, T, D, D, doutbf, D, a->w2, D, 0.f, dy, D));
+  GemmParams gp{};
+  gp.D = D;
+  gp.err = hdr + WS_LAYER_ERR; gp.err_info = hdr + WS_LAYER_INFO;
+  if (fused) {
+    gp.M = D; gp.N = D; gp.K = T; gp.out = a->dw2;
+    LAYER_CUDA(launch_gemm_tn_reduce(gp, y_hi, y_lo, doutbf, nullptr, sms, st));
+    gp.M = T; gp.N = D; gp.K = D; gp.out = dy;
+    LAYER_CUDA(launch_gemm_nt(gp, doutbf, nullptr, a->w2, sms, st));
+  } else {
+    LAYER_CUBLAS(gemm_rm(h, true, false, D, D, T, y_hi, D, doutbf, D, 0.f, a->dw2, D));
+    LAYER_CUBLAS(gemm_rm(h, true, false, D, D, T, y_lo, D, doutbf, D, 1.f, a->dw2, D));
+    LAYER_CUBLAS(gemm_rm(h, false, true, T, D, D, doutbf, D, a->w2, D, 0.f, dy, D));
+  }
 
   // attention backward: du, dv, dq, dk (FP32), d_rab
   hstu_attn_bwd_args ba{};
@@ -389,10 +414,21 @@ hstu_status_t hstu_layer_bwd(const hstu_attn_desc* d, const hstu_layer_bwd_args*
   // dZ1 = [du|dv|dq|dk] * SiLU'(Z1) ; dW1 = X^T dZ1 ; dX = dOut + dZ1 W1^T
   silu_grad_kernel<<<grid_for(TD), 256, 0, st>>>(grads, a->z1, dz1_hi, dz1_lo, T, D);
   LAYER_CUDA(cudaGetLastError());
+  float* dx = static_cast<float*>(a->dx);
+  if (fused) {
+    // an error of the two GEMMs before the attention is raised into the
+    // workspace's error word here (the attention's plan cleared it)
+    gp.err = hdr + WS_ERR; gp.err_info = hdr + WS_ERR_INFO; gp.carry_err = hdr + WS_LAYER_ERR;
+    gp.M = D; gp.N = 4 * D; gp.K = T; gp.out = a->dw1;
+    LAYER_CUDA(launch_gemm_tn_reduce(gp, a->x, nullptr, dz1_hi, dz1_lo, sms, st));
+    gp.M = T; gp.N = D; gp.K = 4 * D; gp.out = dx; gp.res = static_cast<const float*>(a->dout);
+    LAYER_CUDA(launch_gemm_nt(gp, dz1_hi, dz1_lo, a->w1, sms, st));
+    note_launches(7);  // the y pair, dout to BF16, dW2, dy, SiLU', dW1, dX
+    return HSTU_OK;
+  }
   LAYER_CUBLAS(gemm_rm(h, true, false, D, 4 * D, T, a->x, D, dz1_hi, 4 * D, 0.f, a->dw1, 4 * D));
   LAYER_CUBLAS(gemm_rm(h, true, false, D, 4 * D, T, a->x, D, dz1_lo, 4 * D, 1.f, a->dw1, 4 * D));
   LAYER_CUDA(cudaMemcpyAsync(a->dx, a->dout, sizeof(float) * TD, cudaMemcpyDeviceToDevice, st));
-  float* dx = static_cast<float*>(a->dx);
   LAYER_CUBLAS(gemm_rm(h, false, true, T, D, 4 * D, dz1_hi, 4 * D, a->w1, 4 * D, 1.f, dx, D));
   LAYER_CUBLAS(gemm_rm(h, false, true, T, D, 4 * D, dz1_lo, 4 * D, a->w1, 4 * D, 1.f, dx, D));
   note_launches(3);  // the y pair, dout to BF16, SiLU' (cuBLAS's own kernels not counted)

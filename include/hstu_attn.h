@@ -319,7 +319,12 @@ hstu_status_t hstu_layer_fwd(const hstu_attn_desc* desc, const hstu_layer_fwd_ar
                              void* workspace, size_t workspace_bytes, hstu_stream_t stream);
 
 /* Layer backward: dx, dw1, dw2 and the bias-table gradients, recomputing the
- * attention tile by tile from the saved u, vqk and o. */
+ * attention tile by tile from the saved u, vqk and o.  All pointers device,
+ * 16-byte aligned; outputs are overwritten.  With D % 128 == 0 the four
+ * GEMMs run on the library's tensor-core kernels: dw1 and dw2 are then sums
+ * over ranges of tokens added in no fixed order (FP32 rounding may differ
+ * from call to call); otherwise on cuBLAS.  A tensor-core GEMM's wait that
+ * runs out is reported as HSTU_ERR_TIMEOUT in the workspace's error word. */
 hstu_status_t hstu_layer_bwd(const hstu_attn_desc* desc, const hstu_layer_bwd_args* args,
                              void* workspace, size_t workspace_bytes, hstu_stream_t stream);
 
