@@ -29,6 +29,7 @@
 
 using namespace hstu;
 
+namespace hstu {
 namespace {
 
 size_t align_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
@@ -226,6 +227,7 @@ cublasHandle_t prepare_cublas(cudaStream_t st, void* ws) {
 }
 
 }  // namespace
+}  // namespace hstu
 
 extern "C" {
 

@@ -595,9 +595,16 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     // sequence's rows they land on are unchanged; rows past T are clipped.
     uint8_t* dqs = base + Lay::DQS_OFF + warp * Lay::DQS_WARP;
     const uint32_t dqs_u32 = base_u32 + Lay::DQS_OFF + warp * Lay::DQS_WARP;
-    auto drain_dq = [&](uint32_t g, int qb0, int64_t s0, int hh) -> bool {
+    // The previous tile's gradient MMAs are complete once its dQ^T is: the A
+    // buffer and the dZ^T staging are free again.
+    auto wait_dq = [&](uint32_t g) -> bool {
       if (!mbar_wait(bar(BAR_DQFULL), g & 1, wd, 30)) return false;
       fence_after_sync();
+      return true;
+    };
+    // dQ^T of tile g out of TMEM (its buffer released to the next dQ^T MMA)
+    // and into dq; DQFULL of g has been seen
+    auto drain_dq = [&](int qb0, int64_t s0, int hh) {
       uint32_t qv[16];
       tmem_ld16(lane_base + DQ_COL + hq * 16, qv);
       tmem_wait_ld();
@@ -620,7 +627,6 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           bulk_commit();
         }
       }
-      return true;
     };
     while (ok) {
       ok = mbar_wait(bar(BAR_KVFULL), item_it & 1, wd, 32);
@@ -718,11 +724,8 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
             }
           }
           if (pend) {
-            // the previous tile's gradient MMAs are complete once its dQ^T is:
-            // the A buffer and the dZ^T staging are free again
-            ok = drain_dq(qt_it - 1, pend_q0, s0, hh);
+            ok = wait_dq(qt_it - 1);
             if (!ok) break;
-            pend = false;
           }
           tmem_st8(lane_base + A_COL + hq * 16, ahi);
           tmem_st8(lane_base + A_COL + hq * 16 + 8, alo);
@@ -751,11 +754,8 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
             if (narrow) grad_cols<8, false>(p, sv, dav, ahi, alo, zhi, zlo, kc, hib, t32, t64, racc);
             else grad_cols<8, true>(p, sv, dav, ahi, alo, zhi, zlo, kc, hib, t32, t64, racc);
             if (half == 0 && pend) {
-              // the previous tile's gradient MMAs are complete once its dQ^T is:
-              // the A buffer and the dZ^T staging are free again
-              ok = drain_dq(qt_it - 1, pend_q0, s0, hh);
+              ok = wait_dq(qt_it - 1);
               if (!ok) break;
-              pend = false;
             }
             // A into its TMEM buffer.  Quarter hq owns columns [16 hq, 16 hq + 16):
             // hi pairs in the first 8, lo pairs in the last 8; this half's 8
@@ -775,14 +775,17 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_PREADY));
+        // the previous tile's dQ^T goes out while this tile's gradient MMAs run
+        if (pend) drain_dq(pend_q0, s0, hh);
         pend = true;
         pend_q0 = q0;
         ++qt_it;
       }
       if (!ok) break;
       if (pend) {
-        ok = drain_dq(qt_it - 1, pend_q0, s0, hh);
+        ok = wait_dq(qt_it - 1);
         if (!ok) break;
+        drain_dq(pend_q0, s0, hh);
       }
       // the item's remaining d_rab partial sums
       red_add(kc.drp + P + racc.rt_cur, racc.rt_run, want_rt && racc.rt_cur >= 0);

@@ -90,9 +90,10 @@ def _check_projection(pr, f, T, D, sel=None):
         assert np.all(np.abs(vqk[i] - want) <= bound), key
 
 
-# D = 128 and 256 take the tensor-core projections (f1 over 512 / 1024
-# output columns, f2 over 128 / 256, a ragged last row block); D = 64 the
-# library route (cuBLAS and separate element-wise kernels).
+# D = 128 and 256 take the tensor-core GEMMs (f1 over 512 / 1024 output
+# columns, f2 over 128 / 256, a ragged last row block; the backward's dW2,
+# dy, dW1, dX); D = 64 the library route (cuBLAS and separate element-wise
+# kernels).
 @pytest.mark.parametrize("case", ["ragged", "contexts", "d128", "d64_library"])
 def test_layer_parity_small(case):
     if case == "ragged":
@@ -215,3 +216,31 @@ def test_layer_mid_size_distance_from_the_exact_layer():
     for name, v in dist.items():
         assert v <= EXACT_BOUNDS[name], (name, v)
 
+
+
+def test_layer_tensor_core_route_runs_only_library_kernels():
+    """With D % 128 == 0 every kernel of the layer forward and backward is one
+    of this library's (no cuBLAS GEMM): the kernel names the CUDA profiler
+    records between the two calls, and four GEMMs in the backward."""
+    prof_mod = pytest.importorskip("torch.profiler")
+    b = _small_layer(44, [300, 131, 520], H=2, d=128, nt=16)
+    pr = layer_problem(b)
+    pr.forward()
+    torch.cuda.synchronize()
+    names = {}
+    for phase in ("fwd", "bwd"):
+        with prof_mod.profile(activities=[prof_mod.ProfilerActivity.CUDA]) as prof:
+            pr.forward() if phase == "fwd" else pr.backward()
+            torch.cuda.synchronize()
+        kern = [e.name for e in prof.events()
+                if str(getattr(e, "device_type", "")).endswith("CUDA")
+                and not e.name.startswith(("Memset", "Memcpy"))]
+        if not kern:
+            pytest.skip("the CUDA profiler recorded no kernels here")
+        names[phase] = kern
+    assert pr.device_error() == 0
+    for phase, kern in names.items():
+        foreign = sorted({k for k in kern if "hstu" not in k})
+        assert not foreign, f"{phase}: kernels not from this library: {foreign}"
+    assert sum("hstu_gemm_tc_kernel" in k for k in names["bwd"]) == 4
+    assert sum("hstu_gemm_tc_kernel" in k for k in names["fwd"]) == 2
