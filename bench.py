@@ -27,6 +27,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -79,8 +80,11 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling of SM clocks and throttle reasons.  mark_load()
+    and stop() bracket the loaded span (the soak steps and the timed steps,
+    back to back on the stream); only samples whose timestamps fall inside it
+    enter the summary."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -88,6 +92,19 @@ class ClockSampler:
         self.idx = gpu_index
         self.proc = None
         self.f = None
+        self.t_load = None
+
+    def mark_load(self):
+        self.t_load = time.time()
+
+    @staticmethod
+    def _epoch(stamp):
+        # nvidia-smi prints local time as "YYYY/MM/DD HH:MM:SS.mmm"
+        try:
+            day, frac = stamp.rsplit(".", 1) if "." in stamp else (stamp, "0")
+            return time.mktime(time.strptime(day.strip(), "%Y/%m/%d %H:%M:%S")) + float("0." + frac.strip())
+        except ValueError:
+            return None
 
     def start(self):
         try:
@@ -100,6 +117,7 @@ class ClockSampler:
             self.proc = None
 
     def stop(self):
+        t_end = time.time()
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         time.sleep(0.15)
@@ -113,22 +131,32 @@ class ClockSampler:
         rows = [ln.strip().split(",") for ln in self.f.read().splitlines() if ln.strip()]
         self.f.close()
         os.unlink(self.f.name)
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        t0 = self.t_load if self.t_load is not None else 0.0
         for r in rows:
             r = [x.strip() for x in r]
-            if len(r) < 9:
+            if len(r) < 10:
                 continue
+            ts = self._epoch(r[0])
+            if ts is not None and not (t0 <= ts <= t_end):
+                continue   # before the load or after it
             try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
+                sm.append(float(r[2]))
+                smax.append(float(r[3]))
             except ValueError:
                 continue
-            for nm, val in zip(names, r[5:9]):
+            try:
+                power.append(float(r[4]))
+            except ValueError:
+                pass
+            for nm, val in zip(names, r[6:10]):
                 if val.lower() == "active":
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_min_mhz": min(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "power_w_max": max(power) if power else None,
                 "samples": len(sm)}
 
 
@@ -452,11 +480,18 @@ def run_gpu(args, wl, rank, world, local_rank):
         pr.backward()
         return n + C.hstu_last_launch_count()
 
+    t_w = time.perf_counter()
     for w in range(max(args.warmup, 0)):
         step(w)
     torch.cuda.synchronize()
+    t_step = (time.perf_counter() - t_w) / max(args.warmup, 1)
     for pr in probs:
         assert pr.device_error() == 0, "device error during warm-up"
+    # Soak: untimed steps queued directly before the timed ones, so the clock
+    # record covers about args.soak_s seconds of sustained load ending with the
+    # timed region (a timed region of a few milliseconds alone falls between
+    # two clock samples).
+    n_soak = int(min(20000, math.ceil(args.soak_s / max(t_step, 1e-5)))) if args.soak_s > 0 else 0
 
     # ---- timed region: K steps, kernel events on the launching stream
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
@@ -483,7 +518,10 @@ def run_gpu(args, wl, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize()
     clock.start()
-    time.sleep(0.3)  # let the sampler start before the region
+    time.sleep(0.3)  # let the sampler start before the load
+    clock.mark_load()
+    for k in range(n_soak):
+        step(k)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
     if graph is not None:
@@ -595,7 +633,7 @@ def run_gpu(args, wl, rank, world, local_rank):
                           "max": per_batch[-1],
                           "note": "each resident batch once, in a separate untimed pass with step-boundary events"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clocks}
+            "clocks": dict(clocks, span=f"{n_soak} untimed steps queued directly before the timed ones, then the timed steps")}
     print(json.dumps(line), flush=True)
 
 
@@ -673,6 +711,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--soak-s", type=float, default=1.5,
+                    help="seconds of untimed steps queued right before the timed ones, under the clock sampler")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the CPU baseline")

@@ -21,7 +21,9 @@
 // output RMS on heavy-tailed batches.
 //
 // Roles (576 threads): warps 0-15 epilogue (TMEM lane quarter warp%4, column
-// quarter warp/4), warp 16 TMA producer, warp 17 MMA issuer and TMEM owner.
+// quarter warp/4), warp 16 TMA producer, warp 17 MMA issuer and TMEM owner
+// (the whole warp runs the issue loop, so its operands stay warp-uniform, and
+// one elected lane issues each MMA and commit).
 // The planner lists the key blocks longest-first and the producer takes its
 // block index as its first work item and every later one from a global
 // counter (greedy LPT), passing it to the other roles in a shared-memory slot
@@ -475,7 +477,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
+    {   // the whole warp runs the issue loop (its values stay warp-uniform); one elected lane issues
       constexpr uint32_t IDESC_S = idesc_bf16(BK, BQ, false, false);    // M=128 keys, N=64 queries
       constexpr uint32_t IDESC_DVK = idesc_bf16(BK, D, false, true);    // A K-major, B MN-major
       constexpr uint32_t IDESC_DQ = idesc_bf16(D, BQ, true, true);      // A = K^T, B = dZ^T, MN-major
@@ -506,22 +508,22 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         for (int kk = 0; kk < BQ / 16; ++kk) {   // K = 64 queries: 4 steps of 16
           const uint32_t a_hi = tmem + A_COL + 16u * kk;
           const uint32_t acc0 = (first && kk == 0) ? 0u : 1u;
-          mma_ts_w(tmem + DV_COL, a_hi, dh_s + kk * 2048, IDESC_DVK, acc0);
-          mma_ts_w(tmem + DV_COL, a_hi + 8, dh_s + kk * 2048, IDESC_DVK, 1u);
-          mma_ts_w(tmem + DV_COL, a_hi, dl_s + kk * 2048, IDESC_DVK, 1u);
-          mma_ss_w(tmem + DK_COL, zh_km + kk * 32, q_s + kk * 2048, IDESC_DVK, acc0);
-          mma_ss_w(tmem + DK_COL, zl_km + kk * 32, q_s + kk * 2048, IDESC_DVK, 1u);
+          mma_ts_e(tmem + DV_COL, a_hi, dh_s + kk * 2048, IDESC_DVK, acc0);
+          mma_ts_e(tmem + DV_COL, a_hi + 8, dh_s + kk * 2048, IDESC_DVK, 1u);
+          mma_ts_e(tmem + DV_COL, a_hi, dl_s + kk * 2048, IDESC_DVK, 1u);
+          mma_ss_e(tmem + DK_COL, zh_km + kk * 32, q_s + kk * 2048, IDESC_DVK, acc0);
+          mma_ss_e(tmem + DK_COL, zl_km + kk * 32, q_s + kk * 2048, IDESC_DVK, 1u);
         }
-        mma_commit(bar(BAR_QEMPTY + st));   // the Q / dO stage is read by no later MMA
+        mma_commit_e(bar(BAR_QEMPTY + st));   // the Q / dO stage is read by no later MMA
         if (!mbar_wait(bar(BAR_DQEMPTY), (g & 1) ^ 1, wd, 27)) return false;
         fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {   // K = 128 keys: 8 steps of 16
-          mma_ss_w(tmem + DQ_COL, k_mn + kk * 2048, zh_mn + kk * 2048, IDESC_DQ, kk > 0 ? 1u : 0u);
-          mma_ss_w(tmem + DQ_COL, k_mn + kk * 2048, zl_mn + kk * 2048, IDESC_DQ, 1u);
+          mma_ss_e(tmem + DQ_COL, k_mn + kk * 2048, zh_mn + kk * 2048, IDESC_DQ, kk > 0 ? 1u : 0u);
+          mma_ss_e(tmem + DQ_COL, k_mn + kk * 2048, zl_mn + kk * 2048, IDESC_DQ, 1u);
         }
-        if (last) mma_commit(bar(BAR_KVEMPTY));   // K and V of this item are read by no later MMA
-        mma_commit(bar(BAR_DQFULL));
+        if (last) mma_commit_e(bar(BAR_KVEMPTY));   // K and V of this item are read by no later MMA
+        mma_commit_e(bar(BAR_DQFULL));
         return true;
       };
       while (ok) {
@@ -547,16 +549,16 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ka = (kk >> 2) * Lay::KBOX + (kk & 3) * 32;
             const uint32_t qb = (kk >> 2) * Lay::QBOX + (kk & 3) * 32;
-            mma_ss_w(tmem + S_COL, k_km + ka, q_s + qb, IDESC_S, kk > 0 ? 1u : 0u);
+            mma_ss_e(tmem + S_COL, k_km + ka, q_s + qb, IDESC_S, kk > 0 ? 1u : 0u);
           }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ka = (kk >> 2) * Lay::KBOX + (kk & 3) * 32;
             const uint32_t qb = (kk >> 2) * Lay::QBOX + (kk & 3) * 32;
-            mma_ss_w(tmem + DA_COL, v_km + ka, dh_s + qb, IDESC_S, kk > 0 ? 1u : 0u);
-            mma_ss_w(tmem + DA_COL, v_km + ka, dl_s + qb, IDESC_S, 1u);
+            mma_ss_e(tmem + DA_COL, v_km + ka, dh_s + qb, IDESC_S, kk > 0 ? 1u : 0u);
+            mma_ss_e(tmem + DA_COL, v_km + ka, dl_s + qb, IDESC_S, 1u);
           }
-          mma_commit(bar(BAR_SFULL));
+          mma_commit_e(bar(BAR_SFULL));
           if (have_prev) {
             ok = issue_grad(prev, prev_st, first, false);
             first = false;
@@ -568,11 +570,11 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         }
         if (ok && have_prev) ok = issue_grad(prev, prev_st, first, true);
         if (!ok) break;
-        if (!have_prev) mma_commit(bar(BAR_KVEMPTY));   // an item without tiles (none is planned)
-        mma_commit(bar(BAR_DKVFULL));
+        if (!have_prev) mma_commit_e(bar(BAR_KVEMPTY));   // an item without tiles (none is planned)
+        mma_commit_e(bar(BAR_DKVFULL));
         ++item_it;
       }
-      mma_commit(bar(BAR_DRAIN));
+      mma_commit_e(bar(BAR_DRAIN));
       drain_wait(bar(BAR_DRAIN), 0);
     }
   } else {
