@@ -218,6 +218,23 @@ def test_layer_mid_size_distance_from_the_exact_layer():
 
 
 
+def test_layer_tensor_core_route_counts_its_own_kernels():
+    """With D % 128 == 0 the backward is ten kernels of this library: the
+    attention backward's planner, norm-gate and attention kernels, then the
+    y pair, dOut to BF16, the dW2 and dy GEMMs, SiLU' and the dW1 and dX
+    GEMMs; the cuBLAS route (D = 64) counts six (its GEMMs are cuBLAS's)."""
+    from hstu_jagged_attention_02_gb300 import binding as C
+    for b, want in ((_small_layer(45, [300, 131, 520], H=2, d=128, nt=16), 10),
+                    (_small_layer(46, [200, 77, 310], H=1, d=64), 6)):
+        pr = layer_problem(b)
+        pr.forward()
+        pr.backward()
+        n = C.hstu_last_launch_count()
+        torch.cuda.synchronize()
+        assert pr.device_error() == 0
+        assert n == want, (b.H * b.d_v, n)
+
+
 def test_layer_tensor_core_route_runs_only_library_kernels():
     """With D % 128 == 0 every kernel of the layer forward and backward is one
     of this library's (no cuBLAS GEMM): the kernel names the CUDA profiler
