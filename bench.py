@@ -16,6 +16,12 @@ With --workload layer it measures the full HSTU layer instead (x W1, SiLU
 split, the same attention, LayerNorm gate, y W2 + x, forward + backward on 8
 sequences of 8K-32K tokens at D = 512), counting the projections' FLOPs too.
 
+The e2e figure runs the same steps through the C ABI from pinned host
+buffers, every step's inputs uploaded and its result read back (a training
+step's parameter gradients, an inference request's candidate outputs), the
+copies on two streams overlapping the neighbouring steps' compute;
+e2e.all_outputs reads back every output and gradient instead.
+
 With --graph the K timed steps are captured once as a CUDA graph and the
 timed region replays it (the per-kernel events of the library's timing hook
 are part of the graph); by default they are launched one by one.
@@ -243,6 +249,12 @@ class AttentionWorkload:
                 if t is not None]
         return ins, outs
 
+    def result(self, pr):
+        # what a training step reads back: the gradients of the attention's own
+        # parameters (the bias tables); the activation gradients stay on the
+        # device for the layer below
+        return [t for t in (pr.d_rab_pos, pr.d_rab_time) if t is not None]
+
     def oracle_step(self, b):
         from oracle import oracle as O
         d = self.dropout()
@@ -297,6 +309,10 @@ class LayerWorkload(AttentionWorkload):
                            pr.rab_time, pr.x, pr.w1, pr.w2, pr.dout) if t is not None]
         outs = [t for t in (pr.out, pr.dx, pr.dw1, pr.dw2, pr.d_rab_pos, pr.d_rab_time) if t is not None]
         return ins, outs
+
+    def result(self, pr):
+        # the layer's parameter gradients (W1, W2, the bias tables)
+        return [t for t in (pr.dw1, pr.dw2, pr.d_rab_pos, pr.d_rab_time) if t is not None]
 
     def oracle_step(self, b):
         from oracle import oracle as O
@@ -357,6 +373,9 @@ class DeltaWorkload(AttentionWorkload):
         ins = [t for t in (pr.cand_offsets, pr.cache_offsets, pr.cand_ts, pr.rab_pos, pr.rab_time,
                            pr.q, pr.k, pr.v, pr.u) if t is not None]
         return ins, [pr.o, pr.y]
+
+    def result(self, pr):
+        return [pr.y]   # the candidates' outputs: the response to the request
 
     def oracle_step(self, b):
         from oracle import oracle as O
@@ -566,6 +585,10 @@ def run_gpu(args, wl, rank, world, local_rank):
 
     # ---- end to end through the C ABI with host buffers
     e2e = run_e2e(args, wl, probs, flops, stream, world)
+    e2e["read_back"] = "the step's result: " + ("the candidates' outputs" if not wl.has_backward
+                                                 else "the parameter gradients (activation gradients stay on the device)")
+    e2e_all = run_e2e(args, wl, probs, flops, stream, world, all_outputs=True)
+    e2e["all_outputs"] = {k: e2e_all[k] for k in ("value", "d2h_bytes_per_step", "ms_per_step")}
 
     if rank != 0:
         return
@@ -637,10 +660,13 @@ def run_gpu(args, wl, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, wl, probs, flops, stream, world):
+def run_e2e(args, wl, probs, flops, stream, world, all_outputs=False):
     """Same metric through the public C ABI with pinned host buffers: each step
     copies its inputs host -> device, runs forward + backward and copies the
-    results back.  The copies run on two copy streams and overlap the compute
+    step's result back: the parameter gradients of a training step (the
+    activation gradients stay on the device for the layer below), the
+    candidates' outputs of an inference request, or with all_outputs every
+    output and gradient.  The copies run on two copy streams and overlap the compute
     of the neighbouring steps, as a training loop's input prefetch and result
     drain would (each batch has its own device buffers; a step's upload waits
     until the download of the previous step that used those buffers is done,
@@ -651,6 +677,8 @@ def run_e2e(args, wl, probs, flops, stream, world):
     hosts = []
     for pr in probs:
         ins, outs = wl.host_io(pr)
+        if not all_outputs:
+            outs = wl.result(pr)
         h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in ins]
         h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
         hosts.append((ins, h_in, outs, h_out))

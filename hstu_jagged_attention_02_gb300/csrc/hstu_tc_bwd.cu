@@ -347,7 +347,8 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     // ------------------------------------------------------------ producer
     uint32_t item_it = 0, qt_it = 0, kv_phases = 0;
     bool kv_copy = false;                 // the last KVFULL phase carries a copy
-    uint32_t armed[kQStages] = {0, 0};
+    static_assert(kQStages == 2, "per-stage counters hold two stages");
+    Count2 armed;
     bool ok = true;
     // The next work item is claimed only once the current one's loads are all
     // issued (claiming earlier pairs items up statically and loses the
@@ -465,7 +466,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(full);
-          armed[stage] += 1;
+          armed.add(stage, 1);
         }
         ++qt_it;
       }

@@ -377,9 +377,10 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   if (warp == kProducerWarp) {
     // ------------------------------------------------- producer: Q, K, times
     uint32_t kv_it = 0, q_it = 0;
-    uint32_t armed[kStages] = {0, 0};    // K phases armed per stage
-    uint32_t q_phases[kQBufs] = {0, 0};  // phases used per Q buffer (a copy or the final no-work arrive)
-    bool q_copy[kQBufs] = {false, false}; // the buffer's last phase carries a copy
+    static_assert(kStages == 2 && kQBufs == 2, "per-stage counters hold two stages");
+    Count2 armed;       // K phases armed per stage
+    Count2 q_phases;    // phases used per Q buffer (a copy or the final no-work arrive)
+    Count2 q_copy;      // 1: the buffer's last phase carries a copy
     bool ok = true;
     // The next work item is claimed only once the current one's loads are all
     // issued (claiming earlier pairs items up statically and loses the
@@ -432,8 +433,8 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(bar(BAR_QFULL + qb));  // without a copy the slot says: no more work
-        q_phases[qb] += 1;
-        q_copy[qb] = valid;
+        q_phases.add(qb, 1);
+        q_copy.set(qb, valid ? 1u : 0u);
       }
       ++q_it;
       if (!valid) break;
@@ -464,7 +465,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           for (int c = 0; c < L::NCH; ++c)
             tma_load_2d(sK0 + stage * L::K_BYTES + c * L::BOX, cached ? &tmk2 : &tmk, bar(BAR_KFULL + stage),
                         h * D + c * 64, y);
-          armed[stage] += 1;
+          armed.add(stage, 1);
           // K and V two tiles ahead into L2, so their loads, issued once a
           // stage frees up, do not wait on HBM
           if (kb + 2 < nkb) {
@@ -519,7 +520,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
     // it issues V loads as soon as a V stage is free, independently of K
     if (lane == 0) {
       uint32_t kv_it = 0, q_it = 0;
-      uint32_t armed[kStages] = {0, 0};
+      Count2 armed;
       bool ok = true;
       while (ok) {
         const uint32_t qb = q_it % kQBufs;
@@ -541,7 +542,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           for (int c = 0; c < L::NCH; ++c)
             tma_load_2d(sV0 + stage * L::K_BYTES + c * L::BOX, cached ? &tmv2 : &tmv, bar(BAR_VFULL + stage),
                         sl.h * D + c * 64, y);
-          armed[stage] += 1;
+          armed.add(stage, 1);
           ++kv_it;
         }
         ++q_it;

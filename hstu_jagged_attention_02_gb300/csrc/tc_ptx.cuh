@@ -53,6 +53,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Two per-stage counters of a two-stage ring held in registers: indexed by
+// a run-time stage through selects, not as an array in local memory.
+struct Count2 {
+  uint32_t c0 = 0, c1 = 0;
+  __device__ __forceinline__ void add(int i, uint32_t v) {
+    c0 += i == 0 ? v : 0u;
+    c1 += i == 0 ? 0u : v;
+  }
+  __device__ __forceinline__ void set(int i, uint32_t v) {
+    c0 = i == 0 ? v : c0;
+    c1 = i == 0 ? c1 : v;
+  }
+  __device__ __forceinline__ uint32_t operator[](int i) const { return i == 0 ? c0 : c1; }
+};
+
 // Shared abort state of a CTA: the first role whose wait runs out of time sets
 // it; every other role checks it while waiting and gives up too.
 struct Watchdog {
