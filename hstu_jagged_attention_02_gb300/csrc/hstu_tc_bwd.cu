@@ -48,7 +48,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t DV_COL = 0, DK_COL = 128, S_COL = 256, DA_COL = 320, A_COL = 384, DQ_COL = 448;
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum : int { BAR_KVFULL = 0, BAR_KVEMPTY, BAR_QFULL, BAR_QEMPTY = BAR_QFULL + kQStages,
+enum : int { BAR_KFULL = 0, BAR_KEMPTY, BAR_VFULL, BAR_VEMPTY, BAR_QFULL, BAR_QEMPTY = BAR_QFULL + kQStages,
              BAR_SFULL = BAR_QEMPTY + kQStages, BAR_SEMPTY, BAR_PREADY, BAR_DQFULL, BAR_DQEMPTY,
              BAR_DKVFULL, BAR_DKVEMPTY, BAR_DRAIN, BAR_COUNT };
 
@@ -292,8 +292,10 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   const bool want_rp = has_rp && p.d_rab_pos, want_rt = has_rt && p.d_rab_time;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(BAR_KVFULL), 1);
-    mbar_init(bar(BAR_KVEMPTY), 1);
+    mbar_init(bar(BAR_KFULL), 1);
+    mbar_init(bar(BAR_KEMPTY), 1);
+    mbar_init(bar(BAR_VFULL), 1);
+    mbar_init(bar(BAR_VEMPTY), 1);
     for (int s = 0; s < kQStages; ++s) {
       mbar_init(bar(BAR_QFULL + s), 1);
       mbar_init(bar(BAR_QEMPTY + s), 1);
@@ -345,8 +347,8 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    uint32_t item_it = 0, qt_it = 0, kv_phases = 0;
-    bool kv_copy = false;                 // the last KVFULL phase carries a copy
+    uint32_t item_it = 0, qt_it = 0, k_phases = 0, v_phases = 0;
+    bool k_copy = false;                  // the last KFULL phase carries a copy
     static_assert(kQStages == 2, "per-stage counters hold two stages");
     Count2 armed;
     bool ok = true;
@@ -375,38 +377,61 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         const int row = k0 + lane + 32 * x;
         kv[x] = (valid && p.ts && row < n) ? p.ts[s0 + row] : tbase;
       }
-      if (lane == 0) ok = mbar_wait(bar(BAR_KVEMPTY), (item_it & 1) ^ 1, wd, 21);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      // the K/V copy starts before the key timestamps arrive; the phase
-      // completes with the copy and the arrive below, after they are staged
-      if (lane == 0 && valid) {
-        mbar_expect_tx(bar(BAR_KVFULL), 4 * Lay::KBOX);
-        const int y = (int)(s0 + k0);
-        for (int c = 0; c < 2; ++c) {
-          tma_load_2d(sK + c * Lay::KBOX, &tmk, bar(BAR_KVFULL), h * D + c * 64, y);
-          tma_load_2d(sV + c * Lay::KBOX, &tmv, bar(BAR_KVFULL), h * D + c * 64, y);
+      // V first: its buffer is free once the previous item's last dA^T is
+      // computed, a tile before K's (read by the last dQ^T)
+      if (valid) {
+        if (lane == 0) ok = mbar_wait(bar(BAR_VEMPTY), (v_phases & 1) ^ 1, wd, 33);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(BAR_VFULL), 2 * Lay::KBOX);
+          const int y = (int)(s0 + k0);
+          for (int c = 0; c < 2; ++c)
+            tma_load_2d(sV + c * Lay::KBOX, &tmv, bar(BAR_VFULL), h * D + c * 64, y);
         }
+        ++v_phases;
       }
-      bool kw = false;
+      // K, the key timestamps and the slot, once the previous item's last
+      // dQ^T is done: after the item's first query tile is on its way (so
+      // that tile's copy overlaps the previous item's end), or now for an
+      // item without tiles and for the final no-work slot
+      bool k_done = false;
+      auto stage_k = [&]() -> bool {
+        if (lane == 0) ok = mbar_wait(bar(BAR_KEMPTY), (item_it & 1) ^ 1, wd, 34);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) return false;
+        // the K copy starts before the key timestamps are staged; the phase
+        // completes with the copy and the arrive below
+        if (lane == 0 && valid) {
+          mbar_expect_tx(bar(BAR_KFULL), 2 * Lay::KBOX);
+          const int y = (int)(s0 + k0);
+          for (int c = 0; c < 2; ++c)
+            tma_load_2d(sK + c * Lay::KBOX, &tmk, bar(BAR_KFULL), h * D + c * 64, y);
+        }
+        bool kw = false;
 #pragma unroll
-      for (int x = 0; x < BK / 32; ++x) kw |= ts_wide(kv[x] - tbase);
-      const bool item_wide = __any_sync(0xffffffffu, kw);
+        for (int x = 0; x < BK / 32; ++x) kw |= ts_wide(kv[x] - tbase);
+        const bool item_wide = __any_sync(0xffffffffu, kw);
 #pragma unroll
-      for (int x = 0; x < BK / 32; ++x) kts_s[lane + 32 * x] = kv[x];
-      if (lane == 0) {
-        slot->s0 = s0; slot->tbase = tbase; slot->valid = valid ? 1 : 0;
-        slot->h = h; slot->k0 = k0; slot->n = n; slot->c = it.c; slot->h_end = it.h_end;
-        slot->wide = item_wide ? 1 : 0;
+        for (int x = 0; x < BK / 32; ++x) kts_s[lane + 32 * x] = kv[x];
+        if (lane == 0) {
+          slot->s0 = s0; slot->tbase = tbase; slot->valid = valid ? 1 : 0;
+          slot->h = h; slot->k0 = k0; slot->n = n; slot->c = it.c; slot->h_end = it.h_end;
+          slot->wide = item_wide ? 1 : 0;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(BAR_KFULL));  // without a copy the slot says: no more work
+          k_phases += 1;
+          k_copy = valid;
+        }
+        k_done = true;
+        return true;
+      };
+      if (!valid) {
+        stage_k();
+        break;
       }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(BAR_KVFULL));  // without a copy the slot says: no more work
-        kv_phases += 1;
-        kv_copy = valid;
-      }
-      ++item_it;
-      if (!valid) break;
       const int nqt = (n + BQ - 1) / BQ;
       for (int qt = bwd_q_begin(k0, it.c, BQ); ok && qt < nqt; ++qt) {
         const int q0 = qt * BQ;
@@ -469,12 +494,16 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           armed.add(stage, 1);
         }
         ++qt_it;
+        if (!k_done && !stage_k()) break;
       }
+      if (ok && !k_done) ok = stage_k();   // an item without tiles (none is planned)
+      ++item_it;
     }
     if (lane == 0) {
       for (int s = 0; s < kQStages; ++s)
         if (armed[s]) drain_wait(bar(BAR_QFULL + s), (armed[s] - 1) & 1);
-      if (kv_copy) drain_wait(bar(BAR_KVFULL), (kv_phases - 1) & 1);
+      if (k_copy) drain_wait(bar(BAR_KFULL), (k_phases - 1) & 1);
+      if (v_phases) drain_wait(bar(BAR_VFULL), (v_phases - 1) & 1);
     }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
@@ -523,20 +552,23 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           mma_ss_e(tmem + DQ_COL, k_mn + kk * 2048, zh_mn + kk * 2048, IDESC_DQ, kk > 0 ? 1u : 0u);
           mma_ss_e(tmem + DQ_COL, k_mn + kk * 2048, zl_mn + kk * 2048, IDESC_DQ, 1u);
         }
-        if (last) mma_commit_e(bar(BAR_KVEMPTY));   // K and V of this item are read by no later MMA
+        if (last) mma_commit_e(bar(BAR_KEMPTY));   // K of this item is read by no later MMA
         mma_commit_e(bar(BAR_DQFULL));
         return true;
       };
       while (ok) {
-        ok = mbar_wait(bar(BAR_KVFULL), item_it & 1, wd, 23);
+        ok = mbar_wait(bar(BAR_KFULL), item_it & 1, wd, 23);
         if (!ok) break;
         fence_after_sync();
         const ItemSlot sl = *slot;
         if (!sl.valid) break;
-        bool have_prev = false, first = true;
+        bool have_prev = false, first = true, v_ready = false;
         uint32_t prev = 0, prev_st = 0;
         const int nqt = (sl.n + BQ - 1) / BQ;
-        for (int qt = bwd_q_begin(sl.k0, sl.c, BQ); ok && qt < nqt; ++qt) {
+        const int qb0 = bwd_q_begin(sl.k0, sl.c, BQ);
+        int q_last = nqt - 1;   // the item's last query tile the mask keeps (V is released after its dA^T)
+        while (q_last >= qb0 && tile_class(q_last * BQ, sl.k0, BQ, BK, sl.n, sl.c, sl.h_end) == 0) --q_last;
+        for (int qt = qb0; ok && qt < nqt; ++qt) {
           if (tile_class(qt * BQ, sl.k0, BQ, BK, sl.n, sl.c, sl.h_end) == 0) continue;
           const uint32_t stage = qt_it % kQStages;
           ok = mbar_wait(bar(BAR_QFULL + stage), (qt_it / kQStages) & 1, wd, 25) &&
@@ -552,6 +584,12 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
             const uint32_t qb = (kk >> 2) * Lay::QBOX + (kk & 3) * 32;
             mma_ss_e(tmem + S_COL, k_km + ka, q_s + qb, IDESC_S, kk > 0 ? 1u : 0u);
           }
+          if (!v_ready) {
+            ok = mbar_wait(bar(BAR_VFULL), item_it & 1, wd, 35);
+            if (!ok) break;
+            fence_after_sync();
+            v_ready = true;
+          }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ka = (kk >> 2) * Lay::KBOX + (kk & 3) * 32;
@@ -560,6 +598,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
             mma_ss_e(tmem + DA_COL, v_km + ka, dl_s + qb, IDESC_S, 1u);
           }
           mma_commit_e(bar(BAR_SFULL));
+          if (qt == q_last) mma_commit_e(bar(BAR_VEMPTY));   // V of this item is read by no later MMA
           if (have_prev) {
             ok = issue_grad(prev, prev_st, first, false);
             first = false;
@@ -571,7 +610,12 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         }
         if (ok && have_prev) ok = issue_grad(prev, prev_st, first, true);
         if (!ok) break;
-        if (!have_prev) mma_commit_e(bar(BAR_KVEMPTY));   // an item without tiles (none is planned)
+        if (!have_prev) {   // an item without tiles (none is planned): release its buffers as they are
+          ok = mbar_wait(bar(BAR_VFULL), item_it & 1, wd, 35);
+          if (!ok) break;
+          mma_commit_e(bar(BAR_VEMPTY));
+          mma_commit_e(bar(BAR_KEMPTY));
+        }
         mma_commit_e(bar(BAR_DKVFULL));
         ++item_it;
       }
@@ -632,7 +676,7 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       }
     };
     while (ok) {
-      ok = mbar_wait(bar(BAR_KVFULL), item_it & 1, wd, 32);
+      ok = mbar_wait(bar(BAR_KFULL), item_it & 1, wd, 32);
       if (!ok) break;
       // the slot stays until this item's last tile is handed over; keep what
       // the dV / dK write-out needs in registers
