@@ -258,6 +258,61 @@ __device__ __forceinline__ float grad_fast16(const AttnParams& p, const uint32_t
   return acc.x + acc.y;
 }
 
+// All 16 query columns of this thread's key row are allowed and their
+// position bucket is saturated (P - 1), but the time bucket may change along
+// the columns: the bias is the far position term plus each column's time
+// term.  A and dZ as packed BF16 hi/lo pairs; returns the sum of the 16 dZ
+// (the far position bucket's share) and carries the time buckets' run sums
+// in acc.  32-bit relative times only.
+__device__ __forceinline__ float grad_time16(const AttnParams& p, const uint32_t (&sv)[16], const uint32_t (&dav)[16],
+                                             float rbp, const float* tpt, const int32_t* ts32, int32_t tj32,
+                                             float kC, float inv_n, bool want_rt, float* drt, RabAcc& acc,
+                                             uint32_t (&ahi)[8], uint32_t (&alo)[8], uint32_t (&zhi)[8],
+                                             uint32_t (&zlo)[8]) {
+  const float2 one2 = make_float2(1.f, 1.f), inv_n2 = make_float2(inv_n, inv_n);
+  float2 sum2 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < 16; c += 2) {
+    int d0 = ts32[c] - tj32, d1 = ts32[c + 1] - tj32;
+    d0 = d0 < 0 ? -d0 : d0;
+    d1 = d1 < 0 ? -d1 : d1;
+    int bt0 = 32 - __clz(d0), bt1 = 32 - __clz(d1);
+    bt0 = bt0 < p.Tb - 1 ? bt0 : p.Tb - 1;
+    bt1 = bt1 < p.Tb - 1 ? bt1 : p.Tb - 1;
+    const float2 b2 = make_float2(rbp + tpt[bt0], rbp + tpt[bt1]);
+    const float2 w2 = __ffma2_rn(p.kA2, make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), b2);
+    const float2 d2 = __fadd2_rn(one2, make_float2(ex2_approx(w2.x), ex2_approx(w2.y)));
+    const float2 sg2 = make_float2(rcp_approx(d2.x), rcp_approx(d2.y));
+    const float2 z2 = make_float2(w2.x * p.kZ, w2.y * p.kZ);
+    const float2 a2 = __fmul2_rn(make_float2(w2.x * kC, w2.y * kC), sg2);
+    const float2 f2 = __ffma2_rn(z2, fsub2(one2, sg2), one2);  // 1 + z (1 - sg)
+    const float2 h2 = __fmul2_rn(__fmul2_rn(make_float2(__uint_as_float(dav[c]), __uint_as_float(dav[c + 1])), sg2), f2);
+    const float2 g2 = __fmul2_rn(h2, inv_n2);
+    sum2 = __fadd2_rn(sum2, g2);
+    if (want_rt) {
+      const int bts[2] = {bt0, bt1};
+      const float gs[2] = {g2.x, g2.y};
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        if (bts[e] == acc.rt_cur) {
+          acc.rt_run += gs[e];
+        } else {
+          red_add(drt + acc.rt_cur, acc.rt_run, acc.rt_cur >= 0);
+          acc.rt_cur = bts[e];
+          acc.rt_run = gs[e];
+        }
+      }
+    }
+    const uint32_t ah = pack_bf16(a2.x, a2.y), zh = pack_bf16(g2.x, g2.y);
+    ahi[c >> 1] = ah;
+    zhi[c >> 1] = zh;
+    const float2 al = bf16_residual2(a2, ah), zl = bf16_residual2(g2, zh);
+    alo[c >> 1] = pack_bf16(al.x, al.y);
+    zlo[c >> 1] = pack_bf16(zl.x, zl.y);
+  }
+  return sum2.x + sum2.y;
+}
+
 // Warps are spread over the four SM sub-partitions, each with a quarter of the
 // register file: with 18 warps two sub-partitions hold five,
 // and 5 x 32 threads x 96 registers = 15360 <= 16384.
@@ -731,6 +786,8 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           const int pb = ib + 15 < kc.h_end ? ib + 15 : kc.h_end;
           fast = pa - kc.pos_j >= P - 1 || kc.pos_j - pb >= P - 1;
         }
+        // all allowed and the position bucket saturated: only the time bucket may vary
+        const bool far_all = fast;
         if (fast && has_rt) {
           const int32_t cmin = cmm_s[stage * 8 + hq * 2], cmax = cmm_s[stage * 8 + hq * 2 + 1];
           int32_t dlo, dhi;
@@ -751,20 +808,30 @@ hstu_bwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         }
         // a key row past the sequence takes the same path with zero
         // constants: its A and dZ (which the dQ products read) are exact zeros
-        if (__all_sync(0xffffffffu, fast || !j_ok)) {
+        // (the warp takes the constant path when all its rows may, else the
+        // far path with per-column time buckets when all its rows are far and
+        // fully allowed, else the general path)
+        const bool all_const = __all_sync(0xffffffffu, fast || !j_ok);
+        if (all_const || (has_rt && narrow && __all_sync(0xffffffffu, far_all || !j_ok))) {
           uint32_t ahi[8], alo[8], zhi[8], zlo[8];
-          const float rb = kc.tp[P - 1] + kc.tp[P + btc];
-          const float sum = grad_fast16(p, svq, daq, rb, j_ok ? p.kC : 0.f, j_ok ? p.inv_n : 0.f, ahi, alo, zhi, zlo);
-          if (want_rp) racc.rp_far += sum;
-          if (want_rt) {
-            if (btc == racc.rt_cur) {
-              racc.rt_run += sum;
-            } else {
-              red_add(kc.drp + P + racc.rt_cur, racc.rt_run, racc.rt_cur >= 0);
-              racc.rt_cur = btc;
-              racc.rt_run = sum;
+          float sum;
+          if (all_const) {
+            const float rb = kc.tp[P - 1] + kc.tp[P + btc];
+            sum = grad_fast16(p, svq, daq, rb, j_ok ? p.kC : 0.f, j_ok ? p.inv_n : 0.f, ahi, alo, zhi, zlo);
+            if (want_rt) {
+              if (btc == racc.rt_cur) {
+                racc.rt_run += sum;
+              } else {
+                red_add(kc.drp + P + racc.rt_cur, racc.rt_run, racc.rt_cur >= 0);
+                racc.rt_cur = btc;
+                racc.rt_run = sum;
+              }
             }
+          } else {
+            sum = grad_time16(p, svq, daq, kc.tp[P - 1], kc.tp + P, ts32_s + stage * BQ + c0, kc.tj32,
+                              j_ok ? p.kC : 0.f, j_ok ? p.inv_n : 0.f, want_rt, kc.drp + P, racc, ahi, alo, zhi, zlo);
           }
+          if (want_rp) racc.rp_far += sum;
           if (pend) {
             ok = wait_dq(qt_it - 1);
             if (!ok) break;
