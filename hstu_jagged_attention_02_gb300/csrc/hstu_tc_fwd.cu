@@ -45,8 +45,8 @@ using namespace tc;
 
 constexpr int BM = kTcTile, BN = kTcTile;
 constexpr int kEpiWarps = 16;
-constexpr int kProducerWarp = 16, kMmaWarp = 17, kVProducerWarp = 18;
-constexpr int kThreads = 19 * 32;
+constexpr int kProducerWarp = 16, kMmaWarp = 17, kVProducerWarp = 18, kPvWarp = 19;
+constexpr int kThreads = 20 * 32;
 constexpr int kStages = 2;      // K ring and V ring, each
 constexpr int kTsSlots = 4;     // key-timestamp slots, released by the epilogue
 constexpr uint32_t kTmemCols = 512;
@@ -59,7 +59,7 @@ enum : int { BAR_QFULL = 0, BAR_QEMPTY = BAR_QFULL + kQBufs, BAR_KFULL = BAR_QEM
              BAR_KEMPTY = BAR_KFULL + kStages, BAR_VFULL = BAR_KEMPTY + kStages, BAR_VEMPTY = BAR_VFULL + kStages,
              BAR_TSFULL = BAR_VEMPTY + kStages, BAR_TSEMPTY = BAR_TSFULL + kTsSlots,
              BAR_SFULL = BAR_TSEMPTY + kTsSlots, BAR_PREADY = BAR_SFULL + 2, BAR_OFULL = BAR_PREADY + 2,
-             BAR_OEMPTY = BAR_OFULL + 2, BAR_DRAIN = BAR_OEMPTY + 2, BAR_COUNT };
+             BAR_OEMPTY = BAR_OFULL + 2, BAR_SFREE = BAR_OEMPTY + 2, BAR_DRAIN = BAR_SFREE + 2, BAR_COUNT };
 
 // A work item as the producer hands it to the other roles (one per Q buffer).
 struct __align__(16) ItemSlot {
@@ -309,7 +309,7 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQBufs; ++s) {
       mbar_init(bar(BAR_QFULL + s), 1);
-      mbar_init(bar(BAR_QEMPTY + s), 1);
+      mbar_init(bar(BAR_QEMPTY + s), 2);   // the S issuer's last S and the P.V issuer's last P.V of the item
     }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(BAR_KFULL + s), 1);
@@ -326,8 +326,9 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
       mbar_init(bar(BAR_PREADY + s), kEpiWarps);
       mbar_init(bar(BAR_OFULL + s), 1);
       mbar_init(bar(BAR_OEMPTY + s), kEpiWarps);
+      mbar_init(bar(BAR_SFREE + s), 1);
     }
-    mbar_init(bar(BAR_DRAIN), 1);
+    mbar_init(bar(BAR_DRAIN), 2);   // both MMA issuers
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -554,45 +555,19 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         if (armed[s]) drain_wait(bar(BAR_VFULL + s), (armed[s] - 1) & 1);
     }
   } else if (warp == kMmaWarp) {
-    // ----------------------------------------------------------------- MMA
+    // ------------------------------------------------------ MMA: S = Q K^T
+    // Two warps issue the tensor-core work: this one S = Q K^T, warp kPvWarp
+    // the P V products, each with its own barriers, so neither waits for the
+    // other's issue.  S(t) goes into S/P buffer t % 2 once the P V of tile
+    // t - 2 (the buffer's previous tile) is complete (SFREE); an item's Q
+    // buffer is released by this warp's commit after its last S together
+    // with the P V warp's arrival after its last P V.  This warp owns the
+    // TMEM allocation.
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16(BM, BN, false, false);
-      constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, false, true);
-      // descriptors built once; each MMA moves a start address by a constant
       const SDesc q_km = sdesc_w(sQ0, 16, 1024), k_km = sdesc_w(sK0, 16, 1024);
-      const SDesc v_mn = sdesc_w(sV0, L::BOX, 1024);
-      uint32_t kv_it = 0, q_it = 0, o_it = 0;
+      uint32_t kv_it = 0, q_it = 0;
       bool ok = true;
-      // The P.V of the latest S tile is issued after the next S tile, of the
-      // same item or of the next one, so the tensor core computes S(t + 1)
-      // while the epilogue scores tile t, also across items.  The tile that
-      // closes an item commits the item's Q buffer and O buffer with it.
-      struct PendPV {
-        bool have, first, last;
-        uint32_t it, ocol, ob, qb;
-      };
-      PendPV pend{false, false, false, 0, 0, 0, 0};
-      // P of tile t: quarter k/2 of the S buffer, hi at [32 q, 32 q + 16), lo 16 columns later
-      auto issue_pv = [&](const PendPV& pv) -> bool {
-        const uint32_t sb = pv.it & 1, stage = pv.it % kStages;
-        if (!mbar_wait(bar(BAR_PREADY + sb), (pv.it >> 1) & 1, wd, 5) ||
-            !mbar_wait(bar(BAR_VFULL + stage), (pv.it / kStages) & 1, wd, 14))
-          return false;
-        fence_after_sync();
-        const SDesc v_s = v_mn + stage * L::K_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint32_t a_hi = tmem + sb * kSColStride + 32u * (kk >> 1) + 8u * (kk & 1);
-          mma_ts_w(tmem + pv.ocol, a_hi, v_s + kk * 2048, IDESC_PV, (pv.first && kk == 0) ? 0u : 1u);
-          mma_ts_w(tmem + pv.ocol, a_hi + 16, v_s + kk * 2048, IDESC_PV, 1u);
-        }
-        mma_commit(bar(BAR_VEMPTY + stage));
-        if (pv.last) {
-          mma_commit(bar(BAR_QEMPTY + pv.qb));
-          mma_commit(bar(BAR_OFULL + pv.ob));
-        }
-        return true;
-      };
       while (ok) {
         const uint32_t qb = q_it % kQBufs;
         ok = mbar_wait(bar(BAR_QFULL + qb), (q_it / kQBufs) & 1, wd, 3);
@@ -601,15 +576,13 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
         const ItemSlot sl = slots[qb];
         if (!sl.valid) break;
         const SDesc q_s = q_km + qb * L::Q_BYTES;
-        const uint32_t ob = o_it & 1;
-        const uint32_t ocol = ob ? L::O_COL1 : L::O_COL0;
-        bool first = true;
         const int nkb = DELTA ? (sl.L + BN - 1) / BN + 1 : fwd_kv_blocks(sl.q0, sl.n, sl.c, BM, BN);
         for (int kb = 0; ok && kb < nkb; ++kb) {
           const int k0 = kb * BN;
           if (!DELTA && tile_class(sl.q0, k0, BM, BN, sl.n, sl.c, sl.h_end) == 0) continue;
           const uint32_t stage = kv_it % kStages, sb = kv_it & 1;
-          ok = mbar_wait(bar(BAR_KFULL + stage), (kv_it / kStages) & 1, wd, 6);
+          ok = mbar_wait(bar(BAR_KFULL + stage), (kv_it / kStages) & 1, wd, 6) &&
+               mbar_wait(bar(BAR_SFREE + sb), ((kv_it >> 1) & 1) ^ 1, wd, 15);
           if (!ok) break;
           fence_after_sync();
           const SDesc k_s = k_km + stage * L::K_BYTES;
@@ -620,33 +593,64 @@ hstu_fwd_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__
           }
           mma_commit(bar(BAR_SFULL + sb));
           mma_commit(bar(BAR_KEMPTY + stage));   // K is read by no later MMA
-          if (pend.have) {
-            ok = issue_pv(pend);
-            if (!ok) break;
+          ++kv_it;
+        }
+        if (!ok) break;
+        mma_commit(bar(BAR_QEMPTY + qb));   // Q is read by no later MMA
+        ++q_it;
+      }
+      // every MMA issued by this thread is complete before TMEM is released
+      mma_commit(bar(BAR_DRAIN));
+      drain_wait(bar(BAR_DRAIN), 0);
+    }
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------ MMA: O += P V
+    if (lane == 0) {
+      constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, false, true);
+      const SDesc v_mn = sdesc_w(sV0, L::BOX, 1024);
+      uint32_t kv_it = 0, q_it = 0;
+      bool ok = true;
+      while (ok) {
+        const uint32_t qb = q_it % kQBufs, ob = q_it & 1;
+        ok = mbar_wait(bar(BAR_QFULL + qb), (q_it / kQBufs) & 1, wd, 16);
+        if (!ok) break;
+        fence_after_sync();
+        const ItemSlot sl = slots[qb];
+        if (!sl.valid) break;
+        const uint32_t ocol = ob ? L::O_COL1 : L::O_COL0;
+        // this item's P.V go into O buffer ob once the epilogue has written it out
+        ok = mbar_wait(bar(BAR_OEMPTY + ob), ((q_it >> 1) & 1) ^ 1, wd, 4);
+        if (!ok) break;
+        fence_after_sync();
+        bool first = true;
+        const int nkb = DELTA ? (sl.L + BN - 1) / BN + 1 : fwd_kv_blocks(sl.q0, sl.n, sl.c, BM, BN);
+        for (int kb = 0; ok && kb < nkb; ++kb) {
+          const int k0 = kb * BN;
+          if (!DELTA && tile_class(sl.q0, k0, BM, BN, sl.n, sl.c, sl.h_end) == 0) continue;
+          // P of tile t: quarter k/2 of the S buffer, hi at [32 q, 32 q + 16), lo 16 columns later
+          const uint32_t sb = kv_it & 1, stage = kv_it % kStages;
+          ok = mbar_wait(bar(BAR_PREADY + sb), (kv_it >> 1) & 1, wd, 5) &&
+               mbar_wait(bar(BAR_VFULL + stage), (kv_it / kStages) & 1, wd, 14);
+          if (!ok) break;
+          fence_after_sync();
+          const SDesc v_s = v_mn + stage * L::K_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint32_t a_hi = tmem + sb * kSColStride + 32u * (kk >> 1) + 8u * (kk & 1);
+            mma_ts_w(tmem + ocol, a_hi, v_s + kk * 2048, IDESC_PV, (first && kk == 0) ? 0u : 1u);
+            mma_ts_w(tmem + ocol, a_hi + 16, v_s + kk * 2048, IDESC_PV, 1u);
           }
-          if (first) {  // this item's P.V go into O buffer ob once the epilogue has written it out
-            ok = mbar_wait(bar(BAR_OEMPTY + ob), ((o_it >> 1) & 1) ^ 1, wd, 4);
-            if (!ok) break;
-            fence_after_sync();
-          }
-          pend = PendPV{true, first, false, kv_it, ocol, ob, qb};
+          mma_commit(bar(BAR_VEMPTY + stage));
+          mma_commit(bar(BAR_SFREE + sb));   // the S/P buffer may take the next S
           first = false;
           ++kv_it;
         }
         if (!ok) break;
-        if (first) {  // an item without tiles (none is planned): release its buffers as they are
-          ok = mbar_wait(bar(BAR_OEMPTY + ob), ((o_it >> 1) & 1) ^ 1, wd, 4);
-          if (!ok) break;
-          mma_commit(bar(BAR_QEMPTY + qb));
-          mma_commit(bar(BAR_OFULL + ob));
-        } else {
-          pend.last = true;
-        }
+        // the item's last P has been handed over: its slot is read by no one any more
+        mbar_arrive(bar(BAR_QEMPTY + qb));
+        mma_commit(bar(BAR_OFULL + ob));
         ++q_it;
-        ++o_it;
       }
-      if (ok && pend.have) ok = issue_pv(pend);   // the last tile of the last item
-      // every MMA issued by this thread is complete before TMEM is released
       mma_commit(bar(BAR_DRAIN));
       drain_wait(bar(BAR_DRAIN), 0);
     }
