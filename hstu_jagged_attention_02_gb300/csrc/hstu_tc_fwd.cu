@@ -20,13 +20,13 @@
 // c = -1 / (log2(e) N); the bias tables are stored pre-multiplied by
 // -log2(e) so one FFMA gives w.
 //
-// Roles (608 threads): warps 0-15 epilogue (warp w reads TMEM lanes
+// Roles (640 threads): warps 0-15 epilogue (warp w reads TMEM lanes
 // 32*(w%4).. and the 32-column quarter w/4 of each tile), warp 16 TMA
-// producer of Q and K (plus the key timestamps), warp 17 MMA issuer and TMEM
-// owner, warp 18 TMA producer of V.  K and V have rings of their own: a K
-// stage is free once its S = Q K^T is done, so the next tiles' K loads and
-// S products never wait for the P V of the tile before, which is what a
-// shared K/V stage made them do.
+// producer of Q and K (plus the key timestamps), warp 17 S = Q K^T issuer
+// and TMEM owner, warp 18 TMA producer of V, warp 19 O += P V issuer.  K
+// and V have rings of their own: a K stage is free once its S = Q K^T is
+// done, so the next tiles' K loads and S products never wait for the P V of
+// the tile before, which is what a shared K/V stage made them do.
 // TMEM columns: S/P buffers at 0 and 128, O buffers at 256 and 256 + d.
 //
 // Scheduling: the planner lists the query blocks longest-first; the producer
@@ -273,7 +273,7 @@ __device__ __forceinline__ void score32_const(const AttnParams& p, uint32_t scol
 }
 
 // Warps are spread over the four SM sub-partitions, each with a quarter of the
-// register file: with 19 warps three sub-partitions hold five,
+// register file: with 20 warps each sub-partition holds five,
 // and 5 x 32 threads x 96 registers = 15360 <= 16384.
 // DELTA: the delta forward (KV-cached candidates): work items are blocks of
 // up to 128 candidates; their key tiles are every tile of the sequence's
