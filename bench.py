@@ -222,6 +222,7 @@ class AttentionWorkload:
     description = WORKLOAD
     n_batches = N_SEEDS
     dropout_p = 0.0   # --dropout: the fused dropout on y (fixed seed and offset)
+    plan_once = True  # the forward plans the backward too (--plan-each-call: each call plans for itself)
 
     def dropout(self):
         return None if not self.dropout_p else (self.dropout_p, 20240601, 0)
@@ -231,7 +232,7 @@ class AttentionWorkload:
 
     def problem(self, b, dev):
         from hstu_jagged_attention_02_gb300.attention import Problem
-        return Problem(b, device=dev, out_dtype="fp32", dropout=self.dropout())
+        return Problem(b, device=dev, out_dtype="fp32", dropout=self.dropout(), plan_once=self.plan_once)
 
     def flops(self, b):
         """(attention fwd, attention bwd, whole step) useful FLOPs."""
@@ -277,7 +278,9 @@ class AttentionWorkload:
 
     def config(self):
         return {"batches": N_SEEDS, "seeds": f"0..{N_SEEDS - 1} (+rank*{N_SEEDS})",
-                "l2": "inputs larger than L2: 16 distinct resident batches taken in turn"}
+                "l2": "inputs larger than L2: 16 distinct resident batches taken in turn",
+                "planner": ("one launch per step (the forward plans the backward too)" if self.plan_once
+                            else "one launch per call")}
 
 
 class LayerWorkload(AttentionWorkload):
@@ -751,8 +754,12 @@ def main():
                     help="capture the timed steps as a CUDA graph and time its replay")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="fused dropout probability on y (heavy_tailed and layer workloads)")
+    ap.add_argument("--plan-each-call", action="store_true",
+                    help="heavy_tailed: the forward and the backward each run their own planner")
     args = ap.parse_args()
     wl = WORKLOADS[args.workload]()
+    if args.plan_each_call:
+        wl.plan_once = False
     if args.dropout:
         if not wl.has_backward:
             ap.error("--dropout applies to training workloads only")

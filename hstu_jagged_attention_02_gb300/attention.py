@@ -31,10 +31,12 @@ class Problem:
 
     def __init__(self, batch, device="cuda", flags: int = 0, want_y: bool = True,
                  want_stats: bool = False, want_drab: bool = True, out_dtype: str = "fp32",
-                 dropout=None, bwd_flags: int = 0):
+                 dropout=None, bwd_flags: int = 0, plan_once: bool = False):
         # dropout: None or (p, seed, offset) of the fused dropout on y;
         # bwd_flags: flags added for the backward call only (e.g.
-        # HSTU_FLAG_FORCE_SIMT for a BF16 backward without a tensor-core kernel)
+        # HSTU_FLAG_FORCE_SIMT for a BF16 backward without a tensor-core kernel);
+        # plan_once: the forward plans the backward too (HSTU_FLAG_PLAN_BWD)
+        # and the backward reuses that plan (HSTU_FLAG_REUSE_PLAN)
         self.batch = batch
         dev = torch.device(device)
         self.dev = dev
@@ -84,6 +86,9 @@ class Problem:
             norm=batch.norm, ln_eps=batch.eps, flags=flags,
             dropout_p=0.0 if dropout is None else float(dropout[0]))
         self.bwd_flags = bwd_flags
+        self.plan_once = plan_once and batch.dy is not None
+        if self.plan_once:
+            self.bwd_flags |= C.HSTU_FLAG_REUSE_PLAN
         seed, offset = (0, 0) if dropout is None else (int(dropout[1]), int(dropout[2]))
         fwd_b, bwd_b = C.hstu_attn_workspace_size(self.desc)
         self.ws_bytes = max(fwd_b, bwd_b if self.backward_enabled else 0)
@@ -101,7 +106,11 @@ class Problem:
                 _ptr(self.d_rab_time), seed, offset)
 
     def forward(self, stream=None):
-        C.hstu_attn_fwd(self.desc, self.fwd_args, self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
+        d = self.desc
+        if self.plan_once:
+            d = C.hstu_attn_desc.from_buffer_copy(self.desc)
+            d.flags |= C.HSTU_FLAG_PLAN_BWD
+        C.hstu_attn_fwd(d, self.fwd_args, self.ws.data_ptr(), self.ws_bytes, _stream_handle(stream))
 
     def backward(self, stream=None):
         d = C.hstu_attn_desc.from_buffer_copy(self.desc)

@@ -21,6 +21,8 @@ HSTU_NORM_NONE, HSTU_NORM_LAYERNORM = 0, 1
 HSTU_FLAG_FORCE_SIMT = 1 << 0
 HSTU_FLAG_TEST_TIMEOUT = 1 << 1
 HSTU_FLAG_U_FP32 = 1 << 2
+HSTU_FLAG_PLAN_BWD = 1 << 3
+HSTU_FLAG_REUSE_PLAN = 1 << 4
 
 _vp = ctypes.c_void_p
 

@@ -40,13 +40,17 @@ struct KernelTimer {
   ~KernelTimer() { if (b) record_hook_event(b, st); }
 };
 
-constexpr uint32_t kKnownFlags = HSTU_FLAG_FORCE_SIMT | HSTU_FLAG_TEST_TIMEOUT | HSTU_FLAG_U_FP32;
+constexpr uint32_t kKnownFlags = HSTU_FLAG_FORCE_SIMT | HSTU_FLAG_TEST_TIMEOUT | HSTU_FLAG_U_FP32 |
+                                  HSTU_FLAG_PLAN_BWD | HSTU_FLAG_REUSE_PLAN;
 
 size_t align_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
 size_t esize(int dtype) { return dtype == HSTU_BF16 ? 2 : 4; }
 
 struct WsLayout {
   size_t seq_start, tmp, blocks, items, plan_end, dO, dq_acc, drab_part, drab_part_bytes, total;
+  // backward layout only: the second plan region, where a forward called with
+  // HSTU_FLAG_PLAN_BWD keeps the backward's plan, and the metadata it was made from
+  size_t pb_seq_start, pb_tmp, pb_blocks, pb_items, sv_off, sv_t0, sv_nt, sv_nc;
   int cap_blocks;
 };
 
@@ -66,6 +70,14 @@ WsLayout ws_layout(const hstu_attn_desc* d, bool bwd) {
     L.dq_acc = off; off = align_up(off + sizeof(float) * rows * (size_t)d->d_qk);
     L.drab_part_bytes = sizeof(float) * kDrabMaxCtas * (size_t)d->H * (d->num_pos_buckets + d->num_time_buckets);
     L.drab_part = off; off = align_up(off + L.drab_part_bytes);
+    L.pb_seq_start = off; off = align_up(off + sizeof(int) * (size_t)(d->B + 1));
+    L.pb_tmp = off;       off = align_up(off + sizeof(Block) * (size_t)cap);
+    L.pb_blocks = off;    off = align_up(off + sizeof(Block) * (size_t)cap);
+    L.pb_items = off;     off = align_up(off + sizeof(PlanItem) * (size_t)cap);
+    L.sv_off = off;       off = align_up(off + sizeof(int64_t) * (size_t)(d->B + 1));
+    L.sv_t0 = off;        off = align_up(off + sizeof(int64_t) * (size_t)d->B);
+    L.sv_nt = off;        off = align_up(off + sizeof(int32_t) * (size_t)d->B);
+    L.sv_nc = off;        off = align_up(off + sizeof(int32_t) * (size_t)d->B);
   }
   L.total = off;
   return L;
@@ -174,27 +186,40 @@ hstu_status_t check_tc_shape(const hstu_attn_desc* d, bool bwd) {
   return HSTU_ERR_UNSUPPORTED;
 }
 
+// One pass's tiling (the path's tile edges) and the plan region it is written to.
+PlanOut plan_out(int pass, bool tc, char* ws, size_t seq_start, size_t tmp, size_t blocks, size_t items) {
+  PlanOut o{};
+  if (!tc) {
+    o.BM = o.BN = kSimtTile;
+  } else if (pass == 0 || pass == 2) {
+    o.BM = o.BN = kTcTile;
+  } else {
+    o.BM = kTcBwdQTile;  // the tensor-core backward walks 64-row query tiles per 128-row key block
+    o.BN = kTcTile;
+  }
+  o.pass = pass;
+  o.seq_start = reinterpret_cast<int*>(ws + seq_start);
+  o.tmp = reinterpret_cast<Block*>(ws + tmp);
+  o.blocks = reinterpret_cast<Block*>(ws + blocks);
+  o.items = reinterpret_cast<PlanItem*>(ws + items);
+  return o;
+}
+
 PlanParams plan_params(const hstu_attn_desc* d, const int64_t* off, const int32_t* nt, const int32_t* nc,
                        const int64_t* ts, int pass, bool tc, char* ws, const WsLayout& L) {
   PlanParams p{};
   p.off = off; p.nt = nt; p.nc = nc; p.ts = ts;
   p.B = d->B; p.T = d->total_tokens; p.max_n = d->max_seq_len;
-  if (!tc) {
-    p.BM = p.BN = kSimtTile;
-  } else if (pass == 0 || pass == 2) {
-    p.BM = p.BN = kTcTile;
-  } else {
-    p.BM = kTcBwdQTile;  // the tensor-core backward walks 64-row query tiles per 128-row key block
-    p.BN = kTcTile;
-  }
-  p.pass = pass;
   p.hdr = reinterpret_cast<int*>(ws);
-  p.seq_start = reinterpret_cast<int*>(ws + L.seq_start);
-  p.tmp = reinterpret_cast<Block*>(ws + L.tmp);
-  p.blocks = reinterpret_cast<Block*>(ws + L.blocks);
-  p.items = reinterpret_cast<PlanItem*>(ws + L.items);
   p.cap_blocks = L.cap_blocks;
+  p.npass = 1;
+  p.out[0] = plan_out(pass, tc, ws, L.seq_start, L.tmp, L.blocks, L.items);
   return p;
+}
+
+// The kept backward plan (second plan region of a backward-sized workspace).
+PlanOut kept_plan_out(const hstu_attn_desc* d, char* ws, const WsLayout& L) {
+  return plan_out(1, use_tc(d, true), ws, L.pb_seq_start, L.pb_tmp, L.pb_blocks, L.pb_items);
 }
 
 #define HSTU_CUDA_TRY(expr)                                    \
@@ -278,19 +303,29 @@ hstu_status_t hstu_attn_fwd(const hstu_attn_desc* d, const hstu_attn_fwd_args* a
   // token tensors may be NULL only when there are no tokens
   if (!a || !a->seq_offsets || (d->total_tokens > 0 && (!a->q || !a->k || !a->v || !a->o)))
     return HSTU_ERR_INVALID_ARG;
+  if (d->flags & HSTU_FLAG_REUSE_PLAN) return HSTU_ERR_INVALID_ARG;  // a backward-only flag
   for (const void* ptr : {a->q, a->k, a->v, (const void*)a->o, a->u, (const void*)a->y})
     if (ptr && !aligned16(ptr)) return HSTU_ERR_INVALID_ARG;
   clear_detail();
   if ((s = check_tc_shape(d, false)) != HSTU_OK) return s;
-  const WsLayout L = ws_layout(d, false);
+  // keeping the backward's plan takes the backward's workspace
+  const bool keep_bwd = (d->flags & HSTU_FLAG_PLAN_BWD) != 0;
+  const WsLayout L = ws_layout(d, keep_bwd);
   if ((s = check_ws(workspace, workspace_bytes, L.total)) != HSTU_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   g_launches = 0;
 
   const bool tc = use_tc(d, false);
-  const PlanParams pp =
-      plan_params(d, a->seq_offsets, a->num_targets, a->num_contexts, a->timestamps, 0, tc, ws, L);
+  PlanParams pp = plan_params(d, a->seq_offsets, a->num_targets, a->num_contexts, a->timestamps, 0, tc, ws, L);
+  if (keep_bwd) {  // a second CTA of the same launch plans the backward
+    pp.npass = 2;
+    pp.out[1] = kept_plan_out(d, ws, L);
+    pp.sv_off = reinterpret_cast<int64_t*>(ws + L.sv_off);
+    pp.sv_t0 = reinterpret_cast<int64_t*>(ws + L.sv_t0);
+    pp.sv_nt = reinterpret_cast<int32_t*>(ws + L.sv_nt);
+    pp.sv_nc = reinterpret_cast<int32_t*>(ws + L.sv_nc);
+  }
   HSTU_CUDA_TRY(launch_plan(pp, st));
   ++g_launches;
 
@@ -298,7 +333,7 @@ hstu_status_t hstu_attn_fwd(const hstu_attn_desc* d, const hstu_attn_fwd_args* a
   p.off = a->seq_offsets; p.nt = a->num_targets; p.nc = a->num_contexts;
   p.ts = a->timestamps; p.rab_pos = a->rab_pos; p.rab_time = a->timestamps ? a->rab_time : nullptr;
   p.q = a->q; p.k = a->k; p.v = a->v; p.o = a->o;
-  p.hdr = pp.hdr; p.hdr_rw = pp.hdr; p.blocks = pp.blocks; p.items = pp.items;
+  p.hdr = pp.hdr; p.hdr_rw = pp.hdr; p.blocks = pp.out[0].blocks; p.items = pp.out[0].items;
   p.B = d->B; p.H = d->H; p.dqk = d->d_qk; p.dv_dim = d->d_v; p.T = d->total_tokens;
   p.dtype = d->dtype; p.out_dtype = d->out_dtype;
   p.alpha = d->alpha; p.inv_n = 1.0f / (float)d->max_seq_len;
@@ -337,6 +372,7 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
       (d->total_tokens > 0 && (!a->q || !a->k || !a->v || !a->o || !a->dy || !a->dq || !a->dk || !a->dv)))
     return HSTU_ERR_INVALID_ARG;
   if (d->total_tokens > 0 && (a->u == nullptr) != (a->du == nullptr)) return HSTU_ERR_INVALID_ARG;
+  if (d->flags & HSTU_FLAG_PLAN_BWD) return HSTU_ERR_INVALID_ARG;  // a forward-only flag
   for (const void* ptr : {a->q, a->k, a->v, a->o, a->u, a->dy, (const void*)a->dq, (const void*)a->dk,
                           (const void*)a->dv, (const void*)a->du})
     if (ptr && !aligned16(ptr)) return HSTU_ERR_INVALID_ARG;
@@ -349,10 +385,16 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
   g_launches = 0;
 
   const bool tc = use_tc(d, true);
+  // with HSTU_FLAG_REUSE_PLAN no planner runs: the norm-gate backward checks
+  // the plan a forward kept in the second plan region and arms it
+  const bool reuse = (d->flags & HSTU_FLAG_REUSE_PLAN) != 0;
   const PlanParams pp =
       plan_params(d, a->seq_offsets, a->num_targets, a->num_contexts, a->timestamps, 1, tc, ws, L);
-  HSTU_CUDA_TRY(launch_plan(pp, st));
-  ++g_launches;
+  const PlanOut plan = reuse ? kept_plan_out(d, ws, L) : pp.out[0];
+  if (!reuse) {
+    HSTU_CUDA_TRY(launch_plan(pp, st));
+    ++g_launches;
+  }
 
   const size_t rows = (size_t)d->total_tokens * (size_t)d->H;
   // dq is reduced in FP32: straight into the output when it is FP32, else in
@@ -390,6 +432,18 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
       np.zero_a = a->d_rab_pos; np.zero_a_n = a->d_rab_pos ? d->H * d->num_pos_buckets : 0;
       np.zero_b = a->d_rab_time; np.zero_b_n = a->d_rab_time ? d->H * d->num_time_buckets : 0;
     }
+    if (reuse) {
+      np.pc_hdr = pp.hdr;
+      np.pc_off = a->seq_offsets; np.pc_nt = a->num_targets; np.pc_nc = a->num_contexts;
+      np.pc_ts = a->timestamps;
+      np.pc_sv_off = reinterpret_cast<const int64_t*>(ws + L.sv_off);
+      np.pc_sv_t0 = reinterpret_cast<const int64_t*>(ws + L.sv_t0);
+      np.pc_sv_nt = reinterpret_cast<const int32_t*>(ws + L.sv_nt);
+      np.pc_sv_nc = reinterpret_cast<const int32_t*>(ws + L.sv_nc);
+      np.pc_B = d->B;
+      np.pc_tile = plan.BM | (plan.BN << 16);
+      np.pc_max_n = d->max_seq_len;
+    }
     HSTU_CUDA_TRY(launch_norm_gate_bwd(np, st));
     ++g_launches;
   }
@@ -402,7 +456,7 @@ hstu_status_t hstu_attn_bwd(const hstu_attn_desc* d, const hstu_attn_bwd_args* a
   p.d_rab_pos = has_rp ? a->d_rab_pos : nullptr;
   p.d_rab_time = has_rt ? a->d_rab_time : nullptr;
   p.drab_partial = drab_partial;
-  p.hdr = pp.hdr; p.hdr_rw = pp.hdr; p.blocks = pp.blocks; p.items = pp.items;
+  p.hdr = pp.hdr; p.hdr_rw = pp.hdr; p.blocks = plan.blocks; p.items = plan.items;
   p.B = d->B; p.H = d->H; p.dqk = d->d_qk; p.dv_dim = d->d_v; p.T = d->total_tokens;
   p.dtype = d->dtype; p.out_dtype = d->out_dtype;
   p.alpha = d->alpha; p.inv_n = 1.0f / (float)d->max_seq_len;
@@ -432,6 +486,7 @@ hstu_status_t hstu_attn_fwd_delta(const hstu_attn_desc* d, const hstu_attn_delta
   if (s != HSTU_OK) return s;
   if (!a || !a->cand_offsets || !a->cache_offsets || a->cache_tokens < 0) return HSTU_ERR_INVALID_ARG;
   if (d->dropout_p > 0.f) return HSTU_ERR_UNSUPPORTED;  // inference: no dropout
+  if (d->flags & (HSTU_FLAG_PLAN_BWD | HSTU_FLAG_REUSE_PLAN)) return HSTU_ERR_INVALID_ARG;
   if (d->total_tokens > 0 && (!a->q || !a->k || !a->v || !a->o)) return HSTU_ERR_INVALID_ARG;
   if (d->total_tokens > 0 && a->cache_tokens > 0 && (!a->k_cache || !a->v_cache)) return HSTU_ERR_INVALID_ARG;
   if (a->cache_tokens > 0 && (a->cand_timestamps == nullptr) != (a->cache_timestamps == nullptr))
@@ -465,7 +520,7 @@ hstu_status_t hstu_attn_fwd_delta(const hstu_attn_desc* d, const hstu_attn_delta
   p.q = a->q; p.k = a->k; p.v = a->v; p.o = a->o;
   p.off2 = a->cache_offsets; p.ts2 = a->cache_timestamps; p.k2 = a->k_cache; p.v2 = a->v_cache;
   p.T2 = a->cache_tokens;
-  p.hdr = pp.hdr; p.hdr_rw = pp.hdr; p.blocks = pp.blocks; p.items = pp.items;
+  p.hdr = pp.hdr; p.hdr_rw = pp.hdr; p.blocks = pp.out[0].blocks; p.items = pp.out[0].items;
   p.B = d->B; p.H = d->H; p.dqk = d->d_qk; p.dv_dim = d->d_v; p.T = d->total_tokens;
   p.dtype = d->dtype; p.out_dtype = d->out_dtype;
   p.alpha = d->alpha; p.inv_n = 1.0f / (float)d->max_seq_len;

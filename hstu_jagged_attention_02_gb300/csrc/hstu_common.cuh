@@ -27,7 +27,18 @@ enum : int {
   WS_NEXT = 5,      // next work item of the tensor-core kernels (dynamic scheduling)
   WS_LAYER_ERR = 6, // layer input projection: first device error code (raised into WS_ERR later)
   WS_LAYER_INFO = 7,
+  // the backward's tile plan kept by a forward called with HSTU_FLAG_PLAN_BWD
+  // (second plan region of the workspace) and what it was made for
+  WS_PB_VALID = 8,  // 1 while the kept plan is valid; every other planner launch clears it
+  WS_PB_NBLK = 9,   // its block count
+  WS_PB_B = 10,     // sequences
+  WS_PB_T_LO = 11,  // tokens, low and high 32 bits
+  WS_PB_T_HI = 12,
+  WS_PB_TILE = 13,  // query-tile rows | key-tile rows << 16
+  WS_PB_MAXN = 14,  // max_seq_len the metadata was validated against
 };
+// error detail (WS_ERR_INFO) of a backward whose kept plan does not match
+constexpr int kPlanMismatchInfo = -1;
 // Timestamps are staged relative to their sequence's first token; a tile
 // whose relative times all lie within +-2^30 s computes its gaps in 32 bits,
 // any other tile takes the 64-bit path.

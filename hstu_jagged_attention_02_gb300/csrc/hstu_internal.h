@@ -9,6 +9,16 @@
 
 namespace hstu {
 
+// Where one pass of the planner writes its plan.
+struct PlanOut {
+  int pass;         // 0 forward (query blocks), 1 backward (key blocks), 2 delta forward (candidate blocks)
+  int BM, BN;       // tile edges of the path that will run
+  int* seq_start;   // [B+1] scratch
+  Block* tmp;       // [cap_blocks] scratch
+  Block* blocks;    // [cap_blocks] result, longest first
+  PlanItem* items;  // [cap_blocks] the same blocks as full item records (tensor-core kernels)
+};
+
 struct PlanParams {
   const int64_t* off;
   const int32_t* nt;
@@ -17,16 +27,19 @@ struct PlanParams {
   int B;
   int64_t T;
   int max_n;
-  int BM, BN;       // tile edges of the path that will run
-  int pass;         // 0 forward (query blocks), 1 backward (key blocks), 2 delta forward (candidate blocks)
   const int64_t* off2;  // pass 2: cached-token offsets [B+1] (off: candidate offsets)
   int64_t T2;           // pass 2: cached tokens
   int* hdr;         // workspace header
-  int* seq_start;   // [B+1] scratch
-  Block* tmp;       // [cap_blocks] scratch
-  Block* blocks;    // [cap_blocks] result, longest first
-  PlanItem* items;  // [cap_blocks] the same blocks as full item records (tensor-core kernels)
   int cap_blocks;
+  // 1: one CTA plans out[0].  2: a second CTA plans out[1] (the backward) at
+  // the same time and keeps it for a later backward: the WS_PB_* header words
+  // and the metadata below record what it was made from.
+  int npass;
+  PlanOut out[2];
+  int64_t* sv_off;  // npass 2: [B+1] offsets
+  int64_t* sv_t0;   // [B] timestamp of each sequence's first token (0 without timestamps or tokens)
+  int32_t* sv_nt;   // [B] targets (0 when num_targets is NULL)
+  int32_t* sv_nc;   // [B] contexts (0 when num_contexts is NULL)
   int stage_off;    // set by launch_plan: offsets and block starts staged in shared memory
   int stage_rec;    // set by launch_plan: block records staged in shared memory
 };
@@ -108,6 +121,22 @@ struct NormParams {
   int F;           // H * d_v
   int norm;
   float eps;
+  // backward with a kept plan (HSTU_FLAG_REUSE_PLAN): one warp checks that
+  // the plan in the workspace was made for this call's descriptor and
+  // metadata, then arms it for the attention backward (block count, work
+  // counter), or records HSTU_ERR_DEVICE_CHECK and leaves it no work
+  int* pc_hdr;     // workspace header, or NULL (no check)
+  const int64_t* pc_off;
+  const int32_t* pc_nt;
+  const int32_t* pc_nc;
+  const int64_t* pc_ts;
+  const int64_t* pc_sv_off;
+  const int64_t* pc_sv_t0;
+  const int32_t* pc_sv_nt;
+  const int32_t* pc_sv_nc;
+  int pc_B;
+  int pc_tile;     // query-tile rows | key-tile rows << 16 of the backward this call runs
+  int pc_max_n;
 };
 
 // Diagnostics behind HSTU_ERR_CUDA (read with hstu_last_error_detail):

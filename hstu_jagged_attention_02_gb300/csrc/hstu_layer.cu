@@ -10,11 +10,12 @@
 //   o, y = attention(Q, K, V, U)          hstu_attn_fwd (norm and gate per desc)
 //   out = X + y W2                        one tensor-core GEMM, residual in its epilogue
 //
-// and its backward, whose four dense GEMMs are plain library GEMMs (cuBLAS,
-// with its workspace taken from the caller's workspace) around this file's
-// element-wise kernels (SiLU', BF16 pairs).  Where D is not a multiple of
-// 128 the forward takes the same library route: cuBLAS, then the SiLU split
-// and the residual as separate kernels.
+// and its backward: dW2 = y^T dOut and dW1 = X^T dZ1 (split-K, reduce-added),
+// dy = dOut W2^T and dX = dOut + dZ1 W1^T, on the same tensor-core GEMM
+// kernel, around this file's element-wise kernels (SiLU', BF16 pairs).
+// Where D is not a multiple of 128 both passes take the library route:
+// cuBLAS GEMMs (their workspace taken from the caller's workspace), then the
+// SiLU split and the residual as separate kernels.
 //
 // Precision: V, Q, K are BF16 (the attention's MMA operands); the gate U and
 // every accumulation stay FP32.  The computed GEMM operands y and dZ1 enter
@@ -243,6 +244,8 @@ hstu_status_t hstu_layer_fwd(const hstu_attn_desc* d, const hstu_layer_fwd_args*
                              size_t workspace_bytes, hstu_stream_t stream) {
   hstu_status_t s = check_layer_desc(d);
   if (s != HSTU_OK) return s;
+  // the layer plans its attention itself: the plan-keeping flags are not for it
+  if (d->flags & (HSTU_FLAG_PLAN_BWD | HSTU_FLAG_REUSE_PLAN)) return HSTU_ERR_INVALID_ARG;
   if (!a || !a->seq_offsets ||
       (d->total_tokens > 0 &&
        (!a->x || !a->w1 || !a->w2 || !a->out || !a->z1 || !a->u || !a->vqk || !a->o || !a->y)))
@@ -332,6 +335,7 @@ hstu_status_t hstu_layer_bwd(const hstu_attn_desc* d, const hstu_layer_bwd_args*
   hstu_status_t s = check_layer_desc(d);
   if (s != HSTU_OK) return s;
   if (d->flags & HSTU_FLAG_TEST_TIMEOUT) return HSTU_ERR_UNSUPPORTED;   // a forward-only test mode
+  if (d->flags & (HSTU_FLAG_PLAN_BWD | HSTU_FLAG_REUSE_PLAN)) return HSTU_ERR_INVALID_ARG;
   if (!a || !a->seq_offsets ||
       (d->total_tokens > 0 && (!a->x || !a->w1 || !a->w2 || !a->z1 || !a->u || !a->vqk || !a->o || !a->y || !a->dout ||
                                !a->dx || !a->dw1 || !a->dw2)))

@@ -28,6 +28,8 @@ extern "C" hstu_status_t hstu_attn_fwd_noalloc(const hstu_attn_desc* desc, const
   size_t need = 0;
   hstu_status_t s = hstu_attn_workspace_size(desc, &need, nullptr);
   if (s != HSTU_OK) return s;
+  // the built-in scratch holds a forward plan only
+  if (desc->flags & (HSTU_FLAG_PLAN_BWD | HSTU_FLAG_REUSE_PLAN)) return HSTU_ERR_INVALID_ARG;
   if (need > kScratchBytes) {
     char msg[160];
     snprintf(msg, sizeof(msg), "this problem needs %zu bytes of forward scratch; the built-in buffer holds %zu",

@@ -231,14 +231,56 @@ __global__ void __launch_bounds__(kWarps * 32) norm_gate_fwd_kernel(NormParams p
   }
 }
 
+// A backward plan kept by an earlier forward (HSTU_FLAG_REUSE_PLAN), checked
+// by one warp before the attention backward may use it: it must have been
+// made for this call's sequence count, token count, tile edges and
+// max_seq_len, from the same offsets, target and context counts and first
+// timestamps of the sequences (everything the plan depends on).  A match arms
+// it (its block count, the work counter at zero), so it can serve any number
+// of backward calls; otherwise the attention backward gets no work and
+// HSTU_ERR_DEVICE_CHECK is recorded.
+__device__ __noinline__ void check_kept_plan(const NormParams& p) {
+  pdl_wait();  // whatever ran before this grid is complete
+  int* h = p.pc_hdr;
+  const int lane = threadIdx.x & 31;
+  const int64_t T = p.T;
+  const bool key = h[WS_PB_VALID] == 1 && h[WS_PB_B] == p.pc_B && h[WS_PB_T_LO] == (int)(uint32_t)T &&
+                   h[WS_PB_T_HI] == (int)(T >> 32) && h[WS_PB_TILE] == p.pc_tile && h[WS_PB_MAXN] == p.pc_max_n;
+  bool ok = key;
+  if (key) {  // same B and T: the kept offsets (validated when planned) index this call's arrays
+    for (int b = lane; b <= p.pc_B; b += 32) {
+      bool e = p.pc_off[b] == p.pc_sv_off[b];
+      if (b < p.pc_B) {
+        e = e && (p.pc_nt ? p.pc_nt[b] : 0) == p.pc_sv_nt[b] && (p.pc_nc ? p.pc_nc[b] : 0) == p.pc_sv_nc[b];
+        const int64_t s0 = p.pc_sv_off[b];
+        const int64_t t0 = (p.pc_ts && p.pc_sv_off[b + 1] > s0) ? p.pc_ts[s0] : 0;
+        e = e && t0 == p.pc_sv_t0[b];
+      }
+      ok = ok && e;
+    }
+  }
+  ok = __all_sync(0xffffffffu, ok);
+  if (lane == 0) {
+    if (ok) {
+      h[WS_NBLK] = h[WS_PB_NBLK];
+      h[WS_NEXT] = 0;
+    } else {
+      h[WS_NBLK] = 0;
+      set_error(h, HSTU_ERR_DEVICE_CHECK, kPlanMismatchInfo);
+    }
+  }
+}
+
 // du = xn * dy;  g = dy * u;  LayerNorm: dO = rstd * (g - mean(g) - xn * mean(g xn)); none: dO = g
 template <typename TI, typename TO, int VEC, int PER, bool DROP>
 __global__ void __launch_bounds__(kWarps * 32) norm_gate_bwd_kernel(NormParams p) {
   // Launched programmatically after the backward's planner, with which it
   // shares no data: it runs alongside it.  One thread waits for the planner,
   // so this grid completes only after it (the attention backward, launched
-  // normally after this kernel, reads the plan).
+  // normally after this kernel, reads the plan).  Without a planner, warp 0
+  // of CTA 0 checks and arms the kept plan instead.
   if (blockIdx.x == 0 && threadIdx.x == 0) pdl_wait();
+  if (p.pc_hdr && blockIdx.x == 0 && threadIdx.x < 32) check_kept_plan(p);
   if (blockIdx.x == 0) {
     for (int x = threadIdx.x; x < p.zero_a_n; x += blockDim.x) p.zero_a[x] = 0.f;
     for (int x = threadIdx.x; x < p.zero_b_n; x += blockDim.x) p.zero_b[x] = 0.f;

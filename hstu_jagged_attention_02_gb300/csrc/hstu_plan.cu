@@ -66,7 +66,9 @@ __device__ int block_cost(const SeqInfo& s, int blk, int pass, int BM, int BN, i
 
 // Dynamic shared memory: histogram, then (when they fit) the offsets, the
 // block starts per sequence and the block records; otherwise the workspace
-// scratch arrays stand in.
+// scratch arrays stand in.  CTA 0 plans out[0]; with npass == 2, CTA 1 plans
+// the backward's tiling into out[1] at the same time and keeps it for a later
+// backward call (WS_PB_* words, the metadata it was made from).
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(PlanParams p) {
   extern __shared__ __align__(16) uint8_t plan_smem[];
@@ -76,21 +78,29 @@ plan_kernel(PlanParams p) {
   uint8_t* cur = plan_smem + sizeof(int) * kCostBins;
   int64_t* off = const_cast<int64_t*>(p.off);
   if (p.stage_off) { off = reinterpret_cast<int64_t*>(cur); cur += sizeof(int64_t) * ((p.B + 2) & ~1); }
-  int* start = p.seq_start;
+  int* start = nullptr;
   if (p.stage_off) { start = reinterpret_cast<int*>(cur); cur += sizeof(int) * ((p.B + 1 + 3) & ~3); }
-  Block* rec = p.stage_rec ? reinterpret_cast<Block*>(cur) : p.tmp;
+  const bool keep = blockIdx.x == 1;
+  const PlanOut o = keep ? p.out[1] : p.out[0];
+  if (!start) start = o.seq_start;
+  Block* rec = p.stage_rec ? reinterpret_cast<Block*>(cur) : o.tmp;
   const int t = threadIdx.x;
   // the kernel that follows (launched programmatically) may start its own
   // set-up now; it waits for this grid before it reads the plan
   pdl_launch_dependents();
 
   if (t == 0) {
-    p.hdr[WS_ERR] = 0;
-    p.hdr[WS_ERR_INFO] = 0;
-    p.hdr[WS_NBLK] = 0;
-    p.hdr[WS_NTILES] = 0;
-    p.hdr[WS_FLAGS] = 0;
-    p.hdr[WS_NEXT] = 0;
+    if (!keep) {
+      p.hdr[WS_ERR] = 0;
+      p.hdr[WS_ERR_INFO] = 0;
+      p.hdr[WS_NBLK] = 0;
+      p.hdr[WS_NTILES] = 0;
+      p.hdr[WS_FLAGS] = 0;
+      p.hdr[WS_NEXT] = 0;
+    }
+    // a kept backward plan is void from here on: this launch either replaces
+    // it (CTA 1) or plans another batch
+    if (keep || p.npass == 1) p.hdr[WS_PB_VALID] = 0;
     sh_bad = 0;
     sh_bad_b = 0;
   }
@@ -101,28 +111,37 @@ plan_kernel(PlanParams p) {
 
   // 1. validation
   if (t == 0 && (p.off[0] != 0 || p.off[p.B] != p.T)) atomicExch(&sh_bad, 1);
-  if (t == 0 && p.pass == 2 && (p.off2[0] != 0 || p.off2[p.B] != p.T2)) atomicExch(&sh_bad, 1);
+  if (t == 0 && o.pass == 2 && (p.off2[0] != 0 || p.off2[p.B] != p.T2)) atomicExch(&sh_bad, 1);
   for (int b = t; b < p.B; b += kPlanThreads) {
     const int64_t n = off[b + 1] - off[b];
     const int64_t m = p.nt ? p.nt[b] : 0, c = p.nc ? p.nc[b] : 0;
     // pass 2: n candidates after L cached tokens, n + L <= N
-    const int64_t L = p.pass == 2 ? p.off2[b + 1] - p.off2[b] : 0;
+    const int64_t L = o.pass == 2 ? p.off2[b + 1] - p.off2[b] : 0;
     if (n < 0 || L < 0 || n + L > p.max_n || m < 0 || c < 0 || m + c > n) {
       if (atomicExch(&sh_bad, 1) == 0) sh_bad_b = b;
     }
+    if (keep) {
+      p.sv_off[b] = off[b];
+      p.sv_nt[b] = (int32_t)m;
+      p.sv_nc[b] = (int32_t)c;
+    }
   }
+  if (keep && t == 0) p.sv_off[p.B] = off[p.B];
   __syncthreads();
   if (sh_bad) {
-    if (t == 0) {
+    if (t == 0 && !keep) {
       p.hdr[WS_ERR_INFO] = sh_bad_b;
       atomicCAS(p.hdr + WS_ERR, 0, HSTU_ERR_DEVICE_CHECK);
     }
     return;
   }
+  if (keep)  // the offsets are consistent now, so every first token is in range
+    for (int b = t; b < p.B; b += kPlanThreads)
+      p.sv_t0[b] = (p.ts && off[b + 1] > off[b]) ? p.ts[off[b]] : 0;
 
   // 2. blocks per sequence -> exclusive prefix (start[b]), one chunk of
   // kPlanThreads sequences at a time
-  const int BR = p.pass == 1 ? p.BN : p.BM;  // rows per block of this pass
+  const int BR = o.pass == 1 ? o.BN : o.BM;  // rows per block of this pass
   int carry = 0;
   for (int base = 0; base < p.B; base += kPlanThreads) {
     const int b = base + t;
@@ -155,8 +174,8 @@ plan_kernel(PlanParams p) {
     s.c = p.nc ? p.nc[b] : 0;
     s.h_end = s.n - (p.nt ? p.nt[b] : 0);
     const int blk = idx - start[b];
-    const int cached_len = p.pass == 2 ? (int)(p.off2[b + 1] - p.off2[b]) : 0;
-    const int cost = block_cost(s, blk, p.pass, p.BM, p.BN, cached_len);
+    const int cached_len = o.pass == 2 ? (int)(p.off2[b + 1] - p.off2[b]) : 0;
+    const int cost = block_cost(s, blk, o.pass, o.BM, o.BN, cached_len);
     Block r;
     r.b = b; r.blk = blk; r.cost = cost; r.pad = 0;
     rec[idx] = r;
@@ -191,7 +210,7 @@ plan_kernel(PlanParams p) {
   for (int idx = t; idx < nblk; idx += kPlanThreads) {
     const Block r = rec[idx];
     const int pos = atomicAdd(&sh_hist[r.cost < kCostBins ? r.cost : kCostBins - 1], 1);
-    p.blocks[pos] = r;
+    o.blocks[pos] = r;
     PlanItem it;
     it.b = r.b;
     it.blk = r.blk;
@@ -200,11 +219,23 @@ plan_kernel(PlanParams p) {
     it.c = p.nc ? p.nc[r.b] : 0;
     it.h_end = it.n - (p.nt ? p.nt[r.b] : 0);
     it.tbase = (p.ts && it.n > 0) ? p.ts[it.s0] : 0;
-    it.cs0 = p.pass == 2 ? p.off2[r.b] : 0;
-    it.L = p.pass == 2 ? (int)(p.off2[r.b + 1] - it.cs0) : 0;
-    p.items[pos] = it;
+    it.cs0 = o.pass == 2 ? p.off2[r.b] : 0;
+    it.L = o.pass == 2 ? (int)(p.off2[r.b + 1] - it.cs0) : 0;
+    o.items[pos] = it;
   }
-  if (t == 0) p.hdr[WS_NBLK] = nblk;
+  if (t == 0) {
+    if (!keep) {
+      p.hdr[WS_NBLK] = nblk;
+    } else {
+      p.hdr[WS_PB_NBLK] = nblk;
+      p.hdr[WS_PB_B] = p.B;
+      p.hdr[WS_PB_T_LO] = (int)(uint32_t)p.T;
+      p.hdr[WS_PB_T_HI] = (int)(p.T >> 32);
+      p.hdr[WS_PB_TILE] = o.BM | (o.BN << 16);
+      p.hdr[WS_PB_MAXN] = p.max_n;
+      p.hdr[WS_PB_VALID] = 1;
+    }
+  }
 }
 
 // Lists every non-skipped tile of every planned block, walking the blocks the
@@ -212,31 +243,32 @@ plan_kernel(PlanParams p) {
 // key edge.
 __global__ void debug_tiles_kernel(PlanParams p, int32_t* rec, int64_t cap) {
   const int nblk = p.hdr[WS_NBLK];
+  const PlanOut& o = p.out[0];
   for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < nblk; idx += gridDim.x * blockDim.x) {
-    const Block blk = p.blocks[idx];
+    const Block blk = o.blocks[idx];
     const SeqInfo s = seq_info(p.off, p.nt, p.nc, blk.b);
-    if (p.pass == 0) {
-      const int q0 = blk.blk * p.BM;
-      const int nkb = fwd_kv_blocks(q0, s.n, s.c, p.BM, p.BN);
+    if (o.pass == 0) {
+      const int q0 = blk.blk * o.BM;
+      const int nkb = fwd_kv_blocks(q0, s.n, s.c, o.BM, o.BN);
       for (int kb = 0; kb < nkb; ++kb) {
-        const int cls = tile_class(q0, kb * p.BN, p.BM, p.BN, s.n, s.c, s.h_end);
+        const int cls = tile_class(q0, kb * o.BN, o.BM, o.BN, s.n, s.c, s.h_end);
         if (!cls) continue;
         const int slot = atomicAdd(p.hdr + WS_NTILES, 1);
         if (slot < cap) {
           int32_t* r = rec + (int64_t)slot * 6;
-          r[0] = blk.b; r[1] = blk.blk; r[2] = kb; r[3] = cls; r[4] = p.BM; r[5] = p.BN;
+          r[0] = blk.b; r[1] = blk.blk; r[2] = kb; r[3] = cls; r[4] = o.BM; r[5] = o.BN;
         }
       }
     } else {
-      const int k0 = blk.blk * p.BN;
-      const int nqb = (s.n + p.BM - 1) / p.BM;
-      for (int qb = bwd_q_begin(k0, s.c, p.BM); qb < nqb; ++qb) {
-        const int cls = tile_class(qb * p.BM, k0, p.BM, p.BN, s.n, s.c, s.h_end);
+      const int k0 = blk.blk * o.BN;
+      const int nqb = (s.n + o.BM - 1) / o.BM;
+      for (int qb = bwd_q_begin(k0, s.c, o.BM); qb < nqb; ++qb) {
+        const int cls = tile_class(qb * o.BM, k0, o.BM, o.BN, s.n, s.c, s.h_end);
         if (!cls) continue;
         const int slot = atomicAdd(p.hdr + WS_NTILES, 1);
         if (slot < cap) {
           int32_t* r = rec + (int64_t)slot * 6;
-          r[0] = blk.b; r[1] = qb; r[2] = blk.blk; r[3] = cls; r[4] = p.BM; r[5] = p.BN;
+          r[0] = blk.b; r[1] = qb; r[2] = blk.blk; r[3] = cls; r[4] = o.BM; r[5] = o.BN;
         }
       }
     }
@@ -260,7 +292,7 @@ cudaError_t launch_plan(const PlanParams& p_in, cudaStream_t stream) {
   const size_t smem = plan_smem_bytes(p);
   cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  plan_kernel<<<1, kPlanThreads, smem, stream>>>(p);
+  plan_kernel<<<p.npass == 2 ? 2 : 1, kPlanThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

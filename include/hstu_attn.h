@@ -42,6 +42,8 @@
  *    hstu_attn_fwd_noalloc: it uses a fixed buffer built into the library
  *    in place of a workspace, shared by all its calls on a device (its own
  *    comment gives the size limit and the race between overlapping calls).
+ *    What one call leaves in a workspace for a later one is the caller's
+ *    to keep: the backward's plan kept with HSTU_FLAG_PLAN_BWD.
  *  - Calls are stream-ordered and return without synchronising, except
  *    hstu_attn_debug_plan and hstu_get_device_error, which synchronise the
  *    given stream.  Concurrent calls must use distinct workspaces.
@@ -92,6 +94,19 @@ typedef enum { HSTU_NORM_NONE = 0, HSTU_NORM_LAYERNORM = 1 } hstu_norm_t;
 #define HSTU_FLAG_U_FP32 (1u << 2)       /* u is FP32 whatever dtype is (requires out_dtype FP32).  The
                                             gate multiplies y element by element, so a BF16 rounding of u
                                             is never averaged out; q, k, v stay in dtype */
+#define HSTU_FLAG_PLAN_BWD (1u << 3)     /* hstu_attn_fwd only: its planner launch also plans the
+                                            backward's tiling (a second CTA of the same launch) and keeps
+                                            it in the workspace, which must then have the backward's size */
+#define HSTU_FLAG_REUSE_PLAN (1u << 4)   /* hstu_attn_bwd only: launch no planner and use the plan kept by
+                                            the last hstu_attn_fwd with HSTU_FLAG_PLAN_BWD on this
+                                            workspace.  The backward checks on the device that the plan was
+                                            made for the same B, total_tokens, max_seq_len and path, from
+                                            the same seq_offsets, num_targets, num_contexts and first
+                                            timestamp of every sequence; otherwise it computes nothing and
+                                            records HSTU_ERR_DEVICE_CHECK.  A kept plan serves any number of
+                                            backward calls until another planner launch on the workspace
+                                            (any forward, a backward without this flag, a debug plan)
+                                            voids it.  Rejected by the layer, delta and no-alloc calls */
 
 typedef struct {
   uint32_t struct_size;     /* sizeof(hstu_attn_desc) */
@@ -177,7 +192,11 @@ typedef struct {
  * be 256-byte aligned.  Either output pointer may be NULL. */
 hstu_status_t hstu_attn_workspace_size(const hstu_attn_desc* desc, size_t* fwd_bytes, size_t* bwd_bytes);
 
-/* Forward: o = A.V and, if y != NULL, y = Norm(o) * u (eqs. (2), (3)). */
+/* Forward: o = A.V and, if y != NULL, y = Norm(o) * u (eqs. (2), (3)).
+ * One planner launch, the attention kernel and (with y or the statistics) the
+ * norm-gate kernel.  With HSTU_FLAG_PLAN_BWD the planner also plans the
+ * backward, so a training step (forward, then the backward with
+ * HSTU_FLAG_REUSE_PLAN on the same workspace) launches one planner. */
 hstu_status_t hstu_attn_fwd(const hstu_attn_desc* desc, const hstu_attn_fwd_args* args,
                             void* workspace, size_t workspace_bytes, hstu_stream_t stream);
 

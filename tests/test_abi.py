@@ -109,6 +109,42 @@ def test_backward_requires_du_with_u():
     assert lib.hstu_attn_bwd(ctypes.byref(d), ctypes.byref(args), 4096, 1 << 30, None) == C.HSTU_ERR_INVALID_ARG
 
 
+def test_plan_keeping_flags_are_checked_before_any_launch():
+    lib = C.load()
+    d = _desc(total_tokens=1000)
+    f, b = C.hstu_attn_workspace_size(d)
+    assert b > f
+    args = C.hstu_attn_fwd_args()
+    for name in ("seq_offsets", "q", "k", "v", "o"):
+        setattr(args, name, 4096)
+    # keeping the backward's plan takes the backward's workspace
+    d.flags = C.HSTU_FLAG_PLAN_BWD
+    assert lib.hstu_attn_fwd(ctypes.byref(d), ctypes.byref(args), 4096, f, None) == C.HSTU_ERR_WORKSPACE
+    # each flag belongs to one direction
+    d.flags = C.HSTU_FLAG_REUSE_PLAN
+    assert lib.hstu_attn_fwd(ctypes.byref(d), ctypes.byref(args), 4096, 1 << 30, None) == C.HSTU_ERR_INVALID_ARG
+    bargs = C.hstu_attn_bwd_args()
+    for name in ("seq_offsets", "q", "k", "v", "o", "dy", "dq", "dk", "dv"):
+        setattr(bargs, name, 4096)
+    d.flags = C.HSTU_FLAG_PLAN_BWD
+    assert lib.hstu_attn_bwd(ctypes.byref(d), ctypes.byref(bargs), 4096, 1 << 30, None) == C.HSTU_ERR_INVALID_ARG
+    # the layer, delta and no-alloc calls plan for themselves
+    for flag in (C.HSTU_FLAG_PLAN_BWD, C.HSTU_FLAG_REUSE_PLAN):
+        dl = _desc(out_dtype="fp32", total_tokens=1000, flags=flag)
+        for call, a in ((C.hstu_layer_fwd, C.hstu_layer_fwd_args()), (C.hstu_layer_bwd, C.hstu_layer_bwd_args()),
+                        (C.hstu_attn_fwd_delta, C.hstu_attn_delta_args())):
+            if isinstance(a, C.hstu_attn_delta_args):
+                a.cand_offsets = a.cache_offsets = 256
+                for name in ("q", "k", "v", "o"):
+                    setattr(a, name, 4096)
+            with pytest.raises(C.HSTUError) as e:
+                call(dl, a, 256, 1 << 30, None)
+            assert e.value.status == C.HSTU_ERR_INVALID_ARG, (call, flag)
+        with pytest.raises(C.HSTUError) as e:
+            C.hstu_attn_fwd_noalloc(_desc(total_tokens=1000, flags=flag), args, None)
+        assert e.value.status == C.HSTU_ERR_INVALID_ARG
+
+
 def test_status_strings():
     for s in range(7):
         assert C.hstu_status_string(s) and C.hstu_status_string(s) != "unknown status"
