@@ -44,21 +44,22 @@ __device__ int cta_exclusive_scan(int v, int* wsum, int* total) {
   return before + x - v;
 }
 
-// Tiles of one block.  Pass 2 (delta forward): a block of up to BM
+// Tiles of one block that lane gl of a group of G lanes counts (the group's
+// sum is the block's cost).  Pass 2 (delta forward): a block of up to BM
 // candidates sees every cached key tile of its sequence plus one tile of its
 // own keys (the diagonal); cached_len is that sequence's cached-token count.
-__device__ int block_cost(const SeqInfo& s, int blk, int pass, int BM, int BN, int cached_len) {
+__device__ int block_cost_part(const SeqInfo& s, int blk, int pass, int BM, int BN, int cached_len, int gl, int G) {
   int cost = 0;
   if (pass == 2) {
-    cost = (cached_len + BN - 1) / BN + 1;
+    cost = gl == 0 ? (cached_len + BN - 1) / BN + 1 : 0;
   } else if (pass == 0) {
     const int q0 = blk * BM;
     const int nkb = fwd_kv_blocks(q0, s.n, s.c, BM, BN);
-    for (int kb = 0; kb < nkb; ++kb) cost += tile_class(q0, kb * BN, BM, BN, s.n, s.c, s.h_end) != 0;
+    for (int kb = gl; kb < nkb; kb += G) cost += tile_class(q0, kb * BN, BM, BN, s.n, s.c, s.h_end) != 0;
   } else {
     const int k0 = blk * BN;
     const int nqb = (s.n + BM - 1) / BM;
-    for (int qb = bwd_q_begin(k0, s.c, BM); qb < nqb; ++qb)
+    for (int qb = bwd_q_begin(k0, s.c, BM) + gl; qb < nqb; qb += G)
       cost += tile_class(qb * BM, k0, BM, BN, s.n, s.c, s.h_end) != 0;
   }
   return cost;
@@ -80,6 +81,21 @@ plan_kernel(PlanParams p) {
   if (p.stage_off) { off = reinterpret_cast<int64_t*>(cur); cur += sizeof(int64_t) * ((p.B + 2) & ~1); }
   int* start = nullptr;
   if (p.stage_off) { start = reinterpret_cast<int*>(cur); cur += sizeof(int) * ((p.B + 1 + 3) & ~3); }
+  // the per-sequence counts and first timestamps, staged with the offsets
+  const int32_t* nt = p.nt;
+  const int32_t* nc = p.nc;
+  int64_t* t0s = nullptr;
+  if (p.stage_off) {
+    t0s = reinterpret_cast<int64_t*>(cur); cur += sizeof(int64_t) * ((p.B + 1) & ~1);
+    int32_t* nts = reinterpret_cast<int32_t*>(cur); cur += sizeof(int32_t) * ((p.B + 3) & ~3);
+    int32_t* ncs = reinterpret_cast<int32_t*>(cur); cur += sizeof(int32_t) * ((p.B + 3) & ~3);
+    for (int i = threadIdx.x; i < p.B; i += kPlanThreads) {
+      nts[i] = p.nt ? p.nt[i] : 0;
+      ncs[i] = p.nc ? p.nc[i] : 0;
+    }
+    nt = nts;
+    nc = ncs;
+  }
   const bool keep = blockIdx.x == 1;
   const PlanOut o = keep ? p.out[1] : p.out[0];
   if (!start) start = o.seq_start;
@@ -110,11 +126,11 @@ plan_kernel(PlanParams p) {
   __syncthreads();
 
   // 1. validation
-  if (t == 0 && (p.off[0] != 0 || p.off[p.B] != p.T)) atomicExch(&sh_bad, 1);
+  if (t == 0 && (off[0] != 0 || off[p.B] != p.T)) atomicExch(&sh_bad, 1);
   if (t == 0 && o.pass == 2 && (p.off2[0] != 0 || p.off2[p.B] != p.T2)) atomicExch(&sh_bad, 1);
   for (int b = t; b < p.B; b += kPlanThreads) {
     const int64_t n = off[b + 1] - off[b];
-    const int64_t m = p.nt ? p.nt[b] : 0, c = p.nc ? p.nc[b] : 0;
+    const int64_t m = nt ? nt[b] : 0, c = nc ? nc[b] : 0;
     // pass 2: n candidates after L cached tokens, n + L <= N
     const int64_t L = o.pass == 2 ? p.off2[b + 1] - p.off2[b] : 0;
     if (n < 0 || L < 0 || n + L > p.max_n || m < 0 || c < 0 || m + c > n) {
@@ -135,9 +151,11 @@ plan_kernel(PlanParams p) {
     }
     return;
   }
-  if (keep)  // the offsets are consistent now, so every first token is in range
-    for (int b = t; b < p.B; b += kPlanThreads)
-      p.sv_t0[b] = (p.ts && off[b + 1] > off[b]) ? p.ts[off[b]] : 0;
+  // first timestamp of each sequence (the offsets are consistent now, so
+  // every first token is in range): loads issued here, stored to shared
+  // memory only before the scatter, so their latency overlaps steps 2-4
+  int64_t my_t0 = 0;
+  if (t0s && t < p.B && p.ts && off[t + 1] > off[t]) my_t0 = p.ts[off[t]];
 
   // 2. blocks per sequence -> exclusive prefix (start[b]), one chunk of
   // kPlanThreads sequences at a time
@@ -160,28 +178,47 @@ plan_kernel(PlanParams p) {
   }
   __syncthreads();
 
-  // 3. cost of every block, histogram of costs
-  for (int idx = t; idx < nblk; idx += kPlanThreads) {
-    int lo = 0, hi = p.B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (start[mid] <= idx) lo = mid; else hi = mid - 1;
+  // 3. cost of every block, histogram of costs.  While blocks are few, a
+  // group of G lanes walks each block's tiles (a long sequence's blocks walk
+  // up to N / 64 tiles); G = 1 once every thread has blocks of its own.
+  {
+    const int G = nblk <= kPlanThreads / 8 * 4 ? 8 : 1;
+    const int gl = t % G;
+    const unsigned gmask = G == 8 ? 0xffu << ((t & 31) & ~7) : 1u << (t & 31);
+    for (int idx = t / G; idx < nblk; idx += kPlanThreads / G) {
+      int lo = 0, hi = p.B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (start[mid] <= idx) lo = mid; else hi = mid - 1;
+      }
+      const int b = lo;  // the last sequence starting at or before idx (skips empty ones)
+      SeqInfo s;
+      s.s0 = off[b];
+      s.n = (int)(off[b + 1] - s.s0);
+      s.c = nc ? nc[b] : 0;
+      s.h_end = s.n - (nt ? nt[b] : 0);
+      const int blk = idx - start[b];
+      const int cached_len = o.pass == 2 ? (int)(p.off2[b + 1] - p.off2[b]) : 0;
+      int cost = block_cost_part(s, blk, o.pass, o.BM, o.BN, cached_len, gl, G);
+      for (int x = 1; x < G; x <<= 1) cost += __shfl_xor_sync(gmask, cost, x);
+      if (gl == 0) {
+        Block r;
+        r.b = b; r.blk = blk; r.cost = cost; r.pad = 0;
+        rec[idx] = r;
+        atomicAdd(&sh_hist[cost < kCostBins ? cost : kCostBins - 1], 1);
+      }
     }
-    const int b = lo;  // the last sequence starting at or before idx (skips empty ones)
-    SeqInfo s;
-    s.s0 = off[b];
-    s.n = (int)(off[b + 1] - s.s0);
-    s.c = p.nc ? p.nc[b] : 0;
-    s.h_end = s.n - (p.nt ? p.nt[b] : 0);
-    const int blk = idx - start[b];
-    const int cached_len = o.pass == 2 ? (int)(p.off2[b + 1] - p.off2[b]) : 0;
-    const int cost = block_cost(s, blk, o.pass, o.BM, o.BN, cached_len);
-    Block r;
-    r.b = b; r.blk = blk; r.cost = cost; r.pad = 0;
-    rec[idx] = r;
-    atomicAdd(&sh_hist[cost < kCostBins ? cost : kCostBins - 1], 1);
+  }
+  if (t0s) {
+    if (t < p.B) t0s[t] = my_t0;
+    for (int b = t + kPlanThreads; b < p.B; b += kPlanThreads)
+      t0s[b] = (p.ts && off[b + 1] > off[b]) ? p.ts[off[b]] : 0;
   }
   __syncthreads();
+  if (keep && t0s)
+    for (int b = t; b < p.B; b += kPlanThreads) p.sv_t0[b] = t0s[b];
+  if (keep && !t0s)
+    for (int b = t; b < p.B; b += kPlanThreads) p.sv_t0[b] = (p.ts && off[b + 1] > off[b]) ? p.ts[off[b]] : 0;
 
   // 4. exclusive scan of the histogram in descending cost order: thread t
   // owns bins kCostBins-1-4t .. kCostBins-4-4t
@@ -216,9 +253,9 @@ plan_kernel(PlanParams p) {
     it.blk = r.blk;
     it.s0 = off[r.b];
     it.n = (int)(off[r.b + 1] - it.s0);
-    it.c = p.nc ? p.nc[r.b] : 0;
-    it.h_end = it.n - (p.nt ? p.nt[r.b] : 0);
-    it.tbase = (p.ts && it.n > 0) ? p.ts[it.s0] : 0;
+    it.c = nc ? nc[r.b] : 0;
+    it.h_end = it.n - (nt ? nt[r.b] : 0);
+    it.tbase = t0s ? t0s[r.b] : ((p.ts && it.n > 0) ? p.ts[it.s0] : 0);
     it.cs0 = o.pass == 2 ? p.off2[r.b] : 0;
     it.L = o.pass == 2 ? (int)(p.off2[r.b + 1] - it.cs0) : 0;
     o.items[pos] = it;
@@ -280,7 +317,9 @@ __global__ void debug_tiles_kernel(PlanParams p, int32_t* rec, int64_t cap) {
 size_t plan_smem_bytes(const PlanParams& p) {
   size_t bytes = sizeof(int) * kCostBins;
   // every region a multiple of 16 bytes, so the 16-byte block records stay aligned
-  if (p.stage_off) bytes += sizeof(int64_t) * ((p.B + 2) & ~1) + sizeof(int) * ((p.B + 1 + 3) & ~3);
+  if (p.stage_off)
+    bytes += sizeof(int64_t) * ((p.B + 2) & ~1) + sizeof(int) * ((p.B + 1 + 3) & ~3) +
+             sizeof(int64_t) * ((p.B + 1) & ~1) + 2 * sizeof(int32_t) * ((p.B + 3) & ~3);
   if (p.stage_rec) bytes += sizeof(Block) * (size_t)p.cap_blocks;
   return bytes;
 }
