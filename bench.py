@@ -20,7 +20,9 @@ The e2e figure runs the same steps through the C ABI from pinned host
 buffers, every step's inputs uploaded and its result read back (a training
 step's parameter gradients, an inference request's candidate outputs), the
 copies on two streams overlapping the neighbouring steps' compute;
-e2e.all_outputs reads back every output and gradient instead.
+e2e.all_outputs reads back every output and gradient instead.  A heavy-tailed
+batch's inputs sit in one buffer (one transfer per step, as a data loader
+delivers a batch).
 
 With --graph the K timed steps are captured once as a CUDA graph and the
 timed region replays it (the per-kernel events of the library's timing hook
@@ -232,7 +234,8 @@ class AttentionWorkload:
 
     def problem(self, b, dev):
         from hstu_jagged_attention_02_gb300.attention import Problem
-        return Problem(b, device=dev, out_dtype="fp32", dropout=self.dropout(), plan_once=self.plan_once)
+        return Problem(b, device=dev, out_dtype="fp32", dropout=self.dropout(), plan_once=self.plan_once,
+                       packed_inputs=True)
 
     def flops(self, b):
         """(attention fwd, attention bwd, whole step) useful FLOPs."""
@@ -244,8 +247,9 @@ class AttentionWorkload:
         return KERNEL_BYTES_PER_ELEM[role] * b.T * b.H * b.d_qk
 
     def host_io(self, pr):
-        ins = [t for t in (pr.offsets, pr.num_targets, pr.num_contexts, pr.timestamps, pr.rab_pos,
-                           pr.rab_time, pr.q, pr.k, pr.v, pr.u, pr.dy) if t is not None]
+        # a batch's inputs sit in one device buffer, as a data loader would
+        # deliver them: one host-to-device transfer per step
+        ins = [pr.input_buffer]
         outs = [t for t in (pr.y, pr.dq, pr.dk, pr.dvv, pr.du, pr.d_rab_pos, pr.d_rab_time)
                 if t is not None]
         return ins, outs

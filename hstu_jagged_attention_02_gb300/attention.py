@@ -31,12 +31,15 @@ class Problem:
 
     def __init__(self, batch, device="cuda", flags: int = 0, want_y: bool = True,
                  want_stats: bool = False, want_drab: bool = True, out_dtype: str = "fp32",
-                 dropout=None, bwd_flags: int = 0, plan_once: bool = False):
+                 dropout=None, bwd_flags: int = 0, plan_once: bool = False, packed_inputs: bool = False):
         # dropout: None or (p, seed, offset) of the fused dropout on y;
         # bwd_flags: flags added for the backward call only (e.g.
         # HSTU_FLAG_FORCE_SIMT for a BF16 backward without a tensor-core kernel);
         # plan_once: the forward plans the backward too (HSTU_FLAG_PLAN_BWD)
-        # and the backward reuses that plan (HSTU_FLAG_REUSE_PLAN)
+        # and the backward reuses that plan (HSTU_FLAG_REUSE_PLAN);
+        # packed_inputs: every input lives in one device buffer
+        # (self.input_buffer, 256-byte aligned slots), so a host copy of the
+        # whole batch is one transfer
         self.batch = batch
         dev = torch.device(device)
         self.dev = dev
@@ -65,6 +68,9 @@ class Problem:
         self.q, self.k, self.v = up(batch.q, td), up(batch.k, td), up(batch.v, td)
         self.u = up(batch.u, torch.float32 if flags & C.HSTU_FLAG_U_FP32 else td)
         self.dy = up(batch.dy, to)
+        self.input_buffer = None
+        if packed_inputs:
+            self._pack_inputs()
         z = lambda *s, dt=to: torch.empty(*s, device=dev, dtype=dt)
         self.o = z(T, H, dv)
         self.y = z(T, F) if want_y else None
@@ -104,6 +110,27 @@ class Problem:
                 _ptr(self.k), _ptr(self.v), _ptr(self.u), _ptr(self.o), _ptr(self.dy),
                 _ptr(self.dq), _ptr(self.dk), _ptr(self.dvv), _ptr(self.du), _ptr(self.d_rab_pos),
                 _ptr(self.d_rab_time), seed, offset)
+
+    _INPUTS = ("offsets", "num_targets", "num_contexts", "timestamps", "rab_pos", "rab_time", "q", "k", "v",
+               "u", "dy")
+
+    def _pack_inputs(self):
+        """Move every input tensor into one device buffer (views at 256-byte
+        aligned offsets)."""
+        names = [n for n in self._INPUTS if getattr(self, n) is not None]
+        offs, total = {}, 0
+        for n in names:
+            t = getattr(self, n)
+            offs[n] = total
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        buf = torch.empty(max(total, 256), device=self.dev, dtype=torch.uint8)
+        for n in names:
+            t = getattr(self, n)
+            nbytes = t.numel() * t.element_size()
+            view = buf[offs[n]:offs[n] + nbytes].view(t.dtype).view(t.shape)
+            view.copy_(t)
+            setattr(self, n, view)
+        self.input_buffer = buf
 
     def forward(self, stream=None):
         d = self.desc

@@ -120,3 +120,17 @@ def test_plain_forward_voids_the_kept_plan():
     torch.cuda.synchronize()
     assert pr.device_error() == 0
     check(_grads(pr), run_oracle(b), TOL["bf16"])
+
+
+def test_packed_inputs_match_the_oracle():
+    # the benchmark's step: every input in one device buffer, one planner launch
+    b = _ragged_batch("bf16", 128, seed=150)
+    pr = Problem(b, plan_once=True, packed_inputs=True)
+    base = pr.input_buffer.data_ptr()
+    for t in (pr.offsets, pr.timestamps, pr.q, pr.k, pr.v, pr.u, pr.dy):
+        assert base <= t.data_ptr() < base + pr.input_buffer.numel() and t.data_ptr() % 256 == 0
+    pr.forward()
+    pr.backward()
+    torch.cuda.synchronize()
+    assert pr.device_error() == 0
+    check(_grads(pr), run_oracle(b), TOL["bf16"])
