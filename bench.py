@@ -595,7 +595,7 @@ def run_gpu(args, wl, rank, world, local_rank):
     e2e["read_back"] = "the step's result: " + ("the candidates' outputs" if not wl.has_backward
                                                  else "the parameter gradients (activation gradients stay on the device)")
     e2e_all = run_e2e(args, wl, probs, flops, stream, world, all_outputs=True)
-    e2e["all_outputs"] = {k: e2e_all[k] for k in ("value", "d2h_bytes_per_step", "ms_per_step")}
+    e2e["all_outputs"] = {k: e2e_all[k] for k in ("value", "d2h_bytes_per_step", "ms_per_step", "repeats")}
 
     if rank != 0:
         return
@@ -678,7 +678,9 @@ def run_e2e(args, wl, probs, flops, stream, world, all_outputs=False):
     drain would (each batch has its own device buffers; a step's upload waits
     until the download of the previous step that used those buffers is done,
     and its compute waits for its upload).  The timed region runs from before
-    the first upload to after the last download.  Returns the e2e dict."""
+    the first upload to after the last download; it covers at least 100 ms of
+    steps and is timed three times (the median is the value, all three are
+    reported).  Returns the e2e dict."""
     import torch
     nb = len(probs)
     hosts = []
@@ -721,24 +723,39 @@ def run_e2e(args, wl, probs, flops, stream, world, all_outputs=False):
     for w in range(max(args.warmup, 1)):
         one(w)
     torch.cuda.synchronize()
+
+    def timed(k):
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        up.wait_stream(stream)
+        down.wait_stream(stream)
+        for i in range(k):
+            one(i)
+        stream.wait_stream(down)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
+    # The host link and the host thread that issues the copies are shared
+    # with the rest of the machine, so a region of a few milliseconds can
+    # catch a stall: the region is stretched to at least 100 ms of steps and
+    # timed three times, and the median is reported with all three.
     k = args.steps
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    up.wait_stream(stream)
-    down.wait_stream(stream)
-    for i in range(k):
-        one(i)
-    stream.wait_stream(down)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1)
-    fl = sum(flops[i % nb][2] for i in range(k))
-    if world > 1:
-        from hstu_jagged_attention_02_gb300 import dp
-        ms, fl = dp.reduce_step_time(ms, fl, device=torch.device("cuda", torch.cuda.current_device()))
-    return {"value": fl / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": bi,
-            "d2h_bytes_per_step": bo, "ms_per_step": ms / k}
+    ms_first = timed(k)
+    if world == 1 and ms_first < 100.0:   # ranks keep one step count
+        k = min(2000, max(k, int(k * 100.0 / max(ms_first, 1e-3)) + 1))
+    runs = []
+    for _ in range(3):
+        ms = timed(k)
+        fl = sum(flops[i % nb][2] for i in range(k))
+        if world > 1:
+            from hstu_jagged_attention_02_gb300 import dp
+            ms, fl = dp.reduce_step_time(ms, fl, device=torch.device("cuda", torch.cuda.current_device()))
+        runs.append((fl / (ms * 1e-3) / 1e12, ms))
+    value, ms = sorted(runs)[1]
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "ms_per_step": ms / k, "steps": k, "repeats": [round(v, 2) for v, _ in runs]}
 
 
 def main():

@@ -278,7 +278,8 @@ __global__ void __launch_bounds__(kWarps * 32) norm_gate_bwd_kernel(NormParams p
   // shares no data: it runs alongside it.  One thread waits for the planner,
   // so this grid completes only after it (the attention backward, launched
   // normally after this kernel, reads the plan).  Without a planner, warp 0
-  // of CTA 0 checks and arms the kept plan instead.
+  // of CTA 0 checks and arms the kept plan instead, and takes no tokens (its
+  // dependent reads would otherwise delay its tokens past everyone else's).
   if (blockIdx.x == 0 && threadIdx.x == 0) pdl_wait();
   if (p.pc_hdr && blockIdx.x == 0 && threadIdx.x < 32) check_kept_plan(p);
   if (blockIdx.x == 0) {
@@ -288,8 +289,10 @@ __global__ void __launch_bounds__(kWarps * 32) norm_gate_bwd_kernel(NormParams p
   const int lane = threadIdx.x & 31;
   const int F = p.F;
   const bool ln = p.norm == HSTU_NORM_LAYERNORM;
-  const int64_t stride = (int64_t)gridDim.x * kWarps;
-  for (int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); t < p.T; t += stride) {
+  const int skip = p.pc_hdr ? 1 : 0;  // warps numbered from CTA 0's warp 1 when it checks
+  const int64_t stride = (int64_t)gridDim.x * kWarps - skip;
+  const int64_t first = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5) - skip;
+  for (int64_t t = first < 0 ? p.T : first; t < p.T; t += stride) {
     float x[PER][VEC], d[PER][VEC], g[PER][VEC];
     load_row<VEC, PER>(static_cast<const TO*>(p.o) + t * F, F, lane, x);
     load_row<VEC, PER>(static_cast<const TO*>(p.dy) + t * F, F, lane, d);
