@@ -205,14 +205,11 @@ __device__ __forceinline__ void grad_cols(const AttnParams& p, const uint32_t (&
         if (bps[c + e] == p.P - 1) acc.rp_far += dz;
         else red_add(kc.drp + bps[c + e], dz, true);
       }
-      if (kc.want_rt && valid) {
-        if (bts[c + e] == acc.rt_cur) {
-          acc.rt_run += dz;
-        } else {
-          red_add(kc.drp + p.P + acc.rt_cur, acc.rt_run, acc.rt_cur >= 0);
-          acc.rt_cur = bts[c + e];
-          acc.rt_run = dz;
-        }
+      if (kc.want_rt) {
+        const bool flush = valid && bts[c + e] != acc.rt_cur;
+        red_add(kc.drp + p.P + acc.rt_cur, acc.rt_run, flush && acc.rt_cur >= 0);
+        acc.rt_run = flush ? dz : acc.rt_run + dz;
+        acc.rt_cur = flush ? bts[c + e] : acc.rt_cur;
       }
     }
     const uint32_t ah = pack_bf16(av[0], av[1]);
@@ -294,13 +291,10 @@ __device__ __forceinline__ float grad_time16(const AttnParams& p, const uint32_t
       const float gs[2] = {g2.x, g2.y};
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        if (bts[e] == acc.rt_cur) {
-          acc.rt_run += gs[e];
-        } else {
-          red_add(drt + acc.rt_cur, acc.rt_run, acc.rt_cur >= 0);
-          acc.rt_cur = bts[e];
-          acc.rt_run = gs[e];
-        }
+        const bool flush = bts[e] != acc.rt_cur;
+        red_add(drt + acc.rt_cur, acc.rt_run, flush && acc.rt_cur >= 0);
+        acc.rt_run = flush ? gs[e] : acc.rt_run + gs[e];
+        acc.rt_cur = bts[e];
       }
     }
     const uint32_t ah = pack_bf16(a2.x, a2.y), zh = pack_bf16(g2.x, g2.y);

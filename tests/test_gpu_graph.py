@@ -54,11 +54,12 @@ def _capture_and_replay(step, outputs):
     _compare(eager, _snapshot(outputs()))
 
 
-@pytest.mark.parametrize("dropout", [None, (0.2, 31, 7)])
-def test_attention_forward_backward_in_a_graph(dropout):
+@pytest.mark.parametrize("dropout,plan_once", [(None, False), ((0.2, 31, 7), False), (None, True)])
+def test_attention_forward_backward_in_a_graph(dropout, plan_once):
+    # plan_once: the benchmark's step (one planner launch, inputs in one buffer)
     from hstu_jagged_attention_02_gb300.attention import Problem
     b = synth.by_name("heavy_tailed", 3)
-    pr = Problem(b, dropout=dropout)
+    pr = Problem(b, dropout=dropout, plan_once=plan_once, packed_inputs=plan_once)
 
     def step():
         pr.forward()
