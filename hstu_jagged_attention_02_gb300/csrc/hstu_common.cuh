@@ -29,7 +29,7 @@ enum : int {
   WS_LAYER_INFO = 7,
   // the backward's tile plan kept by a forward called with HSTU_FLAG_PLAN_BWD
   // (second plan region of the workspace) and what it was made for
-  WS_PB_VALID = 8,  // 1 while the kept plan is valid; every other planner launch clears it
+  WS_PB_VALID = 8,  // kKeptPlanValid while the kept plan is valid; every other planner launch clears it
   WS_PB_NBLK = 9,   // its block count
   WS_PB_B = 10,     // sequences
   WS_PB_T_LO = 11,  // tokens, low and high 32 bits

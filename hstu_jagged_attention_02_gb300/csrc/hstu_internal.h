@@ -43,6 +43,9 @@ struct PlanParams {
   int stage_off;    // set by launch_plan: offsets and block starts staged in shared memory
   int stage_rec;    // set by launch_plan: block records staged in shared memory
 };
+// WS_PB_VALID while a kept backward plan is valid: a value that fresh or
+// reused workspace memory is unlikely to hold by chance
+constexpr int kKeptPlanValid = 0x4b505431;
 // planner shared-memory staging limits (sequences, blocks)
 constexpr int kPlanStageSeqs = 2048;
 constexpr int kPlanStageBlocks = 8192;

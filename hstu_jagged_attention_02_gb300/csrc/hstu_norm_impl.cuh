@@ -244,7 +244,7 @@ __device__ __noinline__ void check_kept_plan(const NormParams& p) {
   int* h = p.pc_hdr;
   const int lane = threadIdx.x & 31;
   const int64_t T = p.T;
-  const bool key = h[WS_PB_VALID] == 1 && h[WS_PB_B] == p.pc_B && h[WS_PB_T_LO] == (int)(uint32_t)T &&
+  const bool key = h[WS_PB_VALID] == kKeptPlanValid && h[WS_PB_B] == p.pc_B && h[WS_PB_T_LO] == (int)(uint32_t)T &&
                    h[WS_PB_T_HI] == (int)(T >> 32) && h[WS_PB_TILE] == p.pc_tile && h[WS_PB_MAXN] == p.pc_max_n;
   bool ok = key;
   if (key) {  // same B and T: the kept offsets (validated when planned) index this call's arrays

@@ -270,7 +270,7 @@ plan_kernel(PlanParams p) {
       p.hdr[WS_PB_T_HI] = (int)(p.T >> 32);
       p.hdr[WS_PB_TILE] = o.BM | (o.BN << 16);
       p.hdr[WS_PB_MAXN] = p.max_n;
-      p.hdr[WS_PB_VALID] = 1;
+      p.hdr[WS_PB_VALID] = kKeptPlanValid;
     }
   }
 }
