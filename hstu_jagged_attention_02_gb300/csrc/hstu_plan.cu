@@ -7,7 +7,9 @@
 // order gets an LPT-style balance.  This is the "greedy even core split" and
 // "compound-mask skipping" of the Ascend HSTU fused operator (wmrh.cn RecSDK
 // page, "HSTU acceleration operator" paragraph), done on the device so no
-// host synchronisation is needed.
+// host synchronisation is needed.  A forward that also plans the backward
+// launches a second CTA, which plans the backward's tiling at the same time
+// and records what it was made from, so the backward needs no planner launch.
 #include "hstu_internal.h"
 
 namespace hstu {
